@@ -1,0 +1,392 @@
+"""Benchmark: chunked Gated DeltaNet prefill throughput on one GB300.
+
+One step = one ``gdn_prefill_ex`` call over the whole workload (every stage
+of the hot path: the optional short conv, the chunk solve and the chunk-to-
+chunk state propagation), inputs resident in HBM.  Default workload: the
+4096-token prompt, B=1, Hk=Hv=16, dk=dv=128, chunk 64, bf16 q/k/v/out, fp32
+g/beta/state, zero incoming state.
+
+Prints ONE JSON line (rank 0) with tokens/s, the roofline of the dominant
+kernel (algorithmic bytes / CUDA-event time vs the measured HBM peak), the
+end-to-end number through the C ABI with host buffers, the clocks seen during
+the timed region and the float64 CPU oracle timed on the host's cores.
+
+L2: the workload (~70 MB) fits in the 129 MB L2, so the timed steps rotate
+through enough independent copies of the inputs and outputs that each step
+touches buffers last used more than 2 x L2 bytes earlier.
+
+``--impl reference`` times the float64 oracle (the only reference that
+exists for this method) on the host cores instead, on the same workload.
+Under torchrun (N > 1) every rank runs its own replica (the path shards over
+independent prompts with no exchange); rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+WORKLOADS = {
+    2: "prompt4k: B=1, Hk=Hv=16, dk=dv=128, T=4096, chunk 64, bf16 q/k/v/out, fp32 g/beta/state",
+    4: "stress: B=2 x 1024 tokens, H=8, dk=dv=128, chunk 64, bf16, nearly parallel keys",
+    5: "long: B=1, T=65536, Hk=16, Hv=32, dk=dv=128, conv K=4, chunk 64, bf16",
+    3: "ragged: 8 prompts U[1,8192], Hk=16, Hv=32, dk=dv=128, conv K=4, chunk 64, bf16",
+}
+METRIC = "prefill tokens/s (1 GB300) and % of roofline, dk=dv=128, 4096-token prompt"
+
+
+def algorithmic_bytes(p) -> int:
+    """Inputs read once + outputs written once + state in/out (per call)."""
+    es = 2 if str(p.dtype).endswith("bfloat16") else 4
+    T = p.T
+    b = 0
+    if p.conv is not None:
+        K = p.conv["w"].shape[1]
+        b += T * p.channels * es + p.channels * K * 4 + 2 * p.B * p.channels * (K - 1) * 4
+    else:
+        b += T * (2 * p.Hk * p.dk + p.Hv * p.dv) * es
+    b += T * p.Hv * 8                     # g, beta
+    b += T * p.Hv * p.dv * es             # out
+    b += 2 * p.B * p.Hv * p.dk * p.dv * 4  # state in + out
+    b += (p.B + 1) * 4
+    return b
+
+
+def algorithmic_flops(p, C=64) -> int:
+    """Full 64-row tiles: per k-head token 4*C*dk (K K^T, Q K^T); per v-head
+    token 6*dk*dv + 4*C*dv (K S_0, Q S_0, K~^T U; T rhs, P U)."""
+    T = p.T
+    return T * (p.Hk * 4 * C * p.dk + p.Hv * (6 * p.dk * p.dv + 4 * C * p.dv))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "chunked_gated_delta_chunk_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    entry = d.get(kernel_name)
+    if not entry or entry.get("source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_tokens_per_s(p, budget_s=12.0):
+    """The float64 oracle, as it stands, on the host cores: whole workload
+    passes repeated until ``budget_s`` of wall time (at least one)."""
+    import oracle
+    oracle.build_oracle()
+    cores = oracle.max_threads()
+    done, tokens, t0 = 0, 0, time.perf_counter()
+    while True:
+        oracle.oracle_prefill(p.q, p.k, p.v, p.g, p.beta, p.cu_seqlens, p.Hk, p.Hv, p.dk, p.dv,
+                              state_in=p.state_in, conv=p.conv, use_l2norm=p.use_l2norm,
+                              q_scale=p.q_scale)
+        done += 1
+        tokens += p.T
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return tokens / el, cores, f"{done} full passes of the workload ({p.T} tokens each) in {el:.1f} s"
+
+
+def make_workload(cfg):
+    from chunked_gated_delta_chunk_gb300 import inputs
+    p = inputs.make_config(cfg)
+    if cfg == 5:
+        # incoming state: the GPU path's own result for the prior 4096-token prompt
+        from chunked_gated_delta_chunk_gb300 import runner
+        import torch
+        r = runner.prefill(p.prior)
+        p.state_in = r["state_out"]
+        p.conv["state_in"] = r["conv_state_out"]
+        torch.cuda.empty_cache()
+    return p
+
+
+def _prefix(p, S):
+    """The first S tokens of a single-sequence workload (inputs only)."""
+    import copy
+    q = copy.copy(p)
+    q.cu_seqlens = p.cu_seqlens.clone()
+    q.cu_seqlens[-1] = S
+    q.g, q.beta = p.g[:S], p.beta[:S]
+    if p.conv is not None:
+        q.conv = dict(p.conv, x=p.conv["x"][:S])
+    else:
+        q.q, q.k, q.v = p.q[:S], p.k[:S], p.v[:S]
+    return q
+
+
+def run_reference(args, rank, world):
+    """The float64 oracle as it stands, on the host cores, on the same
+    workload; each step is a prefix of the prompt sized so that all steps
+    together take about two minutes (tokens/s is then tokens of the prefix
+    over its time: the oracle's cost is linear in tokens)."""
+    if rank != 0:
+        return
+    import oracle
+    from chunked_gated_delta_chunk_gb300 import inputs
+    oracle.build_oracle()
+    p = inputs.make_config(args.config, with_prior=False)
+    run = lambda q: oracle.oracle_prefill(q.q, q.k, q.v, q.g, q.beta, q.cu_seqlens, q.Hk, q.Hv,
+                                          q.dk, q.dv, state_in=q.state_in, conv=q.conv,
+                                          use_l2norm=q.use_l2norm, q_scale=q.q_scale)
+    if p.B == 1:
+        probe = min(256, p.T)
+        t0 = time.perf_counter()
+        run(_prefix(p, probe))
+        per_token = (time.perf_counter() - t0) / probe
+        S = int(min(p.T, max(64, 120.0 / max(args.steps, 1) / max(per_token, 1e-9))))
+        sample = _prefix(p, S)
+        what = f"first {S} of {p.T} tokens, all heads, per step"
+    else:
+        sample, S = p, p.T
+        what = f"the whole workload ({p.T} tokens) per step"
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        run(sample)
+    total = time.perf_counter() - t_all
+    tps = S * args.steps / total
+    cores = oracle.max_threads()
+    line = {"metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOADS[args.config], "global_batch": p.B, "seq_len": p.T,
+                       "parallelism": "replicas"},
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": what},
+            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from chunked_gated_delta_chunk_gb300 import binding as B
+    from chunked_gated_delta_chunk_gb300 import build as build_mod
+    from chunked_gated_delta_chunk_gb300 import runner
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    build_mod.build()
+
+    p = make_workload(args.config)
+    one = runner.PrefillCall(p, dev)
+    set_bytes = sum(t.numel() * t.element_size() for t in
+                    (one.q, one.k, one.v, one.x, one.g, one.beta, one.state_in, one.out,
+                     one.state_out, one.workspace) if t is not None)
+    nsets = max(1, min(16, -(-2 * L2_BYTES // max(set_bytes, 1)) + 1))
+    calls = [one] + [runner.PrefillCall(p, dev) for _ in range(nsets - 1)]
+    stream = torch.cuda.current_stream(dev)
+
+    for i in range(args.warmup):
+        calls[i % nsets].run(stream)
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        start.record(stream)
+        for i in range(args.steps):
+            calls[i % nsets].run(stream)
+        stop.record(stream)
+        barrier()
+    ms_total = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    tokens_per_s = world * p.T / (ms_step * 1e-3)
+    launches_per_call = len(B.gdn_prefill_plan(one.desc))
+
+    # End to end through the C ABI with host buffers: pinned H2D of the step's
+    # inputs, the call, D2H of out and state_out, every step.
+    host_in = {name: getattr(one, name).cpu().pin_memory() for name in
+               ("q", "k", "v", "x", "g", "beta", "state_in") if getattr(one, name) is not None}
+    host_out = {name: torch.empty(getattr(one, name).shape, dtype=getattr(one, name).dtype).pin_memory()
+                for name in ("out", "state_out")}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    e2e_steps = max(3, min(args.steps, 50))
+    for it in range(e2e_steps + 2):
+        if it == 2:
+            barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        for name, t in host_in.items():
+            getattr(one, name).copy_(t, non_blocking=True)
+        one.run(stream)
+        for name, t in host_out.items():
+            t.copy_(getattr(one, name), non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    hbm, tflops, peak_kind = load_peaks()
+    bytes_alg = algorithmic_bytes(p)
+    flops_alg = algorithmic_flops(p)
+    t_bytes = bytes_alg / (hbm * 1e9)
+    t_flops = flops_alg / (tflops * 1e12)
+    bound = "hbm" if t_bytes >= t_flops else "tensor"
+    plan = B.gdn_prefill_plan(one.desc)
+    dominant = [k for k in plan if k.startswith("chunk_")][0]
+    kern_ms = ms_step  # the chunk kernel is the only launch of a no-conv step
+    if bound == "hbm":
+        achieved = bytes_alg / (kern_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm}
+    else:
+        achieved = flops_alg / (kern_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
+                "frac": achieved / tflops}
+    roof["traffic"] = recorded_traffic(dominant)
+    roof["peak_source"] = peak_kind
+    roof["kernel"] = dominant
+    roof["algorithmic_bytes"] = bytes_alg
+    roof["algorithmic_flops"] = flops_alg
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, cores, sample = cpu_oracle_tokens_per_s(p)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOADS[args.config], "global_batch": p.B, "seq_len": p.T,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": f"rotating {nsets} independent buffer sets "
+                             f"({nsets * set_bytes / 2**20:.0f} MiB > 2 x L2)"},
+            "roofline": roof,
+            "e2e": {"value": world * p.T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_call * args.steps,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

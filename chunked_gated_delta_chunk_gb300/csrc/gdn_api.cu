@@ -1,0 +1,282 @@
+// C ABI of libgdn.so (declared in include/gdn.h): argument validation, launch
+// planning and status codes.  Every check runs before the first enqueue, so a
+// rejected call enqueues nothing; nothing here allocates or synchronises.
+#include <cstdint>
+#include <cstring>
+
+#include "gdn_common.cuh"
+#include "gdn_tc.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+bool head_dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return GDN_OK;
+    g_last_cuda_error = int(e);
+    return GDN_ERR_CUDA;
+}
+
+size_t elem_size(int dtype) { return dtype == GDN_FP32 ? 4 : 2; }
+
+int64_t conv_channels(const gdn_prefill_desc* d) {
+    return 2 * int64_t(d->Hk) * d->dk + int64_t(d->Hv) * d->dv;
+}
+
+// Shape, dtype and option checks shared by prefill and step.
+int check_common(const gdn_prefill_desc* d) {
+    if (d == nullptr) return GDN_ERR_INVALID_ARG;
+    if (d->dtype != GDN_BF16 && d->dtype != GDN_FP32) return GDN_ERR_UNSUPPORTED;
+    if (d->B < 0 || d->Hk <= 0 || d->Hv <= 0) return GDN_ERR_INVALID_ARG;
+    if (d->Hv % d->Hk != 0) return GDN_ERR_UNSUPPORTED;
+    if (!head_dim_ok(d->dk) || !head_dim_ok(d->dv)) return GDN_ERR_UNSUPPORTED;
+    if (d->B > 65535 || d->Hv > 65535) return GDN_ERR_TOO_LARGE;
+    if (d->use_qk_l2norm && !(d->l2_eps >= 0.f)) return GDN_ERR_INVALID_ARG;
+    if (d->conv_x != nullptr) {
+        if (d->conv_w == nullptr) return GDN_ERR_INVALID_ARG;
+        if (d->conv_kernel < 2 || d->conv_kernel > 8) return GDN_ERR_UNSUPPORTED;
+        if (d->conv_act != GDN_ACT_NONE && d->conv_act != GDN_ACT_SILU) return GDN_ERR_UNSUPPORTED;
+        if (!aligned16(d->conv_x)) return GDN_ERR_ALIGN;
+    }
+    if (d->g == nullptr || d->beta == nullptr || d->out == nullptr) return GDN_ERR_INVALID_ARG;
+    if (d->conv_x == nullptr && (d->q == nullptr || d->k == nullptr || d->v == nullptr))
+        return GDN_ERR_INVALID_ARG;
+    if (d->conv_x == nullptr && (!aligned16(d->q) || !aligned16(d->k) || !aligned16(d->v)))
+        return GDN_ERR_ALIGN;
+    if (!aligned16(d->out) || !aligned16(d->state_in) || !aligned16(d->state_out))
+        return GDN_ERR_ALIGN;
+    return GDN_OK;
+}
+
+size_t workspace_needed(const gdn_prefill_desc* d) {
+    if (d->conv_x == nullptr || d->T_total <= 0) return 0;
+    const size_t bytes = size_t(d->T_total) * size_t(conv_channels(d)) * elem_size(d->dtype);
+    return (bytes + 255) & ~size_t(255);
+}
+
+int check_prefill(const gdn_prefill_desc* d) {
+    int st = check_common(d);
+    if (st != GDN_OK) return st;
+    if (d->chunk < 1 || d->chunk > gdn::kMaxChunk) return GDN_ERR_CHUNK;
+    if (d->cu_seqlens == nullptr) return GDN_ERR_INVALID_ARG;
+    if (d->conv_x != nullptr) {
+        if (d->T_total < 0) return GDN_ERR_INVALID_ARG;
+        const size_t need = workspace_needed(d);
+        if (need > 0) {
+            if (d->workspace == nullptr || d->workspace_bytes < need) return GDN_ERR_WORKSPACE;
+            if ((reinterpret_cast<uintptr_t>(d->workspace) & 255u) != 0) return GDN_ERR_WORKSPACE;
+        }
+    }
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void gdn_prefill_desc_init(gdn_prefill_desc* d) {
+    if (d == nullptr) return;
+    std::memset(d, 0, sizeof(*d));
+    d->dtype = GDN_BF16;
+    d->chunk = gdn::kMaxChunk;
+    d->T_total = -1;
+    d->conv_kernel = 4;
+    d->conv_act = GDN_ACT_NONE;
+    d->use_qk_l2norm = 1;
+    d->l2_eps = 1e-6f;
+    d->q_scale = 1.f;
+}
+
+size_t gdn_workspace_bytes(const gdn_prefill_desc* d) {
+    // Only the shape fields matter here; tensor pointers may still be unset.
+    if (d == nullptr) return size_t(-1);
+    if (d->dtype != GDN_BF16 && d->dtype != GDN_FP32) return size_t(-1);
+    if (d->B < 0 || d->Hk <= 0 || d->Hv <= 0 || d->Hv % d->Hk != 0) return size_t(-1);
+    if (!head_dim_ok(d->dk) || !head_dim_ok(d->dv)) return size_t(-1);
+    if (d->conv_x != nullptr && d->T_total < 0) return size_t(-1);
+    return workspace_needed(d);
+}
+
+int gdn_prefill_ex(const gdn_prefill_desc* d, gdn_stream_t stream) {
+    const int st = check_prefill(d);
+    if (st != GDN_OK) return st;
+    if (d->B == 0) return GDN_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    gdn::ChunkParams p{};
+    p.g = d->g;
+    p.beta = d->beta;
+    p.state_in = d->state_in;
+    p.state_out = d->state_out;
+    p.out = d->out;
+    p.cu = d->cu_seqlens;
+    p.t_cap = d->T_total >= 0 ? d->T_total : INT64_MAX;
+    p.B = d->B;
+    p.Hk = d->Hk;
+    p.Hv = d->Hv;
+    p.dk = d->dk;
+    p.dv = d->dv;
+    p.chunk = d->chunk;
+    p.l2norm = d->use_qk_l2norm;
+    p.eps = d->l2_eps;
+    p.q_scale = d->q_scale;
+
+    if (d->conv_x != nullptr) {
+        const int64_t C = conv_channels(d);
+        gdn::ConvParams c{};
+        c.x = d->conv_x;
+        c.w = d->conv_w;
+        c.state_in = d->conv_state_in;
+        c.state_out = d->conv_state_out;
+        c.y = d->workspace;
+        c.cu = d->cu_seqlens;
+        c.T = d->T_total;
+        c.B = d->B;
+        c.C = int(C);
+        c.K = d->conv_kernel;
+        c.act = d->conv_act;
+        int rc = cuda_status(gdn::launch_conv(c, d->dtype, s));
+        if (rc != GDN_OK) return rc;
+        const size_t es = elem_size(d->dtype);
+        const char* y = static_cast<const char*>(d->workspace);
+        p.q = y;
+        p.k = y + size_t(d->Hk) * d->dk * es;
+        p.v = y + size_t(2) * d->Hk * d->dk * es;
+        p.q_stride = p.k_stride = p.v_stride = C;
+        rc = cuda_status(gdn::tc_supported(p, d->dtype) ? gdn::launch_chunk_tc(p, s)
+                                                        : gdn::launch_chunk_simt(p, d->dtype, s));
+        if (rc != GDN_OK) return rc;
+        // The chunk kernels read the workspace, not x, so the conv state can be
+        // advanced last; this also keeps an aliased in/out conv state safe.
+        return cuda_status(gdn::launch_conv_state(c, d->dtype, s));
+    }
+    p.q = d->q;
+    p.k = d->k;
+    p.v = d->v;
+    p.q_stride = p.k_stride = int64_t(d->Hk) * d->dk;
+    p.v_stride = int64_t(d->Hv) * d->dv;
+    return cuda_status(gdn::tc_supported(p, d->dtype) ? gdn::launch_chunk_tc(p, s)
+                                                      : gdn::launch_chunk_simt(p, d->dtype, s));
+}
+
+int gdn_prefill(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                const float* state_in, float* state_out, void* out, const int32_t* cu_seqlens,
+                int B, int Hk, int Hv, int dk, int dv, int chunk, gdn_stream_t stream) {
+    gdn_prefill_desc d;
+    gdn_prefill_desc_init(&d);
+    d.q = q;
+    d.k = k;
+    d.v = v;
+    d.g = g;
+    d.beta = beta;
+    d.state_in = state_in;
+    d.state_out = state_out;
+    d.out = out;
+    d.cu_seqlens = cu_seqlens;
+    d.B = B;
+    d.Hk = Hk;
+    d.Hv = Hv;
+    d.dk = dk;
+    d.dv = dv;
+    d.chunk = chunk;
+    return gdn_prefill_ex(&d, stream);
+}
+
+int gdn_step_ex(const gdn_prefill_desc* d, gdn_stream_t stream) {
+    const int st = check_common(d);
+    if (st != GDN_OK) return st;
+    if (d->cu_seqlens != nullptr) return GDN_ERR_INVALID_ARG;
+    if (d->B == 0) return GDN_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    gdn::StepParams p{};
+    p.q = d->q;
+    p.k = d->k;
+    p.v = d->v;
+    p.conv_x = d->conv_x;
+    p.conv_w = d->conv_w;
+    p.conv_state_in = d->conv_state_in;
+    p.conv_state_out = d->conv_state_out;
+    p.conv_K = d->conv_kernel;
+    p.conv_act = d->conv_act;
+    p.g = d->g;
+    p.beta = d->beta;
+    p.state_in = d->state_in;
+    p.state_out = d->state_out;
+    p.out = d->out;
+    p.B = d->B;
+    p.Hk = d->Hk;
+    p.Hv = d->Hv;
+    p.dk = d->dk;
+    p.dv = d->dv;
+    p.l2norm = d->use_qk_l2norm;
+    p.eps = d->l2_eps;
+    p.q_scale = d->q_scale;
+    int rc = cuda_status(gdn::launch_step(p, d->dtype, s));
+    if (rc != GDN_OK) return rc;
+    return cuda_status(gdn::launch_step_conv_state(p, d->dtype, s));
+}
+
+int gdn_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
+             float* state, void* out, int B, int Hk, int Hv, int dk, int dv,
+             gdn_stream_t stream) {
+    gdn_prefill_desc d;
+    gdn_prefill_desc_init(&d);
+    d.q = q;
+    d.k = k;
+    d.v = v;
+    d.g = g;
+    d.beta = beta;
+    d.state_in = state;
+    d.state_out = state;
+    d.out = out;
+    d.B = B;
+    d.Hk = Hk;
+    d.Hv = Hv;
+    d.dk = dk;
+    d.dv = dv;
+    return gdn_step_ex(&d, stream);
+}
+
+int gdn_prefill_plan(const gdn_prefill_desc* d, const char** names, int max_names) {
+    const int st = check_prefill(d);
+    if (st != GDN_OK) return -st;
+    if (d->B == 0) return 0;
+    const char* plan[3];
+    int n = 0;
+    gdn::ChunkParams p{};
+    p.Hk = d->Hk;
+    p.Hv = d->Hv;
+    p.dk = d->dk;
+    p.dv = d->dv;
+    p.chunk = d->chunk;
+    if (d->conv_x != nullptr && d->T_total > 0) plan[n++] = "conv_kernel";
+    plan[n++] = gdn::tc_supported(p, d->dtype) ? gdn::kTcKernelName : "chunk_simt_kernel";
+    if (d->conv_x != nullptr && d->conv_state_out != nullptr) plan[n++] = "conv_state_kernel";
+    for (int i = 0; i < n && i < max_names; ++i)
+        if (names != nullptr) names[i] = plan[i];
+    return n;
+}
+
+const char* gdn_status_string(int status) {
+    switch (status) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or bad layout)";
+        case GDN_ERR_CHUNK: return "chunk must be in 1..64";
+        case GDN_ERR_UNSUPPORTED: return "unsupported shape or option (dk, dv in {16,32,64,128}; Hv % Hk == 0)";
+        case GDN_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+        case GDN_ERR_CUDA: return "CUDA launch failed";
+        case GDN_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+        case GDN_ERR_TOO_LARGE: return "size beyond what this entry point supports";
+        default: return "unknown status";
+    }
+}
+
+int gdn_last_cuda_error(void) { return g_last_cuda_error; }
+
+int gdn_version(void) { return 100; }
+
+}  // extern "C"

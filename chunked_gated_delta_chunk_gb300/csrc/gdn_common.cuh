@@ -1,0 +1,92 @@
+// Internal declarations shared by the CUDA translation units of libgdn.so.
+// Nothing here is part of the public ABI (include/gdn.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr int kMaxChunk = 64;     // static padding of the triangular solve
+constexpr int kNeumann = 8;       // diagonal block size of the Neumann stage
+
+// Everything a chunk kernel needs.  Token strides are in elements so that q,
+// k, v can be read from separate [T, H, d] tensors or from the [T, C]
+// output of the short convolution.
+struct ChunkParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    int64_t q_stride, k_stride, v_stride;  // elements between consecutive tokens
+    const float* g;
+    const float* beta;
+    const float* state_in;
+    float* state_out;
+    void* out;
+    const int32_t* cu;
+    int64_t t_cap;  // tokens in the buffers (rows at or beyond it are never touched)
+    int B, Hk, Hv, dk, dv, chunk;
+    int l2norm;
+    float eps;
+    float q_scale;
+};
+
+struct ConvParams {
+    const void* x;           // [T, C]
+    const float* w;          // [C, K]
+    const float* state_in;   // [B, C, K-1] or nullptr
+    float* state_out;        // [B, C, K-1] or nullptr
+    void* y;                 // [T, C] (workspace), same dtype as x
+    const int32_t* cu;
+    int64_t T;
+    int B, C, K, act;
+};
+
+struct StepParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* conv_x;      // [B, C] or nullptr
+    const float* conv_w;
+    const float* conv_state_in;
+    float* conv_state_out;
+    int conv_K, conv_act;
+    const float* g;
+    const float* beta;
+    const float* state_in;
+    float* state_out;
+    void* out;
+    int B, Hk, Hv, dk, dv;
+    int l2norm;
+    float eps;
+    float q_scale;
+};
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_chunk_simt(const ChunkParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_conv(const ConvParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_conv_state(const ConvParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_step(const StepParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_step_conv_state(const StepParams& p, int dtype, cudaStream_t s);
+
+// ---- small device helpers --------------------------------------------------
+
+__device__ __forceinline__ float load_elem(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float load_elem(const __nv_bfloat16* p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void store_elem(float* p, int64_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void store_elem(__nv_bfloat16* p, int64_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+}  // namespace gdn

@@ -1,0 +1,135 @@
+"""Device-side plumbing around the C ABI: put a ``Problem`` in device memory,
+allocate its outputs and workspace with torch, and call ``gdn_prefill_ex`` /
+``gdn_step_ex`` through the ctypes binding.  Marshalling only: no arithmetic
+of the method happens here.
+"""
+
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import binding as B
+from .inputs import Problem
+
+DTYPE_CODE = {torch.bfloat16: B.GDN_BF16, torch.float32: B.GDN_FP32}
+
+
+class PrefillCall:
+    """Device buffers and the descriptor of one ``gdn_prefill_ex`` call.
+
+    ``run()`` may be called repeatedly (benchmarking) and enqueues exactly one
+    library call on the given stream.  ``state_in=None`` on the problem means
+    a NULL incoming state (zero state)."""
+
+    def __init__(self, p: Problem, device="cuda", chunk: Optional[int] = None,
+                 state_in: Optional[torch.Tensor] = None, conv_state_in: Optional[torch.Tensor] = None,
+                 write_state: bool = True, write_conv_state: bool = True,
+                 alias_state: bool = False, alias_conv_state: bool = False):
+        self.p = p
+        dev = torch.device(device)
+        self.dev = dev
+        T = p.T
+        self.cu = p.cu_seqlens.to(dev, torch.int32)
+        self.g = p.g.to(dev).contiguous()
+        self.beta = p.beta.to(dev).contiguous()
+        s_in = state_in if state_in is not None else p.state_in
+        self.state_in = None if s_in is None else s_in.to(dev, torch.float32).contiguous()
+        self.out = torch.empty(T, p.Hv, p.dv, dtype=p.dtype, device=dev)
+        if alias_state:
+            assert self.state_in is not None
+            self.state_out = self.state_in
+        else:
+            self.state_out = (torch.empty(p.B, p.Hv, p.dk, p.dv, dtype=torch.float32, device=dev)
+                              if write_state else None)
+        self.q = self.k = self.v = None
+        self.x = self.w = self.cs_in = self.cs_out = self.workspace = None
+        fields = dict(dtype=DTYPE_CODE[p.dtype], B=p.B, Hk=p.Hk, Hv=p.Hv, dk=p.dk, dv=p.dv,
+                      chunk=int(chunk or p.chunk), T_total=T, g=self.g, beta=self.beta,
+                      state_in=self.state_in, state_out=self.state_out, out=self.out,
+                      cu_seqlens=self.cu, use_qk_l2norm=int(p.use_l2norm),
+                      q_scale=float(p.q_scale))
+        if p.conv is not None:
+            self.x = p.conv["x"].to(dev).contiguous()
+            self.w = p.conv["w"].to(dev, torch.float32).contiguous()
+            cs = conv_state_in if conv_state_in is not None else p.conv.get("state_in")
+            self.cs_in = None if cs is None else cs.to(dev, torch.float32).contiguous()
+            K = p.conv["w"].shape[1]
+            if alias_conv_state:
+                assert self.cs_in is not None
+                self.cs_out = self.cs_in
+            else:
+                self.cs_out = (torch.empty(p.B, p.channels, K - 1, dtype=torch.float32, device=dev)
+                               if write_conv_state else None)
+            fields.update(conv_x=self.x, conv_w=self.w, conv_state_in=self.cs_in,
+                          conv_state_out=self.cs_out, conv_kernel=K,
+                          conv_act=int(p.conv.get("act", 0)))
+        else:
+            self.q = p.q.to(dev).contiguous()
+            self.k = p.k.to(dev).contiguous()
+            self.v = p.v.to(dev).contiguous()
+            fields.update(q=self.q, k=self.k, v=self.v)
+        self.desc = B.make_desc(**fields)
+        nbytes = B.gdn_workspace_bytes(self.desc)
+        if nbytes:
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            self.desc.workspace = self.workspace.data_ptr()
+            self.desc.workspace_bytes = nbytes
+        self.workspace_bytes = nbytes
+
+    def run(self, stream=None):
+        B.gdn_prefill_ex(self.desc, stream)
+
+    def results(self):
+        r = {"out": self.out}
+        if self.state_out is not None:
+            r["state_out"] = self.state_out
+        if self.cs_out is not None:
+            r["conv_state_out"] = self.cs_out
+        return r
+
+
+def prefill(p: Problem, device="cuda", **kw):
+    """One synchronous prefill of ``p``; returns CPU tensors."""
+    call = PrefillCall(p, device, **kw)
+    call.run()
+    torch.cuda.synchronize(call.dev)
+    return {k: v.cpu() for k, v in call.results().items()}
+
+
+def step(q, k, v, g, beta, state, Hk, Hv, dk, dv, dtype=torch.bfloat16, conv=None,
+         use_l2norm=True, q_scale=1.0, in_place=True, device="cuda"):
+    """One decode step through ``gdn_step_ex``; tensors are moved to
+    ``device``.  Returns (out, state_out[, conv_state_out]) on the device."""
+    dev = torch.device(device)
+    Bn = g.shape[0]
+    g_d, b_d = g.to(dev).contiguous(), beta.to(dev).contiguous()
+    s_in = None if state is None else state.to(dev, torch.float32).contiguous()
+    s_out = s_in if (in_place and s_in is not None) else torch.empty(
+        Bn, Hv, dk, dv, dtype=torch.float32, device=dev)
+    out = torch.empty(Bn, Hv, dv, dtype=dtype, device=dev)
+    fields = dict(dtype=DTYPE_CODE[dtype], B=Bn, Hk=Hk, Hv=Hv, dk=dk, dv=dv, g=g_d, beta=b_d,
+                  state_in=s_in, state_out=s_out, out=out, use_qk_l2norm=int(use_l2norm),
+                  q_scale=float(q_scale))
+    keep = [g_d, b_d]
+    cs_out = None
+    if conv is not None:
+        x = conv["x"].to(dev).contiguous()
+        w = conv["w"].to(dev, torch.float32).contiguous()
+        cs_in = None if conv.get("state_in") is None else conv["state_in"].to(dev, torch.float32).contiguous()
+        K = w.shape[1]
+        cs_out = cs_in if (in_place and cs_in is not None) else torch.empty(
+            Bn, 2 * Hk * dk + Hv * dv, K - 1, dtype=torch.float32, device=dev)
+        fields.update(conv_x=x, conv_w=w, conv_state_in=cs_in, conv_state_out=cs_out,
+                      conv_kernel=K, conv_act=int(conv.get("act", 0)))
+        keep += [x, w, cs_in]
+    else:
+        qd, kd, vd = (t.to(dev).contiguous() for t in (q, k, v))
+        fields.update(q=qd, k=kd, v=vd)
+        keep += [qd, kd, vd]
+    desc = B.make_desc(**fields)
+    B.gdn_step_ex(desc)
+    torch.cuda.synchronize(dev)
+    del keep
+    return (out, s_out) if conv is None else (out, s_out, cs_out)

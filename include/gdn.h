@@ -1,0 +1,182 @@
+/*
+ * gdn.h — C ABI of libgdn.so: chunked Gated DeltaNet prefill and the
+ * one-token decode step on NVIDIA GB300 (sm_103a).
+ *
+ * The operation (per sequence and value head, fp32 state S of shape [dk, dv]):
+ *
+ *   S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ *   o_t = q_scale * S_t^T q_t
+ *
+ * A prompt is cut into chunks of at most 64 rows and every chunk is solved in
+ * closed form: gamma = cumsum(g) within the chunk,
+ *   (I + A) U = diag(beta) V - diag(beta exp(gamma)) K S_0,
+ *       A_ij = beta_i exp(gamma_i - gamma_j) k_i.k_j  (j < i),
+ *   O   = diag(exp(gamma)) Q S_0 + (exp(gamma_t - gamma_i) q_t.k_i)_{i<=t} U,
+ *   S_S = exp(gamma_S) S_0 + (K * exp(min(gamma_S - gamma, 0)))^T U,
+ * with gamma_S the chunk's last cumulative sum.  Source: "perf(qwen3_5):
+ * prefill text prompts in multi-token chunks" (TensorRT-Model-Connect pull
+ * request 2191), Implementation section and its gamma_S commit message.  The
+ * state is carried from chunk to chunk on the device, as that page's runtime
+ * advances the recurrent state after each chunk (run_prefill_chunks /
+ * commit_prefill), and the prefill reads and writes the same recurrent-state
+ * layout as the decode step.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *   allocates no memory, never synchronises the device or the stream, and
+ *   enqueues all work on `stream` (NULL = the legacy default stream).
+ * - Layouts are row-major and token-major over a packed variable-length
+ *   batch: q, k [T, Hk, dk]; v [T, Hv, dv]; g, beta [T, Hv]; out [T, Hv, dv];
+ *   state [B, Hv, dk, dv].  Value head h reads key head h / (Hv / Hk).
+ * - "bf16" tensors hold __nv_bfloat16 values, "fp32" tensors float.
+ * - g must be <= 0 (a decay); this is a precondition, not checked.
+ * - Validation happens before anything is enqueued: a call that returns a
+ *   non-zero status enqueued nothing.  A GDN_ERR_CUDA status after a launch
+ *   leaves out, state_out and conv_state_out unspecified (there is no
+ *   rollback, as on the page's runtime: the caller re-runs from its own copy
+ *   of the state).  Nothing throws across the ABI.
+ * - Concurrent calls on different streams are safe when they share no output
+ *   buffer.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st* gdn_stream_t;
+
+/* Status codes returned by every entry point. */
+enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, bad cu_seqlens length, ... */
+    GDN_ERR_CHUNK = 2,       /* chunk outside 1..64 (the static 64-row padding of the solve) */
+    GDN_ERR_UNSUPPORTED = 3, /* dk or dv not in {16, 32, 64, 128}, Hv % Hk != 0, bad dtype/act */
+    GDN_ERR_ALIGN = 4,       /* a tensor pointer not 16-byte aligned */
+    GDN_ERR_CUDA = 5,        /* a kernel launch failed (see gdn_last_cuda_error) */
+    GDN_ERR_WORKSPACE = 6,   /* workspace missing, too small or not 256-byte aligned */
+    GDN_ERR_TOO_LARGE = 7    /* a size beyond what the entry point supports */
+};
+
+/* Element type of q, k, v, conv_x and out. */
+enum gdn_dtype { GDN_BF16 = 0, GDN_FP32 = 1 };
+
+/* Activation after the short convolution. */
+enum gdn_act { GDN_ACT_NONE = 0, GDN_ACT_SILU = 1 };
+
+/*
+ * Full description of one prefill call (gdn_prefill_ex) or decode step
+ * (gdn_step_ex).  Zero-initialise, then fill; gdn_prefill_desc_init sets the
+ * defaults (bf16, chunk 64, L2 norm on with eps 1e-6, q_scale 1, conv kernel 4,
+ * no activation).
+ */
+typedef struct gdn_prefill_desc {
+    int dtype;               /* enum gdn_dtype */
+    int B;                   /* number of sequences (>= 0) */
+    int Hk, Hv;              /* key and value heads, Hv % Hk == 0 */
+    int dk, dv;              /* head dims, each in {16, 32, 64, 128} */
+    int chunk;               /* rows per chunk, 1..64 (results do not depend on it) */
+    int64_t T_total;         /* cu_seqlens[B]; required with conv_x, else may be -1 */
+
+    const void* q;           /* [T, Hk, dk] dtype; ignored when conv_x != NULL */
+    const void* k;           /* [T, Hk, dk] dtype; ignored when conv_x != NULL */
+    const void* v;           /* [T, Hv, dv] dtype; ignored when conv_x != NULL */
+    const float* g;          /* [T, Hv] log-decay per token, <= 0 */
+    const float* beta;       /* [T, Hv] delta-rule step size */
+    const float* state_in;   /* [B, Hv, dk, dv]; NULL = zero state */
+    float* state_out;        /* [B, Hv, dk, dv]; NULL = not written; may alias state_in */
+    void* out;               /* [T, Hv, dv] dtype */
+    const int32_t* cu_seqlens; /* device [B+1]: cu[0] = 0, non-decreasing */
+
+    /* Optional depthwise causal short convolution in front ("perf(mamba):
+     * prefill text prompts in multi-token chunks", Implementation,
+     * add_short_conv_rows): channels c in [0, C), C = 2*Hk*dk + Hv*dv, ordered
+     * q | k | v; y_t = act(sum_j w[c, j] * xx[t + j]) over
+     * xx = [conv_state_in[n, c, :], x[seq n, c]]; the new conv state is the
+     * last K-1 columns of xx. */
+    const void* conv_x;      /* [T, C] dtype, or NULL for no convolution */
+    const float* conv_w;     /* [C, K] */
+    const float* conv_state_in; /* [B, C, K-1] oldest first; NULL = zeros */
+    float* conv_state_out;   /* [B, C, K-1]; NULL = not written; may alias conv_state_in */
+    int conv_kernel;         /* K, 2..8 */
+    int conv_act;            /* enum gdn_act */
+
+    int use_qk_l2norm;       /* q, k <- x / sqrt(sum x^2 + l2_eps) per head vector */
+    float l2_eps;
+    float q_scale;           /* o_t = q_scale * S_t^T q_t */
+
+    void* workspace;         /* device scratch, >= gdn_workspace_bytes(desc), 256-aligned */
+    size_t workspace_bytes;
+} gdn_prefill_desc;
+
+/* Fill *d with the defaults listed above (all pointers NULL). */
+void gdn_prefill_desc_init(gdn_prefill_desc* d);
+
+/*
+ * gdn_prefill — chunked prefill, bf16 q/k/v/out, fp32 g/beta/state, q/k L2
+ * normalisation on (eps 1e-6), q_scale 1, no convolution.  Grids are sized
+ * from (B, Hv); cu_seqlens is read on the device, so the total length is not
+ * needed.  Needs no workspace.
+ *   q, k      bf16 [T, Hk, dk]      v, out   bf16 [T, Hv, dv]
+ *   g, beta   fp32 [T, Hv]          state_in / state_out  fp32 [B, Hv, dk, dv]
+ *   cu_seqlens int32 [B+1] (device)  chunk in 1..64
+ * Returns a gdn_status.
+ */
+int gdn_prefill(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                const float* state_in, float* state_out, void* out, const int32_t* cu_seqlens,
+                int B, int Hk, int Hv, int dk, int dv, int chunk, gdn_stream_t stream);
+
+/* gdn_prefill_ex — the general prefill: dtype, short convolution, L2 norm,
+ * q_scale and workspace as described in gdn_prefill_desc. */
+int gdn_prefill_ex(const gdn_prefill_desc* d, gdn_stream_t stream);
+
+/* Device workspace gdn_prefill_ex needs for *d, in bytes (0 if none; it is
+ * non-zero only with a short convolution).  Reads only dtype, B, Hk, Hv, dk,
+ * dv, T_total and whether conv_x is set; returns (size_t)-1 when those are
+ * invalid. */
+size_t gdn_workspace_bytes(const gdn_prefill_desc* d);
+
+/*
+ * gdn_step — one decode token per sequence (the unchanged one-token step of
+ * the page's runtime), bf16, L2 norm on, q_scale 1, no convolution:
+ *   q, k bf16 [B, Hk, dk]; v bf16 [B, Hv, dv]; g, beta fp32 [B, Hv];
+ *   state fp32 [B, Hv, dk, dv], updated in place; out bf16 [B, Hv, dv].
+ */
+int gdn_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
+             float* state, void* out, int B, int Hk, int Hv, int dk, int dv,
+             gdn_stream_t stream);
+
+/* gdn_step_ex — decode step from a description: one token per sequence, so
+ * q, k, v, conv_x, g, beta and out have B rows; cu_seqlens must be NULL and
+ * T_total is ignored; chunk is ignored.  state_in / state_out may alias
+ * (in-place update); conv_state_in / conv_state_out likewise.  No workspace. */
+int gdn_step_ex(const gdn_prefill_desc* d, gdn_stream_t stream);
+
+/* The kernels gdn_prefill_ex launches for *d, in launch order: writes up to
+ * max_names pointers to static, NUL-terminated kernel names into names (which
+ * may be NULL when max_names is 0) and returns how many kernels one call
+ * launches, or minus a gdn_status when *d would be rejected.  Host-only: no
+ * CUDA call, nothing enqueued. */
+int gdn_prefill_plan(const gdn_prefill_desc* d, const char** names, int max_names);
+
+/* Static description of a status code. */
+const char* gdn_status_string(int status);
+
+/* The cudaError_t of the last failed launch on this thread (0 if none). */
+int gdn_last_cuda_error(void);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,146 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+* libgdn.so loads and exports every function include/gdn.h declares;
+* the ctypes mirror of ``gdn_prefill_desc`` has the C layout (checked against
+  a small C program compiled with gcc from the header);
+* argument validation returns the documented status before anything is
+  enqueued (every call here is rejected, or has B = 0, so no CUDA call runs).
+"""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from chunked_gated_delta_chunk_gb300 import binding as B
+from chunked_gated_delta_chunk_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+A = 0x100000          # a 16- and 256-byte aligned fake device address (never dereferenced)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for name in names:
+        assert hasattr(lib, name), name
+    assert sorted(B.EXPORTED) == names
+
+
+def test_desc_layout_matches_c(tmp_path, lib):
+    fields = [f for f, _ in B.gdn_prefill_desc._fields_]
+    src = tmp_path / "layout.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "gdn.h"', 'int main(void){',
+             'printf("%zu\\n", sizeof(gdn_prefill_desc));']
+    lines += [f'printf("%zu\\n", offsetof(gdn_prefill_desc, {f}));' for f in fields]
+    lines += ["return 0;}"]
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                            check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(B.gdn_prefill_desc)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(B.gdn_prefill_desc, f).offset == off, f
+
+
+def _prefill(lib, **kw):
+    args = dict(q=A, k=A, v=A, g=A, beta=A, state_in=A, state_out=A, out=A, cu=A,
+                B=1, Hk=2, Hv=4, dk=128, dv=128, chunk=64)
+    args.update(kw)
+    return lib.gdn_prefill(args["q"], args["k"], args["v"], args["g"], args["beta"],
+                           args["state_in"], args["state_out"], args["out"], args["cu"],
+                           args["B"], args["Hk"], args["Hv"], args["dk"], args["dv"],
+                           args["chunk"], None)
+
+
+@pytest.mark.parametrize("chunk", [0, -1, 65, 128])
+def test_chunk_outside_1_to_64_is_rejected(lib, chunk):
+    assert _prefill(lib, chunk=chunk) == B.GDN_ERR_CHUNK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=48), B.GDN_ERR_UNSUPPORTED), (dict(dv=256), B.GDN_ERR_UNSUPPORTED),
+    (dict(dk=8), B.GDN_ERR_UNSUPPORTED), (dict(Hk=3, Hv=4), B.GDN_ERR_UNSUPPORTED),
+    (dict(Hk=0), B.GDN_ERR_INVALID_ARG), (dict(B=-1), B.GDN_ERR_INVALID_ARG),
+    (dict(q=None), B.GDN_ERR_INVALID_ARG), (dict(g=None), B.GDN_ERR_INVALID_ARG),
+    (dict(beta=None), B.GDN_ERR_INVALID_ARG), (dict(out=None), B.GDN_ERR_INVALID_ARG),
+    (dict(cu=None), B.GDN_ERR_INVALID_ARG),
+    (dict(q=A + 2), B.GDN_ERR_ALIGN), (dict(v=A + 8), B.GDN_ERR_ALIGN),
+    (dict(out=A + 4), B.GDN_ERR_ALIGN), (dict(state_in=A + 4), B.GDN_ERR_ALIGN),
+    (dict(B=70000), B.GDN_ERR_TOO_LARGE),
+])
+def test_invalid_prefill_arguments(lib, kw, status):
+    assert _prefill(lib, **kw) == status
+
+
+def test_empty_batch_is_ok_without_launch(lib):
+    assert _prefill(lib, B=0) == B.GDN_OK
+
+
+def _desc(**kw):
+    base = dict(B=1, Hk=16, Hv=32, dk=128, dv=128, T_total=100, g=A, beta=A, out=A,
+                cu_seqlens=A, conv_x=A, conv_w=A, conv_kernel=4)
+    base.update(kw)
+    return B.make_desc(**base)
+
+
+def test_workspace_size_and_rejection(lib):
+    d = _desc()
+    need = B.gdn_workspace_bytes(d)
+    assert need == ((100 * (2 * 16 * 128 + 32 * 128) * 2 + 255) // 256) * 256
+    assert lib.gdn_prefill_ex(ctypes.byref(d), None) == B.GDN_ERR_WORKSPACE
+    d.workspace, d.workspace_bytes = A, need - 1
+    assert lib.gdn_prefill_ex(ctypes.byref(d), None) == B.GDN_ERR_WORKSPACE
+    d.workspace, d.workspace_bytes = A + 16, need
+    assert lib.gdn_prefill_ex(ctypes.byref(d), None) == B.GDN_ERR_WORKSPACE
+    d32 = _desc(dtype=B.GDN_FP32)
+    assert B.gdn_workspace_bytes(d32) == ((100 * 8192 * 4 + 255) // 256) * 256
+    assert B.gdn_workspace_bytes(_desc(conv_x=None)) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T_total=-1), B.GDN_ERR_INVALID_ARG), (dict(conv_w=None), B.GDN_ERR_INVALID_ARG),
+    (dict(conv_kernel=1), B.GDN_ERR_UNSUPPORTED), (dict(conv_kernel=9), B.GDN_ERR_UNSUPPORTED),
+    (dict(conv_act=2), B.GDN_ERR_UNSUPPORTED), (dict(conv_x=A + 2), B.GDN_ERR_ALIGN),
+    (dict(dtype=5), B.GDN_ERR_UNSUPPORTED),
+])
+def test_invalid_conv_descriptions(lib, kw, status):
+    d = _desc(**kw)
+    d.workspace, d.workspace_bytes = A, 1 << 40
+    assert lib.gdn_prefill_ex(ctypes.byref(d), None) == status
+
+
+def test_step_rejects_cu_seqlens_and_bad_shapes(lib):
+    d = B.make_desc(B=2, Hk=1, Hv=1, dk=16, dv=16, q=A, k=A, v=A, g=A, beta=A, out=A,
+                    state_in=A, state_out=A, cu_seqlens=A)
+    assert lib.gdn_step_ex(ctypes.byref(d), None) == B.GDN_ERR_INVALID_ARG
+    assert lib.gdn_step(A, A, A, A, A, A, A, 1, 1, 1, 24, 16, None) == B.GDN_ERR_UNSUPPORTED
+    assert lib.gdn_step(A, A, A, A, A, A, A + 4, 1, 1, 1, 16, 16, None) == B.GDN_ERR_ALIGN
+    assert lib.gdn_step(A, A, A, A, A, A, A, 0, 1, 1, 16, 16, None) == B.GDN_OK
+
+
+def test_status_strings_and_defaults(lib):
+    for code in range(8):
+        assert B.gdn_status_string(code)
+    assert "chunk" in B.gdn_status_string(B.GDN_ERR_CHUNK)
+    d = B.make_desc()
+    assert (d.dtype, d.chunk, d.T_total, d.conv_kernel, d.use_qk_l2norm) == (B.GDN_BF16, 64, -1, 4, 1)
+    assert abs(d.l2_eps - 1e-6) < 1e-12 and d.q_scale == 1.0
+    assert B.gdn_version() >= 100
