@@ -7,17 +7,12 @@ namespace gdn {
 
 constexpr const char* kTcKernelName = "chunk_tc_kernel";
 
-// True when the tensor-core kernel handles this call (bf16, dk = dv = 128).
+// True when the tensor-core kernel handles this call: bf16 with dk = dv = 128.
 inline bool tc_supported(const ChunkParams& p, int dtype) {
-    (void)p;
-    (void)dtype;
-    return false;
+    return dtype == GDN_BF16 && p.dk == 128 && p.dv == 128;
 }
 
-inline cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
-    (void)p;
-    (void)s;
-    return cudaErrorNotSupported;
-}
+// Encodes the TMA maps and launches one CTA per (value head, sequence).
+cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s);
 
 }  // namespace gdn

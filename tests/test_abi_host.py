@@ -144,3 +144,24 @@ def test_status_strings_and_defaults(lib):
     assert (d.dtype, d.chunk, d.T_total, d.conv_kernel, d.use_qk_l2norm) == (B.GDN_BF16, 64, -1, 4, 1)
     assert abs(d.l2_eps - 1e-6) < 1e-12 and d.q_scale == 1.0
     assert B.gdn_version() >= 100
+
+
+def test_launch_plan_names(lib):
+    """Host-only launch plan: the tensor-core kernel for bf16 with
+    dk = dv = 128, the SIMT kernel otherwise; conv adds its two kernels."""
+    d = B.make_desc(B=1, Hk=2, Hv=4, dk=128, dv=128, q=A, k=A, v=A, g=A, beta=A, out=A,
+                    cu_seqlens=A)
+    assert B.gdn_prefill_plan(d) == ["chunk_tc_kernel"]
+    d32 = B.make_desc(B=1, Hk=2, Hv=4, dk=128, dv=128, q=A, k=A, v=A, g=A, beta=A, out=A,
+                      cu_seqlens=A, dtype=B.GDN_FP32)
+    assert B.gdn_prefill_plan(d32) == ["chunk_simt_kernel"]
+    d64 = B.make_desc(B=1, Hk=2, Hv=4, dk=64, dv=128, q=A, k=A, v=A, g=A, beta=A, out=A,
+                      cu_seqlens=A)
+    assert B.gdn_prefill_plan(d64) == ["chunk_simt_kernel"]
+    dc = _desc(conv_state_out=A)
+    dc.workspace, dc.workspace_bytes = A, 1 << 40
+    assert B.gdn_prefill_plan(dc) == ["conv_kernel", "chunk_tc_kernel", "conv_state_kernel"]
+    bad = B.make_desc(B=1, Hk=2, Hv=4, dk=48, dv=128, q=A, k=A, v=A, g=A, beta=A, out=A,
+                      cu_seqlens=A)
+    with pytest.raises(B.GdnError):
+        B.gdn_prefill_plan(bad)
