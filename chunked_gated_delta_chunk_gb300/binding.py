@@ -36,7 +36,8 @@ GDN_ACT_SILU = 1
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_prefill_desc_init", "gdn_prefill", "gdn_prefill_ex", "gdn_workspace_bytes",
             "gdn_step", "gdn_step_ex", "gdn_prefill_plan", "gdn_status_string",
-            "gdn_last_cuda_error", "gdn_version")
+            "gdn_last_cuda_error", "gdn_version", "gdn_prefill_noalloc",
+            "gdn_noalloc_scratch_bytes")
 
 
 class GdnError(RuntimeError):
@@ -92,6 +93,10 @@ def lib():
             L.gdn_prefill_plan.restype = i
             L.gdn_prefill_plan.argtypes = [ctypes.POINTER(gdn_prefill_desc),
                                            ctypes.POINTER(ctypes.c_char_p), i]
+            L.gdn_prefill_noalloc.restype = i
+            L.gdn_prefill_noalloc.argtypes = [ctypes.POINTER(gdn_prefill_desc), st]
+            L.gdn_noalloc_scratch_bytes.restype = ctypes.c_size_t
+            L.gdn_noalloc_scratch_bytes.argtypes = []
             L.gdn_status_string.restype = ctypes.c_char_p
             L.gdn_status_string.argtypes = [i]
             L.gdn_last_cuda_error.restype = i
@@ -171,6 +176,16 @@ def gdn_prefill_plan(desc: gdn_prefill_desc):
     if n < 0:
         raise GdnError(-n, "gdn_prefill_plan")
     return [names[i].decode() for i in range(n)]
+
+
+def gdn_prefill_noalloc(desc: gdn_prefill_desc, stream=None):
+    """gdn_prefill_ex without a caller workspace: for callers that cannot
+    allocate device memory; uses the library's fixed scratch array."""
+    _check(lib().gdn_prefill_noalloc(ctypes.byref(desc), _stream(stream)), "gdn_prefill_noalloc")
+
+
+def gdn_noalloc_scratch_bytes() -> int:
+    return int(lib().gdn_noalloc_scratch_bytes())
 
 
 def gdn_status_string(status: int) -> str:

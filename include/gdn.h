@@ -166,6 +166,33 @@ int gdn_step_ex(const gdn_prefill_desc* d, gdn_stream_t stream);
  * CUDA call, nothing enqueued. */
 int gdn_prefill_plan(const gdn_prefill_desc* d, const char** names, int max_names);
 
+/*
+ * gdn_prefill_noalloc — gdn_prefill_ex for callers that cannot allocate
+ * device memory (the pages have no counterpart: it is an addition for
+ * users of this library).  Some callers cannot provide the scratch workspace
+ * that a prefill with the short convolution needs: a serving runtime whose
+ * device memory is all handed to its own pool and that may not call
+ * cudaMalloc on the request path, or code that must not allocate because an
+ * allocation can synchronise the device.  This entry point takes the same
+ * description as gdn_prefill_ex (inputs and outputs still come from the
+ * caller) but ignores d->workspace and uses a fixed scratch array inside the
+ * library, gdn_noalloc_scratch_bytes() = 32 MiB, which every GPU that loads
+ * the library keeps reserved until the process exits.  It allocates nothing.
+ *   - A description whose workspace would exceed that size is rejected with
+ *     GDN_ERR_TOO_LARGE (for the conv workspace: T_total * C * element size).
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.  GDN_ERR_CUDA if the lookup fails.
+ *   - Every call shares the one array: calls whose work overlaps on the GPU
+ *     (other streams, other host threads) race on it; serialise them.
+ *   - Without a convolution no scratch is needed and the call is exactly
+ *     gdn_prefill_ex.
+ */
+int gdn_prefill_noalloc(const gdn_prefill_desc* d, gdn_stream_t stream);
+
+/* Size in bytes of the fixed scratch array gdn_prefill_noalloc uses. */
+size_t gdn_noalloc_scratch_bytes(void);
+
 /* Static description of a status code. */
 const char* gdn_status_string(int status);
 
