@@ -1,6 +1,7 @@
 // Tensor-core chunk kernel (bf16, dk = dv = 128) for sm_103a: tcgen05 MMAs
-// with TMEM accumulators, operands in 128-byte-swizzled shared memory fed by
-// TMA, the fp32 state carried in TMEM through the chunks of a sequence.
+// with TMEM accumulators and TMEM-resident A operands, B operands in
+// 128-byte-swizzled shared memory fed by TMA, the fp32 state carried in TMEM
+// through all chunks of a sequence.
 //
 // Method: the chunked delta rule of "perf(qwen3_5): prefill text prompts in
 // multi-token chunks" (Implementation section).  Per chunk of n <= 64 rows
@@ -16,22 +17,26 @@
 // GB300 mapping.  The state is kept transposed, Z = S^T [dv, dk], as an fp32
 // TMEM accumulator (lane = value column j, column = key row d), so that every
 // contraction is an M = 128 tcgen05.mma:
-//   Gram     D_G  = [K; Q] K^T              (M=128, N=64, K=128)  raw q, k
-//   U0^T     D_X  = V^T (T diag beta)^T     (M=128, N=64, K=64)
-//   W^T      D_W  = K^T (T diag(beta Gamma r_k))^T
-//   chain    D_X += Z_bf16 (-W^T)           -> v_new^T = U^T
-//   output   D_O  = Z_bf16 Qs^T             Qs = diag(Gamma r_q) Q
-//   state    Z   <- exp(gamma_S) Z + v_new^T Ks,  Ks = diag(exp(min(gamma_S-gamma,0)) r_k) K
-//   output   D_O += v_new^T P^T             P_ti = exp(gamma_t-gamma_i) r_q,t r_k,i q_t.k_i (i<=t)
-// L2 normalisation of q and k is folded into these row scalings (r = 1/|x|),
-// so the Gram matrices use the raw bf16 inputs.  Every exponent is clamped at
-// zero and evaluated only where its triangular mask keeps the entry.
+//   Gram   D_G  = [K; Q] K^T                         raw bf16 q, k (smem, K-major)
+//   U0^T   D_X  = V^T (T diag beta)^T                T split into bf16 hi + lo
+//   W^T    D_W  = K^T (T diag(beta Gamma r_k))^T     T split into bf16 hi + lo
+//   chain  D_X += Zb (-W^T)          -> U^T          Zb = bf16(Z) in TMEM
+//          D_O  = Zb Qs^T                            Qs = diag(Gamma r_q) Q
+//          Z   += Us^T K   (Z pre-scaled by exp(gamma_S))
+//                                                    Us = U diag(exp(min(gamma_S-gamma,0)) r_k),
+//                                                    bf16 hi + lo, in TMEM
+//          D_O += U^T P^T                            U, P each split into bf16 hi + lo
+// L2 normalisation of q and k is folded into row scalings (r = 1/|x|); every
+// exponent is clamped at zero and only evaluated where its mask keeps it.
+// The hi/lo splits keep every intermediate to ~16 bits before it meets a bf16
+// operand, so in O mainly the bf16 output rounding remains visible.
 //
-// One CTA per (value head, sequence); 8 warps; warp w reads TMEM lanes
-// 32 (w % 4) .. +31 and column half w / 4.  Chunk c + 1 is fetched by TMA
-// while chunk c is processed (two raw stages).  Every mbarrier wait is
-// bounded; on a timeout the CTA records it in a device flag, stops, and
-// still frees its TMEM.
+// Warp specialisation (384 threads): warps 0-3 and 8-11 prepare chunk c + 1
+// (norms, cumsum, masks, inverse, U0 and W) while warps 4-7 run the
+// S-dependent chain of chunk c.  mbarriers hand over each stage; TMA brings
+// the raw tiles of chunk c + 2 while chunk c finishes.  Every wait is
+// bounded; a CTA that runs out records it in a device counter, lets its TMA
+// copies land and still frees its TMEM.
 #include <cuda.h>
 
 #include "gdn_common.cuh"
@@ -46,48 +51,67 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kC = 64;          // chunk rows (padded)
-constexpr int kD = 128;         // dk = dv
-constexpr int kThreads = 256;
-constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kC = 64;                 // chunk rows (padded)
+constexpr int kD = 128;                // dk = dv
+constexpr int kThreads = 384;
+constexpr uint32_t kPrepThreads = 256; // warps 0-3 and 8-11
+constexpr uint32_t kChainThreads = 128;
+constexpr uint32_t kBarPrep = 1, kBarChain = 2;
+constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr int kLdA = kC + 1;
+constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared-memory map (bytes from the 1024-aligned base).
 constexpr uint32_t kStageKQ = 32768;   // [K b0 | Q b0 | K b1 | Q b1], 8 KB each
 constexpr uint32_t kStageV = 16384;    // [V b0 | V b1]
 constexpr uint32_t kStageBytes = kStageKQ + kStageV;
-constexpr uint32_t kOffStage0 = 0;
-constexpr uint32_t kOffP = 2 * kStageBytes;          // P (bf16 [t][i], K-major)      8 KB
-constexpr uint32_t kOffTb = kOffP + 8192;            // T diag(beta)                   8 KB
-constexpr uint32_t kOffTbg = kOffTb + 8192;          // T diag(beta Gamma r_k)         8 KB
-constexpr uint32_t kOffWt = kOffTbg + 8192;          // -W^T (bf16 [d][t], MN-major)  16 KB
-constexpr uint32_t kOffZ = kOffWt + 16384;           // Z bf16 [j][d] K-major         32 KB
-constexpr uint32_t kOffVn = kOffZ + 32768;           // v_new^T bf16 [j][i] K-major   16 KB
-constexpr uint32_t kOffA = kOffVn + 16384;           // A fp32 [64][65]
-constexpr uint32_t kOffT = kOffA + kC * kLdA * 4;    // T fp32 [64][65]
-constexpr uint32_t kOffTmp = kOffT + kC * kLdA * 4;  // inverse scratch, 1536 floats
-constexpr uint32_t kOffVec = kOffTmp + 1536 * 4;     // 8 vectors of 64 floats
-constexpr uint32_t kOffBar = kOffVec + 8 * kC * 4;   // 3 mbarriers + TMEM slot + flags
-constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024; // + alignment slack
+constexpr uint32_t kOffWt = 2 * kStageBytes;             // -W^T bf16 [d][t] MN-major, 16 KB
+constexpr uint32_t kOffP = kOffWt + 16384;               // P [buf][hi|lo] bf16 [t][i], 4 x 8 KB
+constexpr uint32_t kOffTb = kOffP + 4 * 8192;            // Tb hi, Tb lo, Tbg hi, Tbg lo, 4 x 8 KB
+constexpr uint32_t kOffA = kOffTb + 4 * 8192;            // A fp32 [64][65]
+constexpr uint32_t kOffT = kOffA + kC * kLdA * 4;        // T fp32 [64][65]
+constexpr uint32_t kOffTmp = kOffT + kC * kLdA * 4;      // inverse scratch, 1536 floats
+constexpr uint32_t kOffVec = kOffTmp + 1536 * 4;         // vectors
+constexpr uint32_t kVecFloats = 6 * kC + 2 * kC + 2;     // prep vectors + chain vectors
+constexpr uint32_t kOffBar = kOffVec + ((kVecFloats * 4 + 127) / 128) * 128;
+constexpr uint32_t kNumBars = 16;
+constexpr uint32_t kSmemBytes = kOffBar + kNumBars * 8 + 32 + 1024;
+
+// Barrier slots.
+enum : int {
+    B_RAW0 = 0, B_RAW1 = 1,        // TMA tiles of a stage landed
+    B_GRAM = 2, B_W = 3,           // prep MMAs done
+    B_READY0 = 4, B_READY1 = 5,    // prep of a chunk published
+    B_X = 6, B_Z = 7, B_O = 8,     // chain MMAs done
+    B_XREAD = 9,                   // chain has read U^T out of D_X
+    B_WTFREE = 10,                 // chain MMA no longer reads -W^T
+    B_PFREE0 = 11, B_PFREE1 = 12,  // chain MMA no longer reads P of a buffer
+    B_SFREE0 = 13, B_SFREE1 = 14   // chain no longer reads a raw stage
+};
 
 // TMEM columns.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColZ = 0;
-constexpr uint32_t kColX = 128;
-constexpr uint32_t kColG = 192;
-constexpr uint32_t kColW = 256;
-constexpr uint32_t kColO = 320;
+constexpr uint32_t kColZ = 0;      // fp32 Z [128 lanes x 128]
+constexpr uint32_t kColZb = 128;   // bf16 pairs of Z, A operand (64 columns)
+constexpr uint32_t kColX = 192;    // U0^T, then U^T (64)
+constexpr uint32_t kColO = 256;    // O^T (64)
+constexpr uint32_t kColGW = 320;   // Gram, then W^T (64)
+constexpr uint32_t kColU = 384;    // U hi, U lo, Us hi, Us lo (4 x 32)
 
-// Offset of (row, col) in a swizzled K-major tile of 64-column blocks.
+// Offset of (row, col) in a swizzled tile of 64-column blocks (128-byte rows).
 __device__ __forceinline__ uint32_t toff(int row, int col, uint32_t block_stride) {
     const int blk = col >> 6, c = col & 63;
     return uint32_t(blk) * block_stride + uint32_t(row) * 128u +
            (uint32_t(((c >> 3) ^ (row & 7))) << 4) + uint32_t(c & 7) * 2u;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_round(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
 }
 
 __device__ __forceinline__ void store_chunk8(uint8_t* p, const float* v) {
@@ -97,6 +121,18 @@ __device__ __forceinline__ void store_chunk8(uint8_t* p, const float* v) {
     u.z = pack_bf16x2(v[4], v[5]);
     u.w = pack_bf16x2(v[6], v[7]);
     *reinterpret_cast<uint4*>(p) = u;
+}
+
+// hi = bf16(v), lo = bf16(v - hi), 8 values each.
+__device__ __forceinline__ void store_split8(uint8_t* phi, uint8_t* plo, const float* v) {
+    float hi[8], lo[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        hi[q] = bf16_round(v[q]);
+        lo[q] = v[q] - hi[q];
+    }
+    store_chunk8(phi, hi);
+    store_chunk8(plo, lo);
 }
 
 __device__ __forceinline__ void load_chunk8(const uint8_t* p, float* v) {
@@ -110,29 +146,119 @@ __device__ __forceinline__ void load_chunk8(const uint8_t* p, float* v) {
     }
 }
 
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[16], s[16];
+    __syncwarp();
+    GDN_TMEM_LD_X16(taddr, r);
+    GDN_TMEM_LD_X16(taddr + 16, s);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        v[i] = __uint_as_float(r[i]);
+        v[16 + i] = __uint_as_float(s[i]);
+    }
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+    uint32_t r0[16], r1[16], r2[16], r3[16];
+    __syncwarp();
+    GDN_TMEM_LD_X16(taddr, r0);
+    GDN_TMEM_LD_X16(taddr + 16, r1);
+    GDN_TMEM_LD_X16(taddr + 32, r2);
+    GDN_TMEM_LD_X16(taddr + 48, r3);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        v[i] = __uint_as_float(r0[i]);
+        v[16 + i] = __uint_as_float(r1[i]);
+        v[32 + i] = __uint_as_float(r2[i]);
+        v[48 + i] = __uint_as_float(r3[i]);
+    }
+}
+
+// One level of the 2x2 block inversion for diagonal blocks of size S:
+// for every pair of inverted blocks T11, T22 with the off-diagonal block A21
+// of I + A, the lower-left block of the inverse is -T22 A21 T11.  Each of the
+// 256 prep threads owns an RB x CB output block; the inner products run over
+// the full S (the upper triangles of T11 and T22 are zero), fully unrolled so
+// that the shared-memory loads overlap.
+template <int S, int RB, int CB>
+__device__ __forceinline__ void level_products(const float* sA, float* sT, float* sTmp, int pt) {
+    constexpr int kPairs = kC / (2 * S), kTR = S / RB, kTC = S / CB;
+    static_assert(kPairs * kTR * kTC == int(kPrepThreads), "one output block per prep thread");
+    const int pr = pt / (kTR * kTC), rem = pt % (kTR * kTC);
+    const int r0 = (rem / kTC) * RB, c0 = (rem % kTC) * CB;
+    const int o = pr * 2 * S;
+    float* tmp = sTmp + pr * S * S;
+    float acc[RB][CB];
+#pragma unroll
+    for (int i = 0; i < RB; ++i)
+#pragma unroll
+        for (int j = 0; j < CB; ++j) acc[i][j] = 0.f;
+#pragma unroll
+    for (int m = 0; m < S; ++m) {           // tmp = A21 T11
+        float a[RB], bb[CB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) a[i] = sA[(o + S + r0 + i) * kLdA + o + m];
+#pragma unroll
+        for (int j = 0; j < CB; ++j) bb[j] = sT[(o + m) * kLdA + o + c0 + j];
+#pragma unroll
+        for (int i = 0; i < RB; ++i)
+#pragma unroll
+            for (int j = 0; j < CB; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < RB; ++i)
+#pragma unroll
+        for (int j = 0; j < CB; ++j) {
+            tmp[(r0 + i) * S + c0 + j] = acc[i][j];
+            acc[i][j] = 0.f;
+        }
+    named_sync(kBarPrep, kPrepThreads);
+#pragma unroll
+    for (int m = 0; m < S; ++m) {           // T21 = -T22 tmp
+        float a[RB], bb[CB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) a[i] = sT[(o + S + r0 + i) * kLdA + o + S + m];
+#pragma unroll
+        for (int j = 0; j < CB; ++j) bb[j] = tmp[m * S + c0 + j];
+#pragma unroll
+        for (int i = 0; i < RB; ++i)
+#pragma unroll
+            for (int j = 0; j < CB; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < RB; ++i)
+#pragma unroll
+        for (int j = 0; j < CB; ++j) sT[(o + S + r0 + i) * kLdA + o + c0 + j] = -acc[i][j];
+    named_sync(kBarPrep, kPrepThreads);
+}
+
 // T = (I + A)^-1 for the strictly lower 64x64 A (padded rows zero): 8x8
 // diagonal blocks by (I - N)(I + N^2)(I + N^4), then 2x2 block inversion,
-// level by level.  All threads of the CTA take part.
-__device__ void block_inverse_64(const float* sA, float* sT, float* sTmp) {
-    const int tid = threadIdx.x, nth = blockDim.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int idx = tid; idx < kC * kLdA; idx += nth) sT[idx] = 0.f;
-    __syncthreads();
-    if (warp < kC / 8) {
-        const int o = warp * 8;
-        float* N2 = sTmp + warp * 192;
+// level by level.  Run by the 256 prep threads (index pt) with named barriers.
+__device__ void block_inverse_64(const float* sA, float* sT, float* sTmp, int pt) {
+    const int pw = pt >> 5, lane = pt & 31;
+    for (int idx = pt; idx < kC * kLdA; idx += kPrepThreads) sT[idx] = 0.f;
+    named_sync(kBarPrep, kPrepThreads);
+    {
+        const int o = pw * 8;             // 8 prep warps, one 8x8 block each
+        float* N2 = sTmp + pw * 192;
         float* N4 = N2 + 64;
         float* X = N4 + 64;
         for (int e = lane; e < 64; e += 32) {
             const int r = e >> 3, c = e & 7;
             float acc = 0.f;
-            for (int m = 0; m < 8; ++m) acc = fmaf(sA[(o + r) * kLdA + o + m], sA[(o + m) * kLdA + o + c], acc);
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+                acc = fmaf(sA[(o + r) * kLdA + o + m], sA[(o + m) * kLdA + o + c], acc);
             N2[e] = acc;
         }
         __syncwarp();
         for (int e = lane; e < 64; e += 32) {
             const int r = e >> 3, c = e & 7;
             float acc = 0.f, nn2 = 0.f;
+#pragma unroll
             for (int m = 0; m < 8; ++m) {
                 acc = fmaf(N2[r * 8 + m], N2[m * 8 + c], acc);
                 nn2 = fmaf(sA[(o + r) * kLdA + o + m], N2[m * 8 + c], nn2);
@@ -144,32 +270,15 @@ __device__ void block_inverse_64(const float* sA, float* sT, float* sTmp) {
         for (int e = lane; e < 64; e += 32) {
             const int r = e >> 3, c = e & 7;
             float acc = X[e];
+#pragma unroll
             for (int m = 0; m < 8; ++m) acc = fmaf(X[r * 8 + m], N4[m * 8 + c], acc);
             sT[(o + r) * kLdA + o + c] = acc;
         }
     }
-    __syncthreads();
-    for (int size = 8; size < kC; size *= 2) {
-        const int pairs = kC / (2 * size), per = size * size;
-        for (int idx = tid; idx < pairs * per; idx += nth) {
-            const int pr = idx / per, r = (idx / size) % size, c = idx % size;
-            const int o = pr * 2 * size;
-            float acc = 0.f;
-            for (int m = c; m < size; ++m)
-                acc = fmaf(sA[(o + size + r) * kLdA + o + m], sT[(o + m) * kLdA + o + c], acc);
-            sTmp[idx] = acc;
-        }
-        __syncthreads();
-        for (int idx = tid; idx < pairs * per; idx += nth) {
-            const int pr = idx / per, r = (idx / size) % size, c = idx % size;
-            const int o = pr * 2 * size;
-            float acc = 0.f;
-            for (int m = 0; m <= r; ++m)
-                acc = fmaf(sT[(o + size + r) * kLdA + o + size + m], sTmp[pr * per + m * size + c], acc);
-            sT[(o + size + r) * kLdA + o + c] = -acc;
-        }
-        __syncthreads();
-    }
+    named_sync(kBarPrep, kPrepThreads);
+    level_products<8, 1, 1>(sA, sT, sTmp, pt);
+    level_products<16, 1, 2>(sA, sT, sTmp, pt);
+    level_products<32, 2, 2>(sA, sT, sTmp, pt);
 }
 
 struct Maps {
@@ -183,28 +292,27 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     float* sA = reinterpret_cast<float*>(sm + kOffA);
     float* sT = reinterpret_cast<float*>(sm + kOffT);
     float* sTmp = reinterpret_cast<float*>(sm + kOffTmp);
-    float* vGam = reinterpret_cast<float*>(sm + kOffVec);   // gamma (cumsum)
-    float* vEg = vGam + kC;                                 // Gamma = exp(gamma)
-    float* vBeta = vEg + kC;
-    float* vRk = vBeta + kC;                                // 1/|k_i|
-    float* vRq = vRk + kC;                                  // 1/|q_t|
-    float* vEnd = vRq + kC;                                 // exp(min(gamma_S - gamma_i, 0)) r_k,i
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);   // [0,1] TMA stages, [2] MMA
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + 24);
-    int* s_err = reinterpret_cast<int*>(sm + kOffBar + 28);
+    float* vGam = reinterpret_cast<float*>(sm + kOffVec);   // prep: g, then gamma * log2(e)
+    float* vEg = vGam + kC;                                 // prep: Gamma
+    float* vBeta = vEg + kC;                                // prep: beta
+    float* vRk = vBeta + kC;                                // prep: 1/|k_i|
+    float* vRq = vRk + kC;                                  // prep: 1/|q_t|
+    float* vEnd = vRq + kC;                                 // prep: exp(min(gamma_S - gamma_i, 0)) r_k,i
+    float* cE = vEnd + kC;                                  // chain: [2][64] end weights
+    float* cGS = cE + 2 * kC;                               // chain: [2] exp(gamma_S)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + kNumBars * 8);
+    volatile int* s_err = reinterpret_cast<volatile int*>(sm + kOffBar + kNumBars * 8 + 4);
+    int* s_tma_last = reinterpret_cast<int*>(sm + kOffBar + kNumBars * 8 + 8);   // [2]
 
     const int h = blockIdx.x, n = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
-    const int row = quarter * 32 + lane;                // TMEM lane owned by this thread
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;                 // TMEM lane of this thread
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    const bool is_chain = warp >= 4 && warp < 8;
     const int kh = h / (p.Hv / p.Hk);
     const int Hv = p.Hv;
-
-    const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(p.q);
-    const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
-    const __nv_bfloat16* gv = static_cast<const __nv_bfloat16*>(p.v);
-    __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(p.out);
 
     int64_t t_end_all = p.cu[p.B];
     if (t_end_all > p.t_cap) t_end_all = p.t_cap;
@@ -212,17 +320,18 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     t0 = t0 < 0 ? 0 : (t0 > t_end_all ? t_end_all : t0);
     t1 = t1 < t0 ? t0 : (t1 > t_end_all ? t_end_all : t1);
     const int nchunks = int((t1 - t0 + p.chunk - 1) / p.chunk);
+    const size_t sbase = (size_t(n) * Hv + h) * kD * kD;
 
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        mbar_init(&bars[2], 1);
+        for (int i = 0; i < int(kNumBars); ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         *s_err = 0;
+        s_tma_last[0] = s_tma_last[1] = -1;
         tma_prefetch_desc(&maps.q);
         tma_prefetch_desc(&maps.k);
         tma_prefetch_desc(&maps.v);
     }
+    __syncwarp();
     if (warp == 0) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
@@ -231,364 +340,473 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tZ = tmem + kColZ, tX = tmem + kColX, tG = tmem + kColG, tW = tmem + kColW,
-                   tO = tmem + kColO;
+    const uint32_t tZ = tmem + kColZ, tZb = tmem + kColZb, tX = tmem + kColX, tO = tmem + kColO,
+                   tGW = tmem + kColGW, tU = tmem + kColU;
 
-    // Chunk fetch: TMA when the 64-row box lies inside the buffers, else
-    // plain loads (zero beyond the last token).  Returns true when TMA was used.
-    auto tma_ok = [&](int64_t cs) { return cs + kC <= t_end_all; };
-    int tma_last_issued = -1;     // thread 0 only: last chunk whose TMA was issued
+    auto stage_ptr = [&](int c) { return sm + uint32_t(c & 1) * kStageBytes; };
+    auto chunk_start = [&](int c) { return t0 + int64_t(c) * p.chunk; };
+    auto tma_ok = [&](int c) { return chunk_start(c) + kC <= t_end_all; };
     auto issue_tma = [&](int c) {
-        const int st = c & 1;
-        tma_last_issued = c;
-        uint8_t* kq = sm + kOffStage0 + st * kStageBytes;
+        uint8_t* kq = stage_ptr(c);
         uint8_t* vv = kq + kStageKQ;
-        const int y = int(t0 + int64_t(c) * p.chunk);
-        mbar_arrive_expect_tx(&bars[st], kStageBytes);
-        tma_load_2d(kq + 0, &maps.k, &bars[st], kh * kD, y);
-        tma_load_2d(kq + 16384, &maps.k, &bars[st], kh * kD + 64, y);
-        tma_load_2d(kq + 8192, &maps.q, &bars[st], kh * kD, y);
-        tma_load_2d(kq + 24576, &maps.q, &bars[st], kh * kD + 64, y);
-        tma_load_2d(vv + 0, &maps.v, &bars[st], h * kD, y);
-        tma_load_2d(vv + 8192, &maps.v, &bars[st], h * kD + 64, y);
+        uint64_t* bar = &bars[B_RAW0 + (c & 1)];
+        const int y = int(chunk_start(c));
+        s_tma_last[c & 1] = c;
+        mbar_arrive_expect_tx(bar, kStageBytes);
+        tma_load_2d(kq + 0, &maps.k, bar, kh * kD, y);
+        tma_load_2d(kq + 16384, &maps.k, bar, kh * kD + 64, y);
+        tma_load_2d(kq + 8192, &maps.q, bar, kh * kD, y);
+        tma_load_2d(kq + 24576, &maps.q, bar, kh * kD + 64, y);
+        tma_load_2d(vv + 0, &maps.v, bar, h * kD, y);
+        tma_load_2d(vv + 8192, &maps.v, bar, h * kD + 64, y);
     };
-    auto manual_load = [&](int c) {
-        const int st = c & 1;
-        uint8_t* kq = sm + kOffStage0 + st * kStageBytes;
-        uint8_t* vv = kq + kStageKQ;
-        const int64_t cs = t0 + int64_t(c) * p.chunk;
-        for (int idx = tid; idx < kC * 16; idx += kThreads) {      // (row, 8-col chunk)
-            const int r = idx >> 4, cc = (idx & 15) * 8;
-            const int64_t t = cs + r;
-            uint4 zk = make_uint4(0, 0, 0, 0), zq = zk, zv = zk;
-            if (t < t_end_all) {
-                zk = *reinterpret_cast<const uint4*>(gk + t * p.k_stride + kh * kD + cc);
-                zq = *reinterpret_cast<const uint4*>(gq + t * p.q_stride + kh * kD + cc);
-                zv = *reinterpret_cast<const uint4*>(gv + t * p.v_stride + int64_t(h) * kD + cc);
-            }
-            *reinterpret_cast<uint4*>(kq + toff(r, cc, 16384)) = zk;
-            *reinterpret_cast<uint4*>(kq + 8192 + toff(r, cc, 16384)) = zq;
-            *reinterpret_cast<uint4*>(vv + toff(r, cc, 8192)) = zv;
-        }
-    };
+    // A failed (timed-out) wait marks this thread; each group votes at its
+    // barriers (named_sync_or) and leaves its loop together.
+    auto wait = [&](int slot, uint32_t parity) { return mbar_wait(&bars[slot], parity, kWaitLimit); };
 
-    bool ok = true;
-    uint32_t mma_phase = 0;
-    auto wait_mma = [&]() {
-        if (!mbar_wait(&bars[2], mma_phase, kWaitLimit)) ok = false;
-        mma_phase ^= 1u;
-        tc_fence_after();
-    };
-    // Make every thread agree on `ok` (a barrier is needed at this point anyway).
-    auto sync_ok = [&]() {
-        if (!ok) atomicExch(s_err, 1);
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        ok = (*s_err == 0);
-    };
-
-    // ---- initial state -> Z (fp32 in TMEM) and Z bf16 (shared) --------------
-    {
-        const size_t sb = (size_t(n) * Hv + h) * kD * kD;
-        for (int cb = 0; cb < 64; cb += 16) {
-            float v[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int d = half * 64 + cb + i;
-                v[i] = p.state_in ? p.state_in[sb + size_t(d) * kD + row] : 0.f;
-            }
-            tmem_st16(tZ + lane_addr + half * 64 + cb, v);
-            store_chunk8(sm + kOffZ + toff(row, half * 64 + cb, 16384), v);
-            store_chunk8(sm + kOffZ + toff(row, half * 64 + cb + 8, 16384), v + 8);
-        }
-        tmem_st_wait();
-        fence_proxy_async_smem();
+    if (tid == 0) {
+        if (nchunks > 0 && tma_ok(0)) issue_tma(0);
+        if (nchunks > 1 && tma_ok(1)) issue_tma(1);
     }
-    if (nchunks > 0 && tid == 0 && tma_ok(t0)) issue_tma(0);
-    sync_ok();
+    __syncwarp();
 
-    for (int c = 0; c < nchunks && ok; ++c) {
-        const int st = c & 1;
-        uint8_t* kq = sm + kOffStage0 + st * kStageBytes;
-        uint8_t* vv = kq + kStageKQ;
-        const int64_t cs = t0 + int64_t(c) * p.chunk;
-        const int rows = int(t1 - cs < p.chunk ? t1 - cs : p.chunk);
-
-        // ---- fetch: this chunk (manual if needed), prefetch the next ------------
-        const bool this_tma = tma_ok(cs);
-        if (!this_tma) {
-            manual_load(c);
-            fence_proxy_async_smem();
-        }
-        if (tid == 0 && c + 1 < nchunks && tma_ok(cs + p.chunk)) {
-            fence_proxy_async_smem();
-            issue_tma(c + 1);
-        }
-        if (tid < kC) {
-            const bool in = tid < rows;
-            vGam[tid] = in ? p.g[(cs + tid) * Hv + h] : 0.f;
-            vBeta[tid] = in ? p.beta[(cs + tid) * Hv + h] : 0.f;
-        }
-        if (this_tma && !mbar_wait(&bars[st], uint32_t((c >> 1) & 1), kWaitLimit)) ok = false;
-        sync_ok();
-        if (!ok) break;
-
-        // ---- phase 1: cumsum, row norms; issue the Gram MMA -------------------
-        if (warp == 0) {
-            // inclusive scan of g over 64 rows: 2 values per lane
-            float a = vGam[2 * lane], b = vGam[2 * lane + 1];
-            b += a;
-            float s = b;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_up_sync(0xffffffffu, s, o);
-                if (lane >= o) s += u;
+    if (!is_chain) {
+        // ================================================================ prep
+        // Thread 0 alone polls mbarriers; the group learns the outcome through
+        // a voting named barrier (many pollers would starve the other warps).
+        const int pt = tid < 128 ? tid : tid - 128;      // 0..255
+        const int pw = pt >> 5;                          // prep warp 0..7
+        const int phalf = tid >= 256 ? 1 : 0;            // column half of TMEM reads
+        const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(p.q);
+        const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
+        const __nv_bfloat16* gv = static_cast<const __nv_bfloat16*>(p.v);
+        const uint32_t id_gram = idesc_bf16(128, 64, 0, 0);
+        const uint32_t id_uw = idesc_bf16(128, 64, 1, 0);   // A MN-major, B K-major
+        const uint64_t dTb = smem_desc(smem_u32(sm + kOffTb), 16, 1024, kSwizzle128B);
+        float g_next = 0.f, b_next = 0.f;
+        if (pt < kC && nchunks > 0) {
+            const int64_t t = chunk_start(0) + pt;
+            if (pt < p.chunk && t < t1) {
+                g_next = p.g[t * Hv + h];
+                b_next = p.beta[t * Hv + h];
             }
-            const float excl = s - b;
-            a += excl;
-            b = s;
-            vGam[2 * lane] = a;
-            vGam[2 * lane + 1] = b;
         }
-        {
-            // 128 rows (K 0..63, Q 0..63): warp w takes rows 16w .. 16w+15
-            for (int rr = 0; rr < 16; ++rr) {
-                const int r = warp * 16 + rr;
+        bool fail = false;
+        for (int c = 0; c < nchunks; ++c) {
+            const int b = c & 1;
+            uint8_t* kq = stage_ptr(c);
+            uint8_t* vv = kq + kStageKQ;
+            const int64_t cs = chunk_start(c);
+            const int rows = int(t1 - cs < p.chunk ? t1 - cs : p.chunk);
+            // ---- g, beta of this chunk; prefetch the next chunk's ---------------
+            if (pt < kC) {
+                vGam[pt] = g_next;
+                vBeta[pt] = b_next;
+                g_next = b_next = 0.f;
+                const int64_t t = cs + p.chunk + pt;
+                if (c + 1 < nchunks && pt < p.chunk && t < t1) {
+                    g_next = p.g[t * Hv + h];
+                    b_next = p.beta[t * Hv + h];
+                }
+            }
+            // ---- raw tiles ----------------------------------------------------
+            bool lf = false;
+            if (tma_ok(c)) {
+                if (tid == 0) lf = !wait(B_RAW0 + b, uint32_t((c >> 1) & 1));
+            } else {
+                if (tid == 0 && c >= 2) lf = !wait(B_SFREE0 + b, uint32_t(((c - 2) >> 1) & 1));
+                __syncwarp();
+                if (named_sync_or(kBarPrep, kPrepThreads, lf)) { fail = true; break; }
+                for (int idx = pt; idx < kC * 16; idx += kPrepThreads) {
+                    const int r = idx >> 4, cc = (idx & 15) * 8;
+                    const int64_t t = cs + r;
+                    uint4 zk = make_uint4(0, 0, 0, 0), zq = zk, zv = zk;
+                    if (t < t_end_all) {
+                        zk = *reinterpret_cast<const uint4*>(gk + t * p.k_stride + kh * kD + cc);
+                        zq = *reinterpret_cast<const uint4*>(gq + t * p.q_stride + kh * kD + cc);
+                        zv = *reinterpret_cast<const uint4*>(gv + t * p.v_stride + int64_t(h) * kD + cc);
+                    }
+                    *reinterpret_cast<uint4*>(kq + toff(r, cc, 16384)) = zk;
+                    *reinterpret_cast<uint4*>(kq + 8192 + toff(r, cc, 16384)) = zq;
+                    *reinterpret_cast<uint4*>(vv + toff(r, cc, 8192)) = zv;
+                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            tc_fence_before();
+            if (named_sync_or(kBarPrep, kPrepThreads, lf)) { fail = true; break; }
+            tc_fence_after();
+            // ---- Gram MMA; cumsum (log2 domain); row norms ----------------------
+            if (tid == 0) {
+                const uint64_t d0 = smem_desc(smem_u32(kq), 16, 1024, kSwizzle128B);
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
+                    umma_f16(tGW, d0 + (off >> 4), d0 + (off >> 4), id_gram, s > 0);
+                }
+                umma_commit(&bars[B_GRAM]);
+            }
+            __syncwarp();
+            if (pw == 0) {
+                float a = vGam[2 * lane], bb = vGam[2 * lane + 1];
+                bb += a;
+                float s = bb;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float u = __shfl_up_sync(0xffffffffu, s, o);
+                    if (lane >= o) s += u;
+                }
+                a += s - bb;
+                vGam[2 * lane] = a * kLog2e;                   // gamma * log2(e)
+                vGam[2 * lane + 1] = s * kLog2e;
+            }
+            {
+                // 128 rows (K 0..63, Q 0..63); two threads per row, 64 columns each
+                const int r = pt >> 1, part = pt & 1;
                 const int isq = r >= kC, tr = r & 63;
                 const uint8_t* base = kq + (isq ? 8192 : 0);
-                const int col = lane * 4;
-                const uint2 u = *reinterpret_cast<const uint2*>(base + toff(tr, col, 16384));
-                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&u);
-                const float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
-                float ss = f0.x * f0.x + f0.y * f0.y + f1.x * f1.x + f1.y * f1.y;
-                ss = warp_sum(ss);
-                if (lane == 0) {
-                    const float r_ = p.l2norm ? rsqrtf(ss + p.eps) : 1.f;
-                    (isq ? vRq : vRk)[tr] = r_;
+                float ss = 0.f;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    float v[8];
+                    load_chunk8(base + toff(tr, part * 64 + m * 8, 16384), v);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
                 }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (part == 0) (isq ? vRq : vRk)[tr] = p.l2norm ? rsqrtf(ss + p.eps) : 1.f;
             }
-        }
-        if (tid == 0) {
+            named_sync(kBarPrep, kPrepThreads);
+            if (pt < kC) {
+                const float gm = vGam[pt];
+                vEg[pt] = exp2f(gm);
+                vEnd[pt] = pt < rows ? exp2f(fminf(vGam[rows - 1] - gm, 0.f)) * vRk[pt] : 0.f;
+            }
+            // ---- masks and decays on the Gram matrices --------------------------
+            if (tid == 0) {
+                if (c >= 2) lf = !wait(B_PFREE0 + b, uint32_t(((c - 2) >> 1) & 1));
+                lf = lf || !wait(B_GRAM, uint32_t(c & 1));
+            }
+            __syncwarp();
+            if (named_sync_or(kBarPrep, kPrepThreads, lf)) { fail = true; break; }
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16(128, 64, 0, 0);
-            const uint32_t base = smem_u32(kq);
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
-                umma_f16(tG, smem_desc(base + off, 16, 1024, kSwizzle128B),
-                         smem_desc(base + off, 16, 1024, kSwizzle128B), idesc, s > 0);
+            {
+                float v[32];
+                tmem_ld32(tGW + lane_addr + phalf * 32, v);
+                if (row < kC) {
+                    const int i = row;
+                    const float bi = vBeta[i] * vRk[i], gi = vGam[i];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const int j = phalf * 32 + q;
+                        float a = 0.f;
+                        if (i < rows && j < i) a = bi * exp2f(fminf(gi - vGam[j], 0.f)) * vRk[j] * v[q];
+                        sA[i * kLdA + j] = a;
+                    }
+                } else {
+                    const int t = row - kC;
+                    const float rt = vRq[t], gt = vGam[t];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const int j = phalf * 32 + q;
+                        v[q] = (t < rows && j <= t) ? rt * exp2f(fminf(gt - vGam[j], 0.f)) * vRk[j] * v[q] : 0.f;
+                    }
+                    uint8_t* phi = sm + kOffP + uint32_t(b * 2) * 8192u;
+#pragma unroll
+                    for (int q = 0; q < 32; q += 8) {
+                        const uint32_t o = toff(t, phalf * 32 + q, 8192);
+                        store_split8(phi + o, phi + 8192 + o, v + q);
+                    }
+                }
             }
-            umma_commit(&bars[2]);
-        }
-        __syncthreads();
-        if (tid < kC) {
-            const float gm = vGam[tid];
-            const float gS = vGam[rows - 1];
-            vEg[tid] = expf(gm);
-            vEnd[tid] = tid < rows ? expf(fminf(gS - gm, 0.f)) * vRk[tid] : 0.f;
-        }
-        wait_mma();
-        sync_ok();
-        if (!ok) break;
-
-        // ---- phase 2: masks and decays on the Gram matrices ---------------------
-        {
-            float v[32];
-            tmem_ld16(tG + lane_addr + half * 32, v);
-            tmem_ld16(tG + lane_addr + half * 32 + 16, v + 16);
-            tmem_ld_wait();
-            if (row < kC) {                  // A_ij = beta_i e^{g_i - g_j} r_i r_j k_i.k_j, j < i
-                const int i = row;
-                const float bi = vBeta[i] * vRk[i], gi = vGam[i];
+            named_sync(kBarPrep, kPrepThreads);
+            // ---- blocked inverse; T diag(beta), T diag(beta Gamma r_k) as hi + lo -
+            block_inverse_64(sA, sT, sTmp, pt);
+            for (int idx = pt; idx < kC * 8; idx += kPrepThreads) {
+                const int t = idx >> 3, i0 = (idx & 7) * 8;
+                float a[8], bg[8];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int j = half * 32 + q;
-                    float a = 0.f;
-                    if (i < rows && j < i) a = bi * expf(fminf(gi - vGam[j], 0.f)) * vRk[j] * v[q];
-                    sA[i * kLdA + j] = a;
+                for (int q = 0; q < 8; ++q) {
+                    const int i = i0 + q;
+                    const float tv = sT[t * kLdA + i];
+                    a[q] = tv * vBeta[i];
+                    bg[q] = a[q] * vEg[i] * vRk[i];
                 }
-            } else {                         // P_tj = e^{g_t - g_j} r_q,t r_k,j q_t.k_j, j <= t
-                const int t = row - kC;
-                const float rt = vRq[t], gt = vGam[t];
-                float w[32];
+                const uint32_t o = toff(t, i0, 8192);
+                store_split8(sm + kOffTb + o, sm + kOffTb + 8192 + o, a);
+                store_split8(sm + kOffTb + 16384 + o, sm + kOffTb + 24576 + o, bg);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarPrep, kPrepThreads);
+            if (tid == 0) {
+                if (c > 0) lf = !wait(B_XREAD, uint32_t((c - 1) & 1));
+                if (!lf) {
+                    tc_fence_after();
+                    const uint64_t dV = smem_desc(smem_u32(vv), 8192, 1024, kSwizzle128B);
+                    const uint64_t dK = smem_desc(smem_u32(kq), 16384, 1024, kSwizzle128B);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int j = half * 32 + q;
-                    w[q] = (t < rows && j <= t) ? rt * expf(fminf(gt - vGam[j], 0.f)) * vRk[j] * v[q] : 0.f;
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            // U0^T = V^T Tb^T ;  W^T = K^T Tbg^T
+                            umma_f16(tX, dV + uint64_t(s * 2048 >> 4), dTb + uint64_t((part * 8192 + s * 32) >> 4),
+                                     id_uw, part > 0 || s > 0);
+                            umma_f16(tGW, dK + uint64_t(s * 2048 >> 4),
+                                     dTb + uint64_t((16384 + part * 8192 + s * 32) >> 4), id_uw, part > 0 || s > 0);
+                        }
+                    umma_commit(&bars[B_W]);
+                    lf = !wait(B_W, uint32_t(c & 1));
+                    if (c >= 1) lf = lf || !wait(B_WTFREE, uint32_t((c - 1) & 1));
                 }
+            }
+            __syncwarp();
+            // ---- -W^T to shared; scaled Q rows in place; chain scalars ---------
+            if (named_sync_or(kBarPrep, kPrepThreads, lf)) { fail = true; break; }
+            tc_fence_after();
+            {
+                float v[32];
+                tmem_ld32(tGW + lane_addr + phalf * 32, v);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] = -v[q];
 #pragma unroll
                 for (int q = 0; q < 32; q += 8)
-                    store_chunk8(sm + kOffP + toff(t, half * 32 + q, 8192), w + q);
+                    store_chunk8(sm + kOffWt + toff(row, phalf * 32 + q, 16384), v + q);
             }
-        }
-        __syncthreads();
-
-        // ---- phase 3: blocked inverse; T diag(beta), T diag(beta Gamma r_k) -----
-        block_inverse_64(sA, sT, sTmp);
-        for (int idx = tid; idx < kC * 8; idx += kThreads) {
-            const int t = idx >> 3, i0 = (idx & 7) * 8;
-            float a[8], b[8];
+            for (int idx = pt; idx < kC * 16; idx += kPrepThreads) {
+                const int r = idx >> 4, cc = (idx & 15) * 8;
+                uint8_t* ptr = kq + 8192 + toff(r, cc, 16384);
+                const float f = r < rows ? vEg[r] * vRq[r] : 0.f;
+                float v[8];
+                load_chunk8(ptr, v);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int i = i0 + q;
-                const float tv = sT[t * kLdA + i];
-                a[q] = tv * vBeta[i];
-                b[q] = a[q] * vEg[i] * vRk[i];
+                for (int q = 0; q < 8; ++q) v[q] *= f;
+                store_chunk8(ptr, v);
             }
-            store_chunk8(sm + kOffTb + toff(t, i0, 8192), a);
-            store_chunk8(sm + kOffTbg + toff(t, i0, 8192), b);
+            if (pt < kC) cE[b * kC + pt] = vEnd[pt];
+            if (pt == 0) cGS[b] = vEg[rows - 1];
+            __syncwarp();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarPrep, kPrepThreads);
+            if (tid == 0) mbar_arrive(&bars[B_READY0 + b]);
+            __syncwarp();
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t idesc = idesc_bf16(128, 64, 1, 0);   // A MN-major, B K-major
-            const uint32_t vb = smem_u32(vv), kb = smem_u32(kq);
-            const uint32_t tb = smem_u32(sm + kOffTb), tbg = smem_u32(sm + kOffTbg);
-            for (int s = 0; s < 4; ++s) {
-                // U0^T = V^T Tb^T : A = V (rows i, cols j), B = Tb [t][i]
-                umma_f16(tX, smem_desc(vb + s * 2048, 8192, 1024, kSwizzle128B),
-                         smem_desc(tb + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
-                // W^T = K^T Tbg^T : A = K (rows i, cols d), B = Tbg [t][i]
-                umma_f16(tW, smem_desc(kb + s * 2048, 16384, 1024, kSwizzle128B),
-                         smem_desc(tbg + s * 32, 16, 1024, kSwizzle128B), idesc, s > 0);
-            }
-            umma_commit(&bars[2]);
-        }
-        wait_mma();
-        sync_ok();
-        if (!ok) break;
-
-        // ---- phase 4: -W^T to shared; scale Q and K rows in place --------------
-        {
-            float v[32];
-            tmem_ld16(tW + lane_addr + half * 32, v);
-            tmem_ld16(tW + lane_addr + half * 32 + 16, v + 16);
-            tmem_ld_wait();
+        if (fail) *s_err = 1;
+    } else {
+        // ================================================================ chain
+        // Thread 128 polls the mbarriers and issues the chain MMAs; the group
+        // follows through voting named barriers.
+        const int ct = tid - 128;                        // == row
+        const bool lead = ct == 0;
+        __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(p.out);
+        const uint32_t id_x = idesc_bf16(128, 64, 0, 1);    // B = -W^T, MN-major
+        const uint32_t id_o = idesc_bf16(128, 64, 0, 0);    // B = Qs or P, K-major
+        const uint32_t id_z = idesc_bf16(128, 128, 0, 1);   // B = raw K, MN-major [i][d]
+        const uint64_t dWt = smem_desc(smem_u32(sm + kOffWt), 16384, 1024, kSwizzle128B);
+        bool fail = false;
+        // output rows of the previous chunk, kept as bf16 pairs until the next
+        // chunk's MMAs are in flight
+        uint32_t opk[32];
+        int64_t o_cs = 0;
+        int o_rows = 0;
+        if (nchunks == 0) {
+            if (p.state_out)
+                for (int d = 0; d < kD; ++d)
+                    p.state_out[sbase + size_t(d) * kD + row] =
+                        p.state_in ? p.state_in[sbase + size_t(d) * kD + row] : 0.f;
+        } else {
+            // ---- incoming state: Zb = bf16(Z), Z <- exp(gamma_S(0)) Z -----------
+            bool lf = lead && !wait(B_READY0, 0);
+            __syncwarp();
+            fail = named_sync_or(kBarChain, kChainThreads, lf);
+            const float gs0 = cGS[0];
+            for (int hf = 0; hf < 2; ++hf) {
+                float z[64];
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = -v[q];
+                for (int i = 0; i < 64; ++i)
+                    z[i] = p.state_in ? p.state_in[sbase + size_t(hf * 64 + i) * kD + row] : 0.f;
+                uint32_t zb[32];
 #pragma unroll
-            for (int q = 0; q < 32; q += 8)
-                store_chunk8(sm + kOffWt + toff(row, half * 32 + q, 16384), v + q);
-        }
-        for (int idx = tid; idx < 2 * kC * 16; idx += kThreads) {
-            const int isq = idx >= kC * 16, r = (idx >> 4) & 63, cc = (idx & 15) * 8;
-            uint8_t* ptr = kq + (isq ? 8192 : 0) + toff(r, cc, 16384);
-            const float f = isq ? (r < rows ? vEg[r] * vRq[r] : 0.f) : vEnd[r];
-            float v[8];
-            load_chunk8(ptr, v);
+                for (int i = 0; i < 32; ++i) zb[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
+                GDN_TMEM_ST_X16(tZb + lane_addr + hf * 32, zb);
+                GDN_TMEM_ST_X16(tZb + lane_addr + hf * 32 + 16, (zb + 16));
 #pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] *= f;
-            store_chunk8(ptr, v);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t zb = smem_u32(sm + kOffZ), wt = smem_u32(sm + kOffWt), kb = smem_u32(kq);
-            const uint32_t id_x = idesc_bf16(128, 64, 0, 1);   // B MN-major
-            const uint32_t id_o = idesc_bf16(128, 64, 0, 0);
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t za = zb + uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
-                // D_X (= U0^T) += Z (-W^T)
-                umma_f16(tX, smem_desc(za, 16, 1024, kSwizzle128B),
-                         smem_desc(wt + s * 2048, 16384, 1024, kSwizzle128B), id_x, 1);
-                // D_O = Z Qs^T : B = Qs [t][d] K-major
-                const uint32_t qb = kb + 8192 + uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
-                umma_f16(tO, smem_desc(za, 16, 1024, kSwizzle128B),
-                         smem_desc(qb, 16, 1024, kSwizzle128B), id_o, s > 0);
-            }
-            umma_commit(&bars[2]);
-        }
-        wait_mma();
-        sync_ok();
-        if (!ok) break;
-
-        // ---- phase 5: v_new^T to shared; Z <- exp(gamma_S) Z --------------------
-        {
-            float v[32];
-            tmem_ld16(tX + lane_addr + half * 32, v);
-            tmem_ld16(tX + lane_addr + half * 32 + 16, v + 16);
-            tmem_ld_wait();
-#pragma unroll
-            for (int q = 0; q < 32; q += 8)
-                store_chunk8(sm + kOffVn + toff(row, half * 32 + q, 16384), v + q);
-            const float eS = vEg[rows - 1];
-            for (int cb = 0; cb < 64; cb += 16) {
-                float z[16];
-                tmem_ld16(tZ + lane_addr + half * 64 + cb, z);
-                tmem_ld_wait();
-#pragma unroll
-                for (int q = 0; q < 16; ++q) z[q] *= eS;
-                tmem_st16(tZ + lane_addr + half * 64 + cb, z);
+                for (int i = 0; i < 64; ++i) z[i] *= gs0;
+                tmem_st16(tZ + lane_addr + hf * 64, z);
+                tmem_st16(tZ + lane_addr + hf * 64 + 16, z + 16);
+                tmem_st16(tZ + lane_addr + hf * 64 + 32, z + 32);
+                tmem_st16(tZ + lane_addr + hf * 64 + 48, z + 48);
             }
             tmem_st_wait();
+            tc_fence_before();
+            named_sync(kBarChain, kChainThreads);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
+        for (int c = 0; c < nchunks && !fail; ++c) {
+            const int b = c & 1;
+            uint8_t* kq = stage_ptr(c);
+            const int64_t cs = chunk_start(c);
+            const int rows = int(t1 - cs < p.chunk ? t1 - cs : p.chunk);
+            // ---- U^T = U0^T - Zb W^T ;  O^T = Zb Qs^T --------------------------
+            bool lf = false;
+            if (lead) {
+                lf = !wait(B_READY0 + b, uint32_t((c >> 1) & 1));
+                if (!lf) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int s = 0; s < 8; ++s)
+                        umma_f16_tmemA(tX, tZb + s * 8, dWt + uint64_t(s * 2048 >> 4), id_x, 1);
+                    umma_commit(&bars[B_X]);
+                    const uint64_t dQ = smem_desc(smem_u32(kq + 8192), 16, 1024, kSwizzle128B);
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
+                        umma_f16_tmemA(tO, tZb + s * 8, dQ + (off >> 4), id_o, s > 0);
+                    }
+                }
+            }
+            __syncwarp();
+            // previous chunk's output rows, while the MMAs run
+            if (c > 0) {
+                __nv_bfloat16* dst = gout + (o_cs * Hv + h) * kD + row;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&opk[i]);
+                    if (2 * i < o_rows) dst[int64_t(2 * i) * Hv * kD] = pr.x;
+                    if (2 * i + 1 < o_rows) dst[int64_t(2 * i + 1) * Hv * kD] = pr.y;
+                }
+            }
+            if (lead && !lf) lf = !wait(B_X, uint32_t(c & 1));
+            __syncwarp();
+            if (named_sync_or(kBarChain, kChainThreads, lf)) { fail = true; break; }
             tc_fence_after();
-            const uint32_t vn = smem_u32(sm + kOffVn), kb = smem_u32(kq), pb = smem_u32(sm + kOffP);
-            const uint32_t id_z = idesc_bf16(128, 128, 0, 1);  // B = Ks MN-major [i][d]
-            const uint32_t id_o = idesc_bf16(128, 64, 0, 0);   // B = P [t][i] K-major
-            for (int s = 0; s < 4; ++s) {
-                umma_f16(tZ, smem_desc(vn + s * 32, 16, 1024, kSwizzle128B),
-                         smem_desc(kb + s * 2048, 16384, 1024, kSwizzle128B), id_z, 1);
-                umma_f16(tO, smem_desc(vn + s * 32, 16, 1024, kSwizzle128B),
-                         smem_desc(pb + s * 32, 16, 1024, kSwizzle128B), id_o, 1);
-            }
-            umma_commit(&bars[2]);
-        }
-        wait_mma();
-        sync_ok();
-        if (!ok) break;
-
-        // ---- phase 6: output rows; Z bf16 for the next chunk --------------------
-        {
-            float v[32];
-            tmem_ld16(tO + lane_addr + half * 32, v);
-            tmem_ld16(tO + lane_addr + half * 32 + 16, v + 16);
-            tmem_ld_wait();
+            if (lead) mbar_arrive(&bars[B_WTFREE]);
+            __syncwarp();
+            // ---- U (hi, lo) and Us = U diag(e) (hi, lo) into TMEM --------------
+            for (int hf = 0; hf < 2; ++hf) {
+                float x[32];
+                tmem_ld32(tX + lane_addr + hf * 32, x);
+                const float* e = cE + b * kC + hf * 32;
+                uint32_t uh[16], ul[16], sh[16], sl[16];
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const int t = half * 32 + q;
-                if (t < rows)
-                    gout[((cs + t) * Hv + h) * kD + row] = __float2bfloat16_rn(v[q] * p.q_scale);
+                for (int i = 0; i < 16; ++i) {
+                    const float a0 = x[2 * i], a1 = x[2 * i + 1];
+                    const float h0 = bf16_round(a0), h1 = bf16_round(a1);
+                    uh[i] = pack_bf16x2(h0, h1);
+                    ul[i] = pack_bf16x2(a0 - h0, a1 - h1);
+                    const float s0 = a0 * e[2 * i], s1 = a1 * e[2 * i + 1];
+                    const float g0 = bf16_round(s0), g1 = bf16_round(s1);
+                    sh[i] = pack_bf16x2(g0, g1);
+                    sl[i] = pack_bf16x2(s0 - g0, s1 - g1);
+                }
+                GDN_TMEM_ST_X16(tU + lane_addr + 0 + hf * 16, uh);
+                GDN_TMEM_ST_X16(tU + lane_addr + 32 + hf * 16, ul);
+                GDN_TMEM_ST_X16(tU + lane_addr + 64 + hf * 16, sh);
+                GDN_TMEM_ST_X16(tU + lane_addr + 96 + hf * 16, sl);
             }
-            for (int cb = 0; cb < 64; cb += 16) {
-                float z[16];
-                tmem_ld16(tZ + lane_addr + half * 64 + cb, z);
-                tmem_ld_wait();
-                store_chunk8(sm + kOffZ + toff(row, half * 64 + cb, 16384), z);
-                store_chunk8(sm + kOffZ + toff(row, half * 64 + cb + 8, 16384), z + 8);
+            tmem_st_wait();
+            tc_fence_before();
+            named_sync(kBarChain, kChainThreads);
+            if (lead) {
+                mbar_arrive(&bars[B_XREAD]);
+                tc_fence_after();
+                const uint64_t dK = smem_desc(smem_u32(kq), 16384, 1024, kSwizzle128B);
+                const uint64_t dP = smem_desc(smem_u32(sm + kOffP + uint32_t(b * 2) * 8192u), 16, 1024,
+                                              kSwizzle128B);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        umma_f16_tmemA(tZ, tU + 64 + part * 32 + s * 8, dK + uint64_t(s * 2048 >> 4), id_z, 1);
+                umma_commit(&bars[B_Z]);
+                // (U hi, P hi), (U hi, P lo), (U lo, P hi)
+#pragma unroll
+                for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        umma_f16_tmemA(tO, tU + (pr == 2 ? 32 : 0) + s * 8,
+                                       dP + uint64_t(((pr == 1 ? 8192 : 0) + s * 32) >> 4), id_o, 1);
+                umma_commit(&bars[B_O]);
+            }
+            __syncwarp();
+            // ---- new state: Zb = bf16(Z); Z <- exp(gamma_S(c+1)) Z --------------
+            const bool has_next = c + 1 < nchunks;
+            if (lead) {
+                lf = !wait(B_Z, uint32_t(c & 1));
+                if (!lf) {
+                    mbar_arrive(&bars[B_SFREE0 + b]);
+                    if (c + 2 < nchunks && tma_ok(c + 2)) issue_tma(c + 2);
+                    if (has_next) lf = !wait(B_READY0 + (b ^ 1), uint32_t(((c + 1) >> 1) & 1));
+                }
+            }
+            __syncwarp();
+            if (named_sync_or(kBarChain, kChainThreads, lf)) { fail = true; break; }
+            tc_fence_after();
+            const float gsn = has_next ? cGS[b ^ 1] : 1.f;
+            for (int hf = 0; hf < 2; ++hf) {
+                float z[64];
+                tmem_ld64(tZ + lane_addr + hf * 64, z);
+                uint32_t zb[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) zb[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
+                GDN_TMEM_ST_X16(tZb + lane_addr + hf * 32, zb);
+                GDN_TMEM_ST_X16(tZb + lane_addr + hf * 32 + 16, (zb + 16));
+                if (has_next) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) z[i] *= gsn;
+                    tmem_st16(tZ + lane_addr + hf * 64, z);
+                    tmem_st16(tZ + lane_addr + hf * 64 + 16, z + 16);
+                    tmem_st16(tZ + lane_addr + hf * 64 + 32, z + 32);
+                    tmem_st16(tZ + lane_addr + hf * 64 + 48, z + 48);
+                } else if (p.state_out) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) p.state_out[sbase + size_t(hf * 64 + i) * kD + row] = z[i];
+                }
+            }
+            tmem_st_wait();
+            // ---- output rows to registers (stored during the next chunk) --------
+            if (lead) lf = !wait(B_O, uint32_t(c & 1));
+            __syncwarp();
+            if (named_sync_or(kBarChain, kChainThreads, lf)) { fail = true; break; }
+            tc_fence_after();
+            for (int hf = 0; hf < 2; ++hf) {
+                float o[32];
+                tmem_ld32(tO + lane_addr + hf * 32, o);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    opk[hf * 16 + i] = pack_bf16x2(o[2 * i] * p.q_scale, o[2 * i + 1] * p.q_scale);
+            }
+            o_cs = cs;
+            o_rows = rows;
+            tc_fence_before();
+            named_sync(kBarChain, kChainThreads);
+            if (lead) mbar_arrive(&bars[B_PFREE0 + b]);
+            __syncwarp();
+        }
+        if (!fail && nchunks > 0) {
+            __nv_bfloat16* dst = gout + (o_cs * Hv + h) * kD + row;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&opk[i]);
+                if (2 * i < o_rows) dst[int64_t(2 * i) * Hv * kD] = pr.x;
+                if (2 * i + 1 < o_rows) dst[int64_t(2 * i + 1) * Hv * kD] = pr.y;
             }
         }
-        fence_proxy_async_smem();
-        sync_ok();
+        if (fail) *s_err = 1;
     }
 
-    // ---- final state ------------------------------------------------------------
-    if (ok && p.state_out) {
-        const size_t sb = (size_t(n) * Hv + h) * kD * kD;
-        for (int cb = 0; cb < 64; cb += 16) {
-            float z[16];
-            tmem_ld16(tZ + lane_addr + half * 64 + cb, z);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) p.state_out[sb + size_t(half * 64 + cb + i) * kD + row] = z[i];
-        }
-    }
-    if (!ok && tid == 0) {
-        atomicAdd(&g_tc_timeouts, 1);
-        // Let a TMA copy still in flight land before the CTA's shared memory
-        // goes away (bounded like every other wait).
-        if (tma_last_issued >= 0)
-            mbar_wait(&bars[tma_last_issued & 1], uint32_t((tma_last_issued >> 1) & 1), kWaitLimit);
-    }
+    // ---- teardown -----------------------------------------------------------------
     tc_fence_before();
+    __syncthreads();
+    if (*s_err && tid == 0) {
+        atomicAdd(&g_tc_timeouts, 1);
+        // let TMA copies still in flight land before shared memory goes away
+        for (int st = 0; st < 2; ++st) {
+            const int c = s_tma_last[st];
+            if (c >= 0) mbar_wait(&bars[B_RAW0 + st], uint32_t((c >> 1) & 1), kWaitLimit);
+        }
+    }
+    __syncwarp();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }

@@ -107,6 +107,43 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// Same with the A operand in TMEM: lane m holds row m, 32-bit column c holds
+// the bf16 pair (k = 2c in the low half, k = 2c + 1 in the high half); one
+// K = 16 step spans 8 columns.
+__device__ __forceinline__ void umma_f16_tmemA(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32).  bar.sync is the
+// .aligned form: all lanes of a warp must execute it together, so the warp is
+// reconverged first (elected-lane sections leave it diverged).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+    __syncwarp();
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads:
+// every thread gets the same answer, so a group can leave a loop together.
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    __syncwarp();
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(uint32_t(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // The mbarrier receives one arrival once all previously issued tcgen05.mma of
 // this thread have completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -167,6 +204,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     uint32_t r[16];
+    __syncwarp();
     GDN_TMEM_LD_X16(taddr, r);
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
@@ -174,6 +212,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
     uint32_t r[16];
+    __syncwarp();
 #pragma unroll
     for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(v[i]);
     GDN_TMEM_ST_X16(taddr, r);
