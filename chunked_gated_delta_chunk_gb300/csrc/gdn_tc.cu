@@ -72,7 +72,7 @@ constexpr uint32_t kOffA = kOffTb + 4 * 8192;            // A fp32 [64][65]
 constexpr uint32_t kOffT = kOffA + kC * kLdA * 4;        // T fp32 [64][65]
 constexpr uint32_t kOffTmp = kOffT + kC * kLdA * 4;      // inverse scratch, 1536 floats
 constexpr uint32_t kOffVec = kOffTmp + 1536 * 4;         // vectors
-constexpr uint32_t kVecFloats = 6 * kC + 2 * kC + 2;     // prep vectors + chain vectors
+constexpr uint32_t kVecFloats = 8 * kC + 2 * 2 * kC + 2 * kC + 2;   // prep, staging, chain
 constexpr uint32_t kOffBar = kOffVec + ((kVecFloats * 4 + 127) / 128) * 128;
 constexpr uint32_t kNumBars = 16;
 constexpr uint32_t kSmemBytes = kOffBar + kNumBars * 8 + 32 + 1024;
@@ -108,6 +108,15 @@ __device__ __forceinline__ uint32_t toff(int row, int col, uint32_t block_stride
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22; results
+// below the smallest normal flush to zero).  Every exponent here is <= 0, so
+// the values lie in (0, 1].
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ float bf16_round(float x) {
@@ -242,37 +251,63 @@ __device__ void block_inverse_64(const float* sA, float* sT, float* sTmp, int pt
     for (int idx = pt; idx < kC * kLdA; idx += kPrepThreads) sT[idx] = 0.f;
     named_sync(kBarPrep, kPrepThreads);
     {
-        const int o = pw * 8;             // 8 prep warps, one 8x8 block each
-        float* N2 = sTmp + pw * 192;
-        float* N4 = N2 + 64;
-        float* X = N4 + 64;
-        for (int e = lane; e < 64; e += 32) {
-            const int r = e >> 3, c = e & 7;
+        // 8 prep warps, one 8x8 diagonal block each.  Lane owns rows r and
+        // r + 4 of column c (r = lane >> 3, c = lane & 7); matrices of the
+        // block are exchanged through per-warp scratch in shared memory.
+        const int o = pw * 8;
+        const int r = lane >> 3, c = lane & 7;
+        float* W0 = sTmp + pw * 192;      // N^2, then N^4
+        float* W1 = W0 + 64;              // X = (I - N)(I + N^2)
+        float nrow[2][8], ncol[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            nrow[0][m] = sA[(o + r) * kLdA + o + m];
+            nrow[1][m] = sA[(o + r + 4) * kLdA + o + m];
+            ncol[m] = sA[(o + m) * kLdA + o + c];
+        }
+        float n2[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
             float acc = 0.f;
 #pragma unroll
-            for (int m = 0; m < 8; ++m)
-                acc = fmaf(sA[(o + r) * kLdA + o + m], sA[(o + m) * kLdA + o + c], acc);
-            N2[e] = acc;
+            for (int m = 0; m < 8; ++m) acc = fmaf(nrow[h2][m], ncol[m], acc);
+            n2[h2] = acc;
+            W0[(r + 4 * h2) * 8 + c] = acc;
         }
         __syncwarp();
-        for (int e = lane; e < 64; e += 32) {
-            const int r = e >> 3, c = e & 7;
-            float acc = 0.f, nn2 = 0.f;
+        float n2row[2][8], n2col[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            n2row[0][m] = W0[r * 8 + m];
+            n2row[1][m] = W0[(r + 4) * 8 + m];
+            n2col[m] = W0[m * 8 + c];
+        }
+        float n4[2], x[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            float a4 = 0.f, nn2 = 0.f;
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
-                acc = fmaf(N2[r * 8 + m], N2[m * 8 + c], acc);
-                nn2 = fmaf(sA[(o + r) * kLdA + o + m], N2[m * 8 + c], nn2);
+                a4 = fmaf(n2row[h2][m], n2col[m], a4);
+                nn2 = fmaf(nrow[h2][m], n2col[m], nn2);
             }
-            N4[e] = acc;
-            X[e] = (r == c ? 1.f : 0.f) - sA[(o + r) * kLdA + o + c] + N2[e] - nn2;
+            n4[h2] = a4;
+            // X = (I - N)(I + N^2) = I - N + N^2 - N N^2
+            x[h2] = ((r + 4 * h2) == c ? 1.f : 0.f) - sA[(o + r + 4 * h2) * kLdA + o + c] + n2[h2] - nn2;
         }
         __syncwarp();
-        for (int e = lane; e < 64; e += 32) {
-            const int r = e >> 3, c = e & 7;
-            float acc = X[e];
 #pragma unroll
-            for (int m = 0; m < 8; ++m) acc = fmaf(X[r * 8 + m], N4[m * 8 + c], acc);
-            sT[(o + r) * kLdA + o + c] = acc;
+        for (int h2 = 0; h2 < 2; ++h2) {
+            W0[(r + 4 * h2) * 8 + c] = n4[h2];
+            W1[(r + 4 * h2) * 8 + c] = x[h2];
+        }
+        __syncwarp();
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            float acc = x[h2];                 // X (I + N^4)
+#pragma unroll
+            for (int m = 0; m < 8; ++m) acc = fmaf(W1[(r + 4 * h2) * 8 + m], W0[m * 8 + c], acc);
+            sT[(o + r + 4 * h2) * kLdA + o + c] = acc;
         }
     }
     named_sync(kBarPrep, kPrepThreads);
@@ -298,7 +333,11 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     float* vRk = vBeta + kC;                                // prep: 1/|k_i|
     float* vRq = vRk + kC;                                  // prep: 1/|q_t|
     float* vEnd = vRq + kC;                                 // prep: exp(min(gamma_S - gamma_i, 0)) r_k,i
-    float* cE = vEnd + kC;                                  // chain: [2][64] end weights
+    float* vFb = vEnd + kC;                                 // prep: beta_i (column factor)
+    float* vFbg = vFb + kC;                                 // prep: beta_i Gamma_i r_k,i
+    float* sG = vFbg + kC;                                  // prep: [2][64] g staging (cp.async)
+    float* sB = sG + 2 * kC;                                // prep: [2][64] beta staging
+    float* cE = sB + 2 * kC;                                // chain: [2][64] end weights
     float* cGS = cE + 2 * kC;                               // chain: [2] exp(gamma_S)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + kNumBars * 8);
@@ -383,14 +422,24 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         const uint32_t id_gram = idesc_bf16(128, 64, 0, 0);
         const uint32_t id_uw = idesc_bf16(128, 64, 1, 0);   // A MN-major, B K-major
         const uint64_t dTb = smem_desc(smem_u32(sm + kOffTb), 16, 1024, kSwizzle128B);
-        float g_next = 0.f, b_next = 0.f;
-        if (pt < kC && nchunks > 0) {
-            const int64_t t = chunk_start(0) + pt;
-            if (pt < p.chunk && t < t1) {
-                g_next = p.g[t * Hv + h];
-                b_next = p.beta[t * Hv + h];
+        // g and beta of chunk c arrive in staging slot c & 1 by cp.async,
+        // issued one chunk ahead (rows past the sequence are zero).
+        auto stage_gb = [&](int c) {
+            if (pt < kC) {
+                const int64_t t = chunk_start(c) + pt;
+                float* dg = sG + (c & 1) * kC + pt;
+                float* db = sB + (c & 1) * kC + pt;
+                if (pt < p.chunk && t < t1) {
+                    cp_async4(dg, p.g + t * Hv + h);
+                    cp_async4(db, p.beta + t * Hv + h);
+                } else {
+                    *dg = 0.f;
+                    *db = 0.f;
+                }
             }
-        }
+            cp_async_commit();
+        };
+        if (nchunks > 0) stage_gb(0);
         bool fail = false;
         for (int c = 0; c < nchunks; ++c) {
             const int b = c & 1;
@@ -398,17 +447,14 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             uint8_t* vv = kq + kStageKQ;
             const int64_t cs = chunk_start(c);
             const int rows = int(t1 - cs < p.chunk ? t1 - cs : p.chunk);
-            // ---- g, beta of this chunk; prefetch the next chunk's ---------------
+            // ---- g, beta of this chunk (staged); stage the next chunk's ----------
+            cp_async_wait_all();
+            named_sync(kBarPrep, kPrepThreads);
             if (pt < kC) {
-                vGam[pt] = g_next;
-                vBeta[pt] = b_next;
-                g_next = b_next = 0.f;
-                const int64_t t = cs + p.chunk + pt;
-                if (c + 1 < nchunks && pt < p.chunk && t < t1) {
-                    g_next = p.g[t * Hv + h];
-                    b_next = p.beta[t * Hv + h];
-                }
+                vGam[pt] = sG[b * kC + pt];
+                vBeta[pt] = sB[b * kC + pt];
             }
+            if (c + 1 < nchunks) stage_gb(c + 1);
             // ---- raw tiles ----------------------------------------------------
             bool lf = false;
             if (tma_ok(c)) {
@@ -437,7 +483,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             if (named_sync_or(kBarPrep, kPrepThreads, lf)) { fail = true; break; }
             tc_fence_after();
             // ---- Gram MMA; cumsum (log2 domain); row norms ----------------------
-            if (tid == 0) {
+            if (tid == 32) {
                 const uint64_t d0 = smem_desc(smem_u32(kq), 16, 1024, kSwizzle128B);
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
@@ -479,8 +525,11 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             named_sync(kBarPrep, kPrepThreads);
             if (pt < kC) {
                 const float gm = vGam[pt];
-                vEg[pt] = exp2f(gm);
+                const float eg = exp2f(gm);
+                vEg[pt] = eg;
                 vEnd[pt] = pt < rows ? exp2f(fminf(vGam[rows - 1] - gm, 0.f)) * vRk[pt] : 0.f;
+                vFb[pt] = vBeta[pt];
+                vFbg[pt] = vBeta[pt] * eg * vRk[pt];
             }
             // ---- masks and decays on the Gram matrices --------------------------
             if (tid == 0) {
@@ -500,7 +549,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     for (int q = 0; q < 32; ++q) {
                         const int j = phalf * 32 + q;
                         float a = 0.f;
-                        if (i < rows && j < i) a = bi * exp2f(fminf(gi - vGam[j], 0.f)) * vRk[j] * v[q];
+                        if (i < rows && j < i) a = bi * fast_exp2(fminf(gi - vGam[j], 0.f)) * vRk[j] * v[q];
                         sA[i * kLdA + j] = a;
                     }
                 } else {
@@ -509,7 +558,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
                         const int j = phalf * 32 + q;
-                        v[q] = (t < rows && j <= t) ? rt * exp2f(fminf(gt - vGam[j], 0.f)) * vRk[j] * v[q] : 0.f;
+                        v[q] = (t < rows && j <= t) ? rt * fast_exp2(fminf(gt - vGam[j], 0.f)) * vRk[j] * v[q] : 0.f;
                     }
                     uint8_t* phi = sm + kOffP + uint32_t(b * 2) * 8192u;
 #pragma unroll
@@ -524,13 +573,16 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             block_inverse_64(sA, sT, sTmp, pt);
             for (int idx = pt; idx < kC * 8; idx += kPrepThreads) {
                 const int t = idx >> 3, i0 = (idx & 7) * 8;
-                float a[8], bg[8];
+                float a[8], bg[8], fb[8], fbg[8];
+                *reinterpret_cast<float4*>(fb) = *reinterpret_cast<const float4*>(vFb + i0);
+                *reinterpret_cast<float4*>(fb + 4) = *reinterpret_cast<const float4*>(vFb + i0 + 4);
+                *reinterpret_cast<float4*>(fbg) = *reinterpret_cast<const float4*>(vFbg + i0);
+                *reinterpret_cast<float4*>(fbg + 4) = *reinterpret_cast<const float4*>(vFbg + i0 + 4);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const int i = i0 + q;
-                    const float tv = sT[t * kLdA + i];
-                    a[q] = tv * vBeta[i];
-                    bg[q] = a[q] * vEg[i] * vRk[i];
+                    const float tv = sT[t * kLdA + i0 + q];
+                    a[q] = tv * fb[q];
+                    bg[q] = tv * fbg[q];
                 }
                 const uint32_t o = toff(t, i0, 8192);
                 store_split8(sm + kOffTb + o, sm + kOffTb + 8192 + o, a);
@@ -556,23 +608,9 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                                      dTb + uint64_t((16384 + part * 8192 + s * 32) >> 4), id_uw, part > 0 || s > 0);
                         }
                     umma_commit(&bars[B_W]);
-                    lf = !wait(B_W, uint32_t(c & 1));
-                    if (c >= 1) lf = lf || !wait(B_WTFREE, uint32_t((c - 1) & 1));
                 }
             }
-            __syncwarp();
-            // ---- -W^T to shared; scaled Q rows in place; chain scalars ---------
-            if (named_sync_or(kBarPrep, kPrepThreads, lf)) { fail = true; break; }
-            tc_fence_after();
-            {
-                float v[32];
-                tmem_ld32(tGW + lane_addr + phalf * 32, v);
-#pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] = -v[q];
-#pragma unroll
-                for (int q = 0; q < 32; q += 8)
-                    store_chunk8(sm + kOffWt + toff(row, phalf * 32 + q, 16384), v + q);
-            }
+            // ---- while U0/W run: scaled Q rows in place; chain scalars ----------
             for (int idx = pt; idx < kC * 16; idx += kPrepThreads) {
                 const int r = idx >> 4, cc = (idx & 15) * 8;
                 uint8_t* ptr = kq + 8192 + toff(r, cc, 16384);
@@ -585,7 +623,22 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             }
             if (pt < kC) cE[b * kC + pt] = vEnd[pt];
             if (pt == 0) cGS[b] = vEg[rows - 1];
-            __syncwarp();
+            if (tid == 0 && !lf) {
+                lf = !wait(B_W, uint32_t(c & 1));
+                if (c >= 1) lf = lf || !wait(B_WTFREE, uint32_t((c - 1) & 1));
+            }
+            // ---- -W^T to shared ------------------------------------------------
+            if (named_sync_or(kBarPrep, kPrepThreads, lf)) { fail = true; break; }
+            tc_fence_after();
+            {
+                float v[32];
+                tmem_ld32(tGW + lane_addr + phalf * 32, v);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] = -v[q];
+#pragma unroll
+                for (int q = 0; q < 32; q += 8)
+                    store_chunk8(sm + kOffWt + toff(row, phalf * 32 + q, 16384), v + q);
+            }
             fence_proxy_async_smem();
             tc_fence_before();
             named_sync(kBarPrep, kPrepThreads);
