@@ -52,10 +52,46 @@ int check_common(const gdn_prefill_desc* d) {
     return GDN_OK;
 }
 
-size_t workspace_needed(const gdn_prefill_desc* d) {
+size_t conv_workspace(const gdn_prefill_desc* d) {
     if (d->conv_x == nullptr || d->T_total <= 0) return 0;
     const size_t bytes = size_t(d->T_total) * size_t(conv_channels(d)) * elem_size(d->dtype);
     return (bytes + 255) & ~size_t(255);
+}
+
+constexpr int kSMs = 152;   // GB300: 2 dies x 76 SMs
+
+// Chunks per segment of the segment-parallel scan, or 0 for one pass.  The
+// scan costs about two passes over a segment (maps, then outputs), so it pays
+// from three segments per sequence; segments are sized so that the first
+// phase (one full segment plus two maps per later segment, per value head and
+// sequence) fills the GPU once.
+int segment_chunks(const gdn_prefill_desc* d) {
+    if (d->dtype != GDN_BF16 || d->dk != 128 || d->dv != 128) return 0;   // tensor-core path only
+    if (d->T_total <= 0 || d->B <= 0 || d->segment_chunks < 0) return 0;
+    const int64_t chunks = (d->T_total + d->chunk - 1) / d->chunk;
+    if (d->segment_chunks > 0) return d->segment_chunks < chunks ? d->segment_chunks : 0;
+    const int64_t units = int64_t(d->Hv) * d->B;
+    const int64_t nseg = (kSMs / units + 1) / 2;
+    if (nseg < 3) return 0;
+    const int64_t per_seq = (chunks + d->B - 1) / d->B;
+    const int64_t len = (per_seq + nseg - 1) / nseg;
+    return len >= 2 ? int(len) : 0;
+}
+
+int64_t segment_slots(const gdn_prefill_desc* d, int seg_chunks) {
+    const int64_t seg_tokens = int64_t(seg_chunks) * d->chunk;
+    return d->T_total / seg_tokens + d->B + 1;
+}
+
+size_t segment_workspace(const gdn_prefill_desc* d, int seg_chunks) {
+    if (seg_chunks <= 0) return 0;
+    const size_t bytes = size_t(d->Hv) * size_t(segment_slots(d, seg_chunks)) * 3 * size_t(d->dk) *
+                         size_t(d->dv) * sizeof(float);
+    return (bytes + 255) & ~size_t(255);
+}
+
+size_t workspace_needed(const gdn_prefill_desc* d) {
+    return conv_workspace(d) + segment_workspace(d, segment_chunks(d));
 }
 
 int check_prefill(const gdn_prefill_desc* d) {
@@ -65,7 +101,7 @@ int check_prefill(const gdn_prefill_desc* d) {
     if (d->cu_seqlens == nullptr) return GDN_ERR_INVALID_ARG;
     if (d->conv_x != nullptr) {
         if (d->T_total < 0) return GDN_ERR_INVALID_ARG;
-        const size_t need = workspace_needed(d);
+        const size_t need = conv_workspace(d);
         if (need > 0) {
             if (d->workspace == nullptr || d->workspace_bytes < need) return GDN_ERR_WORKSPACE;
             if ((reinterpret_cast<uintptr_t>(d->workspace) & 255u) != 0) return GDN_ERR_WORKSPACE;
@@ -98,6 +134,7 @@ size_t gdn_workspace_bytes(const gdn_prefill_desc* d) {
     if (d->B < 0 || d->Hk <= 0 || d->Hv <= 0 || d->Hv % d->Hk != 0) return size_t(-1);
     if (!head_dim_ok(d->dk) || !head_dim_ok(d->dv)) return size_t(-1);
     if (d->conv_x != nullptr && d->T_total < 0) return size_t(-1);
+    if (d->chunk < 1 || d->chunk > gdn::kMaxChunk) return size_t(-1);
     return workspace_needed(d);
 }
 
@@ -124,6 +161,19 @@ int gdn_prefill_ex(const gdn_prefill_desc* d, gdn_stream_t stream) {
     p.l2norm = d->use_qk_l2norm;
     p.eps = d->l2_eps;
     p.q_scale = d->q_scale;
+    {
+        // segment-parallel scan when chosen and the workspace holds its maps
+        const int sc = segment_chunks(d);
+        const size_t conv_bytes = conv_workspace(d);
+        if (sc > 0 && d->workspace != nullptr &&
+            d->workspace_bytes >= conv_bytes + segment_workspace(d, sc)) {
+            const int64_t seg_tokens = int64_t(sc) * d->chunk;
+            p.seg_chunks = sc;
+            p.seg_ws = reinterpret_cast<float*>(static_cast<char*>(d->workspace) + conv_bytes);
+            p.seg_slots = segment_slots(d, sc);
+            p.seg_max = int((d->T_total + seg_tokens - 1) / seg_tokens);
+        }
+    }
 
     if (d->conv_x != nullptr) {
         const int64_t C = conv_channels(d);
@@ -245,7 +295,7 @@ int gdn_prefill_plan(const gdn_prefill_desc* d, const char** names, int max_name
     const int st = check_prefill(d);
     if (st != GDN_OK) return -st;
     if (d->B == 0) return 0;
-    const char* plan[3];
+    const char* plan[5];
     int n = 0;
     gdn::ChunkParams p{};
     p.Hk = d->Hk;
@@ -254,7 +304,16 @@ int gdn_prefill_plan(const gdn_prefill_desc* d, const char** names, int max_name
     p.dv = d->dv;
     p.chunk = d->chunk;
     if (d->conv_x != nullptr && d->T_total > 0) plan[n++] = "conv_kernel";
-    plan[n++] = gdn::tc_supported(p, d->dtype) ? gdn::kTcKernelName : "chunk_simt_kernel";
+    const bool tc = gdn::tc_supported(p, d->dtype);
+    plan[n++] = tc ? gdn::kTcKernelName : "chunk_simt_kernel";
+    const int sc = tc ? segment_chunks(d) : 0;
+    if (sc > 0 && d->workspace != nullptr &&
+        d->workspace_bytes >= conv_workspace(d) + segment_workspace(d, sc)) {
+        const int64_t seg_tokens = int64_t(sc) * d->chunk;
+        const int64_t seg_max = (d->T_total + seg_tokens - 1) / seg_tokens;
+        if (seg_max >= 3) plan[n++] = "seg_combine_kernel";
+        if (seg_max >= 2) plan[n++] = gdn::kTcKernelName;
+    }
     if (d->conv_x != nullptr && d->conv_state_out != nullptr) plan[n++] = "conv_state_kernel";
     for (int i = 0; i < n && i < max_names; ++i)
         if (names != nullptr) names[i] = plan[i];

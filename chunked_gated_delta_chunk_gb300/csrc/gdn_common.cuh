@@ -32,7 +32,24 @@ struct ChunkParams {
     int l2norm;
     float eps;
     float q_scale;
+    // Segment-parallel scan (tensor-core path only).  seg_phase 0: one pass
+    // over every sequence.  Phase 1: segment 0 of each sequence in full,
+    // every later segment s twice, from a zero state (offset B_s) and from
+    // the identity with V = 0 (transition M_s).  Phase 2: every segment
+    // s >= 1 in full from its start state S_s.  seg_ws holds, per value head
+    // and segment slot, three [dk, dv] fp32 matrices B, M, S; the slot of
+    // (sequence n, segment s) is cu[n] / (seg_chunks * chunk) + n + s.
+    int seg_chunks;
+    int seg_phase;
+    float* seg_ws;
+    int64_t seg_slots;       // slots per value head
+    int seg_max;             // most segments any sequence can have (grid size)
 };
+
+// Segment slot of (sequence n, segment s).
+__host__ __device__ inline int64_t seg_slot(int64_t seq_start, int n, int s, int64_t seg_tokens) {
+    return seq_start / seg_tokens + n + s;
+}
 
 struct ConvParams {
     const void* x;           // [T, C]
@@ -67,6 +84,7 @@ struct StepParams {
 
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_chunk_simt(const ChunkParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_seg_combine(const ChunkParams& p, cudaStream_t s);
 cudaError_t launch_conv(const ConvParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_conv_state(const ConvParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_step(const StepParams& p, int dtype, cudaStream_t s);

@@ -60,6 +60,7 @@ constexpr uint32_t kBarPrep = 1, kBarChain = 2;
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr int kLdA = kC + 1;
 constexpr float kLog2e = 1.4426950408889634f;
+enum : int { kModeFull = 0, kModeOffset = 1, kModeTransition = 2 };
 
 // Shared-memory map (bytes from the 1024-aligned base).
 constexpr uint32_t kStageKQ = 32768;   // [K b0 | Q b0 | K b1 | Q b1], 8 KB each
@@ -358,8 +359,46 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     int64_t t0 = p.cu[n], t1 = p.cu[n + 1];
     t0 = t0 < 0 ? 0 : (t0 > t_end_all ? t_end_all : t0);
     t1 = t1 < t0 ? t0 : (t1 > t_end_all ? t_end_all : t1);
-    const int nchunks = int((t1 - t0 + p.chunk - 1) / p.chunk);
+    const int seq_chunks = int((t1 - t0 + p.chunk - 1) / p.chunk);
     const size_t sbase = (size_t(n) * Hv + h) * kD * kD;
+
+    // ---- which part of the sequence this CTA runs, and in which mode ------------
+    int seg = 0, mode = kModeFull;
+    if (p.seg_phase == 1 && blockIdx.z > 0) {
+        seg = int(blockIdx.z + 1) / 2;
+        mode = (blockIdx.z & 1) ? kModeOffset : kModeTransition;
+    } else if (p.seg_phase == 2) {
+        seg = int(blockIdx.z) + 1;
+    }
+    const int seg_len = p.seg_phase ? p.seg_chunks : seq_chunks;
+    const int c_begin = seg * seg_len;
+    const int c_end = p.seg_phase ? min(c_begin + seg_len, seq_chunks) : seq_chunks;
+    if (c_begin >= c_end && !(seg == 0 && mode == kModeFull)) return;   // no such segment
+    const int nchunks = c_end > c_begin ? c_end - c_begin : 0;
+    t0 += int64_t(c_begin) * p.chunk;                   // first token of this CTA's part
+    const bool last_seg = c_end >= seq_chunks;
+    const bool write_out = mode == kModeFull;
+    float* slot = nullptr;                              // B, M, S of this segment
+    float* next_slot = nullptr;                         // of the next segment
+    if (p.seg_phase) {
+        const int64_t seg_tokens = int64_t(p.seg_chunks) * p.chunk;
+        const int64_t sl = seg_slot(p.cu[n], n, seg, seg_tokens);
+        slot = p.seg_ws + (size_t(h) * p.seg_slots + sl) * 3 * kD * kD;
+        next_slot = slot + 3 * kD * kD;
+    }
+    // incoming state: state_in (segment 0), S_s (later segments in full), zero
+    // (offset pass) or the identity (transition pass)
+    const float* init_src = seg == 0 ? (p.state_in ? p.state_in + sbase : nullptr)
+                                     : (mode == kModeFull ? slot + 2 * kD * kD : nullptr);
+    const bool init_identity = mode == kModeTransition;
+    // final state: state_out (last segment), S_1 (segment 0 of phase 1), B_s / M_s
+    float* final_dst = nullptr;
+    if (mode == kModeFull) {
+        if (last_seg) final_dst = p.state_out ? p.state_out + sbase : nullptr;
+        else if (p.seg_phase == 1) final_dst = next_slot + 2 * kD * kD;
+    } else {
+        final_dst = slot + (mode == kModeOffset ? 0 : kD * kD);
+    }
 
     if (tid == 0) {
         for (int i = 0; i < int(kNumBars); ++i) mbar_init(&bars[i], 1);
@@ -601,9 +640,10 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     for (int part = 0; part < 2; ++part)
 #pragma unroll
                         for (int s = 0; s < 4; ++s) {
-                            // U0^T = V^T Tb^T ;  W^T = K^T Tbg^T
-                            umma_f16(tX, dV + uint64_t(s * 2048 >> 4), dTb + uint64_t((part * 8192 + s * 32) >> 4),
-                                     id_uw, part > 0 || s > 0);
+                            // U0^T = V^T Tb^T (V = 0 in the transition pass) ;  W^T = K^T Tbg^T
+                            if (mode != kModeTransition)
+                                umma_f16(tX, dV + uint64_t(s * 2048 >> 4),
+                                         dTb + uint64_t((part * 8192 + s * 32) >> 4), id_uw, part > 0 || s > 0);
                             umma_f16(tGW, dK + uint64_t(s * 2048 >> 4),
                                      dTb + uint64_t((16384 + part * 8192 + s * 32) >> 4), id_uw, part > 0 || s > 0);
                         }
@@ -664,10 +704,9 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         int64_t o_cs = 0;
         int o_rows = 0;
         if (nchunks == 0) {
-            if (p.state_out)
+            if (final_dst)
                 for (int d = 0; d < kD; ++d)
-                    p.state_out[sbase + size_t(d) * kD + row] =
-                        p.state_in ? p.state_in[sbase + size_t(d) * kD + row] : 0.f;
+                    final_dst[size_t(d) * kD + row] = init_src ? init_src[size_t(d) * kD + row] : 0.f;
         } else {
             // ---- incoming state: Zb = bf16(Z), Z <- exp(gamma_S(0)) Z -----------
             bool lf = lead && !wait(B_READY0, 0);
@@ -677,8 +716,10 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             for (int hf = 0; hf < 2; ++hf) {
                 float z[64];
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    z[i] = p.state_in ? p.state_in[sbase + size_t(hf * 64 + i) * kD + row] : 0.f;
+                for (int i = 0; i < 64; ++i) {
+                    const int d = hf * 64 + i;
+                    z[i] = init_src ? init_src[size_t(d) * kD + row] : (init_identity && d == row ? 1.f : 0.f);
+                }
                 uint32_t zb[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) zb[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
@@ -708,7 +749,8 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     tc_fence_after();
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
-                        umma_f16_tmemA(tX, tZb + s * 8, dWt + uint64_t(s * 2048 >> 4), id_x, 1);
+                        umma_f16_tmemA(tX, tZb + s * 8, dWt + uint64_t(s * 2048 >> 4), id_x,
+                                       mode != kModeTransition || s > 0);
                     umma_commit(&bars[B_X]);
                     const uint64_t dQ = smem_desc(smem_u32(kq + 8192), 16, 1024, kSwizzle128B);
 #pragma unroll
@@ -811,9 +853,9 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     tmem_st16(tZ + lane_addr + hf * 64 + 16, z + 16);
                     tmem_st16(tZ + lane_addr + hf * 64 + 32, z + 32);
                     tmem_st16(tZ + lane_addr + hf * 64 + 48, z + 48);
-                } else if (p.state_out) {
+                } else if (final_dst) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) p.state_out[sbase + size_t(hf * 64 + i) * kD + row] = z[i];
+                    for (int i = 0; i < 64; ++i) final_dst[size_t(hf * 64 + i) * kD + row] = z[i];
                 }
             }
             tmem_st_wait();
@@ -830,7 +872,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     opk[hf * 16 + i] = pack_bf16x2(o[2 * i] * p.q_scale, o[2 * i + 1] * p.q_scale);
             }
             o_cs = cs;
-            o_rows = rows;
+            o_rows = write_out ? rows : 0;
             tc_fence_before();
             named_sync(kBarChain, kChainThreads);
             if (lead) mbar_arrive(&bars[B_PFREE0 + b]);
@@ -862,6 +904,59 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     __syncwarp();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Phase 2 of the segment scan: S_{s+1} = M_s S_s + B_s for s = 1 .. nseg - 2,
+// per (value head, sequence), in fp32.  Columns of the state evolve
+// independently, so each CTA owns 8 of them and keeps its slab of S in
+// shared memory from one segment to the next.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineCols = 8;
+
+__global__ void __launch_bounds__(kCombineThreads) seg_combine_kernel(const ChunkParams p) {
+    const int h = blockIdx.x, n = blockIdx.y, slab = blockIdx.z;
+    int64_t t_end_all = p.cu[p.B];
+    if (t_end_all > p.t_cap) t_end_all = p.t_cap;
+    int64_t t0 = p.cu[n], t1 = p.cu[n + 1];
+    t0 = t0 < 0 ? 0 : (t0 > t_end_all ? t_end_all : t0);
+    t1 = t1 < t0 ? t0 : (t1 > t_end_all ? t_end_all : t1);
+    const int seq_chunks = int((t1 - t0 + p.chunk - 1) / p.chunk);
+    const int nseg = (seq_chunks + p.seg_chunks - 1) / p.seg_chunks;
+    if (nseg < 3) return;
+    const int64_t seg_tokens = int64_t(p.seg_chunks) * p.chunk;
+    const float* base = p.seg_ws + (size_t(h) * p.seg_slots + seg_slot(p.cu[n], n, 0, seg_tokens)) * 3 * kD * kD;
+    float* wbase = const_cast<float*>(base);
+    __shared__ float sS[kD][kCombineCols];
+    const int tid = threadIdx.x, r = tid >> 1, cj = (tid & 1) * 4, c0 = slab * kCombineCols + cj;
+    for (int idx = tid; idx < kD * kCombineCols; idx += kCombineThreads) {
+        const int k = idx / kCombineCols, j = idx % kCombineCols;
+        sS[k][j] = base[size_t(1) * 3 * kD * kD + 2 * kD * kD + size_t(k) * kD + slab * kCombineCols + j];
+    }
+    __syncthreads();
+    for (int s = 1; s + 1 < nseg; ++s) {
+        const float* Bs = base + size_t(s) * 3 * kD * kD;
+        const float* Ms = Bs + kD * kD;
+        float4 acc = *reinterpret_cast<const float4*>(Bs + size_t(r) * kD + c0);
+#pragma unroll 4
+        for (int k = 0; k < kD; k += 4) {
+            const float4 m = *reinterpret_cast<const float4*>(Ms + size_t(r) * kD + k);
+            const float mk[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                acc.x = fmaf(mk[kk], sS[k + kk][cj + 0], acc.x);
+                acc.y = fmaf(mk[kk], sS[k + kk][cj + 1], acc.y);
+                acc.z = fmaf(mk[kk], sS[k + kk][cj + 2], acc.z);
+                acc.w = fmaf(mk[kk], sS[k + kk][cj + 3], acc.w);
+            }
+        }
+        __syncthreads();
+        sS[r][cj + 0] = acc.x;
+        sS[r][cj + 1] = acc.y;
+        sS[r][cj + 2] = acc.z;
+        sS[r][cj + 3] = acc.w;
+        *reinterpret_cast<float4*>(wbase + size_t(s + 1) * 3 * kD * kD + 2 * kD * kD + size_t(r) * kD + c0) = acc;
+        __syncthreads();
+    }
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -914,7 +1009,22 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemBytes));
     if (e != cudaSuccess) return e;
-    chunk_tc_kernel<<<dim3(p.Hv, p.B), kThreads, kSmemBytes, s>>>(p, maps);
+    if (p.seg_chunks <= 0 || p.seg_max < 2) {
+        ChunkParams q = p;
+        q.seg_phase = 0;
+        chunk_tc_kernel<<<dim3(p.Hv, p.B, 1), kThreads, kSmemBytes, s>>>(q, maps);
+        return cudaGetLastError();
+    }
+    ChunkParams q = p;
+    q.seg_phase = 1;                                  // segment 0 in full; B_s and M_s
+    chunk_tc_kernel<<<dim3(p.Hv, p.B, 2 * p.seg_max - 1), kThreads, kSmemBytes, s>>>(q, maps);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (p.seg_max >= 3) {                             // S_{s+1} = M_s S_s + B_s
+        seg_combine_kernel<<<dim3(p.Hv, p.B, kD / kCombineCols), kCombineThreads, 0, s>>>(q);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    q.seg_phase = 2;                                  // segments >= 1 in full
+    chunk_tc_kernel<<<dim3(p.Hv, p.B, p.seg_max - 1), kThreads, kSmemBytes, s>>>(q, maps);
     return cudaGetLastError();
 }
 

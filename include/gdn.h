@@ -114,6 +114,14 @@ typedef struct gdn_prefill_desc {
 
     void* workspace;         /* device scratch, >= gdn_workspace_bytes(desc), 256-aligned */
     size_t workspace_bytes;
+
+    /* Segment-parallel chunk scan (bf16, dk = dv = 128, T_total known, and a
+     * workspace): each sequence is cut into segments of this many chunks that
+     * run in parallel (every segment's affine map from a zero state and from
+     * the identity, a short fp32 combine of the maps, then every segment from
+     * its true start state).  0 = chosen from the shape (on only when it
+     * gives at least three segments per sequence on 152 SMs), < 0 = off. */
+    int segment_chunks;
 } gdn_prefill_desc;
 
 /* Fill *d with the defaults listed above (all pointers NULL). */
@@ -137,10 +145,12 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* g, con
  * q_scale and workspace as described in gdn_prefill_desc. */
 int gdn_prefill_ex(const gdn_prefill_desc* d, gdn_stream_t stream);
 
-/* Device workspace gdn_prefill_ex needs for *d, in bytes (0 if none; it is
- * non-zero only with a short convolution).  Reads only dtype, B, Hk, Hv, dk,
- * dv, T_total and whether conv_x is set; returns (size_t)-1 when those are
- * invalid. */
+/* Device workspace gdn_prefill_ex needs for *d, in bytes (0 if none): the
+ * output of the short convolution, plus the per-segment maps of the
+ * segment-parallel scan when that is chosen.  Reads only dtype, B, Hk, Hv,
+ * dk, dv, chunk, T_total, segment_chunks and whether conv_x is set; returns
+ * (size_t)-1 when those are invalid.  A workspace too small for the segment
+ * maps (but enough for the convolution) runs the scan in one pass. */
 size_t gdn_workspace_bytes(const gdn_prefill_desc* d);
 
 /*

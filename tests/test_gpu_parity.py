@@ -233,3 +233,41 @@ def test_prefill_then_decode_equals_token_loop():
                           c2.state_out, 1, 2, 128, 128)
     res = {"out": torch.cat([c1.out.cpu(), c2.out.cpu(), out.cpu()]), "state_out": st.cpu()}
     compare(res, ref, TOL_BF16)
+
+
+# ---------------------------------------------------------------- segment scan
+@pytest.mark.parametrize("seg,lengths,chunk", [
+    (1, [300], 64), (2, [640], 64), (3, [64 * 7 + 5], 64), (4, [1, 200, 0, 900], 64),
+    (2, [333, 64 * 6], 32), (5, [4096], 64)])
+def test_segment_scan_matches_oracle(seg, lengths, chunk):
+    """The segment-parallel scan (maps of every segment from a zero state and
+    from the identity, fp32 combine, then every segment from its start
+    state) equals the token loop; segments end on full and partial chunks."""
+    p = inputs.make_problem(40 + seg, lengths, 2, 4, 128, 128, chunk=chunk)
+    call = runner.PrefillCall(p, segment_chunks=seg)
+    from chunked_gated_delta_chunk_gb300 import binding as B
+    plan = B.gdn_prefill_plan(call.desc)
+    assert plan.count("chunk_tc_kernel") == 2, plan
+    call.run()
+    torch.cuda.synchronize()
+    compare({k: v.cpu() for k, v in call.results().items()}, run_oracle(p), TOL_BF16)
+
+
+def test_segment_scan_with_conv_and_gqa():
+    p = inputs.make_problem(50, [700, 90], 2, 4, 128, 128, conv_kernel=4)
+    call = runner.PrefillCall(p, segment_chunks=3)
+    call.run()
+    torch.cuda.synchronize()
+    compare({k: v.cpu() for k, v in call.results().items()}, run_oracle(p), TOL_BF16)
+
+
+def test_segment_scan_off_equals_on_bits_of_segment_zero():
+    """Segment 0 runs the same pass with or without the scan, so its output
+    rows are bit-identical."""
+    p = inputs.make_problem(51, [1000], 1, 2, 128, 128)
+    a = runner.PrefillCall(p, segment_chunks=-1)
+    b = runner.PrefillCall(p, segment_chunks=4)
+    a.run()
+    b.run()
+    torch.cuda.synchronize()
+    assert torch.equal(a.out[:256], b.out[:256])
