@@ -58,7 +58,7 @@ constexpr uint32_t kPrepThreads = 256; // warps 0-3 and 8-11
 constexpr uint32_t kChainThreads = 128;
 constexpr uint32_t kBarPrep = 1, kBarChain = 2;
 constexpr uint32_t kWaitLimit = 1u << 20;
-constexpr int kLdA = kC + 1;
+constexpr int kLdA = kC + 4;         // fp32 row stride of A and T: 16-byte aligned rows
 constexpr float kLog2e = 1.4426950408889634f;
 enum : int { kModeFull = 0, kModeOffset = 1, kModeTransition = 2 };
 
@@ -69,14 +69,15 @@ constexpr uint32_t kStageBytes = kStageKQ + kStageV;
 constexpr uint32_t kOffWt = 2 * kStageBytes;             // -W^T bf16 [d][t] MN-major, 16 KB
 constexpr uint32_t kOffP = kOffWt + 16384;               // P [buf][hi|lo] bf16 [t][i], 4 x 8 KB
 constexpr uint32_t kOffTb = kOffP + 4 * 8192;            // Tb hi, Tb lo, Tbg hi, Tbg lo, 4 x 8 KB
-constexpr uint32_t kOffA = kOffTb + 4 * 8192;            // A fp32 [64][65]
-constexpr uint32_t kOffT = kOffA + kC * kLdA * 4;        // T fp32 [64][65]
+constexpr uint32_t kOffA = kOffTb + 4 * 8192;            // A fp32 [64][68]
+constexpr uint32_t kOffT = kOffA + kC * kLdA * 4;        // T fp32 [64][68]
 constexpr uint32_t kOffTmp = kOffT + kC * kLdA * 4;      // inverse scratch, 1536 floats
 constexpr uint32_t kOffVec = kOffTmp + 1536 * 4;         // vectors
 constexpr uint32_t kVecFloats = 8 * kC + 2 * 2 * kC + 2 * kC + 2;   // prep, staging, chain
 constexpr uint32_t kOffBar = kOffVec + ((kVecFloats * 4 + 127) / 128) * 128;
 constexpr uint32_t kNumBars = 16;
 constexpr uint32_t kSmemBytes = kOffBar + kNumBars * 8 + 32 + 1024;
+static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-block limit");
 
 // Barrier slots.
 enum : int {
@@ -194,6 +195,7 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
 // that the shared-memory loads overlap.
 template <int S, int RB, int CB>
 __device__ __forceinline__ void level_products(const float* sA, float* sT, float* sTmp, int pt) {
+    static_assert(CB == 1 || CB == 2, "column block of 1 or 2");
     constexpr int kPairs = kC / (2 * S), kTR = S / RB, kTC = S / CB;
     static_assert(kPairs * kTR * kTC == int(kPrepThreads), "one output block per prep thread");
     const int pr = pt / (kTR * kTC), rem = pt % (kTR * kTC);
@@ -205,17 +207,30 @@ __device__ __forceinline__ void level_products(const float* sA, float* sT, float
     for (int i = 0; i < RB; ++i)
 #pragma unroll
         for (int j = 0; j < CB; ++j) acc[i][j] = 0.f;
+    // tmp = A21 T11: rows of A21 read 4 at a time (16-byte aligned rows)
 #pragma unroll
-    for (int m = 0; m < S; ++m) {           // tmp = A21 T11
-        float a[RB], bb[CB];
-#pragma unroll
-        for (int i = 0; i < RB; ++i) a[i] = sA[(o + S + r0 + i) * kLdA + o + m];
-#pragma unroll
-        for (int j = 0; j < CB; ++j) bb[j] = sT[(o + m) * kLdA + o + c0 + j];
+    for (int m = 0; m < S; m += 4) {
+        float4 a[RB];
 #pragma unroll
         for (int i = 0; i < RB; ++i)
+            a[i] = *reinterpret_cast<const float4*>(sA + (o + S + r0 + i) * kLdA + o + m);
 #pragma unroll
-            for (int j = 0; j < CB; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+        for (int mm = 0; mm < 4; ++mm) {
+            float bb[CB];
+            if constexpr (CB == 2) {
+                const float2 t2 = *reinterpret_cast<const float2*>(sT + (o + m + mm) * kLdA + o + c0);
+                bb[0] = t2.x;
+                bb[1] = t2.y;
+            } else {
+                bb[0] = sT[(o + m + mm) * kLdA + o + c0];
+            }
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const float ai = mm == 0 ? a[i].x : mm == 1 ? a[i].y : mm == 2 ? a[i].z : a[i].w;
+#pragma unroll
+                for (int j = 0; j < CB; ++j) acc[i][j] = fmaf(ai, bb[j], acc[i][j]);
+            }
+        }
     }
 #pragma unroll
     for (int i = 0; i < RB; ++i)
@@ -225,17 +240,30 @@ __device__ __forceinline__ void level_products(const float* sA, float* sT, float
             acc[i][j] = 0.f;
         }
     named_sync(kBarPrep, kPrepThreads);
+    // T21 = -T22 tmp
 #pragma unroll
-    for (int m = 0; m < S; ++m) {           // T21 = -T22 tmp
-        float a[RB], bb[CB];
-#pragma unroll
-        for (int i = 0; i < RB; ++i) a[i] = sT[(o + S + r0 + i) * kLdA + o + S + m];
-#pragma unroll
-        for (int j = 0; j < CB; ++j) bb[j] = tmp[m * S + c0 + j];
+    for (int m = 0; m < S; m += 4) {
+        float4 a[RB];
 #pragma unroll
         for (int i = 0; i < RB; ++i)
+            a[i] = *reinterpret_cast<const float4*>(sT + (o + S + r0 + i) * kLdA + o + S + m);
 #pragma unroll
-            for (int j = 0; j < CB; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+        for (int mm = 0; mm < 4; ++mm) {
+            float bb[CB];
+            if constexpr (CB == 2) {
+                const float2 t2 = *reinterpret_cast<const float2*>(tmp + (m + mm) * S + c0);
+                bb[0] = t2.x;
+                bb[1] = t2.y;
+            } else {
+                bb[0] = tmp[(m + mm) * S + c0];
+            }
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const float ai = mm == 0 ? a[i].x : mm == 1 ? a[i].y : mm == 2 ? a[i].z : a[i].w;
+#pragma unroll
+                for (int j = 0; j < CB; ++j) acc[i][j] = fmaf(ai, bb[j], acc[i][j]);
+            }
+        }
     }
 #pragma unroll
     for (int i = 0; i < RB; ++i)
@@ -585,11 +613,16 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     const int i = row;
                     const float bi = vBeta[i] * vRk[i], gi = vGam[i];
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const int j = phalf * 32 + q;
-                        float a = 0.f;
-                        if (i < rows && j < i) a = bi * fast_exp2(fminf(gi - vGam[j], 0.f)) * vRk[j] * v[q];
-                        sA[i * kLdA + j] = a;
+                    for (int q = 0; q < 32; q += 4) {
+                        float a4[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int j = phalf * 32 + q + u;
+                            a4[u] = (i < rows && j < i) ? bi * fast_exp2(fminf(gi - vGam[j], 0.f)) * vRk[j] * v[q + u] : 0.f;
+                        }
+                        // 16-byte stores: with the 68-float row stride the 8 lanes of
+                        // each store phase hit disjoint banks
+                        *reinterpret_cast<float4*>(sA + i * kLdA + phalf * 32 + q) = make_float4(a4[0], a4[1], a4[2], a4[3]);
                     }
                 } else {
                     const int t = row - kC;
@@ -617,11 +650,13 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 *reinterpret_cast<float4*>(fb + 4) = *reinterpret_cast<const float4*>(vFb + i0 + 4);
                 *reinterpret_cast<float4*>(fbg) = *reinterpret_cast<const float4*>(vFbg + i0);
                 *reinterpret_cast<float4*>(fbg + 4) = *reinterpret_cast<const float4*>(vFbg + i0 + 4);
+                float tr[8];
+                *reinterpret_cast<float4*>(tr) = *reinterpret_cast<const float4*>(sT + t * kLdA + i0);
+                *reinterpret_cast<float4*>(tr + 4) = *reinterpret_cast<const float4*>(sT + t * kLdA + i0 + 4);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const float tv = sT[t * kLdA + i0 + q];
-                    a[q] = tv * fb[q];
-                    bg[q] = tv * fbg[q];
+                    a[q] = tr[q] * fb[q];
+                    bg[q] = tr[q] * fbg[q];
                 }
                 const uint32_t o = toff(t, i0, 8192);
                 store_split8(sm + kOffTb + o, sm + kOffTb + 8192 + o, a);
