@@ -187,88 +187,92 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
     }
 }
 
-// One level of the 2x2 block inversion for diagonal blocks of size S:
-// for every pair of inverted blocks T11, T22 with the off-diagonal block A21
-// of I + A, the lower-left block of the inverse is -T22 A21 T11.  Each of the
-// 256 prep threads owns an RB x CB output block; the inner products run over
-// the full S (the upper triangles of T11 and T22 are zero), fully unrolled so
-// that the shared-memory loads overlap.
-template <int S, int RB, int CB>
-__device__ __forceinline__ void level_products(const float* sA, float* sT, float* sTmp, int pt) {
-    static_assert(CB == 1 || CB == 2, "column block of 1 or 2");
-    constexpr int kPairs = kC / (2 * S), kTR = S / RB, kTC = S / CB;
-    static_assert(kPairs * kTR * kTC == int(kPrepThreads), "one output block per prep thread");
-    const int pr = pt / (kTR * kTC), rem = pt % (kTR * kTC);
-    const int r0 = (rem / kTC) * RB, c0 = (rem % kTC) * CB;
+// x = hi + lo with hi, lo in tf32 (10 stored mantissa bits each, round to
+// nearest away); hi + lo carries about 22 bits of x.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+    const float r = x - __uint_as_float(hi);
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+
+// d += a b for one 16x8x8 tf32 warp MMA (fp32 accumulate).  Fragment
+// ownership, with g = lane / 4 and t = lane % 4: a0 (g, t), a1 (g+8, t),
+// a2 (g, t+4), a3 (g+8, t+4); b0 (k=t, n=g), b1 (k=t+4, n=g);
+// d0 (g, 2t), d1 (g, 2t+1), d2 (g+8, 2t), d3 (g+8, 2t+1).
+__device__ __forceinline__ void mma_tf32_16x8x8(float* d, const uint32_t* a, const uint32_t* b) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// d += a b to about fp32 accuracy from three tf32 MMAs (hi hi + hi lo + lo hi,
+// the lo lo term is below fp32 rounding); the cross terms gather in e.
+__device__ __forceinline__ void mma_3xtf32(float* d, float* e, const float* a, const float* b) {
+    uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) split_tf32(a[i], ah[i], al[i]);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) split_tf32(b[i], bh[i], bl[i]);
+    mma_tf32_16x8x8(e, al, bh);
+    mma_tf32_16x8x8(e, ah, bl);
+    mma_tf32_16x8x8(d, ah, bh);
+}
+
+// One level of the 2x2 block inversion for diagonal blocks of size S: for
+// every pair of inverted blocks T11, T22 with the off-diagonal block A21 of
+// I + A, the lower-left block of the inverse is T21 = -T22 (A21 T11).  Both
+// products run as 16x8 tiles on the warp MMA in split tf32, one tile per
+// prep warp (S = 8 uses the upper 8 rows of a tile).  Inner-product steps
+// that meet only the zero upper triangle of T11 or T22 are skipped.
+template <int S>
+__device__ __forceinline__ void level_products(const float* sA, float* sT, float* sTmp, int pw, int lane) {
+    constexpr int kPairs = kC / (2 * S);
+    constexpr bool kRows16 = S >= 16;
+    constexpr int kRT = kRows16 ? S / 16 : 1, kCT = S / 8;
+    constexpr int kTiles = kPairs * kRT * kCT;
+    constexpr int kLdT = S == 8 ? 24 : S + 8;        // conflict-free B-fragment rows
+    static_assert(kTiles <= int(kPrepThreads / 32), "one tile per prep warp");
+    static_assert(kPairs * S * kLdT <= 1536, "tmp fits the inverse scratch");
+    const int g = lane >> 2, t = lane & 3;
+    const bool active = pw < kTiles;
+    const int pr = pw / (kRT * kCT), rem = pw % (kRT * kCT);
+    const int r0 = (rem / kCT) * 16, n0 = (rem % kCT) * 8;
     const int o = pr * 2 * S;
-    float* tmp = sTmp + pr * S * S;
-    float acc[RB][CB];
+    float* tmp = sTmp + pr * S * kLdT;
+    if (active) {
+        // tmp = A21 T11 on rows r0.., columns n0..; T11[m][n] = 0 for m < n
+        float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < RB; ++i)
-#pragma unroll
-        for (int j = 0; j < CB; ++j) acc[i][j] = 0.f;
-    // tmp = A21 T11: rows of A21 read 4 at a time (16-byte aligned rows)
-#pragma unroll
-    for (int m = 0; m < S; m += 4) {
-        float4 a[RB];
-#pragma unroll
-        for (int i = 0; i < RB; ++i)
-            a[i] = *reinterpret_cast<const float4*>(sA + (o + S + r0 + i) * kLdA + o + m);
-#pragma unroll
-        for (int mm = 0; mm < 4; ++mm) {
-            float bb[CB];
-            if constexpr (CB == 2) {
-                const float2 t2 = *reinterpret_cast<const float2*>(sT + (o + m + mm) * kLdA + o + c0);
-                bb[0] = t2.x;
-                bb[1] = t2.y;
-            } else {
-                bb[0] = sT[(o + m + mm) * kLdA + o + c0];
-            }
-#pragma unroll
-            for (int i = 0; i < RB; ++i) {
-                const float ai = mm == 0 ? a[i].x : mm == 1 ? a[i].y : mm == 2 ? a[i].z : a[i].w;
-#pragma unroll
-                for (int j = 0; j < CB; ++j) acc[i][j] = fmaf(ai, bb[j], acc[i][j]);
-            }
+        for (int k0 = 0; k0 < S; k0 += 8) {
+            if (k0 < n0) continue;
+            const float* ar = sA + (o + S + r0 + g) * kLdA + o + k0 + t;
+            const float* br = sT + (o + k0 + t) * kLdA + o + n0 + g;
+            const float a[4] = {ar[0], kRows16 ? ar[8 * kLdA] : 0.f, ar[4], kRows16 ? ar[8 * kLdA + 4] : 0.f};
+            const float b[2] = {br[0], br[4 * kLdA]};
+            mma_3xtf32(d, e, a, b);
         }
+        *reinterpret_cast<float2*>(tmp + (r0 + g) * kLdT + n0 + 2 * t) = make_float2(d[0] + e[0], d[1] + e[1]);
+        if (kRows16)
+            *reinterpret_cast<float2*>(tmp + (r0 + g + 8) * kLdT + n0 + 2 * t) = make_float2(d[2] + e[2], d[3] + e[3]);
     }
-#pragma unroll
-    for (int i = 0; i < RB; ++i)
-#pragma unroll
-        for (int j = 0; j < CB; ++j) {
-            tmp[(r0 + i) * S + c0 + j] = acc[i][j];
-            acc[i][j] = 0.f;
-        }
     named_sync(kBarPrep, kPrepThreads);
-    // T21 = -T22 tmp
+    if (active) {
+        // T21 = -T22 tmp on rows r0.., columns n0..; T22[r][m] = 0 for m > r
+        float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int m = 0; m < S; m += 4) {
-        float4 a[RB];
-#pragma unroll
-        for (int i = 0; i < RB; ++i)
-            a[i] = *reinterpret_cast<const float4*>(sT + (o + S + r0 + i) * kLdA + o + S + m);
-#pragma unroll
-        for (int mm = 0; mm < 4; ++mm) {
-            float bb[CB];
-            if constexpr (CB == 2) {
-                const float2 t2 = *reinterpret_cast<const float2*>(tmp + (m + mm) * S + c0);
-                bb[0] = t2.x;
-                bb[1] = t2.y;
-            } else {
-                bb[0] = tmp[(m + mm) * S + c0];
-            }
-#pragma unroll
-            for (int i = 0; i < RB; ++i) {
-                const float ai = mm == 0 ? a[i].x : mm == 1 ? a[i].y : mm == 2 ? a[i].z : a[i].w;
-#pragma unroll
-                for (int j = 0; j < CB; ++j) acc[i][j] = fmaf(ai, bb[j], acc[i][j]);
-            }
+        for (int k0 = 0; k0 < S; k0 += 8) {
+            if (k0 >= r0 + 16) continue;
+            const float* ar = sT + (o + S + r0 + g) * kLdA + o + S + k0 + t;
+            const float* br = tmp + (k0 + t) * kLdT + n0 + g;
+            const float a[4] = {ar[0], kRows16 ? ar[8 * kLdA] : 0.f, ar[4], kRows16 ? ar[8 * kLdA + 4] : 0.f};
+            const float b[2] = {br[0], br[4 * kLdT]};
+            mma_3xtf32(d, e, a, b);
         }
+        float* out = sT + (o + S + r0 + g) * kLdA + o + n0 + 2 * t;
+        *reinterpret_cast<float2*>(out) = make_float2(-(d[0] + e[0]), -(d[1] + e[1]));
+        if (kRows16) *reinterpret_cast<float2*>(out + 8 * kLdA) = make_float2(-(d[2] + e[2]), -(d[3] + e[3]));
     }
-#pragma unroll
-    for (int i = 0; i < RB; ++i)
-#pragma unroll
-        for (int j = 0; j < CB; ++j) sT[(o + S + r0 + i) * kLdA + o + c0 + j] = -acc[i][j];
     named_sync(kBarPrep, kPrepThreads);
 }
 
@@ -277,8 +281,6 @@ __device__ __forceinline__ void level_products(const float* sA, float* sT, float
 // level by level.  Run by the 256 prep threads (index pt) with named barriers.
 __device__ void block_inverse_64(const float* sA, float* sT, float* sTmp, int pt) {
     const int pw = pt >> 5, lane = pt & 31;
-    for (int idx = pt; idx < kC * kLdA; idx += kPrepThreads) sT[idx] = 0.f;
-    named_sync(kBarPrep, kPrepThreads);
     {
         // 8 prep warps, one 8x8 diagonal block each.  Lane owns rows r and
         // r + 4 of column c (r = lane >> 3, c = lane & 7); matrices of the
@@ -340,9 +342,9 @@ __device__ void block_inverse_64(const float* sA, float* sT, float* sTmp, int pt
         }
     }
     named_sync(kBarPrep, kPrepThreads);
-    level_products<8, 1, 1>(sA, sT, sTmp, pt);
-    level_products<16, 1, 2>(sA, sT, sTmp, pt);
-    level_products<32, 2, 2>(sA, sT, sTmp, pt);
+    level_products<8>(sA, sT, sTmp, pw, lane);
+    level_products<16>(sA, sT, sTmp, pw, lane);
+    level_products<32>(sA, sT, sTmp, pw, lane);
 }
 
 struct Maps {
@@ -506,6 +508,10 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             }
             cp_async_commit();
         };
+        // T is lower triangular: its upper triangle is zeroed once here and
+        // never written again (each chunk writes the diagonal blocks whole
+        // and the blocks below them).
+        for (int idx = pt; idx < kC * kLdA; idx += kPrepThreads) sT[idx] = 0.f;
         if (nchunks > 0) stage_gb(0);
         bool fail = false;
         for (int c = 0; c < nchunks; ++c) {
