@@ -89,8 +89,9 @@ def kernel_source_hash():
 
 
 def recorded_traffic(kernel_name):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    """DRAM bytes (read + write) of the kernel's launches in one step, from
+    the committed ncu summary, if it was taken on the current kernel sources;
+    else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -99,7 +100,7 @@ def recorded_traffic(kernel_name):
     entry = d.get(kernel_name)
     if not entry or entry.get("source_hash") != kernel_source_hash():
         return None
-    return entry.get("dram_bytes_per_launch")
+    return entry.get("dram_bytes_per_step")
 
 
 class ClockSampler:
@@ -292,6 +293,10 @@ def main():
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    launches_per_call = len(B.gdn_prefill_plan(one.desc))
+    # the library brackets each of its launches with CUDA events on the
+    # launch stream: the per-kernel device time of the timed region
+    B.gdn_launch_timer_start(args.steps * launches_per_call)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
@@ -301,13 +306,18 @@ def main():
         stop.record(stream)
         barrier()
     ms_total = start.elapsed_time(stop)
+    B.gdn_launch_timer_stop()
+    records, dropped = B.gdn_launch_timer_read()
+    per_kernel = {}
+    for name, ms in records:
+        tot, n = per_kernel.get(name, (0.0, 0))
+        per_kernel[name] = (tot + ms, n + 1)
     if world > 1:
         t = torch.tensor([ms_total], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_total = float(t.item())
     ms_step = ms_total / args.steps
     tokens_per_s = world * p.T / (ms_step * 1e-3)
-    launches_per_call = len(B.gdn_prefill_plan(one.desc))
 
     # End to end through the C ABI with host buffers: pinned H2D of the step's
     # inputs, the call, D2H of out and state_out, every step.
@@ -343,9 +353,11 @@ def main():
     t_bytes = bytes_alg / (hbm * 1e9)
     t_flops = flops_alg / (tflops * 1e12)
     bound = "hbm" if t_bytes >= t_flops else "tensor"
-    plan = B.gdn_prefill_plan(one.desc)
-    dominant = [k for k in plan if k.startswith("chunk_")][0]
-    kern_ms = ms_step  # the chunk kernel is the only launch of a no-conv step
+    # dominant kernel: the most device time in the timed region; its unit of
+    # work is one step (all of its launches in a step together read the
+    # step's inputs once and write its outputs once, algorithmically)
+    dominant = max(per_kernel, key=lambda k: per_kernel[k][0])
+    kern_ms = per_kernel[dominant][0] / args.steps
     if bound == "hbm":
         achieved = bytes_alg / (kern_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -355,6 +367,12 @@ def main():
         roof = {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
                 "frac": achieved / tflops}
     roof["traffic"] = recorded_traffic(dominant)
+    roof["kernel_ms_per_step"] = kern_ms
+    roof["launches_per_step"] = per_kernel[dominant][1] / args.steps
+    roof["kernels"] = {k: {"launches_per_step": n / args.steps, "ms_per_launch": tot / n,
+                           "share": tot / sum(v[0] for v in per_kernel.values())}
+                       for k, (tot, n) in sorted(per_kernel.items())}
+    roof["untimed_launches"] = dropped
     roof["peak_source"] = peak_kind
     roof["kernel"] = dominant
     roof["algorithmic_bytes"] = bytes_alg

@@ -37,7 +37,8 @@ GDN_ACT_SILU = 1
 EXPORTED = ("gdn_prefill_desc_init", "gdn_prefill", "gdn_prefill_ex", "gdn_workspace_bytes",
             "gdn_step", "gdn_step_ex", "gdn_prefill_plan", "gdn_status_string",
             "gdn_last_cuda_error", "gdn_version", "gdn_prefill_noalloc",
-            "gdn_noalloc_scratch_bytes")
+            "gdn_noalloc_scratch_bytes", "gdn_launch_timer_start", "gdn_launch_timer_stop",
+            "gdn_launch_timer_read")
 
 
 class GdnError(RuntimeError):
@@ -98,6 +99,14 @@ def lib():
             L.gdn_prefill_noalloc.argtypes = [ctypes.POINTER(gdn_prefill_desc), st]
             L.gdn_noalloc_scratch_bytes.restype = ctypes.c_size_t
             L.gdn_noalloc_scratch_bytes.argtypes = []
+            L.gdn_launch_timer_start.restype = i
+            L.gdn_launch_timer_start.argtypes = [i]
+            L.gdn_launch_timer_stop.restype = i
+            L.gdn_launch_timer_stop.argtypes = []
+            L.gdn_launch_timer_read.restype = i
+            L.gdn_launch_timer_read.argtypes = [ctypes.POINTER(ctypes.c_char_p),
+                                                ctypes.POINTER(ctypes.c_float), i,
+                                                ctypes.POINTER(ctypes.c_int)]
             L.gdn_status_string.restype = ctypes.c_char_p
             L.gdn_status_string.argtypes = [i]
             L.gdn_last_cuda_error.restype = i
@@ -187,6 +196,30 @@ def gdn_prefill_noalloc(desc: gdn_prefill_desc, stream=None):
 
 def gdn_noalloc_scratch_bytes() -> int:
     return int(lib().gdn_noalloc_scratch_bytes())
+
+
+def gdn_launch_timer_start(capacity: int):
+    """Record the device time of the next ``capacity`` kernel launches."""
+    _check(lib().gdn_launch_timer_start(int(capacity)), "gdn_launch_timer_start")
+
+
+def gdn_launch_timer_stop():
+    _check(lib().gdn_launch_timer_stop(), "gdn_launch_timer_stop")
+
+
+def gdn_launch_timer_read():
+    """``([(kernel name, ms), ...] in launch order, dropped launches)``."""
+    L = lib()
+    dropped = ctypes.c_int(0)
+    n = L.gdn_launch_timer_read(None, None, 0, ctypes.byref(dropped))
+    if n < 0:
+        raise GdnError(-n, "gdn_launch_timer_read")
+    names = (ctypes.c_char_p * max(n, 1))()
+    ms = (ctypes.c_float * max(n, 1))()
+    m = L.gdn_launch_timer_read(names, ms, n, ctypes.byref(dropped))
+    if m < 0:
+        raise GdnError(-m, "gdn_launch_timer_read")
+    return [(names[i].decode(), float(ms[i])) for i in range(min(n, m))], int(dropped.value)
 
 
 def gdn_status_string(status: int) -> str:

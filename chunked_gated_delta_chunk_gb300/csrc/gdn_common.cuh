@@ -46,6 +46,11 @@ struct ChunkParams {
     int seg_max;             // most segments any sequence can have (grid size)
 };
 
+// Launch timing: bracket a kernel launch with timer_begin / timer_end on the
+// launch stream (no-ops unless gdn_launch_timer_start turned recording on).
+void timer_begin(cudaStream_t s, const char* kernel);
+void timer_end(cudaStream_t s);
+
 // Segment slot of (sequence n, segment s).
 __host__ __device__ inline int64_t seg_slot(int64_t seq_start, int n, int s, int64_t seg_tokens) {
     return seq_start / seg_tokens + n + s;

@@ -104,10 +104,12 @@ cudaError_t launch_conv(const ConvParams& p, int dtype, cudaStream_t s) {
     if (p.T == 0) return cudaSuccess;
     const dim3 grid(unsigned((p.T + kConvTokensPerBlock - 1) / kConvTokensPerBlock),
                     (p.C + kConvThreads - 1) / kConvThreads);
+    timer_begin(s, "conv_kernel");
     if (dtype == GDN_FP32)
         conv_kernel<float><<<grid, kConvThreads, 0, s>>>(p);
     else
         conv_kernel<__nv_bfloat16><<<grid, kConvThreads, 0, s>>>(p);
+    timer_end(s);
     return cudaGetLastError();
 }
 
@@ -115,10 +117,12 @@ cudaError_t launch_conv_state(const ConvParams& p, int dtype, cudaStream_t s) {
     const int64_t n = int64_t(p.B) * p.C;
     if (n == 0 || p.state_out == nullptr) return cudaSuccess;
     const unsigned blocks = unsigned((n + kConvThreads - 1) / kConvThreads);
+    timer_begin(s, "conv_state_kernel");
     if (dtype == GDN_FP32)
         conv_state_kernel<float><<<blocks, kConvThreads, 0, s>>>(p);
     else
         conv_state_kernel<__nv_bfloat16><<<blocks, kConvThreads, 0, s>>>(p);
+    timer_end(s);
     return cudaGetLastError();
 }
 

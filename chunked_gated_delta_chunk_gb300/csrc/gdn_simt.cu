@@ -302,12 +302,16 @@ cudaError_t launch_chunk_simt(const ChunkParams& p, int dtype, cudaStream_t s) {
         e = cudaFuncSetAttribute(chunk_simt_kernel<float>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
+        timer_begin(s, "chunk_simt_kernel");
         chunk_simt_kernel<float><<<grid, kThreads, smem, s>>>(p);
+        timer_end(s);
     } else {
         e = cudaFuncSetAttribute(chunk_simt_kernel<__nv_bfloat16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
+        timer_begin(s, "chunk_simt_kernel");
         chunk_simt_kernel<__nv_bfloat16><<<grid, kThreads, smem, s>>>(p);
+        timer_end(s);
     }
     return cudaGetLastError();
 }

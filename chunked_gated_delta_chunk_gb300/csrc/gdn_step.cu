@@ -149,10 +149,12 @@ cudaError_t launch_step(const StepParams& p, int dtype, cudaStream_t s) {
     if (p.B == 0) return cudaSuccess;
     const int NS = p.dv < 32 ? p.dv : 32;
     const dim3 grid(p.dv / NS, p.Hv, p.B);
+    timer_begin(s, "step_kernel");
     if (dtype == GDN_FP32)
         step_kernel<float><<<grid, kStepThreads, 0, s>>>(p);
     else
         step_kernel<__nv_bfloat16><<<grid, kStepThreads, 0, s>>>(p);
+    timer_end(s);
     return cudaGetLastError();
 }
 
@@ -161,10 +163,12 @@ cudaError_t launch_step_conv_state(const StepParams& p, int dtype, cudaStream_t 
     const int64_t n = int64_t(p.B) * C;
     if (n == 0 || p.conv_x == nullptr || p.conv_state_out == nullptr) return cudaSuccess;
     const unsigned blocks = unsigned((n + 255) / 256);
+    timer_begin(s, "step_conv_state_kernel");
     if (dtype == GDN_FP32)
         step_conv_state_kernel<float><<<blocks, 256, 0, s>>>(p);
     else
         step_conv_state_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(p);
+    timer_end(s);
     return cudaGetLastError();
 }
 

@@ -1053,19 +1053,27 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
     if (p.seg_chunks <= 0 || p.seg_max < 2) {
         ChunkParams q = p;
         q.seg_phase = 0;
+        timer_begin(s, "chunk_tc_kernel");
         chunk_tc_kernel<<<dim3(p.Hv, p.B, 1), kThreads, kSmemBytes, s>>>(q, maps);
+        timer_end(s);
         return cudaGetLastError();
     }
     ChunkParams q = p;
     q.seg_phase = 1;                                  // segment 0 in full; B_s and M_s
+    timer_begin(s, "chunk_tc_kernel");
     chunk_tc_kernel<<<dim3(p.Hv, p.B, 2 * p.seg_max - 1), kThreads, kSmemBytes, s>>>(q, maps);
+    timer_end(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (p.seg_max >= 3) {                             // S_{s+1} = M_s S_s + B_s
+        timer_begin(s, "seg_combine_kernel");
         seg_combine_kernel<<<dim3(p.Hv, p.B, kD / kCombineCols), kCombineThreads, 0, s>>>(q);
+        timer_end(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     q.seg_phase = 2;                                  // segments >= 1 in full
+    timer_begin(s, "chunk_tc_kernel");
     chunk_tc_kernel<<<dim3(p.Hv, p.B, p.seg_max - 1), kThreads, kSmemBytes, s>>>(q, maps);
+    timer_end(s);
     return cudaGetLastError();
 }
 

@@ -203,6 +203,33 @@ int gdn_prefill_noalloc(const gdn_prefill_desc* d, gdn_stream_t stream);
 /* Size in bytes of the fixed scratch array gdn_prefill_noalloc uses. */
 size_t gdn_noalloc_scratch_bytes(void);
 
+/* ---- Launch timing ------------------------------------------------------
+ * A host-side record of how long each kernel launch of the library took on
+ * the GPU, for profiling without an external tool.  The pages define no such
+ * call; it times the operations above.
+ *
+ * gdn_launch_timer_start(capacity) creates `capacity` pairs of CUDA events
+ * (on the current device; capacity 1..1,000,000), forgets earlier records and
+ * turns recording on: from then on every kernel the library launches, from
+ * any entry point, is bracketed by a pair of events recorded on its stream.
+ * Launches beyond the capacity run untimed and are counted as dropped.
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG (capacity out of range) or
+ * GDN_ERR_CUDA (event creation failed).  Not for use during stream capture.
+ *
+ * gdn_launch_timer_stop() turns recording off; the records stay readable.
+ *
+ * gdn_launch_timer_read(names, ms, max, dropped) waits for the recorded
+ * events, writes the kernel name (static string) and duration in
+ * milliseconds of the first min(count, max) launches in launch order, writes
+ * the dropped count to *dropped (if non-NULL) and returns the number of
+ * recorded launches (negative status on a CUDA error); a launch that was
+ * begun but never made (its call failed) reads -1 ms.  names or ms may be
+ * NULL to query the count.  The calls are thread-safe; launches made on
+ * several streams at once are recorded on their own streams. */
+int gdn_launch_timer_start(int capacity);
+int gdn_launch_timer_stop(void);
+int gdn_launch_timer_read(const char** names, float* ms, int max, int* dropped);
+
 /* Static description of a status code. */
 const char* gdn_status_string(int status);
 

@@ -165,3 +165,14 @@ def test_launch_plan_names(lib):
                       cu_seqlens=A)
     with pytest.raises(B.GdnError):
         B.gdn_prefill_plan(bad)
+
+
+def test_launch_timer_host_paths(lib):
+    """The launch timer's argument check and its empty record need no GPU:
+    capacity outside 1..1e6 is rejected before any CUDA call, and reading
+    without a started timer returns no launches."""
+    assert lib.gdn_launch_timer_start(0) == B.GDN_ERR_INVALID_ARG
+    assert lib.gdn_launch_timer_start(1000001) == B.GDN_ERR_INVALID_ARG
+    assert lib.gdn_launch_timer_stop() == B.GDN_OK
+    records, dropped = B.gdn_launch_timer_read()
+    assert records == [] and dropped == 0

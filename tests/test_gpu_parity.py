@@ -271,3 +271,26 @@ def test_segment_scan_off_equals_on_bits_of_segment_zero():
     b.run()
     torch.cuda.synchronize()
     assert torch.equal(a.out[:256], b.out[:256])
+
+
+# ---------------------------------------------------------------- launch timer
+def test_launch_timer_records_every_planned_launch():
+    """With the launch timer on, one call records exactly the kernels its
+    launch plan lists, in order, each with a positive device time; launches
+    past the capacity are counted as dropped."""
+    from chunked_gated_delta_chunk_gb300 import binding as B
+    p = inputs.make_problem(52, [900, 40], 2, 4, 128, 128, conv_kernel=4)
+    call = runner.PrefillCall(p, segment_chunks=4)
+    plan = B.gdn_prefill_plan(call.desc)
+    B.gdn_launch_timer_start(len(plan) + 1)
+    try:
+        call.run()
+        call.run()
+    finally:
+        B.gdn_launch_timer_stop()
+    records, dropped = B.gdn_launch_timer_read()
+    assert [n for n, _ in records] == (plan + plan)[:len(plan) + 1]
+    assert dropped == len(plan) - 1
+    assert all(ms > 0 for _, ms in records)
+    torch.cuda.synchronize()
+    compare({k: v.cpu() for k, v in call.results().items()}, run_oracle(p), TOL_BF16)
