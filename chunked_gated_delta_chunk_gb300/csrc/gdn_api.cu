@@ -60,22 +60,33 @@ size_t conv_workspace(const gdn_prefill_desc* d) {
 
 constexpr int kSMs = 152;   // GB300: 2 dies x 76 SMs
 
-// Chunks per segment of the segment-parallel scan, or 0 for one pass.  The
-// scan costs about two passes over a segment (maps, then outputs), so it pays
-// from three segments per sequence; segments are sized so that the first
-// phase (one full segment plus two maps per later segment, per value head and
-// sequence) fills the GPU once.
+// Chunks per segment of the segment-parallel scan, or 0 for one pass.
+// Cost model in chunk periods of one CTA (one CTA per SM): with n segments of
+// L = ceil(chunks / n) chunks, phase 1 runs (2n - 1) CTAs per (sequence,
+// value head) and phase 2 runs n - 1, each phase taking L + 1 periods per
+// wave of kSMs CTAs; the combine adds about a third of a period per segment.
+// One pass costs chunks + 1 periods in ceil(units / kSMs) waves.  The
+// cheapest n wins; sequence lengths are taken as the batch average.
 int segment_chunks(const gdn_prefill_desc* d) {
     if (d->dtype != GDN_BF16 || d->dk != 128 || d->dv != 128) return 0;   // tensor-core path only
     if (d->T_total <= 0 || d->B <= 0 || d->segment_chunks < 0) return 0;
     const int64_t chunks = (d->T_total + d->chunk - 1) / d->chunk;
     if (d->segment_chunks > 0) return d->segment_chunks < chunks ? d->segment_chunks : 0;
     const int64_t units = int64_t(d->Hv) * d->B;
-    const int64_t nseg = (kSMs / units + 1) / 2;
-    if (nseg < 3) return 0;
     const int64_t per_seq = (chunks + d->B - 1) / d->B;
-    const int64_t len = (per_seq + nseg - 1) / nseg;
-    return len >= 2 ? int(len) : 0;
+    auto waves = [&](int64_t ctas) { return (ctas + kSMs - 1) / kSMs; };
+    double best = double(waves(units) * (per_seq + 1));
+    int best_len = 0;
+    for (int64_t n = 2; n <= 64 && n <= per_seq; ++n) {
+        const int64_t len = (per_seq + n - 1) / n;
+        const double cost = double((waves(units * (2 * n - 1)) + waves(units * (n - 1))) * (len + 1)) +
+                            (n >= 3 ? (n - 2) / 3.0 : 0.0);
+        if (cost < best) {
+            best = cost;
+            best_len = int(len);
+        }
+    }
+    return best_len;
 }
 
 int64_t segment_slots(const gdn_prefill_desc* d, int seg_chunks) {

@@ -37,7 +37,9 @@ struct ChunkParams {
     // every later segment s twice, from a zero state (offset B_s) and from
     // the identity with V = 0 (transition M_s).  Phase 2: every segment
     // s >= 1 in full from its start state S_s.  seg_ws holds, per value head
-    // and segment slot, three [dk, dv] fp32 matrices B, M, S; the slot of
+    // and segment slot, three 128 x 128 fp32 matrices: B_s and S_s row-major
+    // [dk][dv], M_s stored transposed (element (i, j) of M_s at j * dk + i,
+    // which the combine reads column by column); the slot of
     // (sequence n, segment s) is cu[n] / (seg_chunks * chunk) + n + s.
     int seg_chunks;
     int seg_phase;
@@ -45,6 +47,11 @@ struct ChunkParams {
     int64_t seg_slots;       // slots per value head
     int seg_max;             // most segments any sequence can have (grid size)
 };
+
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device; the attribute is set once per (device, kernel, size) rather
+// than on every launch.
+cudaError_t ensure_smem(const void* kernel, int bytes);
 
 // Launch timing: bracket a kernel launch with timer_begin / timer_end on the
 // launch stream (no-ops unless gdn_launch_timer_start turned recording on).

@@ -6,16 +6,17 @@
 //
 // For channel c of sequence n, xx = [state_in[n, c, 0..K-2], x[cu[n].., c]]
 // (oldest first) and y_t = act(sum_{j<K} w[c, j] xx[t + j]); tap K-1 weighs
-// the current token.  HBM-bound: each thread produces one (token, channel)
-// output; consecutive threads take consecutive channels so that every load
-// and store of a warp is one contiguous segment.
+// the current token.  HBM-bound: consecutive threads take consecutive groups
+// of 8 channels, so every 16-byte load and store of a warp is one contiguous
+// 512-byte segment of a token row.
 #include "gdn_common.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int kConvThreads = 256;
-constexpr int kConvTokensPerBlock = 8;
+constexpr int kConvThreads = 128;
+constexpr int kConvRun = 32;            // tokens per thread
+constexpr int kConvGroup = 8;           // token rows loaded together
 
 __device__ __forceinline__ float act_fn(float y, int act) {
     return act == GDN_ACT_SILU ? y / (1.f + expf(-y)) : y;
@@ -33,39 +34,119 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int B, int64_t t) {
     return lo;
 }
 
-template <typename Tin>
+// 8 consecutive channels of one token row as floats (16-byte aligned: C is a
+// multiple of 16 and the row base is 16-byte aligned).
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* v) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void load8(const float* p, float* v) {
+    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float* v) {
+    uint4 u;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(p) = u;
+}
+__device__ __forceinline__ void store8(float* p, const float* v) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// One thread: 8 consecutive channels over a run of kConvRun tokens.  The K-1
+// previous columns of xx stay in registers as a sliding window, so every
+// input row is read once; a sequence start inside the run reloads the window
+// from that sequence's conv state.
+template <typename Tin, int K>
 __global__ void __launch_bounds__(kConvThreads) conv_kernel(const ConvParams p) {
-    const int c = blockIdx.y * kConvThreads + threadIdx.x;
-    if (c >= p.C) return;
+    const int c0 = (blockIdx.y * kConvThreads + threadIdx.x) * 8;
+    if (c0 >= p.C) return;
+    const int64_t t0 = int64_t(blockIdx.x) * kConvRun;
+    if (t0 >= p.T) return;
+    const int64_t t1 = t0 + kConvRun < p.T ? t0 + kConvRun : p.T;
     const Tin* x = static_cast<const Tin*>(p.x);
     Tin* y = static_cast<Tin*>(p.y);
-    const int K = p.K;
-    float w[8];
+    float w[8][K];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) w[j] = j < K ? p.w[int64_t(c) * K + j] : 0.f;
-    const int64_t tb = int64_t(blockIdx.x) * kConvTokensPerBlock;
-    for (int r = 0; r < kConvTokensPerBlock; ++r) {
-        const int64_t t = tb + r;
-        if (t >= p.T) return;
-        const int n = find_seq(p.cu, p.B, t);
-        int64_t start = p.cu[n];
-        if (start > t) start = t;   // only with a malformed cu_seqlens: stay in bounds
-        float acc = 0.f;
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (j < K) {
-                const int64_t tt = t - (K - 1) + j;
-                float xv;
-                if (tt >= start) {
-                    xv = load_elem(x, tt * p.C + c);
-                } else {
-                    const int64_t si = tt - start + (K - 1);   // index into the K-1 state columns
-                    xv = p.state_in ? p.state_in[(int64_t(n) * p.C + c) * (K - 1) + si] : 0.f;
-                }
-                acc = fmaf(w[j], xv, acc);
+        for (int j = 0; j < K; ++j) w[i][j] = p.w[int64_t(c0 + i) * K + j];
+    float win[K - 1][8];        // win[j] = xx column t - (K - 1) + j
+    int n = find_seq(p.cu, p.B, t0);
+    int64_t start = p.cu[n], stop = p.cu[n + 1];
+    // columns t - K + 1 .. t - 1 of sequence n: inputs at or after its start,
+    // else its conv state (oldest first), else zero
+    auto fill_window = [&](int64_t t) {
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) {
+            const int64_t tt = t - (K - 1) + j;
+            if (tt >= start) {
+                load8(x + tt * p.C + c0, win[j]);
+            } else {
+                const int64_t si = tt - start + (K - 1);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    win[j][i] = (p.state_in && si >= 0) ? p.state_in[(int64_t(n) * p.C + c0 + i) * (K - 1) + si] : 0.f;
             }
         }
-        store_elem(y, t * p.C + c, act_fn(acc, p.act));
+    };
+    if (start > t0) start = t0;   // only with a malformed cu_seqlens: stay in bounds
+    fill_window(t0);
+    // one output column from the window and the current input; then slide
+    auto emit = [&](int64_t t, const float* cur) {
+        float out[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < K - 1; ++j) acc = fmaf(w[i][j], win[j][i], acc);
+            acc = fmaf(w[i][K - 1], cur[i], acc);
+            out[i] = act_fn(acc, p.act);
+        }
+        store8(y + t * p.C + c0, out);
+#pragma unroll
+        for (int j = 0; j + 1 < K - 1; ++j)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) win[j][i] = win[j + 1][i];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) win[K - 2][i] = cur[i];
+    };
+    for (int64_t t = t0; t < t1;) {
+        if (t >= stop) {                            // next non-empty sequence starts here
+            while (n + 1 < p.B && int64_t(p.cu[n + 1]) <= t) ++n;
+            start = p.cu[n];
+            stop = p.cu[n + 1];
+            if (start > t) start = t;
+            if (stop <= t) stop = p.T;              // malformed cu_seqlens: stay in bounds
+            fill_window(t);
+        }
+        const int64_t end = t1 < stop ? t1 : stop;  // tokens of this sequence in the run
+        // groups of kConvGroup rows: all loads of a group in flight together
+        for (; t + kConvGroup <= end; t += kConvGroup) {
+            float cur[kConvGroup][8];
+#pragma unroll
+            for (int u = 0; u < kConvGroup; ++u) load8(x + (t + u) * p.C + c0, cur[u]);
+#pragma unroll
+            for (int u = 0; u < kConvGroup; ++u) emit(t + u, cur[u]);
+        }
+        for (; t < end; ++t) {
+            float cur[8];
+            load8(x + t * p.C + c0, cur);
+            emit(t, cur);
+        }
     }
 }
 
@@ -98,17 +179,30 @@ __global__ void __launch_bounds__(kConvThreads) conv_state_kernel(const ConvPara
         if (j < K - 1) p.state_out[idx * (K - 1) + j] = keep[j];
 }
 
+template <typename Tin>
+void launch_conv_k(const ConvParams& p, dim3 grid, cudaStream_t s) {
+    switch (p.K) {
+        case 2: conv_kernel<Tin, 2><<<grid, kConvThreads, 0, s>>>(p); break;
+        case 3: conv_kernel<Tin, 3><<<grid, kConvThreads, 0, s>>>(p); break;
+        case 4: conv_kernel<Tin, 4><<<grid, kConvThreads, 0, s>>>(p); break;
+        case 5: conv_kernel<Tin, 5><<<grid, kConvThreads, 0, s>>>(p); break;
+        case 6: conv_kernel<Tin, 6><<<grid, kConvThreads, 0, s>>>(p); break;
+        case 7: conv_kernel<Tin, 7><<<grid, kConvThreads, 0, s>>>(p); break;
+        default: conv_kernel<Tin, 8><<<grid, kConvThreads, 0, s>>>(p); break;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_conv(const ConvParams& p, int dtype, cudaStream_t s) {
     if (p.T == 0) return cudaSuccess;
-    const dim3 grid(unsigned((p.T + kConvTokensPerBlock - 1) / kConvTokensPerBlock),
-                    (p.C + kConvThreads - 1) / kConvThreads);
+    const dim3 grid(unsigned((p.T + kConvRun - 1) / kConvRun),
+                    (p.C / 8 + kConvThreads - 1) / kConvThreads);
     timer_begin(s, "conv_kernel");
     if (dtype == GDN_FP32)
-        conv_kernel<float><<<grid, kConvThreads, 0, s>>>(p);
+        launch_conv_k<float>(p, grid, s);
     else
-        conv_kernel<__nv_bfloat16><<<grid, kConvThreads, 0, s>>>(p);
+        launch_conv_k<__nv_bfloat16>(p, grid, s);
     timer_end(s);
     return cudaGetLastError();
 }

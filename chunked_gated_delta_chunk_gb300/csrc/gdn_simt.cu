@@ -299,15 +299,13 @@ cudaError_t launch_chunk_simt(const ChunkParams& p, int dtype, cudaStream_t s) {
     if (p.B == 0) return cudaSuccess;
     cudaError_t e;
     if (dtype == GDN_FP32) {
-        e = cudaFuncSetAttribute(chunk_simt_kernel<float>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        e = ensure_smem(reinterpret_cast<const void*>(chunk_simt_kernel<float>), int(smem));
         if (e != cudaSuccess) return e;
         timer_begin(s, "chunk_simt_kernel");
         chunk_simt_kernel<float><<<grid, kThreads, smem, s>>>(p);
         timer_end(s);
     } else {
-        e = cudaFuncSetAttribute(chunk_simt_kernel<__nv_bfloat16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        e = ensure_smem(reinterpret_cast<const void*>(chunk_simt_kernel<__nv_bfloat16>), int(smem));
         if (e != cudaSuccess) return e;
         timer_begin(s, "chunk_simt_kernel");
         chunk_simt_kernel<__nv_bfloat16><<<grid, kThreads, smem, s>>>(p);

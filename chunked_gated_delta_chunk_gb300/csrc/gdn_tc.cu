@@ -894,6 +894,12 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     tmem_st16(tZ + lane_addr + hf * 64 + 16, z + 16);
                     tmem_st16(tZ + lane_addr + hf * 64 + 32, z + 32);
                     tmem_st16(tZ + lane_addr + hf * 64 + 48, z + 48);
+                } else if (final_dst && mode == kModeTransition) {
+                    // M_s transposed: this thread's column of M_s is one contiguous row
+#pragma unroll
+                    for (int i = 0; i < 64; i += 4)
+                        *reinterpret_cast<float4*>(final_dst + size_t(row) * kD + hf * 64 + i) =
+                            make_float4(z[i], z[i + 1], z[i + 2], z[i + 3]);
                 } else if (final_dst) {
 #pragma unroll
                     for (int i = 0; i < 64; ++i) final_dst[size_t(hf * 64 + i) * kD + row] = z[i];
@@ -949,10 +955,20 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 
 // Phase 2 of the segment scan: S_{s+1} = M_s S_s + B_s for s = 1 .. nseg - 2,
 // per (value head, sequence), in fp32.  Columns of the state evolve
-// independently, so each CTA owns 8 of them and keeps its slab of S in
-// shared memory from one segment to the next.
-constexpr int kCombineThreads = 256;
-constexpr int kCombineCols = 8;
+// independently, so each CTA owns kCombineCols of them and keeps its slab of
+// S in shared memory from one segment to the next.  M_s (stored transposed,
+// 64 KB) and the CTA's columns of B_s are staged in shared memory by
+// cp.async, the next segment's copies in flight while the current ones are
+// used.  Four thread groups split the inner dimension k; in a group, thread
+// (rows 4i.., columns 4j..) reads four rows of M_s for one k as one 16-byte
+// word of M_s^T and four columns of S as one broadcast word.  The partial
+// sums meet in shared memory.
+constexpr int kCombineGroups = 4;
+constexpr int kCombineThreads = 128 * kCombineGroups;
+constexpr int kCombineCols = 16;
+constexpr int kCombineBuf = kD * kD + kD * kCombineCols;     // M_s^T, then B_s columns
+constexpr int kCombineSlab = kD * kCombineCols;
+constexpr uint32_t kCombineSmem = (2 * kCombineBuf + (1 + kCombineGroups) * kCombineSlab) * 4;
 
 __global__ void __launch_bounds__(kCombineThreads) seg_combine_kernel(const ChunkParams p) {
     const int h = blockIdx.x, n = blockIdx.y, slab = blockIdx.z;
@@ -965,38 +981,77 @@ __global__ void __launch_bounds__(kCombineThreads) seg_combine_kernel(const Chun
     const int nseg = (seq_chunks + p.seg_chunks - 1) / p.seg_chunks;
     if (nseg < 3) return;
     const int64_t seg_tokens = int64_t(p.seg_chunks) * p.chunk;
-    const float* base = p.seg_ws + (size_t(h) * p.seg_slots + seg_slot(p.cu[n], n, 0, seg_tokens)) * 3 * kD * kD;
-    float* wbase = const_cast<float*>(base);
-    __shared__ float sS[kD][kCombineCols];
-    const int tid = threadIdx.x, r = tid >> 1, cj = (tid & 1) * 4, c0 = slab * kCombineCols + cj;
-    for (int idx = tid; idx < kD * kCombineCols; idx += kCombineThreads) {
-        const int k = idx / kCombineCols, j = idx % kCombineCols;
-        sS[k][j] = base[size_t(1) * 3 * kD * kD + 2 * kD * kD + size_t(k) * kD + slab * kCombineCols + j];
+    float* base = p.seg_ws + (size_t(h) * p.seg_slots + seg_slot(p.cu[n], n, 0, seg_tokens)) * 3 * kD * kD;
+    extern __shared__ __align__(16) float smc[];
+    float* sS = smc + 2 * kCombineBuf;           // [kD][kCombineCols]; M_s^T, B_s in buffer s & 1 before it
+    float* sPart = sS + kCombineSlab;            // partial sums of the groups, [group][kD][kCombineCols]
+    const int tid = threadIdx.x, grp = tid >> 7, lt = tid & 127;
+    const int r0 = (lt & 31) * 4, c0 = (lt >> 5) * 4, k0 = grp * (kD / kCombineGroups);
+    const int col0 = slab * kCombineCols;
+    auto stage = [&](int s) {                    // M_s^T and B_s columns -> buffer s & 1
+        const float* msrc = base + size_t(s) * 3 * kD * kD + kD * kD;
+        float* dst = smc + (s & 1) * kCombineBuf;
+        for (int i = tid; i < kD * kD / 4; i += kCombineThreads) cp_async16(dst + 4 * i, msrc + 4 * i);
+        const float* bsrc = base + size_t(s) * 3 * kD * kD + col0;
+        float* bdst = dst + kD * kD;
+        for (int i = tid; i < kCombineSlab / 4; i += kCombineThreads) {
+            const int row = i / (kCombineCols / 4), c4 = (i % (kCombineCols / 4)) * 4;
+            cp_async16(bdst + row * kCombineCols + c4, bsrc + size_t(row) * kD + c4);
+        }
+        cp_async_commit();
+    };
+    stage(1);
+    for (int i = tid; i < kCombineSlab / 4; i += kCombineThreads) {
+        const int k = i / (kCombineCols / 4), c4 = (i % (kCombineCols / 4)) * 4;
+        *reinterpret_cast<float4*>(sS + k * kCombineCols + c4) =
+            *reinterpret_cast<const float4*>(base + size_t(1) * 3 * kD * kD + 2 * kD * kD + size_t(k) * kD + col0 + c4);
     }
-    __syncthreads();
     for (int s = 1; s + 1 < nseg; ++s) {
-        const float* Bs = base + size_t(s) * 3 * kD * kD;
-        const float* Ms = Bs + kD * kD;
-        float4 acc = *reinterpret_cast<const float4*>(Bs + size_t(r) * kD + c0);
-#pragma unroll 4
-        for (int k = 0; k < kD; k += 4) {
-            const float4 m = *reinterpret_cast<const float4*>(Ms + size_t(r) * kD + k);
-            const float mk[4] = {m.x, m.y, m.z, m.w};
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                acc.x = fmaf(mk[kk], sS[k + kk][cj + 0], acc.x);
-                acc.y = fmaf(mk[kk], sS[k + kk][cj + 1], acc.y);
-                acc.z = fmaf(mk[kk], sS[k + kk][cj + 2], acc.z);
-                acc.w = fmaf(mk[kk], sS[k + kk][cj + 3], acc.w);
-            }
+        if (s + 2 < nseg) {
+            stage(s + 1);
+            cp_async_wait_group<1>();
+        } else {
+            cp_async_wait_group<0>();
         }
         __syncthreads();
-        sS[r][cj + 0] = acc.x;
-        sS[r][cj + 1] = acc.y;
-        sS[r][cj + 2] = acc.z;
-        sS[r][cj + 3] = acc.w;
-        *reinterpret_cast<float4*>(wbase + size_t(s + 1) * 3 * kD * kD + 2 * kD * kD + size_t(r) * kD + c0) = acc;
-        __syncthreads();
+        const float* mt = smc + (s & 1) * kCombineBuf;
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 8
+        for (int k = k0; k < k0 + kD / kCombineGroups; ++k) {
+            const float4 m = *reinterpret_cast<const float4*>(mt + k * kD + r0);       // M[r0..r0+3][k]
+            const float4 v = *reinterpret_cast<const float4*>(sS + k * kCombineCols + c0);
+            const float mr[4] = {m.x, m.y, m.z, m.w}, sv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(mr[i], sv[j], acc[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<float4*>(sPart + grp * kCombineSlab + (r0 + i) * kCombineCols + c0) =
+                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        __syncthreads();                         // partials written; every read of sS done
+        {
+            // one 16-byte word of the slab per thread: B + the groups' partials
+            const int o = tid * 4, row = o / kCombineCols, col = o % kCombineCols;
+            float4 r = *reinterpret_cast<const float4*>(mt + kD * kD + o);
+#pragma unroll
+            for (int g = 0; g < kCombineGroups; ++g) {
+                const float4 q = *reinterpret_cast<const float4*>(sPart + g * kCombineSlab + o);
+                r.x += q.x;
+                r.y += q.y;
+                r.z += q.z;
+                r.w += q.w;
+            }
+            *reinterpret_cast<float4*>(sS + o) = r;
+            *reinterpret_cast<float4*>(base + size_t(s + 1) * 3 * kD * kD + 2 * kD * kD + size_t(row) * kD +
+                                       col0 + col) = r;
+        }
+        __syncthreads();                         // buffer s & 1 fully read: it may be restaged
     }
 }
 
@@ -1047,8 +1102,7 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
         !make_map(&maps.k, p.k, int64_t(p.Hk) * kD, rows, p.k_stride) ||
         !make_map(&maps.v, p.v, int64_t(p.Hv) * kD, rows, p.v_stride))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kSmemBytes));
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(chunk_tc_kernel), int(kSmemBytes));
     if (e != cudaSuccess) return e;
     if (p.seg_chunks <= 0 || p.seg_max < 2) {
         ChunkParams q = p;
@@ -1065,8 +1119,11 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
     timer_end(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (p.seg_max >= 3) {                             // S_{s+1} = M_s S_s + B_s
+        if ((e = ensure_smem(reinterpret_cast<const void*>(seg_combine_kernel), int(kCombineSmem))) !=
+            cudaSuccess)
+            return e;
         timer_begin(s, "seg_combine_kernel");
-        seg_combine_kernel<<<dim3(p.Hv, p.B, kD / kCombineCols), kCombineThreads, 0, s>>>(q);
+        seg_combine_kernel<<<dim3(p.Hv, p.B, kD / kCombineCols), kCombineThreads, kCombineSmem, s>>>(q);
         timer_end(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

@@ -1,10 +1,13 @@
-// Launch timing: every kernel launch of the library can be bracketed by a
-// pair of CUDA events on its stream, so a caller can read the device time of
-// each launch (the bench reports the dominant kernel's own duration this
-// way).  Host-side state only; recording is off unless started.
+// Host-side launch bookkeeping.  Launch timing: every kernel launch of the
+// library can be bracketed by a pair of CUDA events on its stream, so a
+// caller can read the device time of each launch (the bench reports the
+// dominant kernel's own duration this way); recording is off unless started.
+// Kernel attributes: the dynamic shared-memory limit of each kernel is
+// raised once per device instead of on every launch.
 
 #include <atomic>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "gdn_common.cuh"
@@ -57,6 +60,28 @@ void timer_end(cudaStream_t s) {
         g_records[t_open].closed = true;
     }
     t_open = -1;
+}
+
+namespace {
+std::mutex g_attr_mu;
+std::vector<std::pair<std::pair<int, const void*>, int>> g_attr;   // (device, kernel) -> bytes set
+}  // namespace
+
+cudaError_t ensure_smem(const void* kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    for (auto& a : g_attr)
+        if (a.first.first == dev && a.first.second == kernel) {
+            if (a.second >= bytes) return cudaSuccess;
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+            if (e == cudaSuccess) a.second = bytes;
+            return e;
+        }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) g_attr.push_back({{dev, kernel}, bytes});
+    return e;
 }
 
 }  // namespace gdn
