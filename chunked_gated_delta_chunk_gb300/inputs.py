@@ -190,3 +190,59 @@ def make_config(i: int, *, with_prior: bool = True) -> Problem:
     else:
         raise ValueError(f"unknown workload {i}")
     return p
+
+
+# ---------------------------------------------------------------- selective-scan rows
+@dataclass
+class ScanProblem:
+    """Inputs of the selective-scan rows h_t = a_t h_{t-1} + b_t: a, b
+    [T, C] fp32 (token-major), cu_seqlens [B+1] int32, h_in [B, C] fp32 or
+    None (zero state)."""
+    a: torch.Tensor
+    b: torch.Tensor
+    cu_seqlens: torch.Tensor
+    h_in: Optional[torch.Tensor]
+    name: str = ""
+
+    @property
+    def T(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def B(self) -> int:
+        return int(self.cu_seqlens.numel() - 1)
+
+    @property
+    def C(self) -> int:
+        return int(self.a.shape[1])
+
+
+def make_scan_problem(seed: int, lengths, C: int, *, a_mu: float = -2.0, a_sd: float = 1.0,
+                      b_sd: float = 1.0, h_sd: Optional[float] = 0.1, name: str = "") -> ScanProblem:
+    """Decays a = exp(-softplus(N(a_mu, a_sd))) in (0, 1] (the page's decay
+    factors), inputs b ~ N(0, b_sd), incoming state h ~ N(0, h_sd) (None:
+    no state, i.e. zero).  Drawn in fp32 on the CPU."""
+    gen = torch.Generator().manual_seed(seed)
+    cu = _cu(lengths)
+    T = int(cu[-1])
+    a = torch.exp(-torch.nn.functional.softplus(a_mu + a_sd * torch.randn(T, C, generator=gen)))
+    b = b_sd * torch.randn(T, C, generator=gen)
+    h = None if h_sd is None else h_sd * torch.randn(len(lengths), C, generator=gen)
+    return ScanProblem(a.contiguous(), b.contiguous(), cu, h, name)
+
+
+def make_scan_config(i: int) -> ScanProblem:
+    """Selective-scan workloads, sized after the Mamba page's model family
+    (mamba-130m: 1536 inner channels x 16 state entries = 24576 scan channels):
+
+    1. ``scan-tiny``   B=1, C=16, T=75 (64 + 11 rows).
+    2. ``scan-4k``     B=1, C=24576, T=4096 (the benchmark workload).
+    3. ``scan-ragged`` 8 prompts with lengths uniform in [1, 2048], C=1536."""
+    seed = BASE_SEED + 100 + i
+    if i == 1:
+        return make_scan_problem(seed, [75], 16, a_mu=0.0, name="scan-tiny")
+    if i == 2:
+        return make_scan_problem(seed, [4096], 24576, name="scan-4k")
+    if i == 3:
+        return make_scan_problem(seed, ragged_lengths(seed + 100, hi=2048), 1536, name="scan-ragged")
+    raise ValueError(f"unknown scan workload {i}")

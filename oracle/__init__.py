@@ -16,8 +16,12 @@ Contents
                 triangular inverses (forward substitution and the blocked
                 8x8-Neumann / 2x2-level scheme).  It is used to pin the token
                 loop, not as a second reference for the GPU.
+``scan_rows``   the selective-scan rows of the Mamba chunked-prefill pull
+                request (h_t = a_t h_{t-1} + b_t): the plain row loop (C) and
+                the page's chunked Hillis-Steele doubling scan (NumPy).
 """
 
 from .token_loop import (build_oracle, oracle_prefill, oracle_step, oracle_short_conv,  # noqa: F401
                          oracle_l2norm, max_threads)
 from . import chunk_form  # noqa: F401
+from . import scan_rows  # noqa: F401

@@ -258,6 +258,34 @@ int oracle_prefill(const double* q, const double* k, const double* v,
     return fail ? ORACLE_NO_MEMORY : ORACLE_OK;
 }
 
+/*
+ * Selective-scan rows ("perf(mamba): prefill text prompts in multi-token
+ * chunks", Implementation, add_selective_scan_rows): the first-order linear
+ * recurrence h_t = a_t h_{t-1} + b_t per channel, one row at a time, from the
+ * incoming state h_0 = h_in[n, c] (zero when h_in is NULL).
+ *   a, b, h_rows: [T, C] row-major (token-major); h_in, h_out: [B, C].
+ *   h_rows[t, c] = h_t; h_out[n, c] = h after the last row of sequence n
+ *   (h_0 for an empty sequence).
+ */
+int oracle_scan_rows(const double* a, const double* b, const double* h_in,
+                     double* h_out, double* h_rows, const int32_t* cu,
+                     int B, long C)
+{
+    if (!a || !b || !h_out || !h_rows || !cu || B < 0 || C < 0) return ORACLE_BAD_ARG;
+    long items = (long)B * C;
+#pragma omp parallel for schedule(static)
+    for (long it = 0; it < items; ++it) {
+        const long n = it / C, c = it % C;
+        double h = h_in ? h_in[n * C + c] : 0.0;
+        for (long t = cu[n]; t < cu[n + 1]; ++t) {
+            h = a[t * C + c] * h + b[t * C + c];
+            h_rows[t * C + c] = h;
+        }
+        h_out[n * C + c] = h;
+    }
+    return ORACLE_OK;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int oracle_max_threads(void)
 {
