@@ -244,6 +244,154 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+SCAN_METRIC = "selective-scan rows: tokens/s (1 GB300) and % of HBM roofline, 24576 channels, 4096-token prompt"
+SCAN_WORKLOAD = "scan-4k: B=1, T=4096, C=24576 (1536 x 16), fp32 a, b, h"
+
+
+def scan_bytes(p):
+    """a, b read once, h_rows written once, h_in read, h_out written."""
+    return (3 * p.T + 2 * p.B) * p.C * 4
+
+
+def run_scan(args, rank, world):
+    """The selective-scan rows (a next row of the hot-path table): one
+    gdn_scan_rows call over the 4096-row, 24576-channel workload per step."""
+    import torch
+    import torch.distributed as dist
+    from chunked_gated_delta_chunk_gb300 import binding as B
+    from chunked_gated_delta_chunk_gb300 import build as build_mod
+    from chunked_gated_delta_chunk_gb300 import inputs, runner
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+        from oracle import scan_rows as sr
+        oracle.build_oracle()
+        p = inputs.make_scan_config(2)
+        cols = 1024                                  # sampled channels per step
+        a, b, h = p.a[:, :cols].numpy(), p.b[:, :cols].numpy(), p.h_in[:, :cols].numpy()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            sr.oracle_scan_rows(a, b, p.cu_seqlens, h)
+        el = time.perf_counter() - t0
+        tps = p.T * args.steps / el * cols / p.C     # whole-row equivalents
+        line = {"metric": SCAN_METRIC, "value": tps, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "impl": "reference",
+                "config": {"workload": SCAN_WORKLOAD, "global_batch": p.B, "seq_len": p.T,
+                           "parallelism": "replicas"},
+                "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": oracle.max_threads(),
+                                 "kind": "oracle",
+                                 "sample": f"{cols} of {p.C} channels, all {p.T} rows, per step"},
+                "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    build_mod.build()
+    p = inputs.make_scan_config(2)
+    call = runner.ScanCall(p, dev)                   # 1.2 GB per step: larger than L2
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        call.run(stream)
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    B.gdn_launch_timer_start(args.steps * 2)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        start.record(stream)
+        for _ in range(args.steps):
+            call.run(stream)
+        stop.record(stream)
+        barrier()
+    ms_total = start.elapsed_time(stop)
+    B.gdn_launch_timer_stop()
+    records, dropped = B.gdn_launch_timer_read()
+    per_kernel = {}
+    for name, ms in records:
+        tot, n = per_kernel.get(name, (0.0, 0))
+        per_kernel[name] = (tot + ms, n + 1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    dominant = max(per_kernel, key=lambda k: per_kernel[k][0])
+    kern_ms = per_kernel[dominant][0] / per_kernel[dominant][1]
+    hbm, _, peak_kind = load_peaks()
+    nbytes = scan_bytes(p)
+    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": recorded_traffic(dominant), "peak_source": peak_kind, "kernel": dominant,
+            "algorithmic_bytes": nbytes, "kernel_ms_per_launch": kern_ms,
+            "kernels": {k: {"launches_per_step": n / args.steps, "ms_per_launch": tot / n,
+                            "share": tot / sum(v[0] for v in per_kernel.values())}
+                        for k, (tot, n) in sorted(per_kernel.items())},
+            "untimed_launches": dropped}
+    # end to end: a, b (and h_in) from pinned host memory, h_rows and h_out back
+    host_in = {"a": call.a.cpu().pin_memory(), "b": call.b.cpu().pin_memory(),
+               "h_in": call.h_in.cpu().pin_memory()}
+    host_out = {"h_rows": torch.empty_like(call.h_rows, device="cpu").pin_memory(),
+                "h_out": torch.empty_like(call.h_out, device="cpu").pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    e2e_steps = max(3, min(args.steps, 20))
+    for it in range(e2e_steps + 2):
+        if it == 2:
+            barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        for name, t in host_in.items():
+            getattr(call, name).copy_(t, non_blocking=True)
+        call.run(stream)
+        for name, t in host_out.items():
+            t.copy_(getattr(call, name), non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        from oracle import scan_rows as sr
+        oracle.build_oracle()
+        cols = 2048
+        a, b, h = p.a[:, :cols].numpy(), p.b[:, :cols].numpy(), p.h_in[:, :cols].numpy()
+        n, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 10.0:
+            sr.oracle_scan_rows(a, b, p.cu_seqlens, h)
+            n += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": p.T * n / el * cols / p.C, "unit": "tokens/s", "cores": oracle.max_threads(),
+               "kind": "oracle", "sample": f"{n} passes over {cols} of {p.C} channels, all {p.T} rows"}
+    if rank == 0:
+        line = {"metric": SCAN_METRIC, "value": world * p.T / (ms_step * 1e-3), "unit": "tokens/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic",
+                "config": {"workload": SCAN_WORKLOAD, "global_batch": p.B, "seq_len": p.T,
+                           "parallelism": "replicas" if world > 1 else "single",
+                           "l2": f"inputs and outputs {nbytes / 2**20:.0f} MiB per step > L2"},
+                "roofline": roof,
+                "e2e": {"value": world * p.T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "gpu_launches": 2 * args.steps, "clocks": clk.summary(), "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -252,6 +400,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--row", default="gdn", choices=["gdn", "scan"],
+                    help="gdn: the chunked gated delta rule prefill (the headline); "
+                         "scan: the selective-scan rows")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
@@ -259,6 +410,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.row == "scan":
+        run_scan(args, rank, world)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return

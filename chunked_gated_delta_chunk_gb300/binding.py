@@ -38,7 +38,8 @@ EXPORTED = ("gdn_prefill_desc_init", "gdn_prefill", "gdn_prefill_ex", "gdn_works
             "gdn_step", "gdn_step_ex", "gdn_prefill_plan", "gdn_status_string",
             "gdn_last_cuda_error", "gdn_version", "gdn_prefill_noalloc",
             "gdn_noalloc_scratch_bytes", "gdn_launch_timer_start", "gdn_launch_timer_stop",
-            "gdn_launch_timer_read")
+            "gdn_launch_timer_read", "gdn_scan_workspace_bytes", "gdn_scan_rows",
+            "gdn_wait_timeouts")
 
 
 class GdnError(RuntimeError):
@@ -107,6 +108,13 @@ def lib():
             L.gdn_launch_timer_read.argtypes = [ctypes.POINTER(ctypes.c_char_p),
                                                 ctypes.POINTER(ctypes.c_float), i,
                                                 ctypes.POINTER(ctypes.c_int)]
+            L.gdn_scan_workspace_bytes.restype = ctypes.c_size_t
+            L.gdn_scan_workspace_bytes.argtypes = [i, ctypes.c_int64]
+            L.gdn_scan_rows.restype = i
+            L.gdn_scan_rows.argtypes = [vp, vp, vp, vp, vp, vp, i, i, ctypes.c_int64, vp,
+                                        ctypes.c_size_t, st]
+            L.gdn_wait_timeouts.restype = ctypes.c_longlong
+            L.gdn_wait_timeouts.argtypes = []
             L.gdn_status_string.restype = ctypes.c_char_p
             L.gdn_status_string.argtypes = [i]
             L.gdn_last_cuda_error.restype = i
@@ -220,6 +228,29 @@ def gdn_launch_timer_read():
     if m < 0:
         raise GdnError(-m, "gdn_launch_timer_read")
     return [(names[i].decode(), float(ms[i])) for i in range(min(n, m))], int(dropped.value)
+
+
+def gdn_scan_workspace_bytes(C: int, T_total: int) -> int:
+    n = lib().gdn_scan_workspace_bytes(int(C), int(T_total))
+    if n == ctypes.c_size_t(-1).value:
+        raise GdnError(GDN_ERR_INVALID_ARG, "gdn_scan_workspace_bytes")
+    return int(n)
+
+
+def gdn_scan_rows(a, b, h_in, h_out, h_rows, cu_seqlens, B, C, T_total, workspace,
+                  workspace_bytes, stream=None):
+    """h_t = a_t h_{t-1} + b_t per channel over every sequence (device tensors)."""
+    _check(lib().gdn_scan_rows(_ptr(a), _ptr(b), _ptr(h_in), _ptr(h_out), _ptr(h_rows),
+                               _ptr(cu_seqlens), int(B), int(C), int(T_total), _ptr(workspace),
+                               int(workspace_bytes), _stream(stream)), "gdn_scan_rows")
+
+
+def gdn_wait_timeouts() -> int:
+    """Bounded device waits that ran out since load (synchronises the device)."""
+    n = int(lib().gdn_wait_timeouts())
+    if n < 0:
+        raise GdnError(GDN_ERR_CUDA, "gdn_wait_timeouts")
+    return n
 
 
 def gdn_status_string(status: int) -> str:

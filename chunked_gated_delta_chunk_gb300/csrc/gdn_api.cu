@@ -1,6 +1,7 @@
 // C ABI of libgdn.so (declared in include/gdn.h): argument validation, launch
 // planning and status codes.  Every check runs before the first enqueue, so a
 // rejected call enqueues nothing; nothing here allocates or synchronises.
+#include <climits>
 #include <cstdint>
 #include <cstring>
 
@@ -343,6 +344,46 @@ const char* gdn_status_string(int status) {
         case GDN_ERR_TOO_LARGE: return "size beyond what this entry point supports";
         default: return "unknown status";
     }
+}
+
+size_t gdn_scan_workspace_bytes(int C, int64_t T_total) {
+    if (C <= 0 || T_total < 0) return size_t(-1);
+    return gdn::scan_workspace_bytes(C, T_total);
+}
+
+int gdn_scan_rows(const float* a, const float* b, const float* h_in, float* h_out, float* h_rows,
+                  const int32_t* cu_seqlens, int B, int C, int64_t T_total, void* workspace,
+                  size_t workspace_bytes, gdn_stream_t stream) {
+    if (B < 0 || C <= 0 || T_total < 0) return GDN_ERR_INVALID_ARG;
+    if (B == 0) return T_total == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (h_out == nullptr || cu_seqlens == nullptr) return GDN_ERR_INVALID_ARG;
+    if (T_total > 0 && (a == nullptr || b == nullptr || h_rows == nullptr)) return GDN_ERR_INVALID_ARG;
+    if (C % 4 != 0) return GDN_ERR_UNSUPPORTED;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(h_rows)) return GDN_ERR_ALIGN;
+    const int64_t tiles = ((T_total + 63) / 64) * ((int64_t(C) + 127) / 128);
+    if (tiles > INT32_MAX) return GDN_ERR_TOO_LARGE;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+        workspace_bytes < gdn::scan_workspace_bytes(C, T_total))
+        return GDN_ERR_WORKSPACE;
+    gdn::ScanParams p{};
+    p.a = a;
+    p.b = b;
+    p.h_in = h_in;
+    p.h_out = h_out;
+    p.h_rows = h_rows;
+    p.cu = cu_seqlens;
+    p.T = T_total;
+    p.B = B;
+    p.C = C;
+    gdn::scan_bind_workspace(p, workspace);
+    return cuda_status(gdn::launch_scan_rows(p, static_cast<cudaStream_t>(stream)));
+}
+
+long long gdn_wait_timeouts(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    const int a = gdn::tc_read_timeouts(), b = gdn::scan_read_timeouts();
+    if (a < 0 || b < 0) return -1;
+    return (long long)a + b;
 }
 
 int gdn_last_cuda_error(void) { return g_last_cuda_error; }

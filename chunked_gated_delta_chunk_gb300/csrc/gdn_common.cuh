@@ -48,6 +48,31 @@ struct ChunkParams {
     int seg_max;             // most segments any sequence can have (grid size)
 };
 
+// Selective-scan rows (h_t = a_t h_{t-1} + b_t per channel).  a, b, h_rows
+// [T, C] fp32, h_in / h_out [B, C]; the workspace holds the ticket counter,
+// one flag per tile and the tiles' published maps and end states.
+struct ScanParams {
+    const float* a;
+    const float* b;
+    const float* h_in;       // or nullptr (zero state)
+    float* h_out;
+    float* h_rows;
+    const int32_t* cu;
+    int64_t T;
+    int B, C;
+    int n_cb, n_tiles;       // channel blocks; tiles (time chunks x channel blocks)
+    int* ticket;
+    int* flags;              // per tile: 0 none, 1 map published, 2 end state published
+    float* agg_a;            // per tile and channel: the map h -> A h + B of its rows
+    float* agg_b;
+    float* incl;             // per tile and channel: the state after its last row
+};
+size_t scan_workspace_bytes(int C, int64_t T);
+void scan_bind_workspace(ScanParams& p, void* ws);
+cudaError_t launch_scan_rows(const ScanParams& p, cudaStream_t s);
+int scan_read_timeouts();   // bounded waits of the scan that ran out (-1 on a CUDA error)
+int tc_read_timeouts();     // same for the tensor-core chunk kernel
+
 // Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
 // current device; the attribute is set once per (device, kernel, size) rather
 // than on every launch.

@@ -1091,6 +1091,13 @@ bool make_map(CUtensorMap* m, const void* base, int64_t width, int64_t rows, int
 
 }  // namespace
 
+int tc_read_timeouts() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_tc_timeouts, sizeof(int)) != cudaSuccess) return -1;
+    return v;
+}
+
+
 cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
     if (p.B == 0) return cudaSuccess;
     if (encode_fn() == nullptr) return cudaErrorNotSupported;

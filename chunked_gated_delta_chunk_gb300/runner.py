@@ -134,3 +134,36 @@ def step(q, k, v, g, beta, state, Hk, Hv, dk, dv, dtype=torch.bfloat16, conv=Non
     torch.cuda.synchronize(dev)
     del keep
     return (out, s_out) if conv is None else (out, s_out, cs_out)
+
+
+class ScanCall:
+    """Device buffers of one ``gdn_scan_rows`` call over a ``ScanProblem``;
+    ``run()`` enqueues the call on the given stream."""
+
+    def __init__(self, p, device="cuda", alias_state: bool = False):
+        dev = torch.device(device)
+        self.p = p
+        self.a = p.a.to(dev).contiguous()
+        self.b = p.b.to(dev).contiguous()
+        self.cu = p.cu_seqlens.to(dev, torch.int32)
+        self.h_in = None if p.h_in is None else p.h_in.to(dev, torch.float32).contiguous()
+        if alias_state:
+            assert self.h_in is not None
+            self.h_out = self.h_in
+        else:
+            self.h_out = torch.empty(p.B, p.C, dtype=torch.float32, device=dev)
+        self.h_rows = torch.empty(p.T, p.C, dtype=torch.float32, device=dev)
+        self.ws_bytes = B.gdn_scan_workspace_bytes(p.C, p.T)
+        self.workspace = torch.empty(max(self.ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+    def run(self, stream=None):
+        B.gdn_scan_rows(self.a, self.b, self.h_in, self.h_out, self.h_rows, self.cu, self.p.B,
+                        self.p.C, self.p.T, self.workspace, self.ws_bytes, stream)
+
+
+def scan_rows(p, device="cuda", **kw):
+    """One synchronous selective scan of ``p``; returns CPU (h_rows, h_out)."""
+    call = ScanCall(p, device, **kw)
+    call.run()
+    torch.cuda.synchronize(call.a.device)
+    return call.h_rows.cpu(), call.h_out.cpu()

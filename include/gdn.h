@@ -203,6 +203,40 @@ int gdn_prefill_noalloc(const gdn_prefill_desc* d, gdn_stream_t stream);
 /* Size in bytes of the fixed scratch array gdn_prefill_noalloc uses. */
 size_t gdn_noalloc_scratch_bytes(void);
 
+/* ---- Selective-scan rows -------------------------------------------------
+ * h_t = a_t h_{t-1} + b_t per channel over the rows of every sequence: the
+ * add_selective_scan_rows recurrence of "perf(mamba): prefill text prompts in
+ * multi-token chunks" (Implementation), in fp32 like the page.  The page runs
+ * it on chunks of at most 64 rows by doubling rounds, the state carried from
+ * chunk to chunk; one call here covers whole prompts (the result does not
+ * depend on the chunking).
+ *
+ *   a, b        [T_total, C] fp32, token-major (the page's a_t are decays in
+ *               (0, 1]; any finite values are accepted)
+ *   h_in        [B, C] fp32 incoming state, or NULL for a zero state
+ *   h_out       [B, C] fp32 state after each sequence's last row (h_in, or
+ *               zero, for an empty sequence); may alias h_in
+ *   h_rows      [T_total, C] fp32: h_t for every row
+ *   cu_seqlens  [B+1] int32: cu[0] = 0, non-decreasing, cu[B] = T_total
+ *   workspace   gdn_scan_workspace_bytes(C, T_total) bytes, 256-byte aligned,
+ *               caller-owned; needs no initialisation; one call at a time
+ * All pointers are device pointers; the call enqueues two kernels on
+ * `stream`, allocates nothing and does not synchronise.  C must be a
+ * multiple of 4 and a, b, h_rows 16-byte aligned.  Status: GDN_OK;
+ * GDN_ERR_INVALID_ARG (NULL pointer or negative size); GDN_ERR_UNSUPPORTED
+ * (C not a multiple of 4); GDN_ERR_ALIGN; GDN_ERR_WORKSPACE; GDN_ERR_TOO_LARGE
+ * (more than 2^31 - 1 tiles of 64 rows x 128 channels); GDN_ERR_CUDA. */
+size_t gdn_scan_workspace_bytes(int C, int64_t T_total);
+int gdn_scan_rows(const float* a, const float* b, const float* h_in, float* h_out, float* h_rows,
+                  const int32_t* cu_seqlens, int B, int C, int64_t T_total, void* workspace,
+                  size_t workspace_bytes, gdn_stream_t stream);
+
+/* Bounded device waits that ran out since the library was loaded (tensor-core
+ * chunk kernel and selective scan; a CTA whose wait runs out abandons its
+ * work, so every result of the call that hit it is unspecified).  Waits for
+ * the device to finish its work.  Returns the count, or -1 on a CUDA error. */
+long long gdn_wait_timeouts(void);
+
 /* ---- Launch timing ------------------------------------------------------
  * A host-side record of how long each kernel launch of the library took on
  * the GPU, for profiling without an external tool.  The pages define no such

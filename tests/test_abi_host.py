@@ -176,3 +176,28 @@ def test_launch_timer_host_paths(lib):
     assert lib.gdn_launch_timer_stop() == B.GDN_OK
     records, dropped = B.gdn_launch_timer_read()
     assert records == [] and dropped == 0
+
+
+def test_scan_rows_argument_checks(lib):
+    """Selective-scan rows: every invalid call is rejected before any CUDA
+    call (fake device addresses, never dereferenced)."""
+    ws = B.gdn_scan_workspace_bytes(256, 1000)
+    assert ws > 0 and ws % 256 == 0
+    assert B.gdn_scan_workspace_bytes(256, 2000) > ws
+    assert lib.gdn_scan_workspace_bytes(0, 10) == ctypes.c_size_t(-1).value
+    good = dict(a=A, b=A, h_in=None, h_out=A, h_rows=A, cu=A, B=1, C=256, T=1000, ws=A, wsb=ws)
+
+    def call(**kw):
+        d = dict(good, **kw)
+        return lib.gdn_scan_rows(d["a"], d["b"], d["h_in"], d["h_out"], d["h_rows"], d["cu"],
+                                 d["B"], d["C"], d["T"], d["ws"], d["wsb"], None)
+    assert call(B=-1) == B.GDN_ERR_INVALID_ARG
+    assert call(C=0) == B.GDN_ERR_INVALID_ARG
+    assert call(h_out=None) == B.GDN_ERR_INVALID_ARG
+    assert call(a=None) == B.GDN_ERR_INVALID_ARG
+    assert call(C=250) == B.GDN_ERR_UNSUPPORTED
+    assert call(b=A + 4) == B.GDN_ERR_ALIGN
+    assert call(ws=None) == B.GDN_ERR_WORKSPACE
+    assert call(ws=A + 16) == B.GDN_ERR_WORKSPACE
+    assert call(wsb=ws - 1) == B.GDN_ERR_WORKSPACE
+    assert call(B=0, T=0) == B.GDN_OK            # nothing to do, nothing enqueued
