@@ -246,3 +246,73 @@ def make_scan_config(i: int) -> ScanProblem:
     if i == 3:
         return make_scan_problem(seed, ragged_lengths(seed + 100, hi=2048), 1536, name="scan-ragged")
     raise ValueError(f"unknown scan workload {i}")
+
+
+# ---------------------------------------------------------------- RWKV-4 WKV rows
+@dataclass
+class WkvProblem:
+    """Inputs of the RWKV-4 WKV rows: k, v [T, C] fp32, per-channel decay
+    exponent w [C] (exp(w) in (0, 1)) and bonus u [C], cu_seqlens [B+1],
+    state_in [B, 3, C] (num, den, max) or None."""
+    k: torch.Tensor
+    v: torch.Tensor
+    w: torch.Tensor
+    u: torch.Tensor
+    cu_seqlens: torch.Tensor
+    state_in: Optional[torch.Tensor]
+    name: str = ""
+
+    @property
+    def T(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def B(self) -> int:
+        return int(self.cu_seqlens.numel() - 1)
+
+    @property
+    def C(self) -> int:
+        return int(self.k.shape[1])
+
+
+def make_wkv_problem(seed: int, lengths, C: int, *, large_key_frac: float = 0.05,
+                     with_state: bool = True, name: str = "") -> WkvProblem:
+    """Decays w = -exp(U(-5, 3)) and bonuses u ~ N(0.5, 1) per channel (the
+    spread of trained checkpoints the page's test covers); keys k ~ N(0, 1)
+    with a fraction replaced by large keys +-U(20, 40); values v ~ N(0, 1);
+    state num = den * N(0, 1), den = exp(N(0, 1)), max ~ N(0, 2)."""
+    gen = torch.Generator().manual_seed(seed)
+    cu = _cu(lengths)
+    T = int(cu[-1])
+    w = -torch.exp(-5.0 + 8.0 * torch.rand(C, generator=gen))
+    u = 0.5 + torch.randn(C, generator=gen)
+    k = torch.randn(T, C, generator=gen)
+    big = torch.rand(T, C, generator=gen) < large_key_frac
+    sign = torch.where(torch.rand(T, C, generator=gen) < 0.5, -1.0, 1.0)
+    k = torch.where(big, sign * (20.0 + 20.0 * torch.rand(T, C, generator=gen)), k)
+    v = torch.randn(T, C, generator=gen)
+    state = None
+    if with_state:
+        den = torch.exp(torch.randn(len(lengths), C, generator=gen))
+        num = den * torch.randn(len(lengths), C, generator=gen)
+        mx = 2.0 * torch.randn(len(lengths), C, generator=gen)
+        state = torch.stack([num, den, mx], dim=1).contiguous()
+    return WkvProblem(k.contiguous(), v.contiguous(), w, u, cu, state, name)
+
+
+def make_wkv_config(i: int) -> WkvProblem:
+    """WKV workloads, sized after the RWKV-4 family the page builds:
+
+    1. ``wkv-tiny``   B=1, C=16, T=75 (64 + 11 rows).
+    2. ``wkv-4k``     B=1, C=4096 (the 7B model's width), T=4096: the
+                      benchmark workload.
+    3. ``wkv-ragged`` 8 prompts with lengths uniform in [1, 2048], C=768
+                      (the 169M model the page measures)."""
+    seed = BASE_SEED + 200 + i
+    if i == 1:
+        return make_wkv_problem(seed, [75], 16, name="wkv-tiny")
+    if i == 2:
+        return make_wkv_problem(seed, [4096], 4096, name="wkv-4k")
+    if i == 3:
+        return make_wkv_problem(seed, ragged_lengths(seed + 100, hi=2048), 768, name="wkv-ragged")
+    raise ValueError(f"unknown WKV workload {i}")

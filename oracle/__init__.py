@@ -19,9 +19,13 @@ Contents
 ``scan_rows``   the selective-scan rows of the Mamba chunked-prefill pull
                 request (h_t = a_t h_{t-1} + b_t): the plain row loop (C) and
                 the page's chunked Hillis-Steele doubling scan (NumPy).
+``wkv_rows``    the RWKV-4 WKV of the RWKV chunked-prefill pull request: the
+                decoder's (num, den, max) recurrence row by row (C) and the
+                page's chunk form with per-row max shift (NumPy).
 """
 
 from .token_loop import (build_oracle, oracle_prefill, oracle_step, oracle_short_conv,  # noqa: F401
                          oracle_l2norm, max_threads)
 from . import chunk_form  # noqa: F401
 from . import scan_rows  # noqa: F401
+from . import wkv_rows  # noqa: F401

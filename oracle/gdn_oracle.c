@@ -286,6 +286,57 @@ int oracle_scan_rows(const double* a, const double* b, const double* h_in,
     return ORACLE_OK;
 }
 
+/*
+ * RWKV-4 WKV rows ("perf(rwkv): prefill text prompts in multi-token chunks",
+ * Implementation): the one-token decoder's recurrence, one row at a time.
+ * Per channel the state is (num, den, max) with A = num exp(max) and
+ * B = den exp(max) of
+ *   A_t = exp(w) A_{t-1} + exp(k_t) v_t,   B_t = exp(w) B_{t-1} + exp(k_t),
+ * and the output is
+ *   wkv_t = (A_{t-1} + exp(u + k_t) v_t) / (B_{t-1} + exp(u + k_t)).
+ * Every exponential is taken after subtracting the largest exponent of the
+ * sum, as the decoder does.  An absent state is (0, 0, -1e38).
+ *   k, v, wkv: [T, C]; w, u: [C]; state_in / state_out: [B, 3, C] holding
+ *   num, den, max; state_in may be NULL.
+ */
+int oracle_wkv_rows(const double* k, const double* v, const double* w, const double* u,
+                    const double* state_in, double* state_out, double* wkv,
+                    const int32_t* cu, int B, long C)
+{
+    if (!k || !v || !w || !u || !state_out || !wkv || !cu || B < 0 || C < 0) return ORACLE_BAD_ARG;
+    long items = (long)B * C;
+#pragma omp parallel for schedule(static)
+    for (long it = 0; it < items; ++it) {
+        const long n = it / C, c = it % C;
+        double num = 0.0, den = 0.0, mx = -1e38;
+        if (state_in) {
+            num = state_in[(n * 3 + 0) * C + c];
+            den = state_in[(n * 3 + 1) * C + c];
+            mx = state_in[(n * 3 + 2) * C + c];
+        }
+        for (long t = cu[n]; t < cu[n + 1]; ++t) {
+            const double kt = k[t * C + c], vt = v[t * C + c];
+            /* output: A_{t-1} and the bonus term */
+            double ww = u[c] + kt;
+            double p = mx > ww ? mx : ww;
+            double e1 = exp(mx - p), e2 = exp(ww - p);
+            wkv[t * C + c] = (e1 * num + e2 * vt) / (e1 * den + e2);
+            /* state: decay, then add row t */
+            ww = mx + w[c];
+            p = ww > kt ? ww : kt;
+            e1 = exp(ww - p);
+            e2 = exp(kt - p);
+            num = e1 * num + e2 * vt;
+            den = e1 * den + e2;
+            mx = p;
+        }
+        state_out[(n * 3 + 0) * C + c] = num;
+        state_out[(n * 3 + 1) * C + c] = den;
+        state_out[(n * 3 + 2) * C + c] = mx;
+    }
+    return ORACLE_OK;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int oracle_max_threads(void)
 {
