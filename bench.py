@@ -246,40 +246,78 @@ def run_reference(args, rank, world):
 
 SCAN_METRIC = "selective-scan rows: tokens/s (1 GB300) and % of HBM roofline, 24576 channels, 4096-token prompt"
 SCAN_WORKLOAD = "scan-4k: B=1, T=4096, C=24576 (1536 x 16), fp32 a, b, h"
+WKV_METRIC = "RWKV-4 WKV rows: tokens/s (1 GB300) and % of HBM roofline, 4096 channels, 4096-token prompt"
+WKV_WORKLOAD = "wkv-4k: B=1, T=4096, C=4096 (RWKV-4 7B width), fp32 k, v, wkv"
 
 
-def scan_bytes(p):
-    """a, b read once, h_rows written once, h_in read, h_out written."""
-    return (3 * p.T + 2 * p.B) * p.C * 4
+class _RowSpec:
+    """What the bench needs to know about one row recurrence."""
+
+    def __init__(self, kind):
+        from chunked_gated_delta_chunk_gb300 import inputs, runner
+        self.kind = kind
+        if kind == "scan":
+            self.metric, self.workload = SCAN_METRIC, SCAN_WORKLOAD
+            self.p = inputs.make_scan_config(2)
+            self.make_call = runner.ScanCall
+            self.inputs, self.outputs = ("a", "b", "h_in"), ("h_rows", "h_out")
+            # a, b read once, h_rows written once, h_in read, h_out written
+            self.nbytes = (3 * self.p.T + 2 * self.p.B) * self.p.C * 4
+        else:
+            self.metric, self.workload = WKV_METRIC, WKV_WORKLOAD
+            self.p = inputs.make_wkv_config(2)
+            self.make_call = runner.WkvCall
+            self.inputs, self.outputs = ("k", "v", "w", "u", "state_in"), ("wkv", "state_out")
+            # k, v read once, wkv written once, w, u, and the (num, den, max) state in and out
+            self.nbytes = (3 * self.p.T + 2 + 6 * self.p.B) * self.p.C * 4
+
+    def oracle_pass(self, cols):
+        """One float64 oracle pass over the first ``cols`` channels."""
+        p = self.p
+        if self.kind == "scan":
+            from oracle import scan_rows as sr
+            sr.oracle_scan_rows(self._a, self._b, p.cu_seqlens, self._h)
+        else:
+            from oracle import wkv_rows as wr
+            wr.oracle_wkv_rows(self._k, self._v, self._w, self._u, p.cu_seqlens, self._s)
+
+    def sample(self, cols):
+        p = self.p
+        if self.kind == "scan":
+            self._a, self._b, self._h = (p.a[:, :cols].numpy(), p.b[:, :cols].numpy(),
+                                         p.h_in[:, :cols].numpy())
+        else:
+            self._k, self._v = p.k[:, :cols].numpy(), p.v[:, :cols].numpy()
+            self._w, self._u = p.w[:cols].numpy(), p.u[:cols].numpy()
+            self._s = p.state_in[:, :, :cols].numpy()
 
 
-def run_scan(args, rank, world):
-    """The selective-scan rows (a next row of the hot-path table): one
-    gdn_scan_rows call over the 4096-row, 24576-channel workload per step."""
+def run_row(args, rank, world):
+    """A row recurrence of the hot-path table's next rows (the selective-scan
+    rows, the RWKV-4 WKV rows): one library call over its workload per step."""
     import torch
     import torch.distributed as dist
     from chunked_gated_delta_chunk_gb300 import binding as B
     from chunked_gated_delta_chunk_gb300 import build as build_mod
-    from chunked_gated_delta_chunk_gb300 import inputs, runner
+    spec = _RowSpec(args.row)
+    p = spec.p
     if args.impl == "reference":
         if rank != 0:
             return
         import oracle
-        from oracle import scan_rows as sr
         oracle.build_oracle()
-        p = inputs.make_scan_config(2)
-        cols = 1024                                  # sampled channels per step
-        a, b, h = p.a[:, :cols].numpy(), p.b[:, :cols].numpy(), p.h_in[:, :cols].numpy()
+        cols = 1024 if args.row == "scan" else 256     # sampled channels per step
+        spec.sample(cols)
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            sr.oracle_scan_rows(a, b, p.cu_seqlens, h)
+            spec.oracle_pass(cols)
         el = time.perf_counter() - t0
         tps = p.T * args.steps / el * cols / p.C     # whole-row equivalents
-        line = {"metric": SCAN_METRIC, "value": tps, "unit": "tokens/s", "n_gpus": world,
+        line = {"metric": spec.metric, "value": tps, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "impl": "reference",
-                "config": {"workload": SCAN_WORKLOAD, "global_batch": p.B, "seq_len": p.T,
+                "config": {"workload": spec.workload, "global_batch": p.B, "seq_len": p.T,
                            "parallelism": "replicas"},
                 "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": oracle.max_threads(),
                                  "kind": "oracle",
@@ -294,11 +332,13 @@ def run_scan(args, rank, world):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     build_mod.build()
-    p = inputs.make_scan_config(2)
-    call = runner.ScanCall(p, dev)                   # 1.2 GB per step: larger than L2
+    one = spec.make_call(p, dev)
+    set_bytes = spec.nbytes
+    nsets = max(1, min(8, -(-2 * L2_BYTES // max(set_bytes, 1)) + 1))
+    calls = [one] + [spec.make_call(p, dev) for _ in range(nsets - 1)]
     stream = torch.cuda.current_stream(dev)
-    for _ in range(args.warmup):
-        call.run(stream)
+    for i in range(args.warmup):
+        calls[i % nsets].run(stream)
     torch.cuda.synchronize(dev)
 
     def barrier():
@@ -311,8 +351,8 @@ def run_scan(args, rank, world):
     with ClockSampler(local) as clk:
         barrier()
         start.record(stream)
-        for _ in range(args.steps):
-            call.run(stream)
+        for i in range(args.steps):
+            calls[i % nsets].run(stream)
         stop.record(stream)
         barrier()
     ms_total = start.elapsed_time(stop)
@@ -330,20 +370,17 @@ def run_scan(args, rank, world):
     dominant = max(per_kernel, key=lambda k: per_kernel[k][0])
     kern_ms = per_kernel[dominant][0] / per_kernel[dominant][1]
     hbm, _, peak_kind = load_peaks()
-    nbytes = scan_bytes(p)
-    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    achieved = spec.nbytes / (kern_ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "traffic": recorded_traffic(dominant), "peak_source": peak_kind, "kernel": dominant,
-            "algorithmic_bytes": nbytes, "kernel_ms_per_launch": kern_ms,
+            "algorithmic_bytes": spec.nbytes, "kernel_ms_per_launch": kern_ms,
             "kernels": {k: {"launches_per_step": n / args.steps, "ms_per_launch": tot / n,
                             "share": tot / sum(v[0] for v in per_kernel.values())}
                         for k, (tot, n) in sorted(per_kernel.items())},
             "untimed_launches": dropped}
-    # end to end: a, b (and h_in) from pinned host memory, h_rows and h_out back
-    host_in = {"a": call.a.cpu().pin_memory(), "b": call.b.cpu().pin_memory(),
-               "h_in": call.h_in.cpu().pin_memory()}
-    host_out = {"h_rows": torch.empty_like(call.h_rows, device="cpu").pin_memory(),
-                "h_out": torch.empty_like(call.h_out, device="cpu").pin_memory()}
+    # end to end: the inputs from pinned host memory, the outputs back
+    host_in = {n: getattr(one, n).cpu().pin_memory() for n in spec.inputs}
+    host_out = {n: torch.empty_like(getattr(one, n), device="cpu").pin_memory() for n in spec.outputs}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     e2e_steps = max(3, min(args.steps, 20))
@@ -352,36 +389,36 @@ def run_scan(args, rank, world):
             barrier()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-        for name, t in host_in.items():
-            getattr(call, name).copy_(t, non_blocking=True)
-        call.run(stream)
-        for name, t in host_out.items():
-            t.copy_(getattr(call, name), non_blocking=True)
+        for n, t in host_in.items():
+            getattr(one, n).copy_(t, non_blocking=True)
+        one.run(stream)
+        for n, t in host_out.items():
+            t.copy_(getattr(one, n), non_blocking=True)
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
-        from oracle import scan_rows as sr
         oracle.build_oracle()
-        cols = 2048
-        a, b, h = p.a[:, :cols].numpy(), p.b[:, :cols].numpy(), p.h_in[:, :cols].numpy()
+        cols = 2048 if args.row == "scan" else 512
+        spec.sample(cols)
         n, t0 = 0, time.perf_counter()
         while time.perf_counter() - t0 < 10.0:
-            sr.oracle_scan_rows(a, b, p.cu_seqlens, h)
+            spec.oracle_pass(cols)
             n += 1
         el = time.perf_counter() - t0
         cpu = {"value": p.T * n / el * cols / p.C, "unit": "tokens/s", "cores": oracle.max_threads(),
                "kind": "oracle", "sample": f"{n} passes over {cols} of {p.C} channels, all {p.T} rows"}
     if rank == 0:
-        line = {"metric": SCAN_METRIC, "value": world * p.T / (ms_step * 1e-3), "unit": "tokens/s",
+        line = {"metric": spec.metric, "value": world * p.T / (ms_step * 1e-3), "unit": "tokens/s",
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic",
-                "config": {"workload": SCAN_WORKLOAD, "global_batch": p.B, "seq_len": p.T,
+                "config": {"workload": spec.workload, "global_batch": p.B, "seq_len": p.T,
                            "parallelism": "replicas" if world > 1 else "single",
-                           "l2": f"inputs and outputs {nbytes / 2**20:.0f} MiB per step > L2"},
+                           "l2": (f"rotating {nsets} independent buffer sets "
+                                  f"({nsets * set_bytes / 2**20:.0f} MiB > 2 x L2)")},
                 "roofline": roof,
                 "e2e": {"value": world * p.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -400,9 +437,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--row", default="gdn", choices=["gdn", "scan"],
+    ap.add_argument("--row", default="gdn", choices=["gdn", "scan", "wkv"],
                     help="gdn: the chunked gated delta rule prefill (the headline); "
-                         "scan: the selective-scan rows")
+                         "scan: the selective-scan rows; wkv: the RWKV-4 WKV rows")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
@@ -410,8 +447,8 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
-    if args.row == "scan":
-        run_scan(args, rank, world)
+    if args.row != "gdn":
+        run_row(args, rank, world)
         return
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -39,7 +39,7 @@ EXPORTED = ("gdn_prefill_desc_init", "gdn_prefill", "gdn_prefill_ex", "gdn_works
             "gdn_last_cuda_error", "gdn_version", "gdn_prefill_noalloc",
             "gdn_noalloc_scratch_bytes", "gdn_launch_timer_start", "gdn_launch_timer_stop",
             "gdn_launch_timer_read", "gdn_scan_workspace_bytes", "gdn_scan_rows",
-            "gdn_wait_timeouts")
+            "gdn_wait_timeouts", "gdn_wkv_workspace_bytes", "gdn_wkv_rows")
 
 
 class GdnError(RuntimeError):
@@ -113,6 +113,11 @@ def lib():
             L.gdn_scan_rows.restype = i
             L.gdn_scan_rows.argtypes = [vp, vp, vp, vp, vp, vp, i, i, ctypes.c_int64, vp,
                                         ctypes.c_size_t, st]
+            L.gdn_wkv_workspace_bytes.restype = ctypes.c_size_t
+            L.gdn_wkv_workspace_bytes.argtypes = [i, ctypes.c_int64]
+            L.gdn_wkv_rows.restype = i
+            L.gdn_wkv_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, ctypes.c_int64, vp,
+                                       ctypes.c_size_t, st]
             L.gdn_wait_timeouts.restype = ctypes.c_longlong
             L.gdn_wait_timeouts.argtypes = []
             L.gdn_status_string.restype = ctypes.c_char_p
@@ -243,6 +248,22 @@ def gdn_scan_rows(a, b, h_in, h_out, h_rows, cu_seqlens, B, C, T_total, workspac
     _check(lib().gdn_scan_rows(_ptr(a), _ptr(b), _ptr(h_in), _ptr(h_out), _ptr(h_rows),
                                _ptr(cu_seqlens), int(B), int(C), int(T_total), _ptr(workspace),
                                int(workspace_bytes), _stream(stream)), "gdn_scan_rows")
+
+
+def gdn_wkv_workspace_bytes(C: int, T_total: int) -> int:
+    n = lib().gdn_wkv_workspace_bytes(int(C), int(T_total))
+    if n == ctypes.c_size_t(-1).value:
+        raise GdnError(GDN_ERR_INVALID_ARG, "gdn_wkv_workspace_bytes")
+    return int(n)
+
+
+def gdn_wkv_rows(k, v, w, u, state_in, state_out, wkv, cu_seqlens, B, C, T_total, workspace,
+                 workspace_bytes, stream=None):
+    """RWKV-4 WKV over every sequence (device tensors)."""
+    _check(lib().gdn_wkv_rows(_ptr(k), _ptr(v), _ptr(w), _ptr(u), _ptr(state_in), _ptr(state_out),
+                              _ptr(wkv), _ptr(cu_seqlens), int(B), int(C), int(T_total),
+                              _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "gdn_wkv_rows")
 
 
 def gdn_wait_timeouts() -> int:

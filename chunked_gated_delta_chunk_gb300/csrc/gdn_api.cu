@@ -379,11 +379,48 @@ int gdn_scan_rows(const float* a, const float* b, const float* h_in, float* h_ou
     return cuda_status(gdn::launch_scan_rows(p, static_cast<cudaStream_t>(stream)));
 }
 
+size_t gdn_wkv_workspace_bytes(int C, int64_t T_total) {
+    if (C <= 0 || T_total < 0) return size_t(-1);
+    return gdn::wkv_workspace_bytes(C, T_total);
+}
+
+int gdn_wkv_rows(const float* k, const float* v, const float* w, const float* u,
+                 const float* state_in, float* state_out, float* wkv, const int32_t* cu_seqlens,
+                 int B, int C, int64_t T_total, void* workspace, size_t workspace_bytes,
+                 gdn_stream_t stream) {
+    if (B < 0 || C <= 0 || T_total < 0) return GDN_ERR_INVALID_ARG;
+    if (B == 0) return T_total == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (state_out == nullptr || cu_seqlens == nullptr || w == nullptr || u == nullptr)
+        return GDN_ERR_INVALID_ARG;
+    if (T_total > 0 && (k == nullptr || v == nullptr || wkv == nullptr)) return GDN_ERR_INVALID_ARG;
+    if (C % 4 != 0) return GDN_ERR_UNSUPPORTED;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(wkv)) return GDN_ERR_ALIGN;
+    const int64_t tiles = ((T_total + 63) / 64) * ((int64_t(C) + 127) / 128);
+    if (tiles > INT32_MAX) return GDN_ERR_TOO_LARGE;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+        workspace_bytes < gdn::wkv_workspace_bytes(C, T_total))
+        return GDN_ERR_WORKSPACE;
+    gdn::WkvParams p{};
+    p.k = k;
+    p.v = v;
+    p.w = w;
+    p.u = u;
+    p.state_in = state_in;
+    p.state_out = state_out;
+    p.wkv = wkv;
+    p.cu = cu_seqlens;
+    p.T = T_total;
+    p.B = B;
+    p.C = C;
+    gdn::wkv_bind_workspace(p, workspace);
+    return cuda_status(gdn::launch_wkv_rows(p, static_cast<cudaStream_t>(stream)));
+}
+
 long long gdn_wait_timeouts(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-    const int a = gdn::tc_read_timeouts(), b = gdn::scan_read_timeouts();
-    if (a < 0 || b < 0) return -1;
-    return (long long)a + b;
+    const int a = gdn::tc_read_timeouts(), b = gdn::scan_read_timeouts(), c = gdn::wkv_read_timeouts();
+    if (a < 0 || b < 0 || c < 0) return -1;
+    return (long long)a + b + c;
 }
 
 int gdn_last_cuda_error(void) { return g_last_cuda_error; }

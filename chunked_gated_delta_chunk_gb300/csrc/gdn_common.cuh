@@ -71,6 +71,32 @@ size_t scan_workspace_bytes(int C, int64_t T);
 void scan_bind_workspace(ScanParams& p, void* ws);
 cudaError_t launch_scan_rows(const ScanParams& p, cudaStream_t s);
 int scan_read_timeouts();   // bounded waits of the scan that ran out (-1 on a CUDA error)
+
+// RWKV-4 WKV rows.  k, v, wkv [T, C] fp32; w, u [C]; state_in / state_out
+// [B, 3, C] holding num, den, max.  Same ticket / flag workspace as the scan;
+// agg and incl hold (num, den, max) per tile and channel, each component a
+// block of n_tiles * 128 floats.
+struct WkvParams {
+    const float* k;
+    const float* v;
+    const float* w;
+    const float* u;
+    const float* state_in;   // or nullptr (empty state (0, 0, -1e38))
+    float* state_out;
+    float* wkv;
+    const int32_t* cu;
+    int64_t T;
+    int B, C;
+    int n_cb, n_tiles;
+    int* ticket;
+    int* flags;
+    float* agg;              // per tile: the state its rows build from an empty start
+    float* incl;             // per tile: the state after its last row
+};
+size_t wkv_workspace_bytes(int C, int64_t T);
+void wkv_bind_workspace(WkvParams& p, void* ws);
+cudaError_t launch_wkv_rows(const WkvParams& p, cudaStream_t s);
+int wkv_read_timeouts();
 int tc_read_timeouts();     // same for the tensor-core chunk kernel
 
 // Raise a kernel's dynamic shared-memory limit to at least `bytes` on the

@@ -13,6 +13,7 @@
 // b are read from HBM once and h written once.  A sequence start inside a
 // tile resets the map (A = 0, B = h_in), so such a tile needs no look-back.
 #include "gdn_common.cuh"
+#include "rows_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace gdn {
@@ -23,29 +24,10 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kScanRows = 64;
-constexpr int kScanCols = 128;        // one thread per channel
-constexpr uint32_t kScanSpinLimit = 1u << 22;
-
-__device__ __forceinline__ int ld_acquire(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release(int* p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Sequence holding row t: the n with cu[n] <= t < cu[n+1].
-__device__ __forceinline__ int scan_find_seq(const int32_t* cu, int B, int64_t t) {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (int64_t(cu[mid]) <= t) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
-}
+constexpr int kScanRows = rows::kRows;
+constexpr int kScanCols = rows::kCols;        // one thread per channel
+using rows::find_seq;
+using rows::st_release;
 
 // Zero the ticket and the tile flags; end state of every empty sequence.
 __global__ void scan_init_kernel(const ScanParams p) {
@@ -96,7 +78,7 @@ __global__ void __launch_bounds__(kScanCols) scan_rows_kernel(const ScanParams p
     __syncthreads();
 
     // ---- pass 1: the tile's affine map, resets at sequence starts -----------
-    int n = scan_find_seq(p.cu, p.B, t0);
+    int n = find_seq(p.cu, p.B, t0);
     int64_t nstart = p.cu[n], nend = p.cu[n + 1];
     float A = 1.f, Bv = 0.f, h0_last = 0.f;
     int64_t first_start = -1, last_start = -1;       // first and last sequence start in the tile
@@ -145,9 +127,7 @@ __global__ void __launch_bounds__(kScanCols) scan_rows_kernel(const ScanParams p
         for (int pci = ci - 1; pci >= 0 && !done; --pci) {
             const int pidx = pci * p.n_cb + cb;
             if (tid == 0) {
-                int f = 0;
-                uint32_t it = 0;
-                while ((f = ld_acquire(&p.flags[pidx])) == 0 && ++it < kScanSpinLimit) __nanosleep(64);
+                const int f = rows::wait_flag(&p.flags[pidx]);
                 if (f == 0) s_fail = 1;
                 s_flag = f;
             }
@@ -177,7 +157,7 @@ __global__ void __launch_bounds__(kScanCols) scan_rows_kernel(const ScanParams p
 
     // ---- pass 2: h_t from the staged tile ------------------------------------
     if (!live) return;
-    n = scan_find_seq(p.cu, p.B, t0);
+    n = find_seq(p.cu, p.B, t0);
     nstart = p.cu[n];
     nend = p.cu[n + 1];
     float h = s_in;

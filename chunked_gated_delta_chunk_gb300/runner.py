@@ -167,3 +167,37 @@ def scan_rows(p, device="cuda", **kw):
     call.run()
     torch.cuda.synchronize(call.a.device)
     return call.h_rows.cpu(), call.h_out.cpu()
+
+
+class WkvCall:
+    """Device buffers of one ``gdn_wkv_rows`` call over a ``WkvProblem``."""
+
+    def __init__(self, p, device="cuda", alias_state: bool = False):
+        dev = torch.device(device)
+        self.p = p
+        self.k = p.k.to(dev).contiguous()
+        self.v = p.v.to(dev).contiguous()
+        self.w = p.w.to(dev, torch.float32).contiguous()
+        self.u = p.u.to(dev, torch.float32).contiguous()
+        self.cu = p.cu_seqlens.to(dev, torch.int32)
+        self.state_in = None if p.state_in is None else p.state_in.to(dev, torch.float32).contiguous()
+        if alias_state:
+            assert self.state_in is not None
+            self.state_out = self.state_in
+        else:
+            self.state_out = torch.empty(p.B, 3, p.C, dtype=torch.float32, device=dev)
+        self.wkv = torch.empty(p.T, p.C, dtype=torch.float32, device=dev)
+        self.ws_bytes = B.gdn_wkv_workspace_bytes(p.C, p.T)
+        self.workspace = torch.empty(max(self.ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+    def run(self, stream=None):
+        B.gdn_wkv_rows(self.k, self.v, self.w, self.u, self.state_in, self.state_out, self.wkv,
+                       self.cu, self.p.B, self.p.C, self.p.T, self.workspace, self.ws_bytes, stream)
+
+
+def wkv_rows(p, device="cuda", **kw):
+    """One synchronous WKV call over ``p``; returns CPU (wkv, state_out)."""
+    call = WkvCall(p, device, **kw)
+    call.run()
+    torch.cuda.synchronize(call.k.device)
+    return call.wkv.cpu(), call.state_out.cpu()

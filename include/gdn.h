@@ -231,8 +231,41 @@ int gdn_scan_rows(const float* a, const float* b, const float* h_in, float* h_ou
                   const int32_t* cu_seqlens, int B, int C, int64_t T_total, void* workspace,
                   size_t workspace_bytes, gdn_stream_t stream);
 
+/* ---- RWKV-4 WKV rows ------------------------------------------------------
+ * The WKV of RWKV-4 time mixing over the rows of every sequence, as the
+ * one-token decoder of "perf(rwkv): prefill text prompts in multi-token
+ * chunks" (Implementation) computes it.  Per channel the state is
+ * (num, den, max), A = num exp(max) and B = den exp(max), of
+ *   A_t = exp(w) A_{t-1} + exp(k_t) v_t,   B_t = exp(w) B_{t-1} + exp(k_t),
+ * and row t outputs
+ *   wkv_t = (A_{t-1} + exp(u + k_t) v_t) / (B_{t-1} + exp(u + k_t)),
+ * every exponential taken after subtracting the largest exponent of its sum.
+ * The page builds each chunk of at most 64 rows as one exponent tensor; one
+ * call here covers whole prompts (the result does not depend on chunking).
+ *
+ *   k, v        [T_total, C] fp32, token-major
+ *   w, u        [C] fp32 per-channel decay exponent (exp(w) the decay) and bonus
+ *   state_in    [B, 3, C] fp32 (num, den, max) or NULL for the empty state
+ *               (0, 0, -1e38)
+ *   state_out   [B, 3, C] fp32 state after each sequence's last row (state_in,
+ *               or the empty state, for an empty sequence); may alias state_in.
+ *               The triple is one representation of (A, B): (num c, den c,
+ *               max - log c) is the same state.
+ *   wkv         [T_total, C] fp32 outputs
+ *   cu_seqlens  [B+1] int32: cu[0] = 0, non-decreasing, cu[B] = T_total
+ *   workspace   gdn_wkv_workspace_bytes(C, T_total) bytes, 256-byte aligned,
+ *               caller-owned; needs no initialisation; one call at a time
+ * Device pointers; two kernels enqueued on `stream`; nothing allocated, no
+ * synchronisation.  C must be a multiple of 4 and k, v, wkv 16-byte aligned.
+ * Status codes as for gdn_scan_rows. */
+size_t gdn_wkv_workspace_bytes(int C, int64_t T_total);
+int gdn_wkv_rows(const float* k, const float* v, const float* w, const float* u,
+                 const float* state_in, float* state_out, float* wkv, const int32_t* cu_seqlens,
+                 int B, int C, int64_t T_total, void* workspace, size_t workspace_bytes,
+                 gdn_stream_t stream);
+
 /* Bounded device waits that ran out since the library was loaded (tensor-core
- * chunk kernel and selective scan; a CTA whose wait runs out abandons its
+ * chunk kernel, selective scan and WKV rows; a CTA whose wait runs out abandons its
  * work, so every result of the call that hit it is unspecified).  Waits for
  * the device to finish its work.  Returns the count, or -1 on a CUDA error. */
 long long gdn_wait_timeouts(void);

@@ -201,3 +201,24 @@ def test_scan_rows_argument_checks(lib):
     assert call(ws=A + 16) == B.GDN_ERR_WORKSPACE
     assert call(wsb=ws - 1) == B.GDN_ERR_WORKSPACE
     assert call(B=0, T=0) == B.GDN_OK            # nothing to do, nothing enqueued
+
+
+def test_wkv_rows_argument_checks(lib):
+    """RWKV-4 WKV rows: invalid calls are rejected before any CUDA call."""
+    ws = B.gdn_wkv_workspace_bytes(256, 1000)
+    assert ws > B.gdn_scan_workspace_bytes(256, 1000) and ws % 256 == 0
+    good = dict(k=A, v=A, w=A, u=A, s_in=None, s_out=A, wkv=A, cu=A, B=1, C=256, T=1000,
+                ws=A, wsb=ws)
+
+    def call(**kw):
+        d = dict(good, **kw)
+        return lib.gdn_wkv_rows(d["k"], d["v"], d["w"], d["u"], d["s_in"], d["s_out"], d["wkv"],
+                                d["cu"], d["B"], d["C"], d["T"], d["ws"], d["wsb"], None)
+    assert call(B=-1) == B.GDN_ERR_INVALID_ARG
+    assert call(w=None) == B.GDN_ERR_INVALID_ARG
+    assert call(s_out=None) == B.GDN_ERR_INVALID_ARG
+    assert call(k=None) == B.GDN_ERR_INVALID_ARG
+    assert call(C=6) == B.GDN_ERR_UNSUPPORTED
+    assert call(wkv=A + 8) == B.GDN_ERR_ALIGN
+    assert call(wsb=ws - 256) == B.GDN_ERR_WORKSPACE
+    assert call(B=0, T=0) == B.GDN_OK
