@@ -5,11 +5,16 @@
 
 #include <stdint.h>
 
+#include "tc_ptx.cuh"
+
 namespace gdn {
 namespace rows {
 
-constexpr int kRows = 64;              // rows of a tile
-constexpr int kCols = 128;             // channels of a tile (one thread each)
+constexpr int kRows = 256;             // rows of a tile
+constexpr int kCols = 32;              // channels of a tile (one lane each)
+constexpr int kWarps = 4;              // warp w owns rows 64 w .. 64 w + 63
+constexpr int kThreads = 32 * kWarps;
+constexpr int kWarpRows = kRows / kWarps;
 constexpr uint32_t kSpinLimit = 1u << 22;
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -32,6 +37,43 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int B, int64_t t) {
         else hi = mid - 1;
     }
     return lo;
+}
+
+constexpr int kChains = 4;             // independent row chains per thread
+constexpr int kChainRows = kWarpRows / kChains;
+enum : int { kRowStart = 1, kRowEnd = 2 };
+
+// Sequence and start / end marks of the tile's rows (all threads of the CTA
+// share the rows); the caller synchronises before reading them.
+__device__ __forceinline__ void fill_row_info(const int32_t* cu, int B, int64_t t0, int nrow, int tid,
+                                              int* seq, int* mark) {
+    for (int r = tid; r < nrow; r += kThreads) {
+        const int64_t t = t0 + r;
+        const int n = find_seq(cu, B, t);
+        seq[r] = n;
+        mark[r] = (t == cu[n] ? kRowStart : 0) | (t == int64_t(cu[n + 1]) - 1 ? kRowEnd : 0);
+    }
+}
+
+// Stage rows [t0, t0 + nrow) x channels [c0, c0 + kCols) of two [T, C] fp32
+// arrays into [kRows][kCols] shared tiles by 16-byte cp.async (C a multiple
+// of 4); rows and channels outside are zero.
+__device__ __forceinline__ void stage_tile(float* sx, float* sy, const float* x, const float* y,
+                                           int64_t t0, int nrow, int c0, int C, int tid) {
+    for (int i = tid; i < kRows * (kCols / 4); i += kThreads) {
+        const int r = i / (kCols / 4), q = (i % (kCols / 4)) * 4;
+        float* dx = sx + r * kCols + q;
+        float* dy = sy + r * kCols + q;
+        if (r < nrow && c0 + q < C) {
+            const int64_t off = (t0 + r) * C + c0 + q;
+            ptx::cp_async16(dx, x + off);
+            ptx::cp_async16(dy, y + off);
+        } else {
+            *reinterpret_cast<float4*>(dx) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(dy) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    ptx::cp_async_commit();
 }
 
 // Thread 0 waits (bounded) until the tile flag is non-zero; returns it, or 0

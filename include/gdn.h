@@ -225,7 +225,7 @@ size_t gdn_noalloc_scratch_bytes(void);
  * multiple of 4 and a, b, h_rows 16-byte aligned.  Status: GDN_OK;
  * GDN_ERR_INVALID_ARG (NULL pointer or negative size); GDN_ERR_UNSUPPORTED
  * (C not a multiple of 4); GDN_ERR_ALIGN; GDN_ERR_WORKSPACE; GDN_ERR_TOO_LARGE
- * (more than 2^31 - 1 tiles of 64 rows x 128 channels); GDN_ERR_CUDA. */
+ * (more than 2^31 - 1 tiles of 256 rows x 32 channels); GDN_ERR_CUDA. */
 size_t gdn_scan_workspace_bytes(int C, int64_t T_total);
 int gdn_scan_rows(const float* a, const float* b, const float* h_in, float* h_out, float* h_rows,
                   const int32_t* cu_seqlens, int B, int C, int64_t T_total, void* workspace,
