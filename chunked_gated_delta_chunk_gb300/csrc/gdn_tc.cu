@@ -585,12 +585,14 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 const int isq = r >= kC, tr = r & 63;
                 const uint8_t* base = kq + (isq ? 8192 : 0);
                 float ss = 0.f;
+                if (write_out || !isq) {                   // q is not used by the map passes
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    float v[8];
-                    load_chunk8(base + toff(tr, part * 64 + m * 8, 16384), v);
+                    for (int m = 0; m < 8; ++m) {
+                        float v[8];
+                        load_chunk8(base + toff(tr, part * 64 + m * 8, 16384), v);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
+                        for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
+                    }
                 }
                 ss += __shfl_xor_sync(0xffffffffu, ss, 1);
                 if (part == 0) (isq ? vRq : vRk)[tr] = p.l2norm ? rsqrtf(ss + p.eps) : 1.f;
@@ -630,7 +632,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                         // each store phase hit disjoint banks
                         *reinterpret_cast<float4*>(sA + i * kLdA + phalf * 32 + q) = make_float4(a4[0], a4[1], a4[2], a4[3]);
                     }
-                } else {
+                } else if (write_out) {
                     const int t = row - kC;
                     const float rt = vRq[t], gt = vGam[t];
 #pragma unroll
@@ -692,7 +694,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 }
             }
             // ---- while U0/W run: scaled Q rows in place; chain scalars ----------
-            for (int idx = pt; idx < kC * 16; idx += kPrepThreads) {
+            for (int idx = pt; write_out && idx < kC * 16; idx += kPrepThreads) {
                 const int r = idx >> 4, cc = (idx & 15) * 8;
                 uint8_t* ptr = kq + 8192 + toff(r, cc, 16384);
                 const float f = r < rows ? vEg[r] * vRq[r] : 0.f;
@@ -793,11 +795,13 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                         umma_f16_tmemA(tX, tZb + s * 8, dWt + uint64_t(s * 2048 >> 4), id_x,
                                        mode != kModeTransition || s > 0);
                     umma_commit(&bars[B_X]);
-                    const uint64_t dQ = smem_desc(smem_u32(kq + 8192), 16, 1024, kSwizzle128B);
+                    if (write_out) {                  // the map passes write no outputs
+                        const uint64_t dQ = smem_desc(smem_u32(kq + 8192), 16, 1024, kSwizzle128B);
 #pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
-                        umma_f16_tmemA(tO, tZb + s * 8, dQ + (off >> 4), id_o, s > 0);
+                        for (int s = 0; s < 8; ++s) {
+                            const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
+                            umma_f16_tmemA(tO, tZb + s * 8, dQ + (off >> 4), id_o, s > 0);
+                        }
                     }
                 }
             }
@@ -855,14 +859,16 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     for (int s = 0; s < 4; ++s)
                         umma_f16_tmemA(tZ, tU + 64 + part * 32 + s * 8, dK + uint64_t(s * 2048 >> 4), id_z, 1);
                 umma_commit(&bars[B_Z]);
-                // (U hi, P hi), (U hi, P lo), (U lo, P hi)
+                if (write_out) {
+                    // (U hi, P hi), (U hi, P lo), (U lo, P hi)
 #pragma unroll
-                for (int pr = 0; pr < 3; ++pr)
+                    for (int pr = 0; pr < 3; ++pr)
 #pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        umma_f16_tmemA(tO, tU + (pr == 2 ? 32 : 0) + s * 8,
-                                       dP + uint64_t(((pr == 1 ? 8192 : 0) + s * 32) >> 4), id_o, 1);
-                umma_commit(&bars[B_O]);
+                        for (int s = 0; s < 4; ++s)
+                            umma_f16_tmemA(tO, tU + (pr == 2 ? 32 : 0) + s * 8,
+                                           dP + uint64_t(((pr == 1 ? 8192 : 0) + s * 32) >> 4), id_o, 1);
+                    umma_commit(&bars[B_O]);
+                }
             }
             __syncwarp();
             // ---- new state: Zb = bf16(Z); Z <- exp(gamma_S(c+1)) Z --------------
@@ -907,16 +913,18 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             }
             tmem_st_wait();
             // ---- output rows to registers (stored during the next chunk) --------
-            if (lead) lf = !wait(B_O, uint32_t(c & 1));
-            __syncwarp();
-            if (named_sync_or(kBarChain, kChainThreads, lf)) { fail = true; break; }
-            tc_fence_after();
-            for (int hf = 0; hf < 2; ++hf) {
-                float o[32];
-                tmem_ld32(tO + lane_addr + hf * 32, o);
+            if (write_out) {
+                if (lead) lf = !wait(B_O, uint32_t(c & 1));
+                __syncwarp();
+                if (named_sync_or(kBarChain, kChainThreads, lf)) { fail = true; break; }
+                tc_fence_after();
+                for (int hf = 0; hf < 2; ++hf) {
+                    float o[32];
+                    tmem_ld32(tO + lane_addr + hf * 32, o);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    opk[hf * 16 + i] = pack_bf16x2(o[2 * i] * p.q_scale, o[2 * i + 1] * p.q_scale);
+                    for (int i = 0; i < 16; ++i)
+                        opk[hf * 16 + i] = pack_bf16x2(o[2 * i] * p.q_scale, o[2 * i + 1] * p.q_scale);
+                }
             }
             o_cs = cs;
             o_rows = write_out ? rows : 0;
