@@ -316,3 +316,70 @@ def make_wkv_config(i: int) -> WkvProblem:
     if i == 3:
         return make_wkv_problem(seed, ragged_lengths(seed + 100, hi=2048), 768, name="wkv-ragged")
     raise ValueError(f"unknown WKV workload {i}")
+
+
+# ---------------------------------------------------------------- attention rows
+@dataclass
+class AttnProblem:
+    """Inputs of the full-attention rows: q [T, Hq, D], k, v [T, Hkv, D]
+    (bf16 values), a KV cache k_cache, v_cache [B, Hkv, cap, D] holding
+    cache_len[n] rows per sequence, cu_seqlens [B+1]."""
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    cache_len: torch.Tensor
+    cu_seqlens: torch.Tensor
+    scale: float
+    name: str = ""
+
+    @property
+    def T(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def B(self) -> int:
+        return int(self.cu_seqlens.numel() - 1)
+
+
+def make_attn_problem(seed: int, lengths, cache_lens, Hq: int, Hkv: int, D: int = 128, cap: Optional[int] = None,
+                      *, dtype: torch.dtype = torch.bfloat16, name: str = "") -> AttnProblem:
+    """q, k, v ~ N(0, 1); the cache's first cache_len[n] rows ~ N(0, 1), the
+    rest of its capacity zero; scale 1 / sqrt(D)."""
+    gen = torch.Generator().manual_seed(seed)
+    cu = _cu(lengths)
+    T = int(cu[-1])
+    B = len(lengths)
+    if cap is None:
+        cap = max(int(c) + int(n) for c, n in zip(cache_lens, lengths))
+        cap = max(64, -(-cap // 64) * 64)
+    q = torch.randn(T, Hq, D, generator=gen)
+    k = torch.randn(T, Hkv, D, generator=gen)
+    v = torch.randn(T, Hkv, D, generator=gen)
+    kc = torch.zeros(B, Hkv, cap, D)
+    vc = torch.zeros(B, Hkv, cap, D)
+    for n, c in enumerate(cache_lens):
+        kc[n, :, :c] = torch.randn(Hkv, int(c), D, generator=gen)
+        vc[n, :, :c] = torch.randn(Hkv, int(c), D, generator=gen)
+    r = lambda x: _round(x, dtype)
+    return AttnProblem(r(q), r(k), r(v), r(kc), r(vc), torch.tensor(cache_lens, dtype=torch.int32), cu,
+                       1.0 / D ** 0.5, name)
+
+
+def make_attn_config(i: int) -> AttnProblem:
+    """Attention workloads (GQA 16 query / 2 kv heads, head dim 128, bf16):
+
+    1. ``attn-tiny``  11 rows (the page's 7 + 4 test shape) over a 5-row cache, Hq=4, Hkv=2.
+    2. ``attn-4k``    one 4096-row prompt, empty cache: the benchmark workload.
+    3. ``attn-ragged`` 4 prompts U[1, 1024] over caches U[0, 2048]."""
+    seed = BASE_SEED + 300 + i
+    if i == 1:
+        return make_attn_problem(seed, [11], [5], 4, 2, name="attn-tiny")
+    if i == 2:
+        return make_attn_problem(seed, [4096], [0], 16, 2, name="attn-4k")
+    if i == 3:
+        lens = ragged_lengths(seed + 100, n=4, hi=1024)
+        caches = ragged_lengths(seed + 200, n=4, lo=0, hi=2048)
+        return make_attn_problem(seed, lens, caches, 16, 2, name="attn-ragged")
+    raise ValueError(f"unknown attention workload {i}")

@@ -22,6 +22,9 @@ Contents
 ``wkv_rows``    the RWKV-4 WKV of the RWKV chunked-prefill pull request: the
                 decoder's (num, den, max) recurrence row by row (C) and the
                 page's chunk form with per-row max shift (NumPy).
+``attn_rows``   full-attention rows over a KV cache plus the chunk's causal
+                prefix (the Qwen3.5 page's full-attention layers), float64
+                NumPy.
 """
 
 from .token_loop import (build_oracle, oracle_prefill, oracle_step, oracle_short_conv,  # noqa: F401
@@ -29,3 +32,4 @@ from .token_loop import (build_oracle, oracle_prefill, oracle_step, oracle_short
 from . import chunk_form  # noqa: F401
 from . import scan_rows  # noqa: F401
 from . import wkv_rows  # noqa: F401
+from . import attn_rows  # noqa: F401
