@@ -39,7 +39,7 @@ EXPORTED = ("gdn_prefill_desc_init", "gdn_prefill", "gdn_prefill_ex", "gdn_works
             "gdn_last_cuda_error", "gdn_version", "gdn_prefill_noalloc",
             "gdn_noalloc_scratch_bytes", "gdn_launch_timer_start", "gdn_launch_timer_stop",
             "gdn_launch_timer_read", "gdn_scan_workspace_bytes", "gdn_scan_rows",
-            "gdn_wait_timeouts", "gdn_wkv_workspace_bytes", "gdn_wkv_rows")
+            "gdn_wait_timeouts", "gdn_wkv_workspace_bytes", "gdn_wkv_rows", "gdn_attn_rows")
 
 
 class GdnError(RuntimeError):
@@ -118,6 +118,9 @@ def lib():
             L.gdn_wkv_rows.restype = i
             L.gdn_wkv_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, ctypes.c_int64, vp,
                                        ctypes.c_size_t, st]
+            L.gdn_attn_rows.restype = i
+            L.gdn_attn_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_int64,
+                                        ctypes.c_float, st]
             L.gdn_wait_timeouts.restype = ctypes.c_longlong
             L.gdn_wait_timeouts.argtypes = []
             L.gdn_status_string.restype = ctypes.c_char_p
@@ -264,6 +267,16 @@ def gdn_wkv_rows(k, v, w, u, state_in, state_out, wkv, cu_seqlens, B, C, T_total
                               _ptr(wkv), _ptr(cu_seqlens), int(B), int(C), int(T_total),
                               _ptr(workspace), int(workspace_bytes), _stream(stream)),
            "gdn_wkv_rows")
+
+
+def gdn_attn_rows(q, k, v, k_cache, v_cache, cache_len, o, cu_seqlens, B, Hq, Hkv, head_dim,
+                  cache_capacity, T_total, scale=0.0, stream=None):
+    """Attention over the KV cache plus the chunk's causal prefix; appends the
+    chunk's k / v rows to the cache (device tensors)."""
+    _check(lib().gdn_attn_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len),
+                               _ptr(o), _ptr(cu_seqlens), int(B), int(Hq), int(Hkv), int(head_dim),
+                               int(cache_capacity), int(T_total), float(scale), _stream(stream)),
+           "gdn_attn_rows")
 
 
 def gdn_wait_timeouts() -> int:

@@ -416,11 +416,48 @@ int gdn_wkv_rows(const float* k, const float* v, const float* w, const float* u,
     return cuda_status(gdn::launch_wkv_rows(p, static_cast<cudaStream_t>(stream)));
 }
 
+int gdn_attn_rows(const void* q, const void* k, const void* v, void* k_cache, void* v_cache,
+                  const int32_t* cache_len, void* o, const int32_t* cu_seqlens, int B, int Hq, int Hkv,
+                  int head_dim, int cache_capacity, int64_t T_total, float scale, gdn_stream_t stream) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || T_total < 0 || cache_capacity <= 0 || !(scale >= 0.f))
+        return GDN_ERR_INVALID_ARG;
+    if (head_dim != 128 || Hq % Hkv != 0) return GDN_ERR_UNSUPPORTED;
+    if (B == 0) return T_total == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (B > 65535 || Hq > 65535 || T_total > INT32_MAX ||
+        int64_t(B) * Hkv * cache_capacity > INT32_MAX)
+        return GDN_ERR_TOO_LARGE;
+    if (cu_seqlens == nullptr || cache_len == nullptr || k_cache == nullptr || v_cache == nullptr)
+        return GDN_ERR_INVALID_ARG;
+    if (T_total > 0 && (q == nullptr || k == nullptr || v == nullptr || o == nullptr))
+        return GDN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(k_cache) ||
+        !aligned16(v_cache))
+        return GDN_ERR_ALIGN;
+    gdn::AttnParams p{};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.o = o;
+    p.cu = cu_seqlens;
+    p.cache_len = cache_len;
+    p.T = T_total;
+    p.max_len = T_total;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.cap = cache_capacity;
+    p.scale = scale > 0.f ? scale : 0.08838834764831845f;   // 1 / sqrt(128)
+    return cuda_status(gdn::launch_attn_rows(p, static_cast<cudaStream_t>(stream)));
+}
+
 long long gdn_wait_timeouts(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-    const int a = gdn::tc_read_timeouts(), b = gdn::scan_read_timeouts(), c = gdn::wkv_read_timeouts();
-    if (a < 0 || b < 0 || c < 0) return -1;
-    return (long long)a + b + c;
+    const int a = gdn::tc_read_timeouts(), b = gdn::scan_read_timeouts(), c = gdn::wkv_read_timeouts(),
+              d = gdn::attn_read_timeouts();
+    if (a < 0 || b < 0 || c < 0 || d < 0) return -1;
+    return (long long)a + b + c + d;
 }
 
 int gdn_last_cuda_error(void) { return g_last_cuda_error; }

@@ -1,0 +1,378 @@
+// Full-attention rows over a KV cache plus the chunk's causal prefix
+// ("perf(qwen3_5): prefill text prompts in multi-token chunks",
+// Implementation: the full-attention layers of a prefill chunk attend over
+// the cache plus the chunk's causal prefix, and the chunk's present k / v
+// rows are appended to the cache).
+//
+// attn_append_kernel writes the prompt's k, v rows into the cache after each
+// sequence's cache_len rows.  attn_rows_kernel then runs one CTA per
+// (128-row query tile, query head, sequence): the query tile stays in shared
+// memory, 128-key tiles of K and V stream through three TMA stages, and
+// per key tile
+//   S = Q K^T                    tcgen05 MMA into TMEM (128 x 128 fp32)
+//   P = exp2(S scale - m)        one query row per thread (its TMEM lane),
+//                                causal / capacity mask, bf16 into TMEM
+//   O += P V                     tcgen05 MMA, A = P from TMEM, fp32 in TMEM
+// with the running row maximum m raised (and O, l rescaled) only when a
+// tile's maximum exceeds it by more than 2^8, so P stays below 256.  The
+// next tile's S MMA runs while the current tile's softmax is computed.
+#include <cuda.h>
+#include <climits>
+
+#include "gdn_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace gdn {
+
+__device__ int g_attn_timeouts = 0;   // bumped by a CTA whose bounded wait ran out
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kAD = 128;              // head dim
+constexpr int kAQ = 128;              // query rows per tile (TMEM lanes)
+constexpr int kAK = 128;              // keys per tile
+constexpr int kAStages = 3;
+constexpr int kAThreads = 128;
+constexpr uint32_t kAWaitLimit = 1u << 20;
+constexpr float kARescale = 8.f;      // log2 headroom before the reference maximum moves
+constexpr uint32_t kATile = kAK * kAD * 2;                 // 32 KB per K or V tile
+constexpr uint32_t kAOffQ = 0;
+constexpr uint32_t kAOffKV = kATile;                       // stage s: K at +2s tiles, V at +2s+1
+constexpr uint32_t kAOffBar = kAOffKV + kAStages * 2 * kATile;
+constexpr uint32_t kASmem = kAOffBar + 8 * 8 + 1024;
+static_assert(kASmem <= 232448, "attention stages above the 227 KB per-block limit");
+constexpr uint32_t kAColS = 0, kAColP = 128, kAColO = 256, kATmemCols = 512;
+enum : int { AB_Q = 0, AB_KV = 1, AB_S = 1 + kAStages, AB_O = 2 + kAStages };
+
+struct AttnMaps {
+    CUtensorMap q, kc, vc;
+};
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ int attn_find_seq(const int32_t* cu, int B, int64_t t) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (int64_t(cu[mid]) <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Prompt rows into the cache: row t of sequence n goes to position
+// cache_len[n] + (t - cu[n]) (rows past the capacity are dropped).
+__global__ void attn_append_kernel(const AttnParams p) {
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;   // (t, kv head, 16-byte word)
+    const int words = kAD / 8;
+    if (i >= p.T * p.Hkv * words) return;
+    const int64_t t = i / (int64_t(p.Hkv) * words);
+    const int kh = int(i / words % p.Hkv), w = int(i % words);
+    const int n = attn_find_seq(p.cu, p.B, t);
+    const int64_t pos = int64_t(p.cache_len[n]) + (t - p.cu[n]);
+    if (pos < 0 || pos >= p.cap) return;
+    const size_t src = (size_t(t) * p.Hkv + kh) * kAD + w * 8;
+    const size_t dst = ((size_t(n) * p.Hkv + kh) * p.cap + pos) * kAD + w * 8;
+    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(p.k);
+    const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(p.v);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.k_cache) + dst) = *reinterpret_cast<const uint4*>(k + src);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.v_cache) + dst) = *reinterpret_cast<const uint4*>(v + src);
+}
+
+__global__ void __launch_bounds__(kAThreads, 1)
+attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
+    extern __shared__ uint8_t attn_smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(attn_smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kAOffBar);
+    __shared__ uint32_t tmem_slot;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int h = blockIdx.y, n = blockIdx.z;
+    const int xt = int(gridDim.x) - 1 - int(blockIdx.x);          // long (late) tiles first
+    const int64_t s0 = p.cu[n];
+    const int L = int(p.cu[n + 1] - s0);
+    const int q0 = xt * kAQ;
+    if (q0 >= L) return;                                          // the whole CTA leaves together
+    const int rows = L - q0 < kAQ ? L - q0 : kAQ;
+    const int clen = p.cache_len[n];
+    const int kh = h / (p.Hq / p.Hkv);
+    int nkeys = clen + q0 + rows;                                 // keys the tile's last row sees
+    if (nkeys > p.cap) nkeys = p.cap;
+    const int ntiles = (nkeys + kAK - 1) / kAK;
+    const int kv_row0 = int((int64_t(n) * p.Hkv + kh) * p.cap);
+
+    if (tid == 0) {
+        for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&maps.q);
+        tma_prefetch_desc(&maps.kc);
+        tma_prefetch_desc(&maps.vc);
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_slot, kATmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t tS = tmem + kAColS, tP = tmem + kAColP, tO = tmem + kAColO;
+    const uint32_t lane_addr = uint32_t(warp * 32) << 16;
+    const uint32_t id_s = idesc_bf16(kAQ, kAK, 0, 0);             // B = K, K-major
+    const uint32_t id_o = idesc_bf16(kAQ, kAD, 0, 1);             // B = V, MN-major [key][d]
+    uint8_t* sQ = sm + kAOffQ;
+    auto sK = [&](int j) { return sm + kAOffKV + uint32_t(j % kAStages) * 2 * kATile; };
+    auto sV = [&](int j) { return sK(j) + kATile; };
+    auto issue_kv = [&](int j) {
+        uint64_t* bar = &bars[AB_KV + j % kAStages];
+        mbar_arrive_expect_tx(bar, 2 * kATile);
+        const int y = kv_row0 + j * kAK;
+        tma_load_2d(sK(j), &maps.kc, bar, 0, y);
+        tma_load_2d(sK(j) + kATile / 2, &maps.kc, bar, 64, y);
+        tma_load_2d(sV(j), &maps.vc, bar, 0, y);
+        tma_load_2d(sV(j) + kATile / 2, &maps.vc, bar, 64, y);
+    };
+    auto issue_s = [&](int j) {                                   // S = Q K_j^T
+        const uint64_t dq = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128B);
+        const uint64_t dk = smem_desc(smem_u32(sK(j)), 16, 1024, kSwizzle128B);
+#pragma unroll
+        for (int s = 0; s < kAD / 16; ++s) {
+            const uint32_t off = uint32_t(s >> 2) * (kATile / 2) + uint32_t(s & 3) * 32u;
+            umma_f16(tS, dq + (off >> 4), dk + (off >> 4), id_s, s > 0);
+        }
+        umma_commit(&bars[AB_S]);
+    };
+    bool fail = false;
+    int last_kv[kAStages] = {-1, -1, -1};                          // thread 0: last tile issued per stage
+    auto issue_kv_t = [&](int j) {
+        issue_kv(j);
+        last_kv[j % kAStages] = j;
+    };
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bars[AB_Q], kATile);
+        tma_load_2d(sQ, &maps.q, &bars[AB_Q], h * kAD, int(s0 + q0));
+        tma_load_2d(sQ + kATile / 2, &maps.q, &bars[AB_Q], h * kAD + 64, int(s0 + q0));
+        for (int j = 0; j < ntiles && j < 2; ++j) issue_kv_t(j);
+        fail = !mbar_wait(&bars[AB_Q], 0, kAWaitLimit) || !mbar_wait(&bars[AB_KV], 0, kAWaitLimit);
+        if (!fail) {
+            tc_fence_after();
+            issue_s(0);
+        }
+    }
+    const float sl2 = p.scale * 1.4426950408889634f;
+    const int pos = clen + q0 + tid;                              // this row sees keys 0 .. pos
+    float m_ref = -INFINITY, l = 0.f;
+    for (int j = 0; j < ntiles; ++j) {
+        if (tid == 0 && !fail) fail = !mbar_wait(&bars[AB_S], uint32_t(j & 1), kAWaitLimit);
+        if (__syncthreads_or(fail)) {
+            fail = true;
+            break;
+        }
+        tc_fence_after();
+        // ---- this row of S_j; the S buffer is then free for S_{j+1} ------------
+        float x[kAK];
+#pragma unroll
+        for (int q = 0; q < kAK; q += 32) {
+            uint32_t r0[16], r1[16];
+            __syncwarp();
+            GDN_TMEM_LD_X16(tS + lane_addr + q, r0);
+            GDN_TMEM_LD_X16(tS + lane_addr + q + 16, r1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                x[q + i] = __uint_as_float(r0[i]);
+                x[q + 16 + i] = __uint_as_float(r1[i]);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0 && j + 1 < ntiles) {
+            fail = !mbar_wait(&bars[AB_KV + (j + 1) % kAStages], uint32_t(((j + 1) / kAStages) & 1), kAWaitLimit);
+            if (!fail) {
+                tc_fence_after();
+                issue_s(j + 1);
+            }
+        }
+        // ---- softmax of the row: mask, running maximum, exponentials ------------
+        const int k0 = j * kAK;
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kAK; ++c) {
+            const int kk = k0 + c;
+            x[c] = (kk <= pos && kk < nkeys) ? x[c] * sl2 : -INFINITY;
+            mt = fmaxf(mt, x[c]);
+        }
+        float f = 1.f;                                            // rescale of O and l
+        if (j == 0) {
+            m_ref = mt;
+        } else if (mt > m_ref + kARescale) {
+            f = ex2(m_ref - mt);
+            m_ref = mt;
+        }
+        l *= f;
+        uint32_t pk[kAK / 2];
+#pragma unroll
+        for (int c = 0; c < kAK; c += 2) {
+            const float e0 = ex2(x[c] - m_ref), e1 = ex2(x[c + 1] - m_ref);
+            pk[c / 2] = pack2(e0, e1);
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&pk[c / 2]);
+            const float2 r = __bfloat1622float2(b);
+            l += r.x + r.y;
+        }
+        // ---- P_j replaces P_{j-1} once O += P_{j-1} V_{j-1} is done -------------
+        if (tid == 0 && !fail && j >= 1) {
+            fail = !mbar_wait(&bars[AB_O], uint32_t((j - 1) & 1), kAWaitLimit);
+            if (!fail && j + 2 < ntiles) issue_kv_t(j + 2);       // into the stage tile j-1 used
+        }
+        if (tid == 0 && !fail && j == 0 && 2 < ntiles) issue_kv_t(2);
+        if (__syncthreads_or(fail)) {
+            fail = true;
+            break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, f != 1.f)) {                  // rescale this warp's rows of O
+#pragma unroll
+            for (int q = 0; q < kAD; q += 16) {
+                float o[16];
+                tmem_ld16(tO + lane_addr + q, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o[i] *= f;
+                tmem_st16(tO + lane_addr + q, o);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kAK / 2; q += 16) {
+            __syncwarp();
+            GDN_TMEM_ST_X16(tP + lane_addr + q, (pk + q));
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint64_t dv = smem_desc(smem_u32(sV(j)), kATile / 2, 1024, kSwizzle128B);
+#pragma unroll
+            for (int s = 0; s < kAK / 16; ++s)
+                umma_f16_tmemA(tO, tP + s * 8, dv + uint64_t(s * 2048 >> 4), id_o, j > 0 || s > 0);
+            umma_commit(&bars[AB_O]);
+        }
+    }
+    // ---- O / l to the output rows ------------------------------------------------
+    if (tid == 0 && !fail) fail = !mbar_wait(&bars[AB_O], uint32_t((ntiles - 1) & 1), kAWaitLimit);
+    if (!__syncthreads_or(fail)) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + ((s0 + q0 + tid) * p.Hq + h) * kAD;
+#pragma unroll
+        for (int q = 0; q < kAD; q += 16) {
+            float o[16];
+            tmem_ld16(tO + lane_addr + q, o);
+            tmem_ld_wait();
+            uint4 w0, w1;
+            w0.x = pack2(o[0] * inv, o[1] * inv);
+            w0.y = pack2(o[2] * inv, o[3] * inv);
+            w0.z = pack2(o[4] * inv, o[5] * inv);
+            w0.w = pack2(o[6] * inv, o[7] * inv);
+            w1.x = pack2(o[8] * inv, o[9] * inv);
+            w1.y = pack2(o[10] * inv, o[11] * inv);
+            w1.z = pack2(o[12] * inv, o[13] * inv);
+            w1.w = pack2(o[14] * inv, o[15] * inv);
+            if (tid < rows) {
+                *reinterpret_cast<uint4*>(out + q) = w0;
+                *reinterpret_cast<uint4*>(out + q + 8) = w1;
+            }
+        }
+    } else if (tid == 0) {
+        atomicAdd(&g_attn_timeouts, 1);
+        // let TMA copies still in flight land before shared memory goes away
+        mbar_wait(&bars[AB_Q], 0, kAWaitLimit);
+        for (int st = 0; st < kAStages; ++st)
+            if (last_kv[st] >= 0)
+                mbar_wait(&bars[AB_KV + st], uint32_t((last_kv[st] / kAStages) & 1), kAWaitLimit);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kATmemCols);
+}
+
+typedef CUresult (*AttnEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                 CUtensorMapFloatOOBfill);
+
+AttnEncodeFn attn_encode_fn() {
+    static AttnEncodeFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<AttnEncodeFn>(f);
+    }
+    return fn;
+}
+
+// bf16 rows of `width` elements, row pitch `pitch` elements; boxes of
+// 64 columns x 128 rows with the 128-byte swizzle.
+bool attn_map(CUtensorMap* m, const void* base, int64_t width, int64_t rows, int64_t pitch) {
+    AttnEncodeFn enc = attn_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cuuint64_t(width), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(pitch) * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_rows(const AttnParams& p, cudaStream_t s) {
+    if (p.B == 0) return cudaSuccess;
+    if (p.T > 0) {
+        const int64_t items = p.T * p.Hkv * (kAD / 8);
+        timer_begin(s, "attn_append_kernel");
+        attn_append_kernel<<<unsigned((items + 255) / 256), 256, 0, s>>>(p);
+        timer_end(s);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (p.T == 0) return cudaSuccess;
+    AttnMaps maps;
+    const int64_t cache_rows = int64_t(p.B) * p.Hkv * p.cap;
+    if (cache_rows > INT32_MAX || p.T > INT32_MAX) return cudaErrorInvalidValue;
+    if (!attn_map(&maps.q, p.q, int64_t(p.Hq) * kAD, p.T, int64_t(p.Hq) * kAD) ||
+        !attn_map(&maps.kc, p.k_cache, kAD, cache_rows, kAD) || !attn_map(&maps.vc, p.v_cache, kAD, cache_rows, kAD))
+        return cudaErrorInvalidValue;
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(attn_rows_kernel), int(kASmem));
+    if (e != cudaSuccess) return e;
+    const unsigned qtiles = unsigned((p.max_len + kAQ - 1) / kAQ);
+    if (qtiles == 0) return cudaSuccess;
+    timer_begin(s, "attn_rows_kernel");
+    attn_rows_kernel<<<dim3(qtiles, p.Hq, p.B), kAThreads, kASmem, s>>>(p, maps);
+    timer_end(s);
+    return cudaGetLastError();
+}
+
+int attn_read_timeouts() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_attn_timeouts, sizeof(int)) != cudaSuccess) return -1;
+    return v;
+}
+
+}  // namespace gdn

@@ -99,6 +99,26 @@ cudaError_t launch_wkv_rows(const WkvParams& p, cudaStream_t s);
 int wkv_read_timeouts();
 int tc_read_timeouts();     // same for the tensor-core chunk kernel
 
+// Full-attention rows over a KV cache plus the chunk's causal prefix: q
+// [T, Hq, 128], k, v [T, Hkv, 128], caches [B, Hkv, cap, 128], o [T, Hq, 128],
+// all bf16; cache_len [B] int32 (device).
+struct AttnParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* k_cache;
+    void* v_cache;
+    void* o;
+    const int32_t* cu;
+    const int32_t* cache_len;
+    int64_t T;
+    int64_t max_len;         // upper bound on any sequence's length (grid size)
+    int B, Hq, Hkv, cap;
+    float scale;
+};
+cudaError_t launch_attn_rows(const AttnParams& p, cudaStream_t s);
+int attn_read_timeouts();
+
 // Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
 // current device; the attribute is set once per (device, kernel, size) rather
 // than on every launch.

@@ -201,3 +201,35 @@ def wkv_rows(p, device="cuda", **kw):
     call.run()
     torch.cuda.synchronize(call.k.device)
     return call.wkv.cpu(), call.state_out.cpu()
+
+
+class AttnCall:
+    """Device buffers of one ``gdn_attn_rows`` call over an ``AttnProblem``
+    (the caches are copied, so ``run()`` may be repeated: it rewrites the
+    same appended rows)."""
+
+    def __init__(self, p, device="cuda"):
+        dev = torch.device(device)
+        self.p = p
+        self.q = p.q.to(dev).contiguous()
+        self.k = p.k.to(dev).contiguous()
+        self.v = p.v.to(dev).contiguous()
+        self.k_cache = p.k_cache.to(dev).contiguous()
+        self.v_cache = p.v_cache.to(dev).contiguous()
+        self.cache_len = p.cache_len.to(dev, torch.int32)
+        self.cu = p.cu_seqlens.to(dev, torch.int32)
+        self.o = torch.empty_like(self.q)
+        self.Hq, self.Hkv, self.D, self.cap = p.q.shape[1], p.k.shape[1], p.q.shape[2], p.k_cache.shape[2]
+
+    def run(self, stream=None):
+        B.gdn_attn_rows(self.q, self.k, self.v, self.k_cache, self.v_cache, self.cache_len, self.o,
+                        self.cu, self.p.B, self.Hq, self.Hkv, self.D, self.cap, self.p.T, self.p.scale,
+                        stream)
+
+
+def attn_rows(p, device="cuda"):
+    """One synchronous attention call; returns CPU (o, k_cache, v_cache)."""
+    call = AttnCall(p, device)
+    call.run()
+    torch.cuda.synchronize(call.q.device)
+    return call.o.cpu(), call.k_cache.cpu(), call.v_cache.cpu()

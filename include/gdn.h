@@ -264,8 +264,37 @@ int gdn_wkv_rows(const float* k, const float* v, const float* w, const float* u,
                  int B, int C, int64_t T_total, void* workspace, size_t workspace_bytes,
                  gdn_stream_t stream);
 
+/* ---- Full-attention rows over a KV cache ---------------------------------
+ * The full-attention layers of a prefill chunk in "perf(qwen3_5): prefill
+ * text prompts in multi-token chunks" (Implementation): the chunk's present
+ * k / v rows are appended to the KV cache, and every query row attends over
+ * the cache plus the chunk's causal prefix.  For sequence n with c =
+ * cache_len[n] cached rows and chunk rows t = 0 .. L_n - 1:
+ *   cache[n, kv, c + t] = (k_t, v_t) for every kv head (rows at or past the
+ *                         capacity are dropped),
+ *   o_t = softmax_j(scale q_t . K[j]) V[j] over cache rows j = 0 .. c + t,
+ * with query head h reading kv head h / (Hq / Hkv).  bf16 tensors, fp32
+ * scores, softmax and accumulation; head_dim must be 128.  cache_len is not
+ * advanced (the caller commits the rows, as the page's runtime does).
+ *
+ *   q           [T_total, Hq, 128] bf16
+ *   k, v        [T_total, Hkv, 128] bf16
+ *   k_cache, v_cache  [B, Hkv, cache_capacity, 128] bf16, updated in place;
+ *               cache_len[n] + L_n must not exceed cache_capacity
+ *   cache_len   [B] int32 (device)
+ *   o           [T_total, Hq, 128] bf16
+ *   cu_seqlens  [B+1] int32: cu[0] = 0, non-decreasing, cu[B] = T_total
+ *   scale       score scale; 0 selects 1 / sqrt(128)
+ * Device pointers, 16-byte aligned; two kernels on `stream`; nothing
+ * allocated.  Status: GDN_OK; GDN_ERR_INVALID_ARG; GDN_ERR_UNSUPPORTED
+ * (head_dim != 128, Hq % Hkv != 0); GDN_ERR_ALIGN; GDN_ERR_TOO_LARGE;
+ * GDN_ERR_CUDA. */
+int gdn_attn_rows(const void* q, const void* k, const void* v, void* k_cache, void* v_cache,
+                  const int32_t* cache_len, void* o, const int32_t* cu_seqlens, int B, int Hq, int Hkv,
+                  int head_dim, int cache_capacity, int64_t T_total, float scale, gdn_stream_t stream);
+
 /* Bounded device waits that ran out since the library was loaded (tensor-core
- * chunk kernel, selective scan and WKV rows; a CTA whose wait runs out abandons its
+ * chunk kernel, selective scan, WKV rows and attention rows; a CTA whose wait runs out abandons its
  * work, so every result of the call that hit it is unspecified).  Waits for
  * the device to finish its work.  Returns the count, or -1 on a CUDA error. */
 long long gdn_wait_timeouts(void);

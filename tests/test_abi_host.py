@@ -222,3 +222,24 @@ def test_wkv_rows_argument_checks(lib):
     assert call(wkv=A + 8) == B.GDN_ERR_ALIGN
     assert call(wsb=ws - 256) == B.GDN_ERR_WORKSPACE
     assert call(B=0, T=0) == B.GDN_OK
+
+
+def test_attn_rows_argument_checks(lib):
+    """Attention rows: invalid calls are rejected before any CUDA call."""
+    good = dict(q=A, k=A, v=A, kc=A, vc=A, cl=A, o=A, cu=A, B=1, Hq=4, Hkv=2, D=128, cap=256, T=100,
+                scale=0.0)
+
+    def call(**kw):
+        d = dict(good, **kw)
+        return lib.gdn_attn_rows(d["q"], d["k"], d["v"], d["kc"], d["vc"], d["cl"], d["o"], d["cu"],
+                                 d["B"], d["Hq"], d["Hkv"], d["D"], d["cap"], d["T"], d["scale"], None)
+    assert call(B=-1) == B.GDN_ERR_INVALID_ARG
+    assert call(cap=0) == B.GDN_ERR_INVALID_ARG
+    assert call(scale=-1.0) == B.GDN_ERR_INVALID_ARG
+    assert call(D=64) == B.GDN_ERR_UNSUPPORTED
+    assert call(Hq=3) == B.GDN_ERR_UNSUPPORTED
+    assert call(q=None) == B.GDN_ERR_INVALID_ARG
+    assert call(cl=None) == B.GDN_ERR_INVALID_ARG
+    assert call(o=A + 2) == B.GDN_ERR_ALIGN
+    assert call(cap=1 << 30) == B.GDN_ERR_TOO_LARGE
+    assert call(B=0, T=0) == B.GDN_OK
