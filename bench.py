@@ -248,6 +248,8 @@ SCAN_METRIC = "selective-scan rows: tokens/s (1 GB300) and % of HBM roofline, 24
 SCAN_WORKLOAD = "scan-4k: B=1, T=4096, C=24576 (1536 x 16), fp32 a, b, h"
 WKV_METRIC = "RWKV-4 WKV rows: tokens/s (1 GB300) and % of HBM roofline, 4096 channels, 4096-token prompt"
 WKV_WORKLOAD = "wkv-4k: B=1, T=4096, C=4096 (RWKV-4 7B width), fp32 k, v, wkv"
+ATTN_METRIC = "full-attention rows: tokens/s (1 GB300) and % of bf16 tensor roofline, 4096-token prompt, Hq=16, Hkv=2, d=128"
+ATTN_WORKLOAD = "attn-4k: B=1, T=4096 over an empty cache, Hq=16, Hkv=2, head dim 128, bf16"
 
 
 class _RowSpec:
@@ -263,6 +265,20 @@ class _RowSpec:
             self.inputs, self.outputs = ("a", "b", "h_in"), ("h_rows", "h_out")
             # a, b read once, h_rows written once, h_in read, h_out written
             self.nbytes = (3 * self.p.T + 2 * self.p.B) * self.p.C * 4
+        elif kind == "attn":
+            self.metric, self.workload = ATTN_METRIC, ATTN_WORKLOAD
+            self.p = inputs.make_attn_config(2)
+            self.make_call = runner.AttnCall
+            self.inputs, self.outputs = ("q", "k", "v", "k_cache", "v_cache"), ("o", "k_cache", "v_cache")
+            p = self.p
+            Hq, Hkv, D = p.q.shape[1], p.k.shape[1], p.q.shape[2]
+            # q, k, v read once, o written once, the appended k / v rows written once
+            self.nbytes = p.T * (2 * Hq + 4 * Hkv) * D * 2
+            # Q K^T and P V over the causal prefix: 4 D flops per (query, visible key)
+            visible = sum((int(c) + i + 1) for c, L in zip(p.cache_len.tolist(),
+                                                             (p.cu_seqlens[1:] - p.cu_seqlens[:-1]).tolist())
+                          for i in range(int(L)))
+            self.nflops = 4 * D * Hq * visible
         else:
             self.metric, self.workload = WKV_METRIC, WKV_WORKLOAD
             self.p = inputs.make_wkv_config(2)
@@ -272,8 +288,14 @@ class _RowSpec:
             self.nbytes = (3 * self.p.T + 2 + 6 * self.p.B) * self.p.C * 4
 
     def oracle_pass(self, cols):
-        """One float64 oracle pass over the first ``cols`` channels."""
+        """One float64 oracle pass over the first ``cols`` channels (query
+        heads for the attention rows)."""
         p = self.p
+        if self.kind == "attn":
+            from oracle import attn_rows as ar
+            ar.oracle_attn_rows(self._q, p.k[:self._rows], p.v[:self._rows], p.k_cache, p.v_cache,
+                                p.cache_len, [0, self._rows], p.scale)
+            return
         if self.kind == "scan":
             from oracle import scan_rows as sr
             sr.oracle_scan_rows(self._a, self._b, p.cu_seqlens, self._h)
@@ -283,6 +305,11 @@ class _RowSpec:
 
     def sample(self, cols):
         p = self.p
+        if self.kind == "attn":
+            # the first ``cols`` query rows, every head (the oracle is quadratic in rows)
+            self._rows = cols
+            self._q = p.q[:cols]
+            return
         if self.kind == "scan":
             self._a, self._b, self._h = (p.a[:, :cols].numpy(), p.b[:, :cols].numpy(),
                                          p.h_in[:, :cols].numpy())
@@ -306,13 +333,14 @@ def run_row(args, rank, world):
             return
         import oracle
         oracle.build_oracle()
-        cols = 1024 if args.row == "scan" else 256     # sampled channels per step
+        cols = {"scan": 1024, "wkv": 256, "attn": 512}[args.row]   # sampled channels (rows) per step
         spec.sample(cols)
         t0 = time.perf_counter()
         for _ in range(args.steps):
             spec.oracle_pass(cols)
         el = time.perf_counter() - t0
-        tps = p.T * args.steps / el * cols / p.C     # whole-row equivalents
+        # whole-row equivalents (attention: rows of the prefix, a lower bound on the full prompt's cost)
+        tps = p.T * args.steps / el * cols / p.C if args.row != "attn" else cols * args.steps / el
         line = {"metric": spec.metric, "value": tps, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -321,7 +349,9 @@ def run_row(args, rank, world):
                            "parallelism": "replicas"},
                 "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": oracle.max_threads(),
                                  "kind": "oracle",
-                                 "sample": f"{cols} of {p.C} channels, all {p.T} rows, per step"},
+                                 "sample": (f"the first {cols} of {p.T} rows, all heads, per step"
+                                            if args.row == "attn" else
+                                            f"{cols} of {p.C} channels, all {p.T} rows, per step")},
                 "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -369,15 +399,21 @@ def run_row(args, rank, world):
     ms_step = ms_total / args.steps
     dominant = max(per_kernel, key=lambda k: per_kernel[k][0])
     kern_ms = per_kernel[dominant][0] / per_kernel[dominant][1]
-    hbm, _, peak_kind = load_peaks()
-    achieved = spec.nbytes / (kern_ms * 1e-3) / 1e9
-    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+    hbm, tflops, peak_kind = load_peaks()
+    if getattr(spec, "nflops", None) and spec.nflops / (tflops * 1e12) > spec.nbytes / (hbm * 1e9):
+        achieved = spec.nflops / (kern_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
+                "frac": achieved / tflops, "algorithmic_flops": spec.nflops}
+    else:
+        achieved = spec.nbytes / (kern_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm}
+    roof.update({
             "traffic": recorded_traffic(dominant), "peak_source": peak_kind, "kernel": dominant,
             "algorithmic_bytes": spec.nbytes, "kernel_ms_per_launch": kern_ms,
             "kernels": {k: {"launches_per_step": n / args.steps, "ms_per_launch": tot / n,
                             "share": tot / sum(v[0] for v in per_kernel.values())}
                         for k, (tot, n) in sorted(per_kernel.items())},
-            "untimed_launches": dropped}
+            "untimed_launches": dropped})
     # end to end: the inputs from pinned host memory, the outputs back
     host_in = {n: getattr(one, n).cpu().pin_memory() for n in spec.inputs}
     host_out = {n: torch.empty_like(getattr(one, n), device="cpu").pin_memory() for n in spec.outputs}
@@ -401,19 +437,24 @@ def run_row(args, rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build_oracle()
-        cols = 2048 if args.row == "scan" else 512
+        cols = {"scan": 2048, "wkv": 512, "attn": 1024}[args.row]
         spec.sample(cols)
         n, t0 = 0, time.perf_counter()
         while time.perf_counter() - t0 < 10.0:
             spec.oracle_pass(cols)
             n += 1
         el = time.perf_counter() - t0
-        cpu = {"value": p.T * n / el * cols / p.C, "unit": "tokens/s", "cores": oracle.max_threads(),
-               "kind": "oracle", "sample": f"{n} passes over {cols} of {p.C} channels, all {p.T} rows"}
+        if args.row == "attn":
+            cpu = {"value": cols * n / el, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+                   "sample": f"{n} passes over the first {cols} of {p.T} rows, all heads"}
+        else:
+            cpu = {"value": p.T * n / el * cols / p.C, "unit": "tokens/s", "cores": oracle.max_threads(),
+                   "kind": "oracle", "sample": f"{n} passes over {cols} of {p.C} channels, all {p.T} rows"}
     if rank == 0:
         line = {"metric": spec.metric, "value": world * p.T / (ms_step * 1e-3), "unit": "tokens/s",
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if args.row == "attn" else "f32",
                 "data": "synthetic",
                 "config": {"workload": spec.workload, "global_batch": p.B, "seq_len": p.T,
                            "parallelism": "replicas" if world > 1 else "single",
@@ -437,9 +478,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--row", default="gdn", choices=["gdn", "scan", "wkv"],
+    ap.add_argument("--row", default="gdn", choices=["gdn", "scan", "wkv", "attn"],
                     help="gdn: the chunked gated delta rule prefill (the headline); "
-                         "scan: the selective-scan rows; wkv: the RWKV-4 WKV rows")
+                         "scan: the selective-scan rows; wkv: the RWKV-4 WKV rows; "
+                         "attn: the full-attention rows over a KV cache")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 

@@ -10,8 +10,9 @@
 // memory, 128-key tiles of K and V stream through three TMA stages, and
 // per key tile
 //   S = Q K^T                    tcgen05 MMA into TMEM (128 x 128 fp32)
-//   P = exp2(S scale - m)        one query row per thread (its TMEM lane),
-//                                causal / capacity mask, bf16 into TMEM
+//   P = exp2(S scale - m)        two threads per query row (its TMEM lane),
+//                                one per half of the keys; causal / capacity
+//                                mask; bf16 into TMEM
 //   O += P V                     tcgen05 MMA, A = P from TMEM, fp32 in TMEM
 // with the running row maximum m raised (and O, l rescaled) only when a
 // tile's maximum exceeds it by more than 2^8, so P stays below 256.  The
@@ -34,14 +35,15 @@ constexpr int kAD = 128;              // head dim
 constexpr int kAQ = 128;              // query rows per tile (TMEM lanes)
 constexpr int kAK = 128;              // keys per tile
 constexpr int kAStages = 3;
-constexpr int kAThreads = 128;
+constexpr int kAThreads = 256;       // two threads per query row: one per half of the keys
 constexpr uint32_t kAWaitLimit = 1u << 20;
 constexpr float kARescale = 8.f;      // log2 headroom before the reference maximum moves
 constexpr uint32_t kATile = kAK * kAD * 2;                 // 32 KB per K or V tile
 constexpr uint32_t kAOffQ = 0;
 constexpr uint32_t kAOffKV = kATile;                       // stage s: K at +2s tiles, V at +2s+1
 constexpr uint32_t kAOffBar = kAOffKV + kAStages * 2 * kATile;
-constexpr uint32_t kASmem = kAOffBar + 8 * 8 + 1024;
+constexpr uint32_t kAOffEx = kAOffBar + 8 * 8;             // [2][kAQ] floats: row maxima, then sums
+constexpr uint32_t kASmem = kAOffEx + 2 * kAQ * 4 + 1024;
 static_assert(kASmem <= 232448, "attention stages above the 227 KB per-block limit");
 constexpr uint32_t kAColS = 0, kAColP = 128, kAColO = 256, kATmemCols = 512;
 enum : int { AB_Q = 0, AB_KV = 1, AB_S = 1 + kAStages, AB_O = 2 + kAStages };
@@ -95,8 +97,11 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
     extern __shared__ uint8_t attn_smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(attn_smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kAOffBar);
+    float* s_ex = reinterpret_cast<float*>(sm + kAOffEx);       // per half and row
     __shared__ uint32_t tmem_slot;
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int row = (warp & 3) * 32 + (tid & 31);                 // TMEM lane = query row
+    const int half = warp >> 2;                                   // keys (and O columns) 64 half ..
     const int h = blockIdx.y, n = blockIdx.z;
     const int xt = int(gridDim.x) - 1 - int(blockIdx.x);          // long (late) tiles first
     const int64_t s0 = p.cu[n];
@@ -127,7 +132,7 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     const uint32_t tS = tmem + kAColS, tP = tmem + kAColP, tO = tmem + kAColO;
-    const uint32_t lane_addr = uint32_t(warp * 32) << 16;
+    const uint32_t lane_addr = uint32_t((warp & 3) * 32) << 16;
     const uint32_t id_s = idesc_bf16(kAQ, kAK, 0, 0);             // B = K, K-major
     const uint32_t id_o = idesc_bf16(kAQ, kAD, 0, 1);             // B = V, MN-major [key][d]
     uint8_t* sQ = sm + kAOffQ;
@@ -170,7 +175,7 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
         }
     }
     const float sl2 = p.scale * 1.4426950408889634f;
-    const int pos = clen + q0 + tid;                              // this row sees keys 0 .. pos
+    const int pos = clen + q0 + row;                              // this row sees keys 0 .. pos
     float m_ref = -INFINITY, l = 0.f;
     for (int j = 0; j < ntiles; ++j) {
         if (tid == 0 && !fail) fail = !mbar_wait(&bars[AB_S], uint32_t(j & 1), kAWaitLimit);
@@ -179,14 +184,17 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
             break;
         }
         tc_fence_after();
-        // ---- this row of S_j; the S buffer is then free for S_{j+1} ------------
-        float x[kAK];
+        // ---- this thread's half of the row of S_j, masked; its maximum is
+        // exchanged at the barrier that also frees the S buffer for S_{j+1} --
+        const int k0 = j * kAK + half * (kAK / 2);
+        float x[kAK / 2];
+        float mh = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < kAK; q += 32) {
+        for (int q = 0; q < kAK / 2; q += 32) {
             uint32_t r0[16], r1[16];
             __syncwarp();
-            GDN_TMEM_LD_X16(tS + lane_addr + q, r0);
-            GDN_TMEM_LD_X16(tS + lane_addr + q + 16, r1);
+            GDN_TMEM_LD_X16(tS + lane_addr + half * (kAK / 2) + q, r0);
+            GDN_TMEM_LD_X16(tS + lane_addr + half * (kAK / 2) + q + 16, r1);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -194,6 +202,13 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
                 x[q + 16 + i] = __uint_as_float(r1[i]);
             }
         }
+#pragma unroll
+        for (int c = 0; c < kAK / 2; ++c) {
+            const int kk = k0 + c;
+            x[c] = (kk <= pos && kk < nkeys) ? x[c] * sl2 : -INFINITY;
+            mh = fmaxf(mh, x[c]);
+        }
+        s_ex[half * kAQ + row] = mh;
         tc_fence_before();
         __syncthreads();
         if (tid == 0 && j + 1 < ntiles) {
@@ -203,15 +218,8 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
                 issue_s(j + 1);
             }
         }
-        // ---- softmax of the row: mask, running maximum, exponentials ------------
-        const int k0 = j * kAK;
-        float mt = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kAK; ++c) {
-            const int kk = k0 + c;
-            x[c] = (kk <= pos && kk < nkeys) ? x[c] * sl2 : -INFINITY;
-            mt = fmaxf(mt, x[c]);
-        }
+        // ---- running maximum and exponentials (both halves agree on m_ref) -------
+        const float mt = fmaxf(s_ex[row], s_ex[kAQ + row]);
         float f = 1.f;                                            // rescale of O and l
         if (j == 0) {
             m_ref = mt;
@@ -220,9 +228,9 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
             m_ref = mt;
         }
         l *= f;
-        uint32_t pk[kAK / 2];
+        uint32_t pk[kAK / 4];
 #pragma unroll
-        for (int c = 0; c < kAK; c += 2) {
+        for (int c = 0; c < kAK / 2; c += 2) {
             const float e0 = ex2(x[c] - m_ref), e1 = ex2(x[c + 1] - m_ref);
             pk[c / 2] = pack2(e0, e1);
             const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&pk[c / 2]);
@@ -240,21 +248,21 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
             break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, f != 1.f)) {                  // rescale this warp's rows of O
+        if (__any_sync(0xffffffffu, f != 1.f)) {                  // rescale this warp's half rows of O
 #pragma unroll
-            for (int q = 0; q < kAD; q += 16) {
+            for (int q = 0; q < kAD / 2; q += 16) {
                 float o[16];
-                tmem_ld16(tO + lane_addr + q, o);
+                tmem_ld16(tO + lane_addr + half * (kAD / 2) + q, o);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) o[i] *= f;
-                tmem_st16(tO + lane_addr + q, o);
+                tmem_st16(tO + lane_addr + half * (kAD / 2) + q, o);
             }
         }
 #pragma unroll
-        for (int q = 0; q < kAK / 2; q += 16) {
+        for (int q = 0; q < kAK / 4; q += 16) {
             __syncwarp();
-            GDN_TMEM_ST_X16(tP + lane_addr + q, (pk + q));
+            GDN_TMEM_ST_X16(tP + lane_addr + half * (kAK / 4) + q, (pk + q));
         }
         tmem_st_wait();
         tc_fence_before();
@@ -270,14 +278,15 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
     }
     // ---- O / l to the output rows ------------------------------------------------
     if (tid == 0 && !fail) fail = !mbar_wait(&bars[AB_O], uint32_t((ntiles - 1) & 1), kAWaitLimit);
+    s_ex[half * kAQ + row] = l;                                   // the loop's last reads of s_ex are done
     if (!__syncthreads_or(fail)) {
         tc_fence_after();
-        const float inv = 1.f / l;
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + ((s0 + q0 + tid) * p.Hq + h) * kAD;
+        const float inv = 1.f / (s_ex[row] + s_ex[kAQ + row]);
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + ((s0 + q0 + row) * p.Hq + h) * kAD + half * (kAD / 2);
 #pragma unroll
-        for (int q = 0; q < kAD; q += 16) {
+        for (int q = 0; q < kAD / 2; q += 16) {
             float o[16];
-            tmem_ld16(tO + lane_addr + q, o);
+            tmem_ld16(tO + lane_addr + half * (kAD / 2) + q, o);
             tmem_ld_wait();
             uint4 w0, w1;
             w0.x = pack2(o[0] * inv, o[1] * inv);
@@ -288,7 +297,7 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
             w1.y = pack2(o[10] * inv, o[11] * inv);
             w1.z = pack2(o[12] * inv, o[13] * inv);
             w1.w = pack2(o[14] * inv, o[15] * inv);
-            if (tid < rows) {
+            if (row < rows) {
                 *reinterpret_cast<uint4*>(out + q) = w0;
                 *reinterpret_cast<uint4*>(out + q + 8) = w1;
             }
