@@ -6,17 +6,17 @@
 //
 // attn_append_kernel writes the prompt's k, v rows into the cache after each
 // sequence's cache_len rows.  attn_rows_kernel then runs one CTA per
-// (128-row query tile, query head, sequence): the query tile stays in shared
-// memory, 128-key tiles of K and V stream through three TMA stages, and
-// per key tile
-//   S = Q K^T                    tcgen05 MMA into TMEM (128 x 128 fp32)
-//   P = exp2(S scale - m)        two threads per query row (its TMEM lane),
-//                                one per half of the keys; causal / capacity
-//                                mask; bf16 into TMEM
-//   O += P V                     tcgen05 MMA, A = P from TMEM, fp32 in TMEM
-// with the running row maximum m raised (and O, l rescaled) only when a
-// tile's maximum exceeds it by more than 2^8, so P stays below 256.  The
-// next tile's S MMA runs while the current tile's softmax is computed.
+// (128-row query tile, query head, sequence), warp-specialised:
+//   warp 8      TMA: the query tile once, key tiles (3 stages) and value
+//               tiles (2 stages) of 128 rows from the cache;
+//   warp 9      tcgen05 MMAs: S_j = Q K_j^T into one of two TMEM buffers, then
+//               O += P_{j-1} V_{j-1} with P (bf16) as the A operand from TMEM;
+//   warps 0-7   softmax, two threads per query row (its TMEM lane), one per
+//               half of the keys: causal / capacity mask, running maximum
+//               (raised, with O and l rescaled, only past 2^8 of headroom),
+//               P = exp2(S scale - m) into TMEM.
+// mbarriers hand every buffer between the roles, so the MMAs of tile j + 1
+// run while tile j's softmax is computed.
 #include <cuda.h>
 #include <climits>
 
@@ -34,19 +34,33 @@ using namespace ptx;
 constexpr int kAD = 128;              // head dim
 constexpr int kAQ = 128;              // query rows per tile (TMEM lanes)
 constexpr int kAK = 128;              // keys per tile
-constexpr int kAStages = 3;
-constexpr int kAThreads = 256;       // two threads per query row: one per half of the keys
+constexpr int kAKStages = 3, kAVStages = 2;
+constexpr int kASoftThreads = 256;    // warps 0-7
+constexpr int kAThreads = kASoftThreads + 64;   // + TMA warp + MMA warp
 constexpr uint32_t kAWaitLimit = 1u << 20;
 constexpr float kARescale = 8.f;      // log2 headroom before the reference maximum moves
-constexpr uint32_t kATile = kAK * kAD * 2;                 // 32 KB per K or V tile
+constexpr uint32_t kATile = kAK * kAD * 2;                 // 32 KB per Q, K or V tile
 constexpr uint32_t kAOffQ = 0;
-constexpr uint32_t kAOffKV = kATile;                       // stage s: K at +2s tiles, V at +2s+1
-constexpr uint32_t kAOffBar = kAOffKV + kAStages * 2 * kATile;
-constexpr uint32_t kAOffEx = kAOffBar + 8 * 8;             // [2][kAQ] floats: row maxima, then sums
-constexpr uint32_t kASmem = kAOffEx + 2 * kAQ * 4 + 1024;
+constexpr uint32_t kAOffK = kATile;
+constexpr uint32_t kAOffV = kAOffK + kAKStages * kATile;
+constexpr uint32_t kAOffBar = kAOffV + kAVStages * kATile;
+constexpr uint32_t kANumBars = 17;
+constexpr uint32_t kAOffEx = kAOffBar + 256;               // [2 parities][2 halves][kAQ] floats: maxima
+constexpr uint32_t kAOffL = kAOffEx + 2 * 2 * kAQ * 4;     // [2 halves][kAQ] floats: row sums
+constexpr uint32_t kASmem = kAOffL + 2 * kAQ * 4 + 1024;
 static_assert(kASmem <= 232448, "attention stages above the 227 KB per-block limit");
-constexpr uint32_t kAColS = 0, kAColP = 128, kAColO = 256, kATmemCols = 512;
-enum : int { AB_Q = 0, AB_KV = 1, AB_S = 1 + kAStages, AB_O = 2 + kAStages };
+constexpr uint32_t kAColS = 0, kAColP = 256, kAColO = 384, kATmemCols = 512;
+enum : int {
+    AB_Q = 0,
+    AB_KFULL = 1,                     // + stage (3)
+    AB_KEMPTY = 4,                    // + stage (3)
+    AB_VFULL = 7,                     // + stage (2)
+    AB_VEMPTY = 9,                    // + stage (2)
+    AB_SFULL = 11,                    // + buffer (2)
+    AB_SEMPTY = 13,                   // + buffer (2), 8 arrivals
+    AB_PFULL = 15,                    // 8 arrivals
+    AB_ODONE = 16
+};
 
 struct AttnMaps {
     CUtensorMap q, kc, vc;
@@ -97,11 +111,11 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
     extern __shared__ uint8_t attn_smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(attn_smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kAOffBar);
-    float* s_ex = reinterpret_cast<float*>(sm + kAOffEx);       // per half and row
+    float* s_ex = reinterpret_cast<float*>(sm + kAOffEx);
+    float* s_l = reinterpret_cast<float*>(sm + kAOffL);
     __shared__ uint32_t tmem_slot;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int row = (warp & 3) * 32 + (tid & 31);                 // TMEM lane = query row
-    const int half = warp >> 2;                                   // keys (and O columns) 64 half ..
+    __shared__ volatile int s_fail;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.y, n = blockIdx.z;
     const int xt = int(gridDim.x) - 1 - int(blockIdx.x);          // long (late) tiles first
     const int64_t s0 = p.cu[n];
@@ -117,11 +131,10 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
     const int kv_row0 = int((int64_t(n) * p.Hkv + kh) * p.cap);
 
     if (tid == 0) {
-        for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < int(kANumBars); ++i)
+            mbar_init(&bars[i], (i == AB_SEMPTY || i == AB_SEMPTY + 1 || i == AB_PFULL) ? 8 : 1);
         fence_mbar_init();
-        tma_prefetch_desc(&maps.q);
-        tma_prefetch_desc(&maps.kc);
-        tma_prefetch_desc(&maps.vc);
+        s_fail = 0;
     }
     if (warp == 0) {
         tmem_alloc(&tmem_slot, kATmemCols);
@@ -131,187 +144,217 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    const uint32_t tS = tmem + kAColS, tP = tmem + kAColP, tO = tmem + kAColO;
-    const uint32_t lane_addr = uint32_t((warp & 3) * 32) << 16;
-    const uint32_t id_s = idesc_bf16(kAQ, kAK, 0, 0);             // B = K, K-major
-    const uint32_t id_o = idesc_bf16(kAQ, kAD, 0, 1);             // B = V, MN-major [key][d]
-    uint8_t* sQ = sm + kAOffQ;
-    auto sK = [&](int j) { return sm + kAOffKV + uint32_t(j % kAStages) * 2 * kATile; };
-    auto sV = [&](int j) { return sK(j) + kATile; };
-    auto issue_kv = [&](int j) {
-        uint64_t* bar = &bars[AB_KV + j % kAStages];
-        mbar_arrive_expect_tx(bar, 2 * kATile);
-        const int y = kv_row0 + j * kAK;
-        tma_load_2d(sK(j), &maps.kc, bar, 0, y);
-        tma_load_2d(sK(j) + kATile / 2, &maps.kc, bar, 64, y);
-        tma_load_2d(sV(j), &maps.vc, bar, 0, y);
-        tma_load_2d(sV(j) + kATile / 2, &maps.vc, bar, 64, y);
+    const uint32_t tP = tmem + kAColP, tO = tmem + kAColO;
+    auto wait = [&](int b, uint32_t parity) {
+        if (s_fail) return false;
+        if (mbar_wait(&bars[b], parity, kAWaitLimit)) return true;
+        s_fail = 1;
+        return false;
     };
-    auto issue_s = [&](int j) {                                   // S = Q K_j^T
-        const uint64_t dq = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128B);
-        const uint64_t dk = smem_desc(smem_u32(sK(j)), 16, 1024, kSwizzle128B);
-#pragma unroll
-        for (int s = 0; s < kAD / 16; ++s) {
-            const uint32_t off = uint32_t(s >> 2) * (kATile / 2) + uint32_t(s & 3) * 32u;
-            umma_f16(tS, dq + (off >> 4), dk + (off >> 4), id_s, s > 0);
-        }
-        umma_commit(&bars[AB_S]);
-    };
-    bool fail = false;
-    int last_kv[kAStages] = {-1, -1, -1};                          // thread 0: last tile issued per stage
-    auto issue_kv_t = [&](int j) {
-        issue_kv(j);
-        last_kv[j % kAStages] = j;
-    };
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bars[AB_Q], kATile);
-        tma_load_2d(sQ, &maps.q, &bars[AB_Q], h * kAD, int(s0 + q0));
-        tma_load_2d(sQ + kATile / 2, &maps.q, &bars[AB_Q], h * kAD + 64, int(s0 + q0));
-        for (int j = 0; j < ntiles && j < 2; ++j) issue_kv_t(j);
-        fail = !mbar_wait(&bars[AB_Q], 0, kAWaitLimit) || !mbar_wait(&bars[AB_KV], 0, kAWaitLimit);
-        if (!fail) {
-            tc_fence_after();
-            issue_s(0);
-        }
-    }
-    const float sl2 = p.scale * 1.4426950408889634f;
-    const int pos = clen + q0 + row;                              // this row sees keys 0 .. pos
-    float m_ref = -INFINITY, l = 0.f;
-    for (int j = 0; j < ntiles; ++j) {
-        if (tid == 0 && !fail) fail = !mbar_wait(&bars[AB_S], uint32_t(j & 1), kAWaitLimit);
-        if (__syncthreads_or(fail)) {
-            fail = true;
-            break;
-        }
-        tc_fence_after();
-        // ---- this thread's half of the row of S_j, masked; its maximum is
-        // exchanged at the barrier that also frees the S buffer for S_{j+1} --
-        const int k0 = j * kAK + half * (kAK / 2);
-        float x[kAK / 2];
-        float mh = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < kAK / 2; q += 32) {
-            uint32_t r0[16], r1[16];
-            __syncwarp();
-            GDN_TMEM_LD_X16(tS + lane_addr + half * (kAK / 2) + q, r0);
-            GDN_TMEM_LD_X16(tS + lane_addr + half * (kAK / 2) + q + 16, r1);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                x[q + i] = __uint_as_float(r0[i]);
-                x[q + 16 + i] = __uint_as_float(r1[i]);
+
+    if (warp == 8) {
+        // ================================================================ TMA
+        if (lane == 0) {
+            tma_prefetch_desc(&maps.q);
+            tma_prefetch_desc(&maps.kc);
+            tma_prefetch_desc(&maps.vc);
+            uint8_t* sQ = sm + kAOffQ;
+            mbar_arrive_expect_tx(&bars[AB_Q], kATile);
+            tma_load_2d(sQ, &maps.q, &bars[AB_Q], h * kAD, int(s0 + q0));
+            tma_load_2d(sQ + kATile / 2, &maps.q, &bars[AB_Q], h * kAD + 64, int(s0 + q0));
+            int k_last[kAKStages] = {-1, -1, -1}, v_last[kAVStages] = {-1, -1};
+            for (int j = 0; j < ntiles; ++j) {
+                const int ks = j % kAKStages, vs = j % kAVStages, y = kv_row0 + j * kAK;
+                if (j >= kAKStages && !wait(AB_KEMPTY + ks, uint32_t((j / kAKStages - 1) & 1))) break;
+                uint8_t* dk = sm + kAOffK + ks * kATile;
+                mbar_arrive_expect_tx(&bars[AB_KFULL + ks], kATile);
+                tma_load_2d(dk, &maps.kc, &bars[AB_KFULL + ks], 0, y);
+                tma_load_2d(dk + kATile / 2, &maps.kc, &bars[AB_KFULL + ks], 64, y);
+                k_last[ks] = j;
+                if (j >= kAVStages && !wait(AB_VEMPTY + vs, uint32_t((j / kAVStages - 1) & 1))) break;
+                uint8_t* dv = sm + kAOffV + vs * kATile;
+                mbar_arrive_expect_tx(&bars[AB_VFULL + vs], kATile);
+                tma_load_2d(dv, &maps.vc, &bars[AB_VFULL + vs], 0, y);
+                tma_load_2d(dv + kATile / 2, &maps.vc, &bars[AB_VFULL + vs], 64, y);
+                v_last[vs] = j;
+            }
+            if (s_fail) {
+                // let the copies still in flight land before shared memory goes away
+                mbar_wait(&bars[AB_Q], 0, kAWaitLimit);
+                for (int st = 0; st < kAKStages; ++st)
+                    if (k_last[st] >= 0) mbar_wait(&bars[AB_KFULL + st], uint32_t((k_last[st] / kAKStages) & 1), kAWaitLimit);
+                for (int st = 0; st < kAVStages; ++st)
+                    if (v_last[st] >= 0) mbar_wait(&bars[AB_VFULL + st], uint32_t((v_last[st] / kAVStages) & 1), kAWaitLimit);
             }
         }
-#pragma unroll
-        for (int c = 0; c < kAK / 2; ++c) {
-            const int kk = k0 + c;
-            x[c] = (kk <= pos && kk < nkeys) ? x[c] * sl2 : -INFINITY;
-            mh = fmaxf(mh, x[c]);
-        }
-        s_ex[half * kAQ + row] = mh;
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0 && j + 1 < ntiles) {
-            fail = !mbar_wait(&bars[AB_KV + (j + 1) % kAStages], uint32_t(((j + 1) / kAStages) & 1), kAWaitLimit);
-            if (!fail) {
+        __syncwarp();
+    } else if (warp == 9) {
+        // ================================================================ MMA
+        if (lane == 0) {
+            const uint32_t id_s = idesc_bf16(kAQ, kAK, 0, 0);     // B = K, K-major
+            const uint32_t id_o = idesc_bf16(kAQ, kAD, 0, 1);     // B = V, MN-major [key][d]
+            const uint64_t dq = smem_desc(smem_u32(sm + kAOffQ), 16, 1024, kSwizzle128B);
+            auto issue_pv = [&](int j) {                          // O += P_j V_j
+                if (!wait(AB_VFULL + j % kAVStages, uint32_t((j / kAVStages) & 1))) return false;
+                if (!wait(AB_PFULL, uint32_t(j & 1))) return false;
                 tc_fence_after();
-                issue_s(j + 1);
-            }
-        }
-        // ---- running maximum and exponentials (both halves agree on m_ref) -------
-        const float mt = fmaxf(s_ex[row], s_ex[kAQ + row]);
-        float f = 1.f;                                            // rescale of O and l
-        if (j == 0) {
-            m_ref = mt;
-        } else if (mt > m_ref + kARescale) {
-            f = ex2(m_ref - mt);
-            m_ref = mt;
-        }
-        l *= f;
-        uint32_t pk[kAK / 4];
+                const uint64_t dv = smem_desc(smem_u32(sm + kAOffV + (j % kAVStages) * kATile), kATile / 2, 1024,
+                                              kSwizzle128B);
 #pragma unroll
-        for (int c = 0; c < kAK / 2; c += 2) {
-            const float e0 = ex2(x[c] - m_ref), e1 = ex2(x[c + 1] - m_ref);
-            pk[c / 2] = pack2(e0, e1);
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&pk[c / 2]);
-            const float2 r = __bfloat1622float2(b);
-            l += r.x + r.y;
+                for (int s = 0; s < kAK / 16; ++s)
+                    umma_f16_tmemA(tO, tP + s * 8, dv + uint64_t(s * 2048 >> 4), id_o, j > 0 || s > 0);
+                umma_commit(&bars[AB_ODONE]);
+                umma_commit(&bars[AB_VEMPTY + j % kAVStages]);
+                return true;
+            };
+            bool ok = wait(AB_Q, 0);
+            for (int j = 0; ok && j < ntiles; ++j) {
+                const int b = j & 1;
+                ok = wait(AB_KFULL + j % kAKStages, uint32_t((j / kAKStages) & 1));
+                if (ok && j >= 2) ok = wait(AB_SEMPTY + b, uint32_t(((j >> 1) - 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t dk = smem_desc(smem_u32(sm + kAOffK + (j % kAKStages) * kATile), 16, 1024, kSwizzle128B);
+#pragma unroll
+                for (int s = 0; s < kAD / 16; ++s) {
+                    const uint32_t off = uint32_t(s >> 2) * (kATile / 2) + uint32_t(s & 3) * 32u;
+                    umma_f16(tmem + kAColS + b * kAK, dq + (off >> 4), dk + (off >> 4), id_s, s > 0);
+                }
+                umma_commit(&bars[AB_SFULL + b]);
+                umma_commit(&bars[AB_KEMPTY + j % kAKStages]);
+                if (j >= 1) ok = issue_pv(j - 1);
+            }
+            if (ok && ntiles > 0) issue_pv(ntiles - 1);
         }
-        // ---- P_j replaces P_{j-1} once O += P_{j-1} V_{j-1} is done -------------
-        if (tid == 0 && !fail && j >= 1) {
-            fail = !mbar_wait(&bars[AB_O], uint32_t((j - 1) & 1), kAWaitLimit);
-            if (!fail && j + 2 < ntiles) issue_kv_t(j + 2);       // into the stage tile j-1 used
+        __syncwarp();
+    } else {
+        // ================================================================ softmax
+        const int row = (warp & 3) * 32 + lane;                   // TMEM lane = query row
+        const int half = warp >> 2;                               // keys 64 half .. 64 half + 63
+        const uint32_t lane_addr = uint32_t((warp & 3) * 32) << 16;
+        const uint32_t pair_bar = 1 + (warp & 3);                 // warps w and w + 4 share the rows
+        const float sl2 = p.scale * 1.4426950408889634f;
+        const int pos = clen + q0 + row;                          // this row sees keys 0 .. pos
+        float m_ref = -INFINITY, l = 0.f;
+        bool fail = false;
+        for (int j = 0; j < ntiles; ++j) {
+            const int b = j & 1;
+            if (lane == 0) fail = fail || !wait(AB_SFULL + b, uint32_t((j >> 1) & 1));
+            __syncwarp();
+            fail = __shfl_sync(0xffffffffu, fail, 0);
+            tc_fence_after();
+            float x[kAK / 2];
+            if (!fail) {
+#pragma unroll
+                for (int q = 0; q < kAK / 2; q += 32) {
+                    uint32_t r0[16], r1[16];
+                    const uint32_t ta = tmem + kAColS + b * kAK + lane_addr + half * (kAK / 2) + q;
+                    GDN_TMEM_LD_X16(ta, r0);
+                    GDN_TMEM_LD_X16(ta + 16, r1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        x[q + i] = __uint_as_float(r0[i]);
+                        x[q + 16 + i] = __uint_as_float(r1[i]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[AB_SEMPTY + b]);     // this warp is done with S_j
+            // ---- mask and the half-row maximum; the pair agrees on the row's -------
+            const int k0 = j * kAK + half * (kAK / 2);
+            float mh = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kAK / 2; ++c) {
+                const int kk = k0 + c;
+                x[c] = (!fail && kk <= pos && kk < nkeys) ? x[c] * sl2 : -INFINITY;
+                mh = fmaxf(mh, x[c]);
+            }
+            s_ex[(b * 2 + half) * kAQ + row] = mh;
+            if (named_sync_or(pair_bar, 64, fail)) {
+                fail = true;
+                break;
+            }
+            const float mt = fmaxf(s_ex[(b * 2) * kAQ + row], s_ex[(b * 2 + 1) * kAQ + row]);
+            float f = 1.f;                                        // rescale of O and l
+            if (j == 0) {
+                m_ref = mt;
+            } else if (mt > m_ref + kARescale) {
+                f = ex2(m_ref - mt);
+                m_ref = mt;
+            }
+            l *= f;
+            uint32_t pk[kAK / 4];
+#pragma unroll
+            for (int c = 0; c < kAK / 2; c += 2) {
+                const float e0 = ex2(x[c] - m_ref), e1 = ex2(x[c + 1] - m_ref);
+                pk[c / 2] = pack2(e0, e1);
+                const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(&pk[c / 2]);
+                const float2 r = __bfloat1622float2(bb);
+                l += r.x + r.y;
+            }
+            // ---- P_j replaces P_{j-1} once O += P_{j-1} V_{j-1} is done ----------
+            if (lane == 0 && j >= 1) fail = fail || !wait(AB_ODONE, uint32_t((j - 1) & 1));
+            __syncwarp();
+            fail = __shfl_sync(0xffffffffu, fail, 0);
+            tc_fence_after();
+            if (!fail && __any_sync(0xffffffffu, f != 1.f)) {     // rescale this warp's half rows of O
+#pragma unroll
+                for (int q = 0; q < kAD / 2; q += 16) {
+                    float o[16];
+                    tmem_ld16(tO + lane_addr + half * (kAD / 2) + q, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o[i] *= f;
+                    tmem_st16(tO + lane_addr + half * (kAD / 2) + q, o);
+                }
+            }
+            if (!fail) {
+#pragma unroll
+                for (int q = 0; q < kAK / 4; q += 16) {
+                    __syncwarp();
+                    GDN_TMEM_ST_X16(tP + lane_addr + half * (kAK / 4) + q, (pk + q));
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[AB_PFULL]);
         }
-        if (tid == 0 && !fail && j == 0 && 2 < ntiles) issue_kv_t(2);
-        if (__syncthreads_or(fail)) {
-            fail = true;
-            break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, f != 1.f)) {                  // rescale this warp's half rows of O
+        // ---- O / l to the output rows -------------------------------------------
+        if (lane == 0 && !fail && ntiles > 0) fail = !wait(AB_ODONE, uint32_t((ntiles - 1) & 1));
+        __syncwarp();
+        fail = __shfl_sync(0xffffffffu, fail, 0);
+        s_l[half * kAQ + row] = l;
+        if (!named_sync_or(pair_bar, 64, fail)) {
+            tc_fence_after();
+            const float inv = 1.f / (s_l[row] + s_l[kAQ + row]);
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + ((s0 + q0 + row) * p.Hq + h) * kAD + half * (kAD / 2);
 #pragma unroll
             for (int q = 0; q < kAD / 2; q += 16) {
                 float o[16];
                 tmem_ld16(tO + lane_addr + half * (kAD / 2) + q, o);
                 tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] *= f;
-                tmem_st16(tO + lane_addr + half * (kAD / 2) + q, o);
+                uint4 w0, w1;
+                w0.x = pack2(o[0] * inv, o[1] * inv);
+                w0.y = pack2(o[2] * inv, o[3] * inv);
+                w0.z = pack2(o[4] * inv, o[5] * inv);
+                w0.w = pack2(o[6] * inv, o[7] * inv);
+                w1.x = pack2(o[8] * inv, o[9] * inv);
+                w1.y = pack2(o[10] * inv, o[11] * inv);
+                w1.z = pack2(o[12] * inv, o[13] * inv);
+                w1.w = pack2(o[14] * inv, o[15] * inv);
+                if (row < rows) {
+                    *reinterpret_cast<uint4*>(out + q) = w0;
+                    *reinterpret_cast<uint4*>(out + q + 8) = w1;
+                }
             }
         }
-#pragma unroll
-        for (int q = 0; q < kAK / 4; q += 16) {
-            __syncwarp();
-            GDN_TMEM_ST_X16(tP + lane_addr + half * (kAK / 4) + q, (pk + q));
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            const uint64_t dv = smem_desc(smem_u32(sV(j)), kATile / 2, 1024, kSwizzle128B);
-#pragma unroll
-            for (int s = 0; s < kAK / 16; ++s)
-                umma_f16_tmemA(tO, tP + s * 8, dv + uint64_t(s * 2048 >> 4), id_o, j > 0 || s > 0);
-            umma_commit(&bars[AB_O]);
-        }
-    }
-    // ---- O / l to the output rows ------------------------------------------------
-    if (tid == 0 && !fail) fail = !mbar_wait(&bars[AB_O], uint32_t((ntiles - 1) & 1), kAWaitLimit);
-    s_ex[half * kAQ + row] = l;                                   // the loop's last reads of s_ex are done
-    if (!__syncthreads_or(fail)) {
-        tc_fence_after();
-        const float inv = 1.f / (s_ex[row] + s_ex[kAQ + row]);
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + ((s0 + q0 + row) * p.Hq + h) * kAD + half * (kAD / 2);
-#pragma unroll
-        for (int q = 0; q < kAD / 2; q += 16) {
-            float o[16];
-            tmem_ld16(tO + lane_addr + half * (kAD / 2) + q, o);
-            tmem_ld_wait();
-            uint4 w0, w1;
-            w0.x = pack2(o[0] * inv, o[1] * inv);
-            w0.y = pack2(o[2] * inv, o[3] * inv);
-            w0.z = pack2(o[4] * inv, o[5] * inv);
-            w0.w = pack2(o[6] * inv, o[7] * inv);
-            w1.x = pack2(o[8] * inv, o[9] * inv);
-            w1.y = pack2(o[10] * inv, o[11] * inv);
-            w1.z = pack2(o[12] * inv, o[13] * inv);
-            w1.w = pack2(o[14] * inv, o[15] * inv);
-            if (row < rows) {
-                *reinterpret_cast<uint4*>(out + q) = w0;
-                *reinterpret_cast<uint4*>(out + q + 8) = w1;
-            }
-        }
-    } else if (tid == 0) {
-        atomicAdd(&g_attn_timeouts, 1);
-        // let TMA copies still in flight land before shared memory goes away
-        mbar_wait(&bars[AB_Q], 0, kAWaitLimit);
-        for (int st = 0; st < kAStages; ++st)
-            if (last_kv[st] >= 0)
-                mbar_wait(&bars[AB_KV + st], uint32_t((last_kv[st] / kAStages) & 1), kAWaitLimit);
     }
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && s_fail) atomicAdd(&g_attn_timeouts, 1);
     if (warp == 0) tmem_dealloc(tmem, kATmemCols);
 }
 
