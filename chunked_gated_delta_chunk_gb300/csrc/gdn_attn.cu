@@ -7,8 +7,8 @@
 // attn_append_kernel writes the prompt's k, v rows into the cache after each
 // sequence's cache_len rows.  attn_rows_kernel then runs one CTA per
 // (128-row query tile, query head, sequence), warp-specialised:
-//   warp 8      TMA: the query tile once, key tiles (3 stages) and value
-//               tiles (2 stages) of 128 rows from the cache;
+//   warp 8      TMA: the query tile once, key tiles (2 stages) and value
+//               tiles (3 stages) of 128 rows from the cache;
 //   warp 9      tcgen05 MMAs: S_j = Q K_j^T into one of two TMEM buffers, then
 //               O += P_{j-1} V_{j-1} with P (bf16) as the A operand from TMEM;
 //   warps 0-7   softmax, two threads per query row (its TMEM lane), one per
@@ -34,10 +34,16 @@ using namespace ptx;
 constexpr int kAD = 128;              // head dim
 constexpr int kAQ = 128;              // query rows per tile (TMEM lanes)
 constexpr int kAK = 128;              // keys per tile
-constexpr int kAKStages = 3, kAVStages = 2;
+// K_j is needed by S_j early in a tile and V_j by O += P_j V_j at its end, so
+// values get the deeper buffering: a key tile refills after S_{j-2}, a value
+// tile after the product of tile j - 3.
+constexpr int kAKStages = 2, kAVStages = 3;
 constexpr int kASoftThreads = 256;    // warps 0-7
 constexpr int kAThreads = kASoftThreads + 64;   // + TMA warp + MMA warp
 constexpr uint32_t kAWaitLimit = 1u << 20;
+// The pipeline's hand-offs are short: waits re-check every ~32 ns instead of
+// sleeping up to the default 2 us (the bound stays well under a second).
+constexpr uint32_t kASuspendNs = 32, kASpinLimit = 1u << 24;
 constexpr float kARescale = 8.f;      // log2 headroom before the reference maximum moves
 constexpr uint32_t kATile = kAK * kAD * 2;                 // 32 KB per Q, K or V tile
 constexpr uint32_t kAOffQ = 0;
@@ -52,15 +58,16 @@ static_assert(kASmem <= 232448, "attention stages above the 227 KB per-block lim
 constexpr uint32_t kAColS = 0, kAColP = 256, kAColO = 384, kATmemCols = 512;
 enum : int {
     AB_Q = 0,
-    AB_KFULL = 1,                     // + stage (3)
-    AB_KEMPTY = 4,                    // + stage (3)
-    AB_VFULL = 7,                     // + stage (2)
-    AB_VEMPTY = 9,                    // + stage (2)
-    AB_SFULL = 11,                    // + buffer (2)
-    AB_SEMPTY = 13,                   // + buffer (2), 8 arrivals
-    AB_PFULL = 15,                    // 8 arrivals
-    AB_ODONE = 16
+    AB_KFULL = 1,                     // + key stage
+    AB_KEMPTY = AB_KFULL + kAKStages,
+    AB_VFULL = AB_KEMPTY + kAKStages, // + value stage
+    AB_VEMPTY = AB_VFULL + kAVStages,
+    AB_SFULL = AB_VEMPTY + kAVStages, // + S buffer (2)
+    AB_SEMPTY = AB_SFULL + 2,         // + S buffer (2), 8 arrivals
+    AB_PFULL = AB_SEMPTY + 2,         // 8 arrivals
+    AB_ODONE = AB_PFULL + 1
 };
+static_assert(AB_ODONE + 1 == int(kANumBars), "barrier count");
 
 struct AttnMaps {
     CUtensorMap q, kc, vc;
@@ -147,7 +154,7 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
     const uint32_t tP = tmem + kAColP, tO = tmem + kAColO;
     auto wait = [&](int b, uint32_t parity) {
         if (s_fail) return false;
-        if (mbar_wait(&bars[b], parity, kAWaitLimit)) return true;
+        if (mbar_wait(&bars[b], parity, kASpinLimit, kASuspendNs)) return true;
         s_fail = 1;
         return false;
     };
@@ -162,7 +169,9 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
             mbar_arrive_expect_tx(&bars[AB_Q], kATile);
             tma_load_2d(sQ, &maps.q, &bars[AB_Q], h * kAD, int(s0 + q0));
             tma_load_2d(sQ + kATile / 2, &maps.q, &bars[AB_Q], h * kAD + 64, int(s0 + q0));
-            int k_last[kAKStages] = {-1, -1, -1}, v_last[kAVStages] = {-1, -1};
+            int k_last[kAKStages], v_last[kAVStages];
+            for (int st = 0; st < kAKStages; ++st) k_last[st] = -1;
+            for (int st = 0; st < kAVStages; ++st) v_last[st] = -1;
             for (int j = 0; j < ntiles; ++j) {
                 const int ks = j % kAKStages, vs = j % kAVStages, y = kv_row0 + j * kAK;
                 if (j >= kAKStages && !wait(AB_KEMPTY + ks, uint32_t((j / kAKStages - 1) & 1))) break;
@@ -262,15 +271,23 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[AB_SEMPTY + b]);     // this warp is done with S_j
-            // ---- mask and the half-row maximum; the pair agrees on the row's -------
+            // ---- mask and the half-row maximum (raw scores; the scale is
+            // positive, so it is applied to the maximum); the pair agrees on the
+            // row's maximum.  Key tiles that every row of this warp sees whole
+            // skip the mask.
             const int k0 = j * kAK + half * (kAK / 2);
-            float mh = -INFINITY;
+            const bool whole = k0 + kAK / 2 - 1 <= clen + q0 + (warp & 3) * 32 && k0 + kAK / 2 <= nkeys;
+            if (fail || !whole) {
 #pragma unroll
-            for (int c = 0; c < kAK / 2; ++c) {
-                const int kk = k0 + c;
-                x[c] = (!fail && kk <= pos && kk < nkeys) ? x[c] * sl2 : -INFINITY;
-                mh = fmaxf(mh, x[c]);
+                for (int c = 0; c < kAK / 2; ++c) {
+                    const int kk = k0 + c;
+                    x[c] = (!fail && kk <= pos && kk < nkeys) ? x[c] : -INFINITY;
+                }
             }
+            float mq[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+            for (int c = 4; c < kAK / 2; ++c) mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+            const float mh = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * sl2;
             s_ex[(b * 2 + half) * kAQ + row] = mh;
             if (named_sync_or(pair_bar, 64, fail)) {
                 fail = true;
@@ -284,16 +301,18 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
                 f = ex2(m_ref - mt);
                 m_ref = mt;
             }
-            l *= f;
+            // P = exp2(scale x - m_ref) as one multiply-add and one 2^x each;
+            // the row sum gathers the fp32 values
             uint32_t pk[kAK / 4];
+            float lq[4] = {0.f, 0.f, 0.f, 0.f};
+            const float nm = -m_ref;
 #pragma unroll
             for (int c = 0; c < kAK / 2; c += 2) {
-                const float e0 = ex2(x[c] - m_ref), e1 = ex2(x[c + 1] - m_ref);
+                const float e0 = ex2(fmaf(x[c], sl2, nm)), e1 = ex2(fmaf(x[c + 1], sl2, nm));
                 pk[c / 2] = pack2(e0, e1);
-                const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(&pk[c / 2]);
-                const float2 r = __bfloat1622float2(bb);
-                l += r.x + r.y;
+                lq[(c >> 1) & 3] += e0 + e1;
             }
+            l = fmaf(l, f, (lq[0] + lq[1]) + (lq[2] + lq[3]));
             // ---- P_j replaces P_{j-1} once O += P_{j-1} V_{j-1} is done ----------
             if (lane == 0 && j >= 1) fail = fail || !wait(AB_ODONE, uint32_t((j - 1) & 1));
             __syncwarp();

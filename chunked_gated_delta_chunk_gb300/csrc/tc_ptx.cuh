@@ -50,10 +50,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
 }
 
 // Wait for the phase with the given parity; false after `limit` attempts
-// (each attempt sleeps at most ~2 us, so the wait is bounded in time).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
+// (each attempt sleeps at most ~suspend_ns, so the wait is bounded in time).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit,
+                                          uint32_t suspend_ns = 2000) {
     for (uint32_t i = 0; i < limit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity, suspend_ns)) return true;
     return false;
 }
 
