@@ -66,7 +66,7 @@ class gdn_prefill_desc(ctypes.Structure):
         ("conv_kernel", ctypes.c_int), ("conv_act", ctypes.c_int),
         ("use_qk_l2norm", ctypes.c_int), ("l2_eps", ctypes.c_float), ("q_scale", ctypes.c_float),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-        ("segment_chunks", ctypes.c_int),
+        ("segment_chunks", ctypes.c_int), ("split_prep", ctypes.c_int),
     ]
 
 

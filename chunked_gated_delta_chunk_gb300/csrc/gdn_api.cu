@@ -64,24 +64,27 @@ constexpr int kSMs = 152;   // GB300: 2 dies x 76 SMs
 // Chunks per segment of the segment-parallel scan, or 0 for one pass.
 // Cost model in chunk periods of one CTA (one CTA per SM): with n segments of
 // L = ceil(chunks / n) chunks, phase 1 runs (2n - 1) CTAs per (sequence,
-// value head) and phase 2 runs n - 1, each phase taking L + 1 periods per
-// wave of kSMs CTAs; the combine adds about a third of a period per segment.
-// One pass costs chunks + 1 periods in ceil(units / kSMs) waves.  The
-// cheapest n wins; sequence lengths are taken as the batch average.
+// value head) and phase 2 runs n - 1, each phase taking L + kStartPeriods
+// periods per wave of kSMs CTAs (a CTA's first chunks run with cold
+// instruction caches and its incoming state still on the way); each of the
+// n - 2 sequential combine steps costs about one period.  One pass costs
+// chunks + kStartPeriods periods in ceil(units / kSMs) waves.  The cheapest n
+// wins; sequence lengths are taken as the batch average.
 int segment_chunks(const gdn_prefill_desc* d) {
     if (d->dtype != GDN_BF16 || d->dk != 128 || d->dv != 128) return 0;   // tensor-core path only
     if (d->T_total <= 0 || d->B <= 0 || d->segment_chunks < 0) return 0;
     const int64_t chunks = (d->T_total + d->chunk - 1) / d->chunk;
     if (d->segment_chunks > 0) return d->segment_chunks < chunks ? d->segment_chunks : 0;
+    constexpr double kStartPeriods = 3.0, kCombinePeriods = 1.0;
     const int64_t units = int64_t(d->Hv) * d->B;
     const int64_t per_seq = (chunks + d->B - 1) / d->B;
     auto waves = [&](int64_t ctas) { return (ctas + kSMs - 1) / kSMs; };
-    double best = double(waves(units) * (per_seq + 1));
+    double best = double(waves(units)) * (double(per_seq) + kStartPeriods);
     int best_len = 0;
     for (int64_t n = 2; n <= 64 && n <= per_seq; ++n) {
         const int64_t len = (per_seq + n - 1) / n;
-        const double cost = double((waves(units * (2 * n - 1)) + waves(units * (n - 1))) * (len + 1)) +
-                            (n >= 3 ? (n - 2) / 3.0 : 0.0);
+        const double cost = double(waves(units * (2 * n - 1)) + waves(units * (n - 1))) * (double(len) + kStartPeriods) +
+                            double(n - 2) * kCombinePeriods;
         if (cost < best) {
             best = cost;
             best_len = int(len);
@@ -102,8 +105,18 @@ size_t segment_workspace(const gdn_prefill_desc* d, int seg_chunks) {
     return (bytes + 255) & ~size_t(255);
 }
 
+// Chunk records of the split preparation: one per (value head, chunk slot),
+// slots t0_n / chunk + n + c (at most T_total / chunk + B + 1 per head).
+int64_t prep_slots(const gdn_prefill_desc* d) { return d->T_total / d->chunk + d->B + 1; }
+
+size_t prep_workspace(const gdn_prefill_desc* d) {
+    if (d->dtype != GDN_BF16 || d->dk != 128 || d->dv != 128) return 0;   // tensor-core path only
+    if (d->T_total <= 0 || d->B <= 0 || d->split_prep < 0) return 0;
+    return size_t(d->Hv) * size_t(prep_slots(d)) * gdn::kPrepRecordBytes;
+}
+
 size_t workspace_needed(const gdn_prefill_desc* d) {
-    return conv_workspace(d) + segment_workspace(d, segment_chunks(d));
+    return conv_workspace(d) + segment_workspace(d, segment_chunks(d)) + prep_workspace(d);
 }
 
 int check_prefill(const gdn_prefill_desc* d) {
@@ -123,6 +136,10 @@ int check_prefill(const gdn_prefill_desc* d) {
 }
 
 }  // namespace
+
+namespace gdn {
+size_t prefill_required_workspace(const gdn_prefill_desc* d) { return conv_workspace(d); }
+}  // namespace gdn
 
 extern "C" {
 
@@ -174,16 +191,23 @@ int gdn_prefill_ex(const gdn_prefill_desc* d, gdn_stream_t stream) {
     p.eps = d->l2_eps;
     p.q_scale = d->q_scale;
     {
-        // segment-parallel scan when chosen and the workspace holds its maps
+        // segment-parallel scan when chosen and the workspace holds its maps;
+        // split preparation when on and the workspace also holds the records
         const int sc = segment_chunks(d);
         const size_t conv_bytes = conv_workspace(d);
-        if (sc > 0 && d->workspace != nullptr &&
-            d->workspace_bytes >= conv_bytes + segment_workspace(d, sc)) {
+        const size_t seg_bytes = segment_workspace(d, sc);
+        const size_t prep_bytes = prep_workspace(d);
+        if (sc > 0 && d->workspace != nullptr && d->workspace_bytes >= conv_bytes + seg_bytes) {
             const int64_t seg_tokens = int64_t(sc) * d->chunk;
             p.seg_chunks = sc;
             p.seg_ws = reinterpret_cast<float*>(static_cast<char*>(d->workspace) + conv_bytes);
             p.seg_slots = segment_slots(d, sc);
             p.seg_max = int((d->T_total + seg_tokens - 1) / seg_tokens);
+        }
+        if (prep_bytes > 0 && d->workspace != nullptr &&
+            d->workspace_bytes >= conv_bytes + seg_bytes + prep_bytes) {
+            p.prep_ws = static_cast<uint8_t*>(d->workspace) + conv_bytes + seg_bytes;
+            p.prep_slots = prep_slots(d);
         }
     }
 
@@ -307,7 +331,7 @@ int gdn_prefill_plan(const gdn_prefill_desc* d, const char** names, int max_name
     const int st = check_prefill(d);
     if (st != GDN_OK) return -st;
     if (d->B == 0) return 0;
-    const char* plan[5];
+    const char* plan[6];
     int n = 0;
     gdn::ChunkParams p{};
     p.Hk = d->Hk;
@@ -317,8 +341,12 @@ int gdn_prefill_plan(const gdn_prefill_desc* d, const char** names, int max_name
     p.chunk = d->chunk;
     if (d->conv_x != nullptr && d->T_total > 0) plan[n++] = "conv_kernel";
     const bool tc = gdn::tc_supported(p, d->dtype);
-    plan[n++] = tc ? gdn::kTcKernelName : "chunk_simt_kernel";
     const int sc = tc ? segment_chunks(d) : 0;
+    const size_t prep_bytes = tc ? prep_workspace(d) : 0;
+    if (prep_bytes > 0 && d->workspace != nullptr &&
+        d->workspace_bytes >= conv_workspace(d) + segment_workspace(d, sc) + prep_bytes)
+        plan[n++] = "chunk_prep_kernel";
+    plan[n++] = tc ? gdn::kTcKernelName : "chunk_simt_kernel";
     if (sc > 0 && d->workspace != nullptr &&
         d->workspace_bytes >= conv_workspace(d) + segment_workspace(d, sc)) {
         const int64_t seg_tokens = int64_t(sc) * d->chunk;

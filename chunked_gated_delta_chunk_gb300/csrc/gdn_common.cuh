@@ -46,6 +46,15 @@ struct ChunkParams {
     float* seg_ws;
     int64_t seg_slots;       // slots per value head
     int seg_max;             // most segments any sequence can have (grid size)
+    // Split preparation (tensor-core path only).  When prep_ws is set, a
+    // separate pass solves every chunk's S-independent part (inverse, U0, W,
+    // the intra-chunk output weights P, the scaled queries) in parallel over
+    // all chunks and stores one record per (value head, chunk slot); the
+    // state pass then only streams the records.  The slot of chunk c of
+    // sequence n is t0_n / chunk + n + c, with t0_n the sequence's clamped
+    // first token.
+    uint8_t* prep_ws;
+    int64_t prep_slots;      // slots per value head
 };
 
 // Selective-scan rows (h_t = a_t h_{t-1} + b_t per channel).  a, b, h_rows
@@ -124,10 +133,17 @@ int attn_read_timeouts();
 // than on every launch.
 cudaError_t ensure_smem(const void* kernel, int bytes);
 
+// The part of gdn_workspace_bytes a prefill cannot run without (the short
+// convolution's output); the segment maps and chunk records are optional.
+size_t prefill_required_workspace(const gdn_prefill_desc* d);
+
 // Launch timing: bracket a kernel launch with timer_begin / timer_end on the
 // launch stream (no-ops unless gdn_launch_timer_start turned recording on).
 void timer_begin(cudaStream_t s, const char* kernel);
 void timer_end(cudaStream_t s);
+
+// Bytes of one chunk record of the split preparation.
+constexpr size_t kPrepRecordBytes = 82432;
 
 // Segment slot of (sequence n, segment s).
 __host__ __device__ inline int64_t seg_slot(int64_t seq_start, int n, int s, int64_t seg_tokens) {

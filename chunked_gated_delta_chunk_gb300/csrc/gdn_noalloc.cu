@@ -57,9 +57,10 @@ size_t gdn_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 int gdn_prefill_noalloc(const gdn_prefill_desc* d, gdn_stream_t stream) {
     if (d == nullptr) return GDN_ERR_INVALID_ARG;
     if (d->conv_x == nullptr) return gdn_prefill_ex(d, stream);   // no scratch needed
-    const size_t need = gdn_workspace_bytes(d);
-    if (need == size_t(-1)) return gdn_prefill_ex(d, stream);    // let it report the error
-    if (need > kNoAllocScratchBytes) return GDN_ERR_TOO_LARGE;
+    if (gdn_workspace_bytes(d) == size_t(-1)) return gdn_prefill_ex(d, stream);   // let it report the error
+    // Only the convolution's output must fit; the segment maps and chunk
+    // records are used when they fit as well.
+    if (gdn::prefill_required_workspace(d) > kNoAllocScratchBytes) return GDN_ERR_TOO_LARGE;
     void* scratch = nullptr;
     const cudaError_t e = scratch_for_current_device(&scratch);
     if (e != cudaSuccess) return GDN_ERR_CUDA;

@@ -57,6 +57,7 @@ constexpr int kThreads = 384;
 constexpr uint32_t kPrepThreads = 256; // warps 0-3 and 8-11
 constexpr uint32_t kChainThreads = 128;
 constexpr uint32_t kBarPrep = 1, kBarChain = 2;
+constexpr uint32_t kBarInit = 3, kBarHelp = 4;   // split preparation: warps 4-11, warps 8-11
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr int kLdA = kC + 4;         // fp32 row stride of A and T: 16-byte aligned rows
 constexpr float kLog2e = 1.4426950408889634f;
@@ -69,13 +70,14 @@ constexpr uint32_t kStageBytes = kStageKQ + kStageV;
 constexpr uint32_t kOffWt = 2 * kStageBytes;             // -W^T bf16 [d][t] MN-major, 16 KB
 constexpr uint32_t kOffP = kOffWt + 16384;               // P [buf][hi|lo] bf16 [t][i], 4 x 8 KB
 constexpr uint32_t kOffTb = kOffP + 4 * 8192;            // Tb hi, Tb lo, Tbg hi, Tbg lo, 4 x 8 KB
+                                                         // (split preparation: -W^T of odd chunks)
 constexpr uint32_t kOffA = kOffTb + 4 * 8192;            // A fp32 [64][68]
 constexpr uint32_t kOffT = kOffA + kC * kLdA * 4;        // T fp32 [64][68]
 constexpr uint32_t kOffTmp = kOffT + kC * kLdA * 4;      // inverse scratch, 1536 floats
 constexpr uint32_t kOffVec = kOffTmp + 1536 * 4;         // vectors
 constexpr uint32_t kVecFloats = 8 * kC + 2 * 2 * kC + 2 * kC + 2;   // prep, staging, chain
 constexpr uint32_t kOffBar = kOffVec + ((kVecFloats * 4 + 127) / 128) * 128;
-constexpr uint32_t kNumBars = 16;
+constexpr uint32_t kNumBars = 18;
 constexpr uint32_t kSmemBytes = kOffBar + kNumBars * 8 + 32 + 1024;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-block limit");
 
@@ -88,7 +90,10 @@ enum : int {
     B_XREAD = 9,                   // chain has read U^T out of D_X
     B_WTFREE = 10,                 // chain MMA no longer reads -W^T
     B_PFREE0 = 11, B_PFREE1 = 12,  // chain MMA no longer reads P of a buffer
-    B_SFREE0 = 13, B_SFREE1 = 14   // chain no longer reads a raw stage
+    B_SFREE0 = 13, B_SFREE1 = 14,  // chain no longer reads a raw stage
+    B_WTFREE1 = 15,                // split preparation: second -W^T buffer free
+    B_OQ = 16,                     // split preparation: O^T = Zb Qs^T done
+    B_ZISS = 17                    // split preparation: Z MMAs of the chunk issued
 };
 
 // TMEM columns.
@@ -351,6 +356,329 @@ struct Maps {
     CUtensorMap q, k, v;
 };
 
+// ---- split preparation ------------------------------------------------------
+// Everything of a chunk that does not depend on the incoming state (norms,
+// cumsum, the masked Gram matrices, the blocked inverse, U0 and W, the
+// intra-chunk output weights P and the scaled queries) is solved by
+// chunk_prep_kernel for all chunks at once, one CTA per (chunk slot, value
+// head), two CTAs per SM.  It stores one record per chunk:
+//   -W^T   [128][64] bf16 image in the 128-byte-swizzled layout the chain MMA
+//          reads from shared memory,
+//   P      hi and lo images [64][64] bf16 (same layout),
+//   Qs     the two 64-column blocks of diag(Gamma r_q) Q, same layout,
+//   U0^T   the TMEM fragments of the 256 preparing threads, 32 fp32 each,
+//          stored in 16-byte groups interleaved across a warp's lanes, so that
+//          the thread with the same role reads them back coalesced,
+//   vec    end weights e_i = exp(min(gamma_S - gamma_i, 0)) r_k,i and
+//          exp(gamma_S).
+// The state kernel then streams the records (bulk copies and one TMEM store
+// of U0^T per chunk) instead of solving them.
+constexpr uint32_t kRecWt = 0;
+constexpr uint32_t kRecP = 16384;
+constexpr uint32_t kRecQ = 32768;
+constexpr uint32_t kRecU = 49152;
+constexpr uint32_t kRecVec = 81920;
+static_assert(kRecVec + 512 == kPrepRecordBytes, "record layout");
+
+// Shared-memory map of the preparation kernel (bytes from the 1024-aligned
+// base).  A lives under Tb: the inverse has read A for the last time before
+// Tb is written.
+constexpr uint32_t kPOffKQ = 0;                          // K b0 | Q b0 | K b1 | Q b1
+constexpr uint32_t kPOffV = kStageKQ;                    // V b0 | V b1
+constexpr uint32_t kPOffTb = kPOffV + 16384;             // Tb hi, lo, Tbg hi, lo (A first)
+constexpr uint32_t kPOffT = kPOffTb + 4 * 8192;
+constexpr uint32_t kPOffTmp = kPOffT + kC * kLdA * 4;
+constexpr uint32_t kPOffVec = kPOffTmp + 1536 * 4;
+constexpr uint32_t kPOffBar = kPOffVec + 8 * kC * 4;
+constexpr uint32_t kPrepSmemBytes = kPOffBar + 3 * 8 + 8 + 1024;
+constexpr uint32_t kPrepTmemCols = 128;                  // Gram, then W^T (64); U0^T (64)
+static_assert(kC * kLdA * 4 <= 4 * 8192, "A fits under Tb");
+static_assert(2 * (kPrepSmemBytes + 1024) <= 233472, "two preparation CTAs per SM");
+
+__global__ void __launch_bounds__(kPrepThreads, 2)
+chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* kq = sm + kPOffKQ;
+    uint8_t* vv = sm + kPOffV;
+    float* sA = reinterpret_cast<float*>(sm + kPOffTb);
+    float* sT = reinterpret_cast<float*>(sm + kPOffT);
+    float* sTmp = reinterpret_cast<float*>(sm + kPOffTmp);
+    float* vGam = reinterpret_cast<float*>(sm + kPOffVec);   // g, then gamma * log2(e)
+    float* vEg = vGam + kC;                                 // Gamma
+    float* vBeta = vEg + kC;
+    float* vRk = vBeta + kC;                                // 1/|k_i|
+    float* vRq = vRk + kC;                                  // 1/|q_t|
+    float* vEnd = vRq + kC;                                 // e_i
+    float* vFb = vEnd + kC;                                 // beta_i
+    float* vFbg = vFb + kC;                                 // beta_i Gamma_i r_k,i
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPOffBar);   // raw tiles, Gram, U0 / W
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kPOffBar + 24);
+
+    const int slot = blockIdx.x, h = blockIdx.y;
+    const int pt = threadIdx.x, pw = pt >> 5, lane = pt & 31;
+    const int phalf = pw >> 2;                              // column half of TMEM reads
+    const int row = (pw & 3) * 32 + lane;                   // TMEM lane of this thread
+    const uint32_t lane_addr = uint32_t((pw & 3) * 32) << 16;
+    const int kh = h / (p.Hv / p.Hk);
+    const int Hv = p.Hv;
+
+    // ---- the chunk of this slot: the last sequence n with t0_n / chunk + n <= slot
+    int64_t t_end_all = p.cu[p.B];
+    if (t_end_all > p.t_cap) t_end_all = p.t_cap;
+    auto seq_first = [&](int m) {
+        const int64_t t = p.cu[m];
+        return t < 0 ? int64_t(0) : (t > t_end_all ? t_end_all : t);
+    };
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (seq_first(mid) / p.chunk + mid <= slot) lo = mid;
+        else hi = mid - 1;
+    }
+    const int n = lo;
+    const int64_t t0 = seq_first(n);
+    int64_t t1 = p.cu[n + 1];
+    t1 = t1 < t0 ? t0 : (t1 > t_end_all ? t_end_all : t1);
+    const int64_t c = int64_t(slot) - (t0 / p.chunk + n);
+    if (c < 0 || c * p.chunk >= t1 - t0) return;            // no chunk in this slot
+    const int64_t cs = t0 + c * p.chunk;
+    const int rows = int(t1 - cs < p.chunk ? t1 - cs : p.chunk);
+    uint8_t* rec = p.prep_ws + (size_t(h) * size_t(p.prep_slots) + size_t(slot)) * kPrepRecordBytes;
+    const bool tma = cs + kC <= t_end_all;
+
+    if (pt == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        if (tma) {
+            tma_prefetch_desc(&maps.q);
+            tma_prefetch_desc(&maps.k);
+            tma_prefetch_desc(&maps.v);
+        }
+    }
+    __syncwarp();
+    if (pw == 0) {
+        tmem_alloc(tmem_slot, kPrepTmemCols);
+        tmem_relinquish();
+    }
+    for (int idx = pt; idx < kC * kLdA; idx += kPrepThreads) sT[idx] = 0.f;   // upper triangle stays 0
+    if (pt < kC) {
+        const int64_t t = cs + pt;
+        vGam[pt] = pt < rows ? p.g[t * Hv + h] : 0.f;
+        vBeta[pt] = pt < rows ? p.beta[t * Hv + h] : 0.f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tGW = tmem, tX = tmem + 64;
+    bool fail = false;
+    do {
+        // ---- raw tiles: TMA when the whole 64-row box lies inside the buffers,
+        // else plain loads (rows past the buffers are zero)
+        if (tma) {
+            if (pt == 0) {
+                const int y = int(cs);
+                mbar_arrive_expect_tx(&bars[0], kStageBytes);
+                tma_load_2d(kq + 0, &maps.k, &bars[0], kh * kD, y);
+                tma_load_2d(kq + 16384, &maps.k, &bars[0], kh * kD + 64, y);
+                tma_load_2d(kq + 8192, &maps.q, &bars[0], kh * kD, y);
+                tma_load_2d(kq + 24576, &maps.q, &bars[0], kh * kD + 64, y);
+                tma_load_2d(vv + 0, &maps.v, &bars[0], h * kD, y);
+                tma_load_2d(vv + 8192, &maps.v, &bars[0], h * kD + 64, y);
+            }
+        } else {
+            const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(p.q);
+            const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
+            const __nv_bfloat16* gv = static_cast<const __nv_bfloat16*>(p.v);
+            for (int idx = pt; idx < kC * 16; idx += kPrepThreads) {
+                const int r = idx >> 4, cc = (idx & 15) * 8;
+                const int64_t t = cs + r;
+                uint4 zk = make_uint4(0, 0, 0, 0), zq = zk, zv = zk;
+                if (t < t_end_all) {
+                    zk = *reinterpret_cast<const uint4*>(gk + t * p.k_stride + kh * kD + cc);
+                    zq = *reinterpret_cast<const uint4*>(gq + t * p.q_stride + kh * kD + cc);
+                    zv = *reinterpret_cast<const uint4*>(gv + t * p.v_stride + int64_t(h) * kD + cc);
+                }
+                *reinterpret_cast<uint4*>(kq + toff(r, cc, 16384)) = zk;
+                *reinterpret_cast<uint4*>(kq + 8192 + toff(r, cc, 16384)) = zq;
+                *reinterpret_cast<uint4*>(vv + toff(r, cc, 8192)) = zv;
+            }
+            fence_proxy_async_smem();
+        }
+        bool lf = false;
+        if (tma && pt == 0) lf = !mbar_wait(&bars[0], 0, kWaitLimit);
+        if (__syncthreads_or(lf)) { fail = true; break; }
+        // ---- Gram MMA [K; Q] K^T; cumsum (log2 domain); row norms -------------
+        tc_fence_after();
+        if (pt == 32) {
+            const uint32_t id_gram = idesc_bf16(128, 64, 0, 0);
+            const uint64_t d0 = smem_desc(smem_u32(kq), 16, 1024, kSwizzle128B);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
+                umma_f16(tGW, d0 + (off >> 4), d0 + (off >> 4), id_gram, s > 0);
+            }
+            umma_commit(&bars[1]);
+        }
+        __syncwarp();
+        if (pw == 0) {
+            float a = vGam[2 * lane], bb = vGam[2 * lane + 1];
+            bb += a;
+            float s = bb;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += u;
+            }
+            a += s - bb;
+            vGam[2 * lane] = a * kLog2e;
+            vGam[2 * lane + 1] = s * kLog2e;
+        }
+        {
+            // 128 rows (K 0..63, Q 0..63); two threads per row, 64 columns each
+            const int r = pt >> 1, part = pt & 1;
+            const int isq = r >= kC, tr = r & 63;
+            const uint8_t* base = kq + (isq ? 8192 : 0);
+            float ss = 0.f;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                float v[8];
+                load_chunk8(base + toff(tr, part * 64 + m * 8, 16384), v);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            if (part == 0) (isq ? vRq : vRk)[tr] = p.l2norm ? rsqrtf(ss + p.eps) : 1.f;
+        }
+        __syncthreads();
+        if (pt < kC) {
+            const float gm = vGam[pt];
+            const float eg = exp2f(gm);
+            vEg[pt] = eg;
+            const float e = pt < rows ? exp2f(fminf(vGam[rows - 1] - gm, 0.f)) * vRk[pt] : 0.f;
+            vEnd[pt] = e;
+            vFb[pt] = vBeta[pt];
+            vFbg[pt] = vBeta[pt] * eg * vRk[pt];
+            reinterpret_cast<float*>(rec + kRecVec)[pt] = e;
+            if (pt == rows - 1) reinterpret_cast<float*>(rec + kRecVec)[kC] = eg;
+        }
+        // ---- masks and decays on the Gram matrices: A to shared, P to the record
+        if (pt == 0) lf = !mbar_wait(&bars[1], 0, kWaitLimit);
+        if (__syncthreads_or(lf)) { fail = true; break; }
+        tc_fence_after();
+        {
+            float v[32];
+            tmem_ld32(tGW + lane_addr + phalf * 32, v);
+            if (row < kC) {
+                const int i = row;
+                const float bi = vBeta[i] * vRk[i], gi = vGam[i];
+#pragma unroll
+                for (int q = 0; q < 32; q += 4) {
+                    float a4[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int j = phalf * 32 + q + u;
+                        a4[u] = (i < rows && j < i) ? bi * fast_exp2(fminf(gi - vGam[j], 0.f)) * vRk[j] * v[q + u] : 0.f;
+                    }
+                    *reinterpret_cast<float4*>(sA + i * kLdA + phalf * 32 + q) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+                }
+            } else {
+                const int t = row - kC;
+                const float rt = vRq[t], gt = vGam[t];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const int j = phalf * 32 + q;
+                    v[q] = (t < rows && j <= t) ? rt * fast_exp2(fminf(gt - vGam[j], 0.f)) * vRk[j] * v[q] : 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 32; q += 8) {
+                    const uint32_t o = toff(t, phalf * 32 + q, 8192);
+                    store_split8(rec + kRecP + o, rec + kRecP + 8192 + o, v + q);
+                }
+            }
+        }
+        __syncthreads();
+        // ---- blocked inverse; T diag(beta), T diag(beta Gamma r_k) as hi + lo --
+        block_inverse_64(sA, sT, sTmp, pt);
+        for (int idx = pt; idx < kC * 8; idx += kPrepThreads) {
+            const int t = idx >> 3, i0 = (idx & 7) * 8;
+            float a[8], bg[8], fb[8], fbg[8], tr[8];
+            *reinterpret_cast<float4*>(fb) = *reinterpret_cast<const float4*>(vFb + i0);
+            *reinterpret_cast<float4*>(fb + 4) = *reinterpret_cast<const float4*>(vFb + i0 + 4);
+            *reinterpret_cast<float4*>(fbg) = *reinterpret_cast<const float4*>(vFbg + i0);
+            *reinterpret_cast<float4*>(fbg + 4) = *reinterpret_cast<const float4*>(vFbg + i0 + 4);
+            *reinterpret_cast<float4*>(tr) = *reinterpret_cast<const float4*>(sT + t * kLdA + i0);
+            *reinterpret_cast<float4*>(tr + 4) = *reinterpret_cast<const float4*>(sT + t * kLdA + i0 + 4);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                a[q] = tr[q] * fb[q];
+                bg[q] = tr[q] * fbg[q];
+            }
+            const uint32_t o = toff(t, i0, 8192);
+            store_split8(sm + kPOffTb + o, sm + kPOffTb + 8192 + o, a);
+            store_split8(sm + kPOffTb + 16384 + o, sm + kPOffTb + 24576 + o, bg);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (pt == 0) {
+            tc_fence_after();
+            const uint32_t id_uw = idesc_bf16(128, 64, 1, 0);   // A MN-major, B K-major
+            const uint64_t dTb = smem_desc(smem_u32(sm + kPOffTb), 16, 1024, kSwizzle128B);
+            const uint64_t dV = smem_desc(smem_u32(vv), 8192, 1024, kSwizzle128B);
+            const uint64_t dK = smem_desc(smem_u32(kq), 16384, 1024, kSwizzle128B);
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    // U0^T = V^T Tb^T ;  W^T = K^T Tbg^T
+                    umma_f16(tX, dV + uint64_t(s * 2048 >> 4), dTb + uint64_t((part * 8192 + s * 32) >> 4), id_uw,
+                             part > 0 || s > 0);
+                    umma_f16(tGW, dK + uint64_t(s * 2048 >> 4), dTb + uint64_t((16384 + part * 8192 + s * 32) >> 4),
+                             id_uw, part > 0 || s > 0);
+                }
+            umma_commit(&bars[2]);
+        }
+        __syncwarp();
+        // ---- while U0 and W run: Qs = diag(Gamma r_q) Q to the record ----------
+        for (int idx = pt; idx < kC * 16; idx += kPrepThreads) {
+            const int r = idx >> 4, cc = (idx & 15) * 8;
+            const float f = r < rows ? vEg[r] * vRq[r] : 0.f;
+            float v[8];
+            load_chunk8(kq + 8192 + toff(r, cc, 16384), v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] *= f;
+            store_chunk8(rec + kRecQ + toff(r, cc, 8192), v);
+        }
+        if (pt == 0) lf = !mbar_wait(&bars[2], 0, kWaitLimit);
+        if (__syncthreads_or(lf)) { fail = true; break; }
+        tc_fence_after();
+        {
+            float v[32];
+            tmem_ld32(tGW + lane_addr + phalf * 32, v);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = -v[q];
+#pragma unroll
+            for (int q = 0; q < 32; q += 8) store_chunk8(rec + kRecWt + toff(row, phalf * 32 + q, 16384), v + q);
+            tmem_ld32(tX + lane_addr + phalf * 32, v);
+            float4* u = reinterpret_cast<float4*>(rec + kRecU) + pw * 8 * 32 + lane;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) u[i * 32] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+    } while (false);
+
+    // ---- teardown: a CTA whose bounded wait ran out lets its copies land ------
+    tc_fence_before();
+    __syncthreads();
+    if (fail && pt == 0) {
+        atomicAdd(&g_tc_timeouts, 1);
+        if (tma) mbar_wait(&bars[0], 0, kWaitLimit);
+    }
+    __syncthreads();
+    if (pw == 0) tmem_dealloc(tmem, kPrepTmemCols);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     extern __shared__ uint8_t smem_raw[];
@@ -405,6 +733,8 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     const int c_end = p.seg_phase ? min(c_begin + seg_len, seq_chunks) : seq_chunks;
     if (c_begin >= c_end && !(seg == 0 && mode == kModeFull)) return;   // no such segment
     const int nchunks = c_end > c_begin ? c_end - c_begin : 0;
+    const bool split = p.prep_ws != nullptr;
+    const int64_t slot0 = t0 / p.chunk + n + c_begin;   // record slot of this CTA's first chunk
     t0 += int64_t(c_begin) * p.chunk;                   // first token of this CTA's part
     const bool last_seg = c_end >= seq_chunks;
     const bool write_out = mode == kModeFull;
@@ -472,13 +802,179 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     // barriers (named_sync_or) and leaves its loop together.
     auto wait = [&](int slot, uint32_t parity) { return mbar_wait(&bars[slot], parity, kWaitLimit); };
 
-    if (tid == 0) {
+    if (tid == 0 && !split) {
         if (nchunks > 0 && tma_ok(0)) issue_tma(0);
         if (nchunks > 1 && tma_ok(1)) issue_tma(1);
     }
     __syncwarp();
 
-    if (!is_chain) {
+    if (!is_chain && split && warp < 4) {
+        // ============================================================== loader
+        // Warps 0-3 stream the chunk records of the split preparation: -W^T, P
+        // and Qs by bulk copy, K by TMA (plain loads at the ragged end of the
+        // buffers), U0^T from global memory into D_X (both column halves of
+        // the thread's TMEM lane), the chain's vectors into shared memory.
+        constexpr uint32_t kLoadThreads = 128;
+        const int pt = tid;
+        const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
+        bool fail = false;
+        for (int c = 0; c < nchunks; ++c) {
+            const int b = c & 1;
+            uint8_t* kq = stage_ptr(c);
+            const uint8_t* rec = p.prep_ws + (size_t(h) * size_t(p.prep_slots) + size_t(slot0 + c)) * kPrepRecordBytes;
+            const bool tk = tma_ok(c);
+            // U0^T of this thread's TMEM lane (the fragments of preparing
+            // warps w and w + 4), loaded early and consumed after XREAD
+            float u[64];
+            if (mode != kModeTransition) {
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const float4* src = reinterpret_cast<const float4*>(rec + kRecU) + (warp + 4 * hf) * 8 * 32 + lane;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 w = __ldg(src + i * 32);
+                        u[hf * 32 + 4 * i] = w.x;
+                        u[hf * 32 + 4 * i + 1] = w.y;
+                        u[hf * 32 + 4 * i + 2] = w.z;
+                        u[hf * 32 + 4 * i + 3] = w.w;
+                    }
+                }
+            }
+            bool lf = false;
+            if (tid == 0) {
+                if (c >= 2) lf = !wait(B_SFREE0 + b, uint32_t(((c - 2) >> 1) & 1));
+                if (c >= 2 && write_out && !lf) lf = !wait(B_PFREE0 + b, uint32_t(((c - 2) >> 1) & 1));
+                if (c >= 2 && !lf) lf = !wait(b ? B_WTFREE1 : B_WTFREE, uint32_t(((c - 2) >> 1) & 1));
+                if (!lf) {
+                    uint64_t* bar = &bars[B_RAW0 + b];
+                    s_tma_last[b] = c;
+                    mbar_arrive_expect_tx(bar, 16384u + (write_out ? 32768u : 0u) + (tk ? 16384u : 0u));
+                    bulk_load(sm + (b ? kOffTb : kOffWt), rec + kRecWt, 16384, bar);
+                    if (write_out) {
+                        bulk_load(sm + kOffP + uint32_t(b * 2) * 8192u, rec + kRecP, 16384, bar);
+                        bulk_load(kq + 8192, rec + kRecQ, 8192, bar);
+                        bulk_load(kq + 24576, rec + kRecQ + 8192, 8192, bar);
+                    }
+                    if (tk) {
+                        const int y = int(chunk_start(c));
+                        tma_load_2d(kq + 0, &maps.k, bar, kh * kD, y);
+                        tma_load_2d(kq + 16384, &maps.k, bar, kh * kD + 64, y);
+                    }
+                }
+            }
+            __syncwarp();
+            if (named_sync_or(kBarPrep, kLoadThreads, lf)) { fail = true; break; }
+            if (!tk) {
+                const int64_t cs = chunk_start(c);
+                for (int idx = pt; idx < kC * 16; idx += kLoadThreads) {
+                    const int r = idx >> 4, cc = (idx & 15) * 8;
+                    const int64_t t = cs + r;
+                    uint4 zk = make_uint4(0, 0, 0, 0);
+                    if (t < t_end_all) zk = *reinterpret_cast<const uint4*>(gk + t * p.k_stride + kh * kD + cc);
+                    *reinterpret_cast<uint4*>(kq + toff(r, cc, 16384)) = zk;
+                }
+                fence_proxy_async_smem();
+            }
+            if (pt < kC) cE[b * kC + pt] = reinterpret_cast<const float*>(rec + kRecVec)[pt];
+            if (pt == kC) cGS[b] = reinterpret_cast<const float*>(rec + kRecVec)[kC];
+            if (mode != kModeTransition) {
+                if (tid == 0 && c >= 1) lf = !wait(B_XREAD, uint32_t((c - 1) & 1));
+                __syncwarp();
+                if (named_sync_or(kBarPrep, kLoadThreads, lf)) { fail = true; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int q = 0; q < 64; q += 16) tmem_st16(tX + lane_addr + q, u + q);
+                tmem_st_wait();
+            }
+            if (tid == 0) lf = !wait(B_RAW0 + b, uint32_t((c >> 1) & 1));
+            __syncwarp();
+            tc_fence_before();
+            if (named_sync_or(kBarPrep, kLoadThreads, lf)) { fail = true; break; }
+            if (tid == 0) mbar_arrive(&bars[B_READY0 + b]);
+            __syncwarp();
+        }
+        if (fail) *s_err = 1;
+    } else if (!is_chain && split) {
+        // ============================================ incoming state, O issuer
+        // Warps 8-11 put the incoming state into TMEM while the loader fetches
+        // the first record (Zb = bf16(S_0^T) and Z = S_0^T, then, once the
+        // first record's exp(gamma_S) is in, Z <- exp(gamma_S) Z) and release
+        // the chain through a named barrier.
+        if (nchunks > 0) {
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                float z[64];
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const int d = hf * 64 + i;
+                    z[i] = init_src ? init_src[size_t(d) * kD + row] : (init_identity && d == row ? 1.f : 0.f);
+                }
+                uint32_t zb[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) zb[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
+                GDN_TMEM_ST_X16(tZb + lane_addr + hf * 32, zb);
+                GDN_TMEM_ST_X16(tZb + lane_addr + hf * 32 + 16, (zb + 16));
+#pragma unroll
+                for (int q = 0; q < 64; q += 16) tmem_st16(tZ + lane_addr + hf * 64 + q, z + q);
+            }
+            tmem_st_wait();
+            bool lf = false;
+            if (tid == 256) lf = !wait(B_READY0, 0);
+            __syncwarp();
+            if (named_sync_or(kBarHelp, 128, lf)) *s_err = 1;
+            const float gs0 = cGS[0];
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                float z[64];
+                tmem_ld64(tZ + lane_addr + hf * 64, z);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) z[i] *= gs0;
+#pragma unroll
+                for (int q = 0; q < 64; q += 16) tmem_st16(tZ + lane_addr + hf * 64 + q, z + q);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            named_sync(kBarInit, 256);
+        }
+        // Warp 8, lane 0: the output MMAs of every chunk, so that the chain's
+        // lead thread (whose MMA issue blocks at the tensor pipe's pace)
+        // only issues the state-critical ones.  O^T = Zb Qs^T goes in after
+        // the chunk's X MMAs have completed, U^T P^T after its Z MMAs were
+        // issued, so neither delays the state chain in the pipe.
+        if (write_out && tid == 256) {
+            const uint32_t id_o = idesc_bf16(128, 64, 0, 0);    // B = Qs or P, K-major
+            bool lf = false;
+            for (int c = 0; c < nchunks && !lf && !*s_err; ++c) {
+                const int b = c & 1;
+                uint8_t* kq = stage_ptr(c);
+                lf = !wait(B_X, uint32_t(c & 1));
+                if (lf) break;
+                tc_fence_after();
+                const uint64_t dQ = smem_desc(smem_u32(kq + 8192), 16, 1024, kSwizzle128B);
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
+                    umma_f16_tmemA(tO, tZb + s * 8, dQ + (off >> 4), id_o, s > 0);
+                }
+                umma_commit(&bars[B_OQ]);
+                lf = !wait(B_ZISS, uint32_t(c & 1));
+                if (lf) break;
+                tc_fence_after();
+                const uint64_t dP = smem_desc(smem_u32(sm + kOffP + uint32_t(b * 2) * 8192u), 16, 1024,
+                                              kSwizzle128B);
+                // (U hi, P hi), (U hi, P lo), (U lo, P hi)
+#pragma unroll
+                for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        umma_f16_tmemA(tO, tU + (pr == 2 ? 32 : 0) + s * 8,
+                                       dP + uint64_t(((pr == 1 ? 8192 : 0) + s * 32) >> 4), id_o, 1);
+                umma_commit(&bars[B_O]);
+            }
+            if (lf) *s_err = 1;
+        }
+        __syncwarp();
+    } else if (!is_chain) {
         // ================================================================ prep
         // Thread 0 alone polls mbarriers; the group learns the outcome through
         // a voting named barrier (many pollers would starve the other warps).
@@ -739,7 +1235,6 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         const uint32_t id_x = idesc_bf16(128, 64, 0, 1);    // B = -W^T, MN-major
         const uint32_t id_o = idesc_bf16(128, 64, 0, 0);    // B = Qs or P, K-major
         const uint32_t id_z = idesc_bf16(128, 128, 0, 1);   // B = raw K, MN-major [i][d]
-        const uint64_t dWt = smem_desc(smem_u32(sm + kOffWt), 16384, 1024, kSwizzle128B);
         bool fail = false;
         // output rows of the previous chunk, kept as bf16 pairs until the next
         // chunk's MMAs are in flight
@@ -750,6 +1245,9 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             if (final_dst)
                 for (int d = 0; d < kD; ++d)
                     final_dst[size_t(d) * kD + row] = init_src ? init_src[size_t(d) * kD + row] : 0.f;
+        } else if (split) {
+            named_sync(kBarInit, 256);                   // warps 8-11 stored the incoming state
+            tc_fence_after();
         } else {
             // ---- incoming state: Zb = bf16(Z), Z <- exp(gamma_S(0)) Z -----------
             bool lf = lead && !wait(B_READY0, 0);
@@ -790,12 +1288,15 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 lf = !wait(B_READY0 + b, uint32_t((c >> 1) & 1));
                 if (!lf) {
                     tc_fence_after();
+                    // -W^T: one buffer inline; two (even, odd chunks) with split preparation
+                    const uint64_t dWt = smem_desc(smem_u32(sm + (split && b ? kOffTb : kOffWt)), 16384, 1024,
+                                                   kSwizzle128B);
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
                         umma_f16_tmemA(tX, tZb + s * 8, dWt + uint64_t(s * 2048 >> 4), id_x,
                                        mode != kModeTransition || s > 0);
                     umma_commit(&bars[B_X]);
-                    if (write_out) {                  // the map passes write no outputs
+                    if (write_out && !split) {        // map passes: no outputs; split: the O issuer
                         const uint64_t dQ = smem_desc(smem_u32(kq + 8192), 16, 1024, kSwizzle128B);
 #pragma unroll
                         for (int s = 0; s < 8; ++s) {
@@ -820,7 +1321,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             __syncwarp();
             if (named_sync_or(kBarChain, kChainThreads, lf)) { fail = true; break; }
             tc_fence_after();
-            if (lead) mbar_arrive(&bars[B_WTFREE]);
+            if (lead) mbar_arrive(&bars[split && b ? B_WTFREE1 : B_WTFREE]);
             __syncwarp();
             // ---- U (hi, lo) and Us = U diag(e) (hi, lo) into TMEM --------------
             for (int hf = 0; hf < 2; ++hf) {
@@ -859,7 +1360,8 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     for (int s = 0; s < 4; ++s)
                         umma_f16_tmemA(tZ, tU + 64 + part * 32 + s * 8, dK + uint64_t(s * 2048 >> 4), id_z, 1);
                 umma_commit(&bars[B_Z]);
-                if (write_out) {
+                if (split) mbar_arrive(&bars[B_ZISS]);
+                if (write_out && !split) {
                     // (U hi, P hi), (U hi, P lo), (U lo, P hi)
 #pragma unroll
                     for (int pr = 0; pr < 3; ++pr)
@@ -875,9 +1377,11 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             const bool has_next = c + 1 < nchunks;
             if (lead) {
                 lf = !wait(B_Z, uint32_t(c & 1));
+                // the O issuer's Zb Qs^T must be done before Zb and the stage are reused
+                if (!lf && split && write_out) lf = !wait(B_OQ, uint32_t(c & 1));
                 if (!lf) {
                     mbar_arrive(&bars[B_SFREE0 + b]);
-                    if (c + 2 < nchunks && tma_ok(c + 2)) issue_tma(c + 2);
+                    if (!split && c + 2 < nchunks && tma_ok(c + 2)) issue_tma(c + 2);
                     if (has_next) lf = !wait(B_READY0 + (b ^ 1), uint32_t(((c + 1) >> 1) & 1));
                 }
             }
@@ -1119,6 +1623,15 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
         return cudaErrorInvalidValue;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(chunk_tc_kernel), int(kSmemBytes));
     if (e != cudaSuccess) return e;
+    if (p.prep_ws != nullptr && p.prep_slots > 0) {   // every chunk's S-independent part, in parallel
+        if (p.prep_slots > INT32_MAX || p.Hv > 65535) return cudaErrorInvalidValue;
+        if ((e = ensure_smem(reinterpret_cast<const void*>(chunk_prep_kernel), int(kPrepSmemBytes))) != cudaSuccess)
+            return e;
+        timer_begin(s, "chunk_prep_kernel");
+        chunk_prep_kernel<<<dim3(unsigned(p.prep_slots), unsigned(p.Hv), 1), kPrepThreads, kPrepSmemBytes, s>>>(p, maps);
+        timer_end(s);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     if (p.seg_chunks <= 0 || p.seg_max < 2) {
         ChunkParams q = p;
         q.seg_phase = 0;

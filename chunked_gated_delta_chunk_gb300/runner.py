@@ -27,7 +27,7 @@ class PrefillCall:
                  state_in: Optional[torch.Tensor] = None, conv_state_in: Optional[torch.Tensor] = None,
                  write_state: bool = True, write_conv_state: bool = True,
                  alias_state: bool = False, alias_conv_state: bool = False,
-                 segment_chunks: int = 0):
+                 segment_chunks: int = 0, split_prep: int = 0):
         self.p = p
         dev = torch.device(device)
         self.dev = dev
@@ -50,7 +50,8 @@ class PrefillCall:
                       chunk=int(chunk or p.chunk), T_total=T, g=self.g, beta=self.beta,
                       state_in=self.state_in, state_out=self.state_out, out=self.out,
                       cu_seqlens=self.cu, use_qk_l2norm=int(p.use_l2norm),
-                      q_scale=float(p.q_scale), segment_chunks=int(segment_chunks))
+                      q_scale=float(p.q_scale), segment_chunks=int(segment_chunks),
+                      split_prep=int(split_prep))
         if p.conv is not None:
             self.x = p.conv["x"].to(dev).contiguous()
             self.w = p.conv["w"].to(dev, torch.float32).contiguous()

@@ -122,6 +122,18 @@ typedef struct gdn_prefill_desc {
      * its true start state).  0 = chosen from the shape (on only when it
      * gives at least three segments per sequence on 152 SMs), < 0 = off. */
     int segment_chunks;
+
+    /* Split preparation (bf16, dk = dv = 128, T_total known, and a
+     * workspace): the part of every chunk that does not depend on the
+     * incoming state (q/k norms, the cumulative decay, the masked Gram
+     * matrices, the blocked inverse T, U0 = T diag(beta) V,
+     * W = T diag(beta exp(gamma)) K, the intra-chunk output weights and the
+     * scaled queries) is solved first for all chunks in parallel and stored
+     * as one 82432-byte record per (value head, chunk slot), Hv *
+     * (T_total / chunk + B + 1) records; the state pass then streams the
+     * records.  The results are the same as without it.  0 = on when the
+     * workspace holds the records, < 0 = off. */
+    int split_prep;
 } gdn_prefill_desc;
 
 /* Fill *d with the defaults listed above (all pointers NULL). */
@@ -145,12 +157,15 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* g, con
  * q_scale and workspace as described in gdn_prefill_desc. */
 int gdn_prefill_ex(const gdn_prefill_desc* d, gdn_stream_t stream);
 
-/* Device workspace gdn_prefill_ex needs for *d, in bytes (0 if none): the
- * output of the short convolution, plus the per-segment maps of the
- * segment-parallel scan when that is chosen.  Reads only dtype, B, Hk, Hv,
- * dk, dv, chunk, T_total, segment_chunks and whether conv_x is set; returns
- * (size_t)-1 when those are invalid.  A workspace too small for the segment
- * maps (but enough for the convolution) runs the scan in one pass. */
+/* Device workspace gdn_prefill_ex uses for *d, in bytes (0 if none), laid
+ * out in this order: the output of the short convolution, the per-segment
+ * maps of the segment-parallel scan when that is chosen, the chunk records of
+ * the split preparation when that is on.  Reads only dtype, B, Hk, Hv, dk,
+ * dv, chunk, T_total, segment_chunks, split_prep and whether conv_x is set;
+ * returns (size_t)-1 when those are invalid.  Only the convolution's part is
+ * required: a workspace too small for the segment maps runs the scan in one
+ * pass, one too small for the records solves each chunk inside the state
+ * pass (same results either way). */
 size_t gdn_workspace_bytes(const gdn_prefill_desc* d);
 
 /*

@@ -103,8 +103,12 @@ def _desc(**kw):
 
 def test_workspace_size_and_rejection(lib):
     d = _desc()
-    need = B.gdn_workspace_bytes(d)
-    assert need == ((100 * (2 * 16 * 128 + 32 * 128) * 2 + 255) // 256) * 256
+    conv = ((100 * (2 * 16 * 128 + 32 * 128) * 2 + 255) // 256) * 256
+    records = 32 * (100 // 64 + 1 + 1) * 82432      # Hv x chunk slots x record bytes
+    assert B.gdn_workspace_bytes(d) == conv + records
+    assert B.gdn_workspace_bytes(_desc(split_prep=-1)) == conv
+    assert B.gdn_workspace_bytes(_desc(dtype=B.GDN_FP32)) == ((100 * 8192 * 4 + 255) // 256) * 256
+    need = conv                                      # only the convolution's output is required
     assert lib.gdn_prefill_ex(ctypes.byref(d), None) == B.GDN_ERR_WORKSPACE
     d.workspace, d.workspace_bytes = A, need - 1
     assert lib.gdn_prefill_ex(ctypes.byref(d), None) == B.GDN_ERR_WORKSPACE
@@ -112,7 +116,9 @@ def test_workspace_size_and_rejection(lib):
     assert lib.gdn_prefill_ex(ctypes.byref(d), None) == B.GDN_ERR_WORKSPACE
     d32 = _desc(dtype=B.GDN_FP32)
     assert B.gdn_workspace_bytes(d32) == ((100 * 8192 * 4 + 255) // 256) * 256
-    assert B.gdn_workspace_bytes(_desc(conv_x=None)) == 0
+    assert B.gdn_workspace_bytes(_desc(conv_x=None)) == records
+    assert B.gdn_workspace_bytes(_desc(conv_x=None, split_prep=-1)) == 0
+    assert B.gdn_workspace_bytes(_desc(conv_x=None, T_total=-1)) == 0
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -148,7 +154,8 @@ def test_status_strings_and_defaults(lib):
 
 def test_launch_plan_names(lib):
     """Host-only launch plan: the tensor-core kernel for bf16 with
-    dk = dv = 128, the SIMT kernel otherwise; conv adds its two kernels."""
+    dk = dv = 128, the SIMT kernel otherwise; conv adds its two kernels, and
+    the split preparation runs first when the workspace holds its records."""
     d = B.make_desc(B=1, Hk=2, Hv=4, dk=128, dv=128, q=A, k=A, v=A, g=A, beta=A, out=A,
                     cu_seqlens=A)
     assert B.gdn_prefill_plan(d) == ["chunk_tc_kernel"]
@@ -160,6 +167,12 @@ def test_launch_plan_names(lib):
     assert B.gdn_prefill_plan(d64) == ["chunk_simt_kernel"]
     dc = _desc(conv_state_out=A)
     dc.workspace, dc.workspace_bytes = A, 1 << 40
+    assert B.gdn_prefill_plan(dc) == ["conv_kernel", "chunk_prep_kernel", "chunk_tc_kernel",
+                                      "conv_state_kernel"]
+    dc.split_prep = -1
+    assert B.gdn_prefill_plan(dc) == ["conv_kernel", "chunk_tc_kernel", "conv_state_kernel"]
+    dc.split_prep = 0
+    dc.workspace_bytes = B.gdn_workspace_bytes(dc) - 1      # no room for the chunk records
     assert B.gdn_prefill_plan(dc) == ["conv_kernel", "chunk_tc_kernel", "conv_state_kernel"]
     bad = B.make_desc(B=1, Hk=2, Hv=4, dk=48, dv=128, q=A, k=A, v=A, g=A, beta=A, out=A,
                       cu_seqlens=A)

@@ -273,6 +273,41 @@ def test_segment_scan_off_equals_on_bits_of_segment_zero():
     assert torch.equal(a.out[:256], b.out[:256])
 
 
+# ---------------------------------------------------------------- split preparation
+@pytest.mark.parametrize("seg,lengths,chunk", [
+    (-1, [300], 64), (-1, [1, 64, 0, 129, 7], 64), (3, [64 * 7 + 5], 64),
+    (4, [1, 200, 0, 900], 64), (2, [333, 64 * 6], 32), (-1, [250, 3], 17)])
+def test_split_preparation_matches_inline_bits_and_oracle(seg, lengths, chunk):
+    """Chunk records solved ahead of the state pass (all chunks in parallel)
+    give the same bits as the preparation inside the state pass: the same
+    arithmetic in the same order, only stored and streamed back.  Both match
+    the token loop.  Ragged ends, empty sequences, chunks below 64 rows and
+    the segment scan's map passes all read records."""
+    from chunked_gated_delta_chunk_gb300 import binding as B
+    p = inputs.make_problem(60 + seg + len(lengths), lengths, 2, 4, 128, 128, chunk=chunk)
+    inline = runner.PrefillCall(p, segment_chunks=seg, split_prep=-1)
+    split = runner.PrefillCall(p, segment_chunks=seg)
+    assert "chunk_prep_kernel" not in B.gdn_prefill_plan(inline.desc)
+    assert B.gdn_prefill_plan(split.desc)[0] == "chunk_prep_kernel"
+    inline.run()
+    split.run()
+    torch.cuda.synchronize()
+    assert torch.equal(inline.out, split.out)
+    assert torch.equal(inline.state_out, split.state_out)
+    compare({k: v.cpu() for k, v in split.results().items()}, run_oracle(p), TOL_BF16)
+
+
+def test_split_preparation_with_conv_gqa_and_aliased_state():
+    p = inputs.make_problem(70, [700, 90, 0, 33], 2, 8, 128, 128, conv_kernel=4)
+    call = runner.PrefillCall(p, segment_chunks=3, alias_state=True, alias_conv_state=True)
+    from chunked_gated_delta_chunk_gb300 import binding as B
+    assert "chunk_prep_kernel" in B.gdn_prefill_plan(call.desc)
+    ref = run_oracle(p)
+    call.run()
+    torch.cuda.synchronize()
+    compare({k: v.cpu() for k, v in call.results().items()}, ref, TOL_BF16)
+
+
 # ---------------------------------------------------------------- launch timer
 def test_launch_timer_records_every_planned_launch():
     """With the launch timer on, one call records exactly the kernels its
