@@ -57,7 +57,6 @@ constexpr int kThreads = 384;
 constexpr uint32_t kPrepThreads = 256; // warps 0-3 and 8-11
 constexpr uint32_t kChainThreads = 128;
 constexpr uint32_t kBarPrep = 1, kBarChain = 2;
-constexpr uint32_t kBarInit = 3, kBarHelp = 4;   // split preparation: warps 4-11, warps 8-11
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr int kLdA = kC + 4;         // fp32 row stride of A and T: 16-byte aligned rows
 constexpr float kLog2e = 1.4426950408889634f;
@@ -395,6 +394,10 @@ constexpr uint32_t kPrepTmemCols = 128;                  // Gram, then W^T (64);
 static_assert(kC * kLdA * 4 <= 4 * 8192, "A fits under Tb");
 static_assert(2 * (kPrepSmemBytes + 1024) <= 233472, "two preparation CTAs per SM");
 
+// Persistent: each CTA takes items (value head, chunk slot) with a grid
+// stride and prefetches the next item's raw tiles (TMA) and g, beta while
+// it finishes the current one, so neither the setup (barriers, TMEM) nor the
+// load latency is paid per chunk.
 __global__ void __launch_bounds__(kPrepThreads, 2)
 chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     extern __shared__ uint8_t smem_raw[];
@@ -415,46 +418,79 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPOffBar);   // raw tiles, Gram, U0 / W
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kPOffBar + 24);
 
-    const int slot = blockIdx.x, h = blockIdx.y;
     const int pt = threadIdx.x, pw = pt >> 5, lane = pt & 31;
     const int phalf = pw >> 2;                              // column half of TMEM reads
     const int row = (pw & 3) * 32 + lane;                   // TMEM lane of this thread
     const uint32_t lane_addr = uint32_t((pw & 3) * 32) << 16;
-    const int kh = h / (p.Hv / p.Hk);
     const int Hv = p.Hv;
+    const int64_t n_items = p.prep_slots * int64_t(Hv);
 
-    // ---- the chunk of this slot: the last sequence n with t0_n / chunk + n <= slot
     int64_t t_end_all = p.cu[p.B];
     if (t_end_all > p.t_cap) t_end_all = p.t_cap;
     auto seq_first = [&](int m) {
         const int64_t t = p.cu[m];
         return t < 0 ? int64_t(0) : (t > t_end_all ? t_end_all : t);
     };
-    int lo = 0, hi = p.B - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (seq_first(mid) / p.chunk + mid <= slot) lo = mid;
-        else hi = mid - 1;
-    }
-    const int n = lo;
-    const int64_t t0 = seq_first(n);
-    int64_t t1 = p.cu[n + 1];
-    t1 = t1 < t0 ? t0 : (t1 > t_end_all ? t_end_all : t1);
-    const int64_t c = int64_t(slot) - (t0 / p.chunk + n);
-    if (c < 0 || c * p.chunk >= t1 - t0) return;            // no chunk in this slot
-    const int64_t cs = t0 + c * p.chunk;
-    const int rows = int(t1 - cs < p.chunk ? t1 - cs : p.chunk);
-    uint8_t* rec = p.prep_ws + (size_t(h) * size_t(p.prep_slots) + size_t(slot)) * kPrepRecordBytes;
-    const bool tma = cs + kC <= t_end_all;
+    // The chunk of item = h * prep_slots + slot: the last sequence n with
+    // t0_n / chunk + n <= slot, chunk c = slot - (t0_n / chunk + n); false
+    // when the slot holds no chunk.
+    struct Item {
+        int h, slot, rows;
+        int64_t cs;
+        bool tma;
+    };
+    auto resolve = [&](int64_t item, Item& it) {
+        it.h = int(item / p.prep_slots);
+        it.slot = int(item % p.prep_slots);
+        int lo = 0, hi = p.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (seq_first(mid) / p.chunk + mid <= it.slot) lo = mid;
+            else hi = mid - 1;
+        }
+        const int64_t t0 = seq_first(lo);
+        int64_t t1 = p.cu[lo + 1];
+        t1 = t1 < t0 ? t0 : (t1 > t_end_all ? t_end_all : t1);
+        const int64_t c = int64_t(it.slot) - (t0 / p.chunk + lo);
+        if (c < 0 || c * p.chunk >= t1 - t0) return false;
+        it.cs = t0 + c * p.chunk;
+        it.rows = int(t1 - it.cs < p.chunk ? t1 - it.cs : p.chunk);
+        it.tma = it.cs + kC <= t_end_all;
+        return true;
+    };
+    auto next_item = [&](int64_t from, Item& it) {
+        for (int64_t i = from; i < n_items; i += gridDim.x)
+            if (resolve(i, it)) return i;
+        return n_items;
+    };
+    auto issue_raw = [&](const Item& it) {      // thread 0: the 64-row boxes of K, Q, V
+        const int kh = it.h / (Hv / p.Hk);
+        const int y = int(it.cs);
+        mbar_arrive_expect_tx(&bars[0], kStageBytes);
+        tma_load_2d(kq + 0, &maps.k, &bars[0], kh * kD, y);
+        tma_load_2d(kq + 16384, &maps.k, &bars[0], kh * kD + 64, y);
+        tma_load_2d(kq + 8192, &maps.q, &bars[0], kh * kD, y);
+        tma_load_2d(kq + 24576, &maps.q, &bars[0], kh * kD + 64, y);
+        tma_load_2d(vv + 0, &maps.v, &bars[0], it.h * kD, y);
+        tma_load_2d(vv + 8192, &maps.v, &bars[0], it.h * kD + 64, y);
+    };
 
+    Item cur;
+    int64_t item = next_item(blockIdx.x, cur);
+    if (item >= n_items) return;                            // no chunk for this CTA
     if (pt == 0) {
         for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
-        if (tma) {
-            tma_prefetch_desc(&maps.q);
-            tma_prefetch_desc(&maps.k);
-            tma_prefetch_desc(&maps.v);
-        }
+        tma_prefetch_desc(&maps.q);
+        tma_prefetch_desc(&maps.k);
+        tma_prefetch_desc(&maps.v);
+        if (cur.tma) issue_raw(cur);
+    }
+    // g, beta of the current item (rows past the chunk are zero)
+    float g_in = 0.f, b_in = 0.f;
+    if (pt < cur.rows) {
+        g_in = p.g[(cur.cs + pt) * Hv + cur.h];
+        b_in = p.beta[(cur.cs + pt) * Hv + cur.h];
     }
     __syncwarp();
     if (pw == 0) {
@@ -462,32 +498,25 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         tmem_relinquish();
     }
     for (int idx = pt; idx < kC * kLdA; idx += kPrepThreads) sT[idx] = 0.f;   // upper triangle stays 0
-    if (pt < kC) {
-        const int64_t t = cs + pt;
-        vGam[pt] = pt < rows ? p.g[t * Hv + h] : 0.f;
-        vBeta[pt] = pt < rows ? p.beta[t * Hv + h] : 0.f;
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tGW = tmem, tX = tmem + 64;
-    bool fail = false;
-    do {
+    uint32_t raw_phase = 0, mma_phase = 0;                 // completed phases of bars[0], of bars[1] / bars[2]
+    bool raw_pending = cur.tma, fail = false;
+    while (item < n_items) {
+        const int h = cur.h, rows = cur.rows;
+        const int kh = h / (Hv / p.Hk);
+        const int64_t cs = cur.cs;
+        uint8_t* rec = p.prep_ws + (size_t(h) * size_t(p.prep_slots) + size_t(cur.slot)) * kPrepRecordBytes;
+        if (pt < kC) {
+            vGam[pt] = g_in;
+            vBeta[pt] = b_in;
+        }
         // ---- raw tiles: TMA when the whole 64-row box lies inside the buffers,
         // else plain loads (rows past the buffers are zero)
-        if (tma) {
-            if (pt == 0) {
-                const int y = int(cs);
-                mbar_arrive_expect_tx(&bars[0], kStageBytes);
-                tma_load_2d(kq + 0, &maps.k, &bars[0], kh * kD, y);
-                tma_load_2d(kq + 16384, &maps.k, &bars[0], kh * kD + 64, y);
-                tma_load_2d(kq + 8192, &maps.q, &bars[0], kh * kD, y);
-                tma_load_2d(kq + 24576, &maps.q, &bars[0], kh * kD + 64, y);
-                tma_load_2d(vv + 0, &maps.v, &bars[0], h * kD, y);
-                tma_load_2d(vv + 8192, &maps.v, &bars[0], h * kD + 64, y);
-            }
-        } else {
+        if (!cur.tma) {
             const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(p.q);
             const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
             const __nv_bfloat16* gv = static_cast<const __nv_bfloat16*>(p.v);
@@ -507,8 +536,12 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             fence_proxy_async_smem();
         }
         bool lf = false;
-        if (tma && pt == 0) lf = !mbar_wait(&bars[0], 0, kWaitLimit);
+        if (cur.tma && pt == 0) lf = !mbar_wait(&bars[0], raw_phase & 1, kWaitLimit);
         if (__syncthreads_or(lf)) { fail = true; break; }
+        if (cur.tma) {
+            ++raw_phase;
+            raw_pending = false;
+        }
         // ---- Gram MMA [K; Q] K^T; cumsum (log2 domain); row norms -------------
         tc_fence_after();
         if (pt == 32) {
@@ -564,7 +597,7 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             if (pt == rows - 1) reinterpret_cast<float*>(rec + kRecVec)[kC] = eg;
         }
         // ---- masks and decays on the Gram matrices: A to shared, P to the record
-        if (pt == 0) lf = !mbar_wait(&bars[1], 0, kWaitLimit);
+        if (pt == 0) lf = !mbar_wait(&bars[1], mma_phase & 1, kWaitLimit);
         if (__syncthreads_or(lf)) { fail = true; break; }
         tc_fence_after();
         {
@@ -651,9 +684,22 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             for (int q = 0; q < 8; ++q) v[q] *= f;
             store_chunk8(rec + kRecQ + toff(r, cc, 8192), v);
         }
-        if (pt == 0) lf = !mbar_wait(&bars[2], 0, kWaitLimit);
+        if (pt == 0) lf = !mbar_wait(&bars[2], mma_phase & 1, kWaitLimit);
         if (__syncthreads_or(lf)) { fail = true; break; }
+        ++mma_phase;
         tc_fence_after();
+        // ---- raw tiles are free: fetch the next item's while this one is stored
+        Item nxt;
+        const int64_t next = next_item(item + gridDim.x, nxt);
+        if (next < n_items) {
+            if (pt == 0 && nxt.tma) issue_raw(nxt);
+            raw_pending = nxt.tma;
+            g_in = b_in = 0.f;
+            if (pt < nxt.rows) {
+                g_in = p.g[(nxt.cs + pt) * Hv + nxt.h];
+                b_in = p.beta[(nxt.cs + pt) * Hv + nxt.h];
+            }
+        }
         {
             float v[32];
             tmem_ld32(tGW + lane_addr + phalf * 32, v);
@@ -666,19 +712,26 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) u[i * 32] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
-    } while (false);
+        tc_fence_before();
+        __syncthreads();                                   // TMEM read, vectors free for the next item
+        item = next;
+        cur = nxt;
+    }
 
     // ---- teardown: a CTA whose bounded wait ran out lets its copies land ------
     tc_fence_before();
     __syncthreads();
     if (fail && pt == 0) {
         atomicAdd(&g_tc_timeouts, 1);
-        if (tma) mbar_wait(&bars[0], 0, kWaitLimit);
+        if (raw_pending) mbar_wait(&bars[0], raw_phase & 1, kWaitLimit);
     }
     __syncthreads();
     if (pw == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
+// kSplit: the preparation comes from chunk records (chunk_prep_kernel) and
+// warps 0-3 stream them; otherwise warps 0-3 and 8-11 solve it inline.
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     extern __shared__ uint8_t smem_raw[];
@@ -708,7 +761,13 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;                 // TMEM lane of this thread
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
-    const bool is_chain = warp >= 4 && warp < 8;
+    // The chain: warps 4-7 (all columns of their TMEM lanes); with split
+    // preparation also warps 8-11, each chain thread then owning one column
+    // half (hc) of its lane.
+    const bool is_chain = kSplit ? warp >= 4 : (warp >= 4 && warp < 8);
+    const int hc = (kSplit && warp >= 8) ? 1 : 0;
+    constexpr int kHalves = kSplit ? 1 : 2;
+    constexpr uint32_t kChainN = kSplit ? 2 * kChainThreads : kChainThreads;
     const int kh = h / (p.Hv / p.Hk);
     const int Hv = p.Hv;
 
@@ -733,7 +792,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     const int c_end = p.seg_phase ? min(c_begin + seg_len, seq_chunks) : seq_chunks;
     if (c_begin >= c_end && !(seg == 0 && mode == kModeFull)) return;   // no such segment
     const int nchunks = c_end > c_begin ? c_end - c_begin : 0;
-    const bool split = p.prep_ws != nullptr;
+    constexpr bool split = kSplit;
     const int64_t slot0 = t0 / p.chunk + n + c_begin;   // record slot of this CTA's first chunk
     t0 += int64_t(c_begin) * p.chunk;                   // first token of this CTA's part
     const bool last_seg = c_end >= seq_chunks;
@@ -814,9 +873,42 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         // and Qs by bulk copy, K by TMA (plain loads at the ragged end of the
         // buffers), U0^T from global memory into D_X (both column halves of
         // the thread's TMEM lane), the chain's vectors into shared memory.
+        // Thread 0 also issues the output MMAs of the chain's previous chunk
+        // (the chain's lead thread, whose MMA issue blocks at the tensor
+        // pipe's pace, then only issues the state-critical ones): O^T =
+        // Zb Qs^T once that chunk's X MMAs have completed and U^T P^T once its
+        // Z MMAs were issued, so neither delays the state chain in the pipe.
         constexpr uint32_t kLoadThreads = 128;
         const int pt = tid;
         const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
+        const uint32_t id_o = idesc_bf16(128, 64, 0, 0);    // B = Qs or P, K-major
+        auto issue_oq = [&](int c) {                        // thread 0: O^T = Zb Qs^T of chunk c
+            if (!wait(B_X, uint32_t(c & 1))) return false;
+            tc_fence_after();
+            const uint64_t dQ = smem_desc(smem_u32(stage_ptr(c) + 8192), 16, 1024, kSwizzle128B);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
+                umma_f16_tmemA(tO, tZb + s * 8, dQ + (off >> 4), id_o, s > 0);
+            }
+            umma_commit(&bars[B_OQ]);
+            return true;
+        };
+        auto issue_op = [&](int c) {                        // thread 0: O^T += U^T P^T of chunk c
+            if (!wait(B_ZISS, uint32_t(c & 1))) return false;
+            tc_fence_after();
+            const uint64_t dP = smem_desc(smem_u32(sm + kOffP + uint32_t((c & 1) * 2) * 8192u), 16, 1024,
+                                          kSwizzle128B);
+            // (U hi, P hi), (U hi, P lo), (U lo, P hi)
+#pragma unroll
+            for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    umma_f16_tmemA(tO, tU + (pr == 2 ? 32 : 0) + s * 8,
+                                   dP + uint64_t(((pr == 1 ? 8192 : 0) + s * 32) >> 4), id_o, 1);
+            umma_commit(&bars[B_O]);
+            return true;
+        };
         bool fail = false;
         for (int c = 0; c < nchunks; ++c) {
             const int b = c & 1;
@@ -877,8 +969,9 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             }
             if (pt < kC) cE[b * kC + pt] = reinterpret_cast<const float*>(rec + kRecVec)[pt];
             if (pt == kC) cGS[b] = reinterpret_cast<const float*>(rec + kRecVec)[kC];
+            if (write_out && c >= 1 && tid == 0) lf = !issue_oq(c - 1);
             if (mode != kModeTransition) {
-                if (tid == 0 && c >= 1) lf = !wait(B_XREAD, uint32_t((c - 1) & 1));
+                if (tid == 0 && c >= 1 && !lf) lf = !wait(B_XREAD, uint32_t((c - 1) & 1));
                 __syncwarp();
                 if (named_sync_or(kBarPrep, kLoadThreads, lf)) { fail = true; break; }
                 tc_fence_after();
@@ -886,94 +979,19 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 for (int q = 0; q < 64; q += 16) tmem_st16(tX + lane_addr + q, u + q);
                 tmem_st_wait();
             }
-            if (tid == 0) lf = !wait(B_RAW0 + b, uint32_t((c >> 1) & 1));
+            if (tid == 0 && !lf) lf = !wait(B_RAW0 + b, uint32_t((c >> 1) & 1));
             __syncwarp();
             tc_fence_before();
             if (named_sync_or(kBarPrep, kLoadThreads, lf)) { fail = true; break; }
             if (tid == 0) mbar_arrive(&bars[B_READY0 + b]);
+            if (write_out && c >= 1 && tid == 0) lf = !issue_op(c - 1);
             __syncwarp();
+            if (named_sync_or(kBarPrep, kLoadThreads, lf)) { fail = true; break; }
         }
-        if (fail) *s_err = 1;
-    } else if (!is_chain && split) {
-        // ============================================ incoming state, O issuer
-        // Warps 8-11 put the incoming state into TMEM while the loader fetches
-        // the first record (Zb = bf16(S_0^T) and Z = S_0^T, then, once the
-        // first record's exp(gamma_S) is in, Z <- exp(gamma_S) Z) and release
-        // the chain through a named barrier.
-        if (nchunks > 0) {
-#pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
-                float z[64];
-#pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const int d = hf * 64 + i;
-                    z[i] = init_src ? init_src[size_t(d) * kD + row] : (init_identity && d == row ? 1.f : 0.f);
-                }
-                uint32_t zb[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) zb[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
-                GDN_TMEM_ST_X16(tZb + lane_addr + hf * 32, zb);
-                GDN_TMEM_ST_X16(tZb + lane_addr + hf * 32 + 16, (zb + 16));
-#pragma unroll
-                for (int q = 0; q < 64; q += 16) tmem_st16(tZ + lane_addr + hf * 64 + q, z + q);
-            }
-            tmem_st_wait();
-            bool lf = false;
-            if (tid == 256) lf = !wait(B_READY0, 0);
-            __syncwarp();
-            if (named_sync_or(kBarHelp, 128, lf)) *s_err = 1;
-            const float gs0 = cGS[0];
-#pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
-                float z[64];
-                tmem_ld64(tZ + lane_addr + hf * 64, z);
-#pragma unroll
-                for (int i = 0; i < 64; ++i) z[i] *= gs0;
-#pragma unroll
-                for (int q = 0; q < 64; q += 16) tmem_st16(tZ + lane_addr + hf * 64 + q, z + q);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            named_sync(kBarInit, 256);
-        }
-        // Warp 8, lane 0: the output MMAs of every chunk, so that the chain's
-        // lead thread (whose MMA issue blocks at the tensor pipe's pace)
-        // only issues the state-critical ones.  O^T = Zb Qs^T goes in after
-        // the chunk's X MMAs have completed, U^T P^T after its Z MMAs were
-        // issued, so neither delays the state chain in the pipe.
-        if (write_out && tid == 256) {
-            const uint32_t id_o = idesc_bf16(128, 64, 0, 0);    // B = Qs or P, K-major
-            bool lf = false;
-            for (int c = 0; c < nchunks && !lf && !*s_err; ++c) {
-                const int b = c & 1;
-                uint8_t* kq = stage_ptr(c);
-                lf = !wait(B_X, uint32_t(c & 1));
-                if (lf) break;
-                tc_fence_after();
-                const uint64_t dQ = smem_desc(smem_u32(kq + 8192), 16, 1024, kSwizzle128B);
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
-                    umma_f16_tmemA(tO, tZb + s * 8, dQ + (off >> 4), id_o, s > 0);
-                }
-                umma_commit(&bars[B_OQ]);
-                lf = !wait(B_ZISS, uint32_t(c & 1));
-                if (lf) break;
-                tc_fence_after();
-                const uint64_t dP = smem_desc(smem_u32(sm + kOffP + uint32_t(b * 2) * 8192u), 16, 1024,
-                                              kSwizzle128B);
-                // (U hi, P hi), (U hi, P lo), (U lo, P hi)
-#pragma unroll
-                for (int pr = 0; pr < 3; ++pr)
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        umma_f16_tmemA(tO, tU + (pr == 2 ? 32 : 0) + s * 8,
-                                       dP + uint64_t(((pr == 1 ? 8192 : 0) + s * 32) >> 4), id_o, 1);
-                umma_commit(&bars[B_O]);
-            }
-            if (lf) *s_err = 1;
-        }
+        if (!fail && write_out && nchunks > 0 && tid == 0)   // the last chunk's outputs
+            fail = !issue_oq(nchunks - 1) || !issue_op(nchunks - 1);
         __syncwarp();
+        if (fail) *s_err = 1;
     } else if (!is_chain) {
         // ================================================================ prep
         // Thread 0 alone polls mbarriers; the group learns the outcome through
@@ -1243,16 +1261,38 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         int o_rows = 0;
         if (nchunks == 0) {
             if (final_dst)
-                for (int d = 0; d < kD; ++d)
+                for (int d = hc * 64; d < (hc + kHalves) * 64; ++d)
                     final_dst[size_t(d) * kD + row] = init_src ? init_src[size_t(d) * kD + row] : 0.f;
         } else if (split) {
-            named_sync(kBarInit, 256);                   // warps 8-11 stored the incoming state
-            tc_fence_after();
+            // ---- incoming state (this thread's column half), loaded while the
+            // loader fetches the first record: Zb = bf16(S_0^T), Z = exp(gamma_S(0)) S_0^T
+            float z[64];
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const int d = hc * 64 + i;
+                z[i] = init_src ? init_src[size_t(d) * kD + row] : (init_identity && d == row ? 1.f : 0.f);
+            }
+            bool lf = lead && !wait(B_READY0, 0);
+            __syncwarp();
+            fail = named_sync_or(kBarChain, kChainN, lf);
+            const float gs0 = cGS[0];
+            uint32_t zb[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) zb[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
+            GDN_TMEM_ST_X16(tZb + lane_addr + hc * 32, zb);
+            GDN_TMEM_ST_X16(tZb + lane_addr + hc * 32 + 16, (zb + 16));
+#pragma unroll
+            for (int i = 0; i < 64; ++i) z[i] *= gs0;
+#pragma unroll
+            for (int q = 0; q < 64; q += 16) tmem_st16(tZ + lane_addr + hc * 64 + q, z + q);
+            tmem_st_wait();
+            tc_fence_before();
+            named_sync(kBarChain, kChainN);
         } else {
             // ---- incoming state: Zb = bf16(Z), Z <- exp(gamma_S(0)) Z -----------
             bool lf = lead && !wait(B_READY0, 0);
             __syncwarp();
-            fail = named_sync_or(kBarChain, kChainThreads, lf);
+            fail = named_sync_or(kBarChain, kChainN, lf);
             const float gs0 = cGS[0];
             for (int hf = 0; hf < 2; ++hf) {
                 float z[64];
@@ -1275,7 +1315,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             }
             tmem_st_wait();
             tc_fence_before();
-            named_sync(kBarChain, kChainThreads);
+            named_sync(kBarChain, kChainN);
         }
         for (int c = 0; c < nchunks && !fail; ++c) {
             const int b = c & 1;
@@ -1311,20 +1351,21 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             if (c > 0) {
                 __nv_bfloat16* dst = gout + (o_cs * Hv + h) * kD + row;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&opk[i]);
+                for (int k = 0; k < kHalves * 16; ++k) {
+                    const int i = hc * 16 + k;          // rows 2i, 2i + 1 of the chunk
+                    const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&opk[k]);
                     if (2 * i < o_rows) dst[int64_t(2 * i) * Hv * kD] = pr.x;
                     if (2 * i + 1 < o_rows) dst[int64_t(2 * i + 1) * Hv * kD] = pr.y;
                 }
             }
             if (lead && !lf) lf = !wait(B_X, uint32_t(c & 1));
             __syncwarp();
-            if (named_sync_or(kBarChain, kChainThreads, lf)) { fail = true; break; }
+            if (named_sync_or(kBarChain, kChainN, lf)) { fail = true; break; }
             tc_fence_after();
             if (lead) mbar_arrive(&bars[split && b ? B_WTFREE1 : B_WTFREE]);
             __syncwarp();
             // ---- U (hi, lo) and Us = U diag(e) (hi, lo) into TMEM --------------
-            for (int hf = 0; hf < 2; ++hf) {
+            for (int hf = hc; hf < hc + kHalves; ++hf) {
                 float x[32];
                 tmem_ld32(tX + lane_addr + hf * 32, x);
                 const float* e = cE + b * kC + hf * 32;
@@ -1347,7 +1388,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             }
             tmem_st_wait();
             tc_fence_before();
-            named_sync(kBarChain, kChainThreads);
+            named_sync(kBarChain, kChainN);
             if (lead) {
                 mbar_arrive(&bars[B_XREAD]);
                 tc_fence_after();
@@ -1386,10 +1427,10 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 }
             }
             __syncwarp();
-            if (named_sync_or(kBarChain, kChainThreads, lf)) { fail = true; break; }
+            if (named_sync_or(kBarChain, kChainN, lf)) { fail = true; break; }
             tc_fence_after();
             const float gsn = has_next ? cGS[b ^ 1] : 1.f;
-            for (int hf = 0; hf < 2; ++hf) {
+            for (int hf = hc; hf < hc + kHalves; ++hf) {
                 float z[64];
                 tmem_ld64(tZ + lane_addr + hf * 64, z);
                 uint32_t zb[32];
@@ -1420,28 +1461,31 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             if (write_out) {
                 if (lead) lf = !wait(B_O, uint32_t(c & 1));
                 __syncwarp();
-                if (named_sync_or(kBarChain, kChainThreads, lf)) { fail = true; break; }
+                if (named_sync_or(kBarChain, kChainN, lf)) { fail = true; break; }
                 tc_fence_after();
-                for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                for (int k = 0; k < kHalves; ++k) {
+                    const int hf = hc + k;
                     float o[32];
                     tmem_ld32(tO + lane_addr + hf * 32, o);
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        opk[hf * 16 + i] = pack_bf16x2(o[2 * i] * p.q_scale, o[2 * i + 1] * p.q_scale);
+                        opk[k * 16 + i] = pack_bf16x2(o[2 * i] * p.q_scale, o[2 * i + 1] * p.q_scale);
                 }
             }
             o_cs = cs;
             o_rows = write_out ? rows : 0;
             tc_fence_before();
-            named_sync(kBarChain, kChainThreads);
+            named_sync(kBarChain, kChainN);
             if (lead) mbar_arrive(&bars[B_PFREE0 + b]);
             __syncwarp();
         }
         if (!fail && nchunks > 0) {
             __nv_bfloat16* dst = gout + (o_cs * Hv + h) * kD + row;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&opk[i]);
+            for (int k = 0; k < kHalves * 16; ++k) {
+                const int i = hc * 16 + k;
+                const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&opk[k]);
                 if (2 * i < o_rows) dst[int64_t(2 * i) * Hv * kD] = pr.x;
                 if (2 * i + 1 < o_rows) dst[int64_t(2 * i + 1) * Hv * kD] = pr.y;
             }
@@ -1621,14 +1665,26 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
         !make_map(&maps.k, p.k, int64_t(p.Hk) * kD, rows, p.k_stride) ||
         !make_map(&maps.v, p.v, int64_t(p.Hv) * kD, rows, p.v_stride))
         return cudaErrorInvalidValue;
-    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(chunk_tc_kernel), int(kSmemBytes));
+    const bool split = p.prep_ws != nullptr && p.prep_slots > 0;
+    const void* state_kernel = split ? reinterpret_cast<const void*>(chunk_tc_kernel<true>)
+                                     : reinterpret_cast<const void*>(chunk_tc_kernel<false>);
+    cudaError_t e = ensure_smem(state_kernel, int(kSmemBytes));
     if (e != cudaSuccess) return e;
-    if (p.prep_ws != nullptr && p.prep_slots > 0) {   // every chunk's S-independent part, in parallel
-        if (p.prep_slots > INT32_MAX || p.Hv > 65535) return cudaErrorInvalidValue;
+    auto launch_state = [&](const ChunkParams& q, unsigned z) {
+        if (split) chunk_tc_kernel<true><<<dim3(q.Hv, q.B, z), kThreads, kSmemBytes, s>>>(q, maps);
+        else chunk_tc_kernel<false><<<dim3(q.Hv, q.B, z), kThreads, kSmemBytes, s>>>(q, maps);
+    };
+    if (split) {                                      // every chunk's S-independent part, in parallel
+        if (p.prep_slots > INT32_MAX) return cudaErrorInvalidValue;
         if ((e = ensure_smem(reinterpret_cast<const void*>(chunk_prep_kernel), int(kPrepSmemBytes))) != cudaSuccess)
             return e;
+        int dev = 0, sms = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        const int64_t items = p.prep_slots * int64_t(p.Hv);
+        const int64_t grid = items < 2 * int64_t(sms) ? items : 2 * int64_t(sms);   // two CTAs per SM
         timer_begin(s, "chunk_prep_kernel");
-        chunk_prep_kernel<<<dim3(unsigned(p.prep_slots), unsigned(p.Hv), 1), kPrepThreads, kPrepSmemBytes, s>>>(p, maps);
+        chunk_prep_kernel<<<unsigned(grid), kPrepThreads, kPrepSmemBytes, s>>>(p, maps);
         timer_end(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
@@ -1636,14 +1692,14 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
         ChunkParams q = p;
         q.seg_phase = 0;
         timer_begin(s, "chunk_tc_kernel");
-        chunk_tc_kernel<<<dim3(p.Hv, p.B, 1), kThreads, kSmemBytes, s>>>(q, maps);
+        launch_state(q, 1);
         timer_end(s);
         return cudaGetLastError();
     }
     ChunkParams q = p;
     q.seg_phase = 1;                                  // segment 0 in full; B_s and M_s
     timer_begin(s, "chunk_tc_kernel");
-    chunk_tc_kernel<<<dim3(p.Hv, p.B, 2 * p.seg_max - 1), kThreads, kSmemBytes, s>>>(q, maps);
+    launch_state(q, unsigned(2 * p.seg_max - 1));
     timer_end(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (p.seg_max >= 3) {                             // S_{s+1} = M_s S_s + B_s
@@ -1657,7 +1713,7 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
     }
     q.seg_phase = 2;                                  // segments >= 1 in full
     timer_begin(s, "chunk_tc_kernel");
-    chunk_tc_kernel<<<dim3(p.Hv, p.B, p.seg_max - 1), kThreads, kSmemBytes, s>>>(q, maps);
+    launch_state(q, unsigned(p.seg_max - 1));
     timer_end(s);
     return cudaGetLastError();
 }
