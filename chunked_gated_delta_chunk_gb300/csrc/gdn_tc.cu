@@ -57,7 +57,11 @@ constexpr int kThreads = 384;
 constexpr uint32_t kPrepThreads = 256; // warps 0-3 and 8-11
 constexpr uint32_t kChainThreads = 128;
 constexpr uint32_t kBarPrep = 1, kBarChain = 2;
-constexpr uint32_t kWaitLimit = 1u << 20;
+// mbarrier waits: attempts of at most kSuspendNs each (a short hint: a
+// waiter suspended for longer can oversleep the phase change), bounded in
+// total to about two seconds.
+constexpr uint32_t kSuspendNs = 32;
+constexpr uint32_t kWaitLimit = 1u << 26;
 constexpr int kLdA = kC + 4;         // fp32 row stride of A and T: 16-byte aligned rows
 constexpr float kLog2e = 1.4426950408889634f;
 enum : int { kModeFull = 0, kModeOffset = 1, kModeTransition = 2 };
@@ -536,7 +540,7 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             fence_proxy_async_smem();
         }
         bool lf = false;
-        if (cur.tma && pt == 0) lf = !mbar_wait(&bars[0], raw_phase & 1, kWaitLimit);
+        if (cur.tma && pt == 0) lf = !mbar_wait(&bars[0], raw_phase & 1, kWaitLimit, kSuspendNs);
         if (__syncthreads_or(lf)) { fail = true; break; }
         if (cur.tma) {
             ++raw_phase;
@@ -597,7 +601,7 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             if (pt == rows - 1) reinterpret_cast<float*>(rec + kRecVec)[kC] = eg;
         }
         // ---- masks and decays on the Gram matrices: A to shared, P to the record
-        if (pt == 0) lf = !mbar_wait(&bars[1], mma_phase & 1, kWaitLimit);
+        if (pt == 0) lf = !mbar_wait(&bars[1], mma_phase & 1, kWaitLimit, kSuspendNs);
         if (__syncthreads_or(lf)) { fail = true; break; }
         tc_fence_after();
         {
@@ -684,7 +688,7 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             for (int q = 0; q < 8; ++q) v[q] *= f;
             store_chunk8(rec + kRecQ + toff(r, cc, 8192), v);
         }
-        if (pt == 0) lf = !mbar_wait(&bars[2], mma_phase & 1, kWaitLimit);
+        if (pt == 0) lf = !mbar_wait(&bars[2], mma_phase & 1, kWaitLimit, kSuspendNs);
         if (__syncthreads_or(lf)) { fail = true; break; }
         ++mma_phase;
         tc_fence_after();
@@ -723,7 +727,7 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     __syncthreads();
     if (fail && pt == 0) {
         atomicAdd(&g_tc_timeouts, 1);
-        if (raw_pending) mbar_wait(&bars[0], raw_phase & 1, kWaitLimit);
+        if (raw_pending) mbar_wait(&bars[0], raw_phase & 1, kWaitLimit, kSuspendNs);
     }
     __syncthreads();
     if (pw == 0) tmem_dealloc(tmem, kPrepTmemCols);
@@ -859,7 +863,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     };
     // A failed (timed-out) wait marks this thread; each group votes at its
     // barriers (named_sync_or) and leaves its loop together.
-    auto wait = [&](int slot, uint32_t parity) { return mbar_wait(&bars[slot], parity, kWaitLimit); };
+    auto wait = [&](int slot, uint32_t parity) { return mbar_wait(&bars[slot], parity, kWaitLimit, kSuspendNs); };
 
     if (tid == 0 && !split) {
         if (nchunks > 0 && tma_ok(0)) issue_tma(0);
@@ -1501,7 +1505,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         // let TMA copies still in flight land before shared memory goes away
         for (int st = 0; st < 2; ++st) {
             const int c = s_tma_last[st];
-            if (c >= 0) mbar_wait(&bars[B_RAW0 + st], uint32_t((c >> 1) & 1), kWaitLimit);
+            if (c >= 0) mbar_wait(&bars[B_RAW0 + st], uint32_t((c >> 1) & 1), kWaitLimit, kSuspendNs);
         }
     }
     __syncwarp();
