@@ -83,6 +83,7 @@ constexpr uint32_t kOffBar = kOffVec + ((kVecFloats * 4 + 127) / 128) * 128;
 constexpr uint32_t kNumBars = 18;
 constexpr uint32_t kSmemBytes = kOffBar + kNumBars * 8 + 32 + 1024;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-block limit");
+static_assert(kOffA % 1024 == 0 && kOffA + 2 * 16384 <= kOffVec, "two output staging tiles where A, T, scratch live");
 
 // Barrier slots.
 enum : int {
@@ -357,6 +358,7 @@ __device__ void block_inverse_64(const float* sA, float* sT, float* sTmp, int pt
 
 struct Maps {
     CUtensorMap q, k, v;
+    CUtensorMap o;            // the output (set with chunk records: tile stores)
 };
 
 // ---- split preparation ------------------------------------------------------
@@ -893,7 +895,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
-                umma_f16_tmemA(tO, tZb + s * 8, dQ + (off >> 4), id_o, s > 0);
+                umma_f16_tmemA((c & 1) ? tGW : tO, tZb + s * 8, dQ + (off >> 4), id_o, s > 0);
             }
             umma_commit(&bars[B_OQ]);
             return true;
@@ -908,7 +910,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             for (int pr = 0; pr < 3; ++pr)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    umma_f16_tmemA(tO, tU + (pr == 2 ? 32 : 0) + s * 8,
+                    umma_f16_tmemA((c & 1) ? tGW : tO, tU + (pr == 2 ? 32 : 0) + s * 8,
                                    dP + uint64_t(((pr == 1 ? 8192 : 0) + s * 32) >> 4), id_o, 1);
             umma_commit(&bars[B_O]);
             return true;
@@ -939,15 +941,13 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             bool lf = false;
             if (tid == 0) {
                 if (c >= 2) lf = !wait(B_SFREE0 + b, uint32_t(((c - 2) >> 1) & 1));
-                if (c >= 2 && write_out && !lf) lf = !wait(B_PFREE0 + b, uint32_t(((c - 2) >> 1) & 1));
                 if (c >= 2 && !lf) lf = !wait(b ? B_WTFREE1 : B_WTFREE, uint32_t(((c - 2) >> 1) & 1));
                 if (!lf) {
                     uint64_t* bar = &bars[B_RAW0 + b];
                     s_tma_last[b] = c;
                     mbar_arrive_expect_tx(bar, 16384u + (write_out ? 32768u : 0u) + (tk ? 16384u : 0u));
                     bulk_load(sm + (b ? kOffTb : kOffWt), rec + kRecWt, 16384, bar);
-                    if (write_out) {
-                        bulk_load(sm + kOffP + uint32_t(b * 2) * 8192u, rec + kRecP, 16384, bar);
+                    if (write_out) {                 // P follows once its buffer is free (below)
                         bulk_load(kq + 8192, rec + kRecQ, 8192, bar);
                         bulk_load(kq + 24576, rec + kRecQ + 8192, 8192, bar);
                     }
@@ -974,6 +974,11 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             if (pt < kC) cE[b * kC + pt] = reinterpret_cast<const float*>(rec + kRecVec)[pt];
             if (pt == kC) cGS[b] = reinterpret_cast<const float*>(rec + kRecVec)[kC];
             if (write_out && c >= 1 && tid == 0) lf = !issue_oq(c - 1);
+            if (write_out && tid == 0 && !lf) {
+                // the chain frees P of chunk c - 2 once that chunk's outputs are complete
+                if (c >= 2) lf = !wait(B_PFREE0 + b, uint32_t(((c - 2) >> 1) & 1));
+                if (!lf) bulk_load(sm + kOffP + uint32_t(b * 2) * 8192u, rec + kRecP, 16384, &bars[B_RAW0 + b]);
+            }
             if (mode != kModeTransition) {
                 if (tid == 0 && c >= 1 && !lf) lf = !wait(B_XREAD, uint32_t((c - 1) & 1));
                 __syncwarp();
@@ -1263,6 +1268,58 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         uint32_t opk[32];
         int64_t o_cs = 0;
         int o_rows = 0;
+        // With records a chunk's output tile is staged in shared memory
+        // ([64 rows][128 columns] bf16, 128-byte swizzle, two buffers where the
+        // inline preparation keeps A, T and its scratch): read out of TMEM as
+        // MMA-ordered fragments and stored transposed (stmatrix), then written
+        // by one TMA store, or as 16-byte rows where the chunk ends inside the
+        // buffers (its other rows belong to the next sequence).
+        uint8_t* const o_stage = sm + kOffA;
+        // O^T of chunk cc (TMEM buffer cc & 1) into staging buffer cc & 1:
+        // this warp's lanes (j) and column half (t) as 16x256b fragments.
+        auto stage_out = [&](int cc) {
+            uint8_t* st = o_stage + uint32_t(cc & 1) * 16384u;
+            const uint32_t tOc = (cc & 1) ? tGW : tO;
+            uint32_t r[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                tmem_ld_16x256b_x2(tOc + (uint32_t(quarter * 32 + 16 * (u >> 1)) << 16) + uint32_t(hc * 32 + 16 * (u & 1)),
+                                   r[u]);
+            tmem_ld_wait();
+            const int m = lane >> 3, rr = lane & 7;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                uint32_t f[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    f[e] = pack_bf16x2(__uint_as_float(r[u][2 * e]) * p.q_scale,
+                                       __uint_as_float(r[u][2 * e + 1]) * p.q_scale);
+                const int t = hc * 32 + 16 * (u & 1) + 8 * (m >> 1) + rr;
+                const int j = quarter * 32 + 16 * (u >> 1) + 8 * (m & 1);
+                stmatrix_x4_trans(smem_u32(st + toff(t, j, 8192)), f);
+            }
+            fence_proxy_async_smem();
+        };
+        // After a barrier: the staged tile of chunk cc to the output, by one
+        // TMA store when every row of the box is this sequence's or lies past
+        // the buffers, else as 16-byte rows.
+        auto write_out_tile = [&](int cc) {
+            const uint8_t* st = o_stage + uint32_t(cc & 1) * 16384u;
+            if (o_rows == kC || o_cs + o_rows >= p.t_cap) {
+                if (lead) {
+                    tma_store_2d(&maps.o, st, h * kD, int(o_cs));
+                    tma_store_2d(&maps.o, st + 8192, h * kD + 64, int(o_cs));
+                }
+            } else {
+                for (int idx = ct; idx < kC * 16; idx += int(kChainN)) {
+                    const int r = idx >> 4, col = (idx & 15) * 8;
+                    if (r < o_rows)
+                        *reinterpret_cast<uint4*>(gout + ((o_cs + r) * Hv + h) * kD + col) =
+                            *reinterpret_cast<const uint4*>(st + toff(r, col, 8192));
+                }
+            }
+            if (lead) bulk_commit_group();
+        };
         if (nchunks == 0) {
             if (final_dst)
                 for (int d = hc * 64; d < (hc + kHalves) * 64; ++d)
@@ -1351,8 +1408,22 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 }
             }
             __syncwarp();
-            // previous chunk's output rows, while the MMAs run
-            if (c > 0) {
+            // previous chunk's output rows, while the MMAs run (with records:
+            // its O^T, once complete, is staged here and written after the
+            // next barrier; its P buffer is free then)
+            bool o_staged = false;
+            if (kSplit && c > 0 && write_out) {
+                if (lead && !lf) {
+                    lf = !wait(B_O, uint32_t((c - 1) & 1));
+                    if (!lf) mbar_arrive(&bars[B_PFREE0 + ((c - 1) & 1)]);
+                    bulk_wait_group_read<1>();           // staging buffer (c - 1) & 1 read by its last store
+                }
+                __syncwarp();
+                if (named_sync_or(kBarChain, kChainN, lf)) { fail = true; break; }
+                tc_fence_after();
+                stage_out(c - 1);
+                o_staged = true;
+            } else if (!kSplit && c > 0) {
                 __nv_bfloat16* dst = gout + (o_cs * Hv + h) * kD + row;
 #pragma unroll
                 for (int k = 0; k < kHalves * 16; ++k) {
@@ -1368,6 +1439,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             tc_fence_after();
             if (lead) mbar_arrive(&bars[split && b ? B_WTFREE1 : B_WTFREE]);
             __syncwarp();
+            if (o_staged) write_out_tile(c - 1);
             // ---- U (hi, lo) and Us = U diag(e) (hi, lo) into TMEM --------------
             for (int hf = hc; hf < hc + kHalves; ++hf) {
                 float x[32];
@@ -1462,7 +1534,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             }
             tmem_st_wait();
             // ---- output rows to registers (stored during the next chunk) --------
-            if (write_out) {
+            if (write_out && !kSplit) {
                 if (lead) lf = !wait(B_O, uint32_t(c & 1));
                 __syncwarp();
                 if (named_sync_or(kBarChain, kChainN, lf)) { fail = true; break; }
@@ -1481,10 +1553,25 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             o_rows = write_out ? rows : 0;
             tc_fence_before();
             named_sync(kBarChain, kChainN);
-            if (lead) mbar_arrive(&bars[B_PFREE0 + b]);
+            if (lead && !kSplit) mbar_arrive(&bars[B_PFREE0 + b]);   // with records: at the next chunk
             __syncwarp();
         }
-        if (!fail && nchunks > 0) {
+        if (kSplit) {
+            if (!fail && write_out && nchunks > 0) {     // the last chunk's outputs
+                bool lf = lead && !wait(B_O, uint32_t((nchunks - 1) & 1));
+                if (lead) bulk_wait_group_read<1>();
+                __syncwarp();
+                if (!named_sync_or(kBarChain, kChainN, lf)) {
+                    tc_fence_after();
+                    stage_out(nchunks - 1);
+                    named_sync(kBarChain, kChainN);
+                    write_out_tile(nchunks - 1);
+                } else {
+                    fail = true;
+                }
+            }
+            if (lead) bulk_wait_all();                   // tile stores done before the CTA exits
+        } else if (!fail && nchunks > 0) {
             __nv_bfloat16* dst = gout + (o_cs * Hv + h) * kD + row;
 #pragma unroll
             for (int k = 0; k < kHalves * 16; ++k) {
@@ -1668,6 +1755,8 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
     if (!make_map(&maps.q, p.q, int64_t(p.Hk) * kD, rows, p.q_stride) ||
         !make_map(&maps.k, p.k, int64_t(p.Hk) * kD, rows, p.k_stride) ||
         !make_map(&maps.v, p.v, int64_t(p.Hv) * kD, rows, p.v_stride))
+        return cudaErrorInvalidValue;
+    if (p.prep_ws != nullptr && !make_map(&maps.o, p.out, int64_t(p.Hv) * kD, rows, int64_t(p.Hv) * kD))
         return cudaErrorInvalidValue;
     const bool split = p.prep_ws != nullptr && p.prep_slots > 0;
     const void* state_kernel = split ? reinterpret_cast<const void*>(chunk_tc_kernel<true>)

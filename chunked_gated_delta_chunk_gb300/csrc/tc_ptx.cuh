@@ -104,6 +104,24 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// Tiled TMA store of a box from shared memory (bulk-group completion); the
+// writing threads must have made their shared-memory stores visible to the
+// async proxy (fence_proxy_async_smem) before a barrier that precedes this.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until all of this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -245,6 +263,26 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(v[i]);
     GDN_TMEM_ST_X16(taddr, r);
+}
+
+// 16 TMEM lanes x 16 32-bit columns per warp (shape 16x256b, two repeats):
+// thread i (g = i / 4, q = i % 4) gets lanes g and g + 8 at columns 2q, 2q + 1
+// (r[0..3]: lane g, lane g + 8) and 8 + 2q, 8 + 2q + 1 (r[4..7]), the order of
+// an m16n8 MMA fragment.
+__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, uint32_t* r) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr));
+}
+
+// Four 8x8 b16 matrices in fragment order (thread g * 4 + q holds row g,
+// columns 2q, 2q + 1 of matrix m in f[m]) stored transposed: stored row r of
+// matrix m (fragment column r, 16 bytes) goes to the address of lane 8m + r.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, const uint32_t* f) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(f[0]),
+                 "r"(f[1]), "r"(f[2]), "r"(f[3])
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {
