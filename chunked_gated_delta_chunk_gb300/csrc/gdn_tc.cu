@@ -387,17 +387,22 @@ static_assert(kRecVec + 512 == kPrepRecordBytes, "record layout");
 
 // Shared-memory map of the preparation kernel (bytes from the 1024-aligned
 // base).  A lives under Tb: the inverse has read A for the last time before
-// Tb is written.
+// Tb is written.  The P images are staged after A (and stored from there
+// before Tb is written), the -W^T image in T's place and the U0^T fragments
+// in Tb's once the MMAs are done; one thread stores staged images with bulk
+// copies, so the record writes are whole lines.
 constexpr uint32_t kPOffKQ = 0;                          // K b0 | Q b0 | K b1 | Q b1
 constexpr uint32_t kPOffV = kStageKQ;                    // V b0 | V b1
 constexpr uint32_t kPOffTb = kPOffV + 16384;             // Tb hi, lo, Tbg hi, lo (A first)
-constexpr uint32_t kPOffT = kPOffTb + 4 * 8192;
+constexpr uint32_t kPOffPst = kPOffTb + kC * kLdA * 4;   // P hi | lo staging, after A
+constexpr uint32_t kPOffT = kPOffPst + 16384;
 constexpr uint32_t kPOffTmp = kPOffT + kC * kLdA * 4;
 constexpr uint32_t kPOffVec = kPOffTmp + 1536 * 4;
 constexpr uint32_t kPOffBar = kPOffVec + 8 * kC * 4;
 constexpr uint32_t kPrepSmemBytes = kPOffBar + 3 * 8 + 8 + 1024;
 constexpr uint32_t kPrepTmemCols = 128;                  // Gram, then W^T (64); U0^T (64)
-static_assert(kC * kLdA * 4 <= 4 * 8192, "A fits under Tb");
+static_assert(kC * kLdA * 4 <= 4 * 8192 && kPOffT >= kPOffTb + 4 * 8192, "A and the P staging beside Tb");
+static_assert(kC * kLdA * 4 >= 16384, "-W^T staging fits in T's place");
 static_assert(2 * (kPrepSmemBytes + 1024) <= 233472, "two preparation CTAs per SM");
 
 // Persistent: each CTA takes items (value head, chunk slot) with a grid
@@ -603,9 +608,15 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             if (pt == rows - 1) reinterpret_cast<float*>(rec + kRecVec)[kC] = eg;
         }
         // ---- masks and decays on the Gram matrices: A to shared, P to the record
-        if (pt == 0) lf = !mbar_wait(&bars[1], mma_phase & 1, kWaitLimit, kSuspendNs);
+        if (pt == 0) {
+            lf = !mbar_wait(&bars[1], mma_phase & 1, kWaitLimit, kSuspendNs);
+            bulk_wait_group_read<0>();                    // the last item's staged images are read
+        }
         if (__syncthreads_or(lf)) { fail = true; break; }
         tc_fence_after();
+        if (mma_phase > 0)                                // T's place held the last -W^T image: T = 0 again
+            for (int idx = pt; idx < kC * kLdA / 4; idx += kPrepThreads)
+                reinterpret_cast<float4*>(sT)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
         {
             float v[32];
             tmem_ld32(tGW + lane_addr + phalf * 32, v);
@@ -633,13 +644,20 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 #pragma unroll
                 for (int q = 0; q < 32; q += 8) {
                     const uint32_t o = toff(t, phalf * 32 + q, 8192);
-                    store_split8(rec + kRecP + o, rec + kRecP + 8192 + o, v + q);
+                    store_split8(sm + kPOffPst + o, sm + kPOffPst + 8192 + o, v + q);
                 }
             }
         }
+        fence_proxy_async_smem();
         __syncthreads();
+        if (pt == 0) {
+            bulk_store(rec + kRecP, sm + kPOffPst, 16384);
+            bulk_commit_group();
+        }
         // ---- blocked inverse; T diag(beta), T diag(beta Gamma r_k) as hi + lo --
         block_inverse_64(sA, sT, sTmp, pt);
+        if (pt == 0) bulk_wait_group_read<0>();             // the P staging, which Tb overlaps
+        __syncthreads();
         for (int idx = pt; idx < kC * 8; idx += kPrepThreads) {
             const int t = idx >> 3, i0 = (idx & 7) * 8;
             float a[8], bg[8], fb[8], fbg[8], tr[8];
@@ -712,14 +730,20 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 #pragma unroll
             for (int q = 0; q < 32; ++q) v[q] = -v[q];
 #pragma unroll
-            for (int q = 0; q < 32; q += 8) store_chunk8(rec + kRecWt + toff(row, phalf * 32 + q, 16384), v + q);
+            for (int q = 0; q < 32; q += 8) store_chunk8(sm + kPOffT + toff(row, phalf * 32 + q, 16384), v + q);
             tmem_ld32(tX + lane_addr + phalf * 32, v);
-            float4* u = reinterpret_cast<float4*>(rec + kRecU) + pw * 8 * 32 + lane;
+            float4* u = reinterpret_cast<float4*>(sm + kPOffTb) + pw * 8 * 32 + lane;
 #pragma unroll
             for (int i = 0; i < 8; ++i) u[i * 32] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();                                   // TMEM read, vectors free for the next item
+        if (pt == 0) {
+            bulk_store(rec + kRecWt, sm + kPOffT, 16384);
+            bulk_store(rec + kRecU, sm + kPOffTb, 32768);
+            bulk_commit_group();
+        }
         item = next;
         cur = nxt;
     }
@@ -731,6 +755,7 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         atomicAdd(&g_tc_timeouts, 1);
         if (raw_pending) mbar_wait(&bars[0], raw_phase & 1, kWaitLimit, kSuspendNs);
     }
+    if (pt == 0) bulk_wait_all();                          // record stores done before the CTA exits
     __syncthreads();
     if (pw == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
