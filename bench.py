@@ -78,10 +78,11 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(sources):
+    """Hash of the kernel's source files (names under the package's csrc/)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunked_gated_delta_chunk_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(sources):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -90,15 +91,20 @@ def kernel_source_hash():
 
 def recorded_traffic(kernel_name):
     """DRAM bytes (read + write) of the kernel's launches in one step, from
-    the committed ncu summary, if it was taken on the current kernel sources;
-    else None."""
+    the committed ncu summary, if it was taken on the kernel's current source
+    files (the entry lists them); else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     entry = d.get(kernel_name)
-    if not entry or entry.get("source_hash") != kernel_source_hash():
+    if not entry or not entry.get("sources"):
+        return None
+    try:
+        if entry.get("source_hash") != kernel_source_hash(entry["sources"]):
+            return None
+    except OSError:
         return None
     return entry.get("dram_bytes_per_step")
 
