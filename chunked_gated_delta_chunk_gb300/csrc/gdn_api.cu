@@ -6,6 +6,7 @@
 #include <cstring>
 
 #include "gdn_common.cuh"
+#include "rows_common.cuh"
 #include "gdn_tc.cuh"
 
 namespace {
@@ -388,7 +389,7 @@ int gdn_scan_rows(const float* a, const float* b, const float* h_in, float* h_ou
     if (T_total > 0 && (a == nullptr || b == nullptr || h_rows == nullptr)) return GDN_ERR_INVALID_ARG;
     if (C % 4 != 0) return GDN_ERR_UNSUPPORTED;
     if (!aligned16(a) || !aligned16(b) || !aligned16(h_rows)) return GDN_ERR_ALIGN;
-    const int64_t tiles = ((T_total + 255) / 256) * ((int64_t(C) + 31) / 32);
+    const int64_t tiles = ((T_total + gdn::rows::kScanRows - 1) / gdn::rows::kScanRows) * ((int64_t(C) + gdn::rows::kCols - 1) / gdn::rows::kCols);
     if (tiles > INT32_MAX) return GDN_ERR_TOO_LARGE;
     if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
         workspace_bytes < gdn::scan_workspace_bytes(C, T_total))
@@ -423,7 +424,7 @@ int gdn_wkv_rows(const float* k, const float* v, const float* w, const float* u,
     if (T_total > 0 && (k == nullptr || v == nullptr || wkv == nullptr)) return GDN_ERR_INVALID_ARG;
     if (C % 4 != 0) return GDN_ERR_UNSUPPORTED;
     if (!aligned16(k) || !aligned16(v) || !aligned16(wkv)) return GDN_ERR_ALIGN;
-    const int64_t tiles = ((T_total + 255) / 256) * ((int64_t(C) + 31) / 32);
+    const int64_t tiles = ((T_total + gdn::rows::kWkvRows - 1) / gdn::rows::kWkvRows) * ((int64_t(C) + gdn::rows::kCols - 1) / gdn::rows::kCols);
     if (tiles > INT32_MAX) return GDN_ERR_TOO_LARGE;
     if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
         workspace_bytes < gdn::wkv_workspace_bytes(C, T_total))

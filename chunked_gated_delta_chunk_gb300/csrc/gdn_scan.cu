@@ -3,11 +3,12 @@
 // prompts in multi-token chunks", Implementation, add_selective_scan_rows).
 //
 // The page scans the rows of one chunk by doubling rounds; here the whole
-// prompt is one HBM-bound pass.  Tiles of 256 rows x 32 channels are taken in
+// prompt is one HBM-bound pass.  Tiles of 64 rows x 32 channels (16 KB, so
+// that many CTAs per SM keep enough loads in flight) are taken in
 // ticket order (a global counter), so every tile's predecessor in time is
 // already running or done.  A CTA stages its tile in shared memory once
-// (cp.async); each of its four warps reduces its 64 rows to the affine map
-// h -> A h + B (as four interleaved chains of 16 rows, so that independent
+// (cp.async); each of its four warps reduces its 16 rows to the affine map
+// h -> A h + B (as four interleaved chains of 4 rows, so that independent
 // multiply-add chains hide the latency); warp 0 composes the tile's map,
 // publishes it, finds the tile's incoming state by looking back over the
 // predecessors' published maps and end states (decoupled look-back),
@@ -29,6 +30,10 @@ namespace {
 
 using namespace ptx;
 using namespace rows;
+
+constexpr int kRows = rows::kScanRows;            // rows of a tile
+constexpr int kWarpRows = kRows / kWarps;          // rows of a warp
+constexpr int kChainRows = kWarpRows / kChains;    // rows of one of a thread's chains
 
 // Zero the ticket and the tile flags; end state of every empty sequence.
 __global__ void scan_init_kernel(const ScanParams p) {
@@ -58,7 +63,7 @@ __global__ void __launch_bounds__(kThreads) scan_rows_kernel(const ScanParams p)
     const int nrow = int(p.T - t0 < kRows ? p.T - t0 : kRows);
     const int c0 = cb * kCols, c = c0 + lane;
     const bool live = c < p.C;
-    stage_tile(sa, sb, p.a, p.b, t0, nrow, c0, p.C, tid);
+    stage_tile<kRows>(sa, sb, p.a, p.b, t0, nrow, c0, p.C, tid);
     fill_row_info(p.cu, p.B, t0, nrow, tid, s_seq, s_mark);
     cp_async_wait_all();
     __syncthreads();
@@ -191,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) scan_rows_kernel(const ScanParams p)
 
 size_t scan_workspace_bytes(int C, int64_t T) {
     const int64_t n_cb = (C + rows::kCols - 1) / rows::kCols;
-    const int64_t n_chunks = (T + rows::kRows - 1) / rows::kRows;
+    const int64_t n_chunks = (T + rows::kScanRows - 1) / rows::kScanRows;
     const int64_t tiles = n_cb * n_chunks;
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     return up(sizeof(int)) + up(size_t(tiles) * sizeof(int)) + 3 * up(size_t(tiles) * rows::kCols * sizeof(float));
@@ -201,7 +206,7 @@ void scan_bind_workspace(ScanParams& p, void* ws) {
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     char* w = static_cast<char*>(ws);
     p.n_cb = (p.C + rows::kCols - 1) / rows::kCols;
-    const int64_t n_chunks = (p.T + rows::kRows - 1) / rows::kRows;
+    const int64_t n_chunks = (p.T + rows::kScanRows - 1) / rows::kScanRows;
     p.n_tiles = int(n_chunks * p.n_cb);
     p.ticket = reinterpret_cast<int*>(w);
     w += up(sizeof(int));
@@ -223,7 +228,7 @@ cudaError_t launch_scan_rows(const ScanParams& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     if (p.n_tiles == 0) return cudaSuccess;
-    const int smem = 2 * rows::kRows * rows::kCols * int(sizeof(float));
+    const int smem = 2 * rows::kScanRows * rows::kCols * int(sizeof(float));
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(scan_rows_kernel), smem);
     if (e != cudaSuccess) return e;
     timer_begin(s, "scan_rows_kernel");

@@ -14,8 +14,8 @@
 // with r the tile's row count, decay adding r w to max, (+) the max-shifted sum
 // of two states and L the tile's state from an empty start; such maps compose
 // in the same form, which is what the look-back combines.  As in the scan, a
-// tile is 256 rows x 32 channels, each warp reduces its 64 rows as four
-// interleaved chains, and a sequence start is settled in the first pass: its
+// tile has 32 channels (here 128 rows, 32 KB), each warp reduces its 32 rows
+// as four interleaved chains, and a sequence start is settled in the first pass: its
 // row's output is written there and the state after it replaces the row in
 // the staged tile, so no state is read after the first pass.
 #include "gdn_common.cuh"
@@ -127,6 +127,10 @@ __global__ void wkv_init_kernel(const WkvParams p) {
 
 __global__ void __launch_bounds__(rows::kThreads) wkv_rows_kernel(const WkvParams p) {
     using namespace rows;
+
+constexpr int kRows = rows::kWkvRows;            // rows of a tile
+constexpr int kWarpRows = kRows / kWarps;          // rows of a warp
+constexpr int kChainRows = kWarpRows / kChains;    // rows of one of a thread's chains
     extern __shared__ __align__(16) float sm_wkv[];
     float* sk = sm_wkv;                               // [kRows][kCols]
     float* sv = sm_wkv + kRows * kCols;
@@ -144,7 +148,7 @@ __global__ void __launch_bounds__(rows::kThreads) wkv_rows_kernel(const WkvParam
     const int c0 = cb * kCols, c = c0 + lane;
     const bool live = c < p.C;
     const size_t tiles = size_t(p.n_tiles);
-    stage_tile(sk, sv, p.k, p.v, t0, nrow, c0, p.C, tid);
+    stage_tile<kRows>(sk, sv, p.k, p.v, t0, nrow, c0, p.C, tid);
     const float w = live ? p.w[c] : 0.f, u = live ? p.u[c] : 0.f;
     fill_row_info(p.cu, p.B, t0, nrow, tid, s_seq, s_mark);
     cp_async_wait_all();
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(rows::kThreads) wkv_rows_kernel(const WkvParam
 }  // namespace
 
 size_t wkv_workspace_bytes(int C, int64_t T) {
-    const int64_t tiles = ((T + rows::kRows - 1) / rows::kRows) * ((C + kCw - 1) / kCw);
+    const int64_t tiles = ((T + rows::kWkvRows - 1) / rows::kWkvRows) * ((C + kCw - 1) / kCw);
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     return up(sizeof(int)) + up(size_t(tiles) * sizeof(int)) + 2 * up(size_t(tiles) * kCw * 3 * sizeof(float));
 }
@@ -292,7 +296,7 @@ void wkv_bind_workspace(WkvParams& p, void* ws) {
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     char* w = static_cast<char*>(ws);
     p.n_cb = (p.C + kCw - 1) / kCw;
-    p.n_tiles = int(((p.T + rows::kRows - 1) / rows::kRows) * p.n_cb);
+    p.n_tiles = int(((p.T + rows::kWkvRows - 1) / rows::kWkvRows) * p.n_cb);
     p.ticket = reinterpret_cast<int*>(w);
     w += up(sizeof(int));
     p.flags = reinterpret_cast<int*>(w);
@@ -312,7 +316,7 @@ cudaError_t launch_wkv_rows(const WkvParams& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     if (p.n_tiles == 0) return cudaSuccess;
-    const int smem = 2 * rows::kRows * kCw * int(sizeof(float));
+    const int smem = 2 * rows::kWkvRows * kCw * int(sizeof(float));
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(wkv_rows_kernel), smem);
     if (e != cudaSuccess) return e;
     timer_begin(s, "wkv_rows_kernel");

@@ -10,11 +10,11 @@
 namespace gdn {
 namespace rows {
 
-constexpr int kRows = 256;             // rows of a tile
+constexpr int kScanRows = 64;          // rows of a selective-scan tile (a, b: 16 KB, many CTAs per SM)
+constexpr int kWkvRows = 128;          // rows of a WKV tile (k, v: 32 KB; the WKV rows carry more arithmetic)
 constexpr int kCols = 32;              // channels of a tile (one lane each)
 constexpr int kWarps = 4;              // warp w owns rows 64 w .. 64 w + 63
 constexpr int kThreads = 32 * kWarps;
-constexpr int kWarpRows = kRows / kWarps;
 constexpr uint32_t kSpinLimit = 1u << 22;
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -40,7 +40,6 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int B, int64_t t) {
 }
 
 constexpr int kChains = 4;             // independent row chains per thread
-constexpr int kChainRows = kWarpRows / kChains;
 enum : int { kRowStart = 1, kRowEnd = 2 };
 
 // Sequence and start / end marks of the tile's rows (all threads of the CTA
@@ -58,9 +57,10 @@ __device__ __forceinline__ void fill_row_info(const int32_t* cu, int B, int64_t 
 // Stage rows [t0, t0 + nrow) x channels [c0, c0 + kCols) of two [T, C] fp32
 // arrays into [kRows][kCols] shared tiles by 16-byte cp.async (C a multiple
 // of 4); rows and channels outside are zero.
+template <int R>
 __device__ __forceinline__ void stage_tile(float* sx, float* sy, const float* x, const float* y,
                                            int64_t t0, int nrow, int c0, int C, int tid) {
-    for (int i = tid; i < kRows * (kCols / 4); i += kThreads) {
+    for (int i = tid; i < R * (kCols / 4); i += kThreads) {
         const int r = i / (kCols / 4), q = (i % (kCols / 4)) * 4;
         float* dx = sx + r * kCols + q;
         float* dy = sy + r * kCols + q;

@@ -219,7 +219,8 @@ def test_scan_rows_argument_checks(lib):
 def test_wkv_rows_argument_checks(lib):
     """RWKV-4 WKV rows: invalid calls are rejected before any CUDA call."""
     ws = B.gdn_wkv_workspace_bytes(256, 1000)
-    assert ws > B.gdn_scan_workspace_bytes(256, 1000) and ws % 256 == 0
+    assert ws > 0 and ws % 256 == 0
+    assert B.gdn_wkv_workspace_bytes(256, 2000) > ws
     good = dict(k=A, v=A, w=A, u=A, s_in=None, s_out=A, wkv=A, cu=A, B=1, C=256, T=1000,
                 ws=A, wsb=ws)
 
