@@ -127,10 +127,9 @@ __global__ void wkv_init_kernel(const WkvParams p) {
 
 __global__ void __launch_bounds__(rows::kThreads) wkv_rows_kernel(const WkvParams p) {
     using namespace rows;
-
-constexpr int kRows = rows::kWkvRows;            // rows of a tile
-constexpr int kWarpRows = kRows / kWarps;          // rows of a warp
-constexpr int kChainRows = kWarpRows / kChains;    // rows of one of a thread's chains
+    constexpr int kRows = rows::kWkvRows;             // rows of a tile
+    constexpr int kWarpRows = kRows / kWarps;         // rows of a warp
+    constexpr int kChainRows = kWarpRows / kChains;   // rows of one of a thread's chains
     extern __shared__ __align__(16) float sm_wkv[];
     float* sk = sm_wkv;                               // [kRows][kCols]
     float* sv = sm_wkv + kRows * kCols;
