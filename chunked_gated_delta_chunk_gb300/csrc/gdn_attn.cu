@@ -10,7 +10,8 @@
 //   warp 8      TMA: the query tile once, key tiles (2 stages) and value
 //               tiles (3 stages) of 128 rows from the cache;
 //   warp 9      tcgen05 MMAs: S_j = Q K_j^T into one of two TMEM buffers, then
-//               O += P_{j-1} V_{j-1} with P (bf16) as the A operand from TMEM;
+//               O += P_{j-1} V_{j-1} with P (bf16, two TMEM buffers) as the A
+//               operand from TMEM;
 //   warps 0-7   softmax, two threads per query row (its TMEM lane), one per
 //               half of the keys: causal / capacity mask, running maximum
 //               (raised, with O and l rescaled, only past 2^8 of headroom),
@@ -50,11 +51,13 @@ constexpr uint32_t kAOffQ = 0;
 constexpr uint32_t kAOffK = kATile;
 constexpr uint32_t kAOffV = kAOffK + kAKStages * kATile;
 constexpr uint32_t kAOffBar = kAOffV + kAVStages * kATile;
-constexpr uint32_t kANumBars = 17;
+constexpr uint32_t kANumBars = 19;
 constexpr uint32_t kAOffEx = kAOffBar + 256;               // [2 parities][2 halves][kAQ] floats: maxima
 constexpr uint32_t kAOffL = kAOffEx + 2 * 2 * kAQ * 4;     // [2 halves][kAQ] floats: row sums
 constexpr uint32_t kASmem = kAOffL + 2 * kAQ * 4 + 1024;
 static_assert(kASmem <= 232448, "attention stages above the 227 KB per-block limit");
+// TMEM: S in two buffers (2 x 128 columns), P (bf16 pairs) in two buffers
+// (2 x 64), O (128)
 constexpr uint32_t kAColS = 0, kAColP = 256, kAColO = 384, kATmemCols = 512;
 enum : int {
     AB_Q = 0,
@@ -64,10 +67,10 @@ enum : int {
     AB_VEMPTY = AB_VFULL + kAVStages,
     AB_SFULL = AB_VEMPTY + kAVStages, // + S buffer (2)
     AB_SEMPTY = AB_SFULL + 2,         // + S buffer (2), 8 arrivals
-    AB_PFULL = AB_SEMPTY + 2,         // 8 arrivals
-    AB_ODONE = AB_PFULL + 1
+    AB_PFULL = AB_SEMPTY + 2,         // + P buffer (2), 8 arrivals
+    AB_ODONE = AB_PFULL + 2           // + P buffer (2): O += P V of that buffer done
 };
-static_assert(AB_ODONE + 1 == int(kANumBars), "barrier count");
+static_assert(AB_ODONE + 2 == int(kANumBars), "barrier count");
 
 struct AttnMaps {
     CUtensorMap q, kc, vc;
@@ -139,7 +142,7 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
 
     if (tid == 0) {
         for (int i = 0; i < int(kANumBars); ++i)
-            mbar_init(&bars[i], (i == AB_SEMPTY || i == AB_SEMPTY + 1 || i == AB_PFULL) ? 8 : 1);
+            mbar_init(&bars[i], (i == AB_SEMPTY || i == AB_SEMPTY + 1 || i == AB_PFULL || i == AB_PFULL + 1) ? 8 : 1);
         fence_mbar_init();
         s_fail = 0;
     }
@@ -205,14 +208,15 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
             const uint64_t dq = smem_desc(smem_u32(sm + kAOffQ), 16, 1024, kSwizzle128B);
             auto issue_pv = [&](int j) {                          // O += P_j V_j
                 if (!wait(AB_VFULL + j % kAVStages, uint32_t((j / kAVStages) & 1))) return false;
-                if (!wait(AB_PFULL, uint32_t(j & 1))) return false;
+                if (!wait(AB_PFULL + (j & 1), uint32_t((j >> 1) & 1))) return false;
                 tc_fence_after();
                 const uint64_t dv = smem_desc(smem_u32(sm + kAOffV + (j % kAVStages) * kATile), kATile / 2, 1024,
                                               kSwizzle128B);
 #pragma unroll
                 for (int s = 0; s < kAK / 16; ++s)
-                    umma_f16_tmemA(tO, tP + s * 8, dv + uint64_t(s * 2048 >> 4), id_o, j > 0 || s > 0);
-                umma_commit(&bars[AB_ODONE]);
+                    umma_f16_tmemA(tO, tP + uint32_t(j & 1) * (kAK / 2) + s * 8, dv + uint64_t(s * 2048 >> 4), id_o,
+                                   j > 0 || s > 0);
+                umma_commit(&bars[AB_ODONE + (j & 1)]);
                 umma_commit(&bars[AB_VEMPTY + j % kAVStages]);
                 return true;
             };
@@ -313,12 +317,15 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
                 lq[(c >> 1) & 3] += e0 + e1;
             }
             l = fmaf(l, f, (lq[0] + lq[1]) + (lq[2] + lq[3]));
-            // ---- P_j replaces P_{j-1} once O += P_{j-1} V_{j-1} is done ----------
-            if (lane == 0 && j >= 1) fail = fail || !wait(AB_ODONE, uint32_t((j - 1) & 1));
+            // ---- P_j goes to buffer j & 1 once O += P_{j-2} V_{j-2} is done; O is
+            // rescaled (rarely) once every product so far is in ---------------
+            const bool resc = __any_sync(0xffffffffu, f != 1.f);
+            if (lane == 0 && j >= 2) fail = fail || !wait(AB_ODONE + b, uint32_t(((j - 2) >> 1) & 1));
+            if (lane == 0 && resc && j >= 1) fail = fail || !wait(AB_ODONE + ((j - 1) & 1), uint32_t(((j - 1) >> 1) & 1));
             __syncwarp();
             fail = __shfl_sync(0xffffffffu, fail, 0);
             tc_fence_after();
-            if (!fail && __any_sync(0xffffffffu, f != 1.f)) {     // rescale this warp's half rows of O
+            if (!fail && resc) {                                  // rescale this warp's half rows of O
 #pragma unroll
                 for (int q = 0; q < kAD / 2; q += 16) {
                     float o[16];
@@ -333,16 +340,17 @@ attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
 #pragma unroll
                 for (int q = 0; q < kAK / 4; q += 16) {
                     __syncwarp();
-                    GDN_TMEM_ST_X16(tP + lane_addr + half * (kAK / 4) + q, (pk + q));
+                    GDN_TMEM_ST_X16(tP + uint32_t(b) * (kAK / 2) + lane_addr + half * (kAK / 4) + q, (pk + q));
                 }
                 tmem_st_wait();
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[AB_PFULL]);
+            if (lane == 0) mbar_arrive(&bars[AB_PFULL + b]);
         }
         // ---- O / l to the output rows -------------------------------------------
-        if (lane == 0 && !fail && ntiles > 0) fail = !wait(AB_ODONE, uint32_t((ntiles - 1) & 1));
+        if (lane == 0 && !fail && ntiles > 0)
+            fail = !wait(AB_ODONE + ((ntiles - 1) & 1), uint32_t(((ntiles - 1) >> 1) & 1));
         __syncwarp();
         fail = __shfl_sync(0xffffffffu, fail, 0);
         s_l[half * kAQ + row] = l;
