@@ -818,9 +818,16 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     } else if (p.seg_phase == 2) {
         seg = int(blockIdx.z) + 1;
     }
-    const int seg_len = p.seg_phase ? p.seg_chunks : seq_chunks;
-    const int c_begin = seg * seg_len;
-    const int c_end = p.seg_phase ? min(c_begin + seg_len, seq_chunks) : seq_chunks;
+    // Segments of seg_chunks chunks; when they do not divide the sequence,
+    // segment 0 is the short one: in phase 1 it is the only full pass, which
+    // costs more per chunk than the map passes beside it.
+    int c_begin = 0, c_end = seq_chunks;
+    if (p.seg_phase) {
+        const int L = p.seg_chunks;
+        const int short_by = ((seq_chunks + L - 1) / L) * L - seq_chunks;
+        c_begin = seg == 0 ? 0 : seg * L - short_by;
+        c_end = min((seg + 1) * L - short_by, seq_chunks);
+    }
     if (c_begin >= c_end && !(seg == 0 && mode == kModeFull)) return;   // no such segment
     const int nchunks = c_end > c_begin ? c_end - c_begin : 0;
     constexpr bool split = kSplit;
