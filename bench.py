@@ -24,6 +24,7 @@ independent prompts with no exchange); rank 0 prints.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -325,6 +326,31 @@ class _RowSpec:
             self._s = p.state_in[:, :, :cols].numpy()
 
 
+def timed_steps(calls, steps, stream, barrier, launches_per_call=0, clocks=None):
+    """Time `steps` library calls on the stream with CUDA events, barrier and
+    device synchronisation on both sides.  launches_per_call > 0 turns the
+    library's launch timer on (CUDA events around every one of its launches),
+    which adds a little time per launch: the headline number is taken with it
+    off, the per-kernel device times in a second region with it on.
+    Returns (ms for all steps, launch records, dropped launches)."""
+    if launches_per_call:
+        B.gdn_launch_timer_start(steps * launches_per_call)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ctx = clocks if clocks is not None else contextlib.nullcontext()
+    with ctx:
+        barrier()
+        start.record(stream)
+        for i in range(steps):
+            calls[i % len(calls)].run(stream)
+        stop.record(stream)
+        barrier()
+    records, dropped = [], 0
+    if launches_per_call:
+        B.gdn_launch_timer_stop()
+        records, dropped = B.gdn_launch_timer_read()
+    return start.elapsed_time(stop), records, dropped
+
+
 def run_row(args, rank, world):
     """A row recurrence of the hot-path table's next rows (the selective-scan
     rows, the RWKV-4 WKV rows): one library call over its workload per step."""
@@ -382,18 +408,9 @@ def run_row(args, rank, world):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    B.gdn_launch_timer_start(args.steps * 2)
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        barrier()
-        start.record(stream)
-        for i in range(args.steps):
-            calls[i % nsets].run(stream)
-        stop.record(stream)
-        barrier()
-    ms_total = start.elapsed_time(stop)
-    B.gdn_launch_timer_stop()
-    records, dropped = B.gdn_launch_timer_read()
+    clk = ClockSampler(local)
+    ms_total, _, _ = timed_steps(calls, args.steps, stream, barrier, clocks=clk)
+    ms_timer, records, dropped = timed_steps(calls, args.steps, stream, barrier, launches_per_call=2)
     per_kernel = {}
     for name, ms in records:
         tot, n = per_kernel.get(name, (0.0, 0))
@@ -419,7 +436,9 @@ def run_row(args, rank, world):
             "kernels": {k: {"launches_per_step": n / args.steps, "ms_per_launch": tot / n,
                             "share": tot / sum(v[0] for v in per_kernel.values())}
                         for k, (tot, n) in sorted(per_kernel.items())},
-            "untimed_launches": dropped})
+            "untimed_launches": dropped,
+            "kernel_times_from": ("a second timed region of the same steps with the library's launch timer on "
+                                  f"({ms_timer / args.steps:.4f} ms per step with it)")})
     # end to end: the inputs from pinned host memory, the outputs back
     host_in = {n: getattr(one, n).cpu().pin_memory() for n in spec.inputs}
     host_out = {n: torch.empty_like(getattr(one, n), device="cpu").pin_memory() for n in spec.outputs}
@@ -533,20 +552,13 @@ def main():
         torch.cuda.synchronize(dev)
 
     launches_per_call = len(B.gdn_prefill_plan(one.desc))
-    # the library brackets each of its launches with CUDA events on the
-    # launch stream: the per-kernel device time of the timed region
-    B.gdn_launch_timer_start(args.steps * launches_per_call)
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        barrier()
-        start.record(stream)
-        for i in range(args.steps):
-            calls[i % nsets].run(stream)
-        stop.record(stream)
-        barrier()
-    ms_total = start.elapsed_time(stop)
-    B.gdn_launch_timer_stop()
-    records, dropped = B.gdn_launch_timer_read()
+    # value: K steps with nothing between the library's launches; then K more
+    # steps with the library bracketing each launch with CUDA events on the
+    # launch stream: the per-kernel device times
+    clk = ClockSampler(local)
+    ms_total, _, _ = timed_steps(calls, args.steps, stream, barrier, clocks=clk)
+    ms_timer, records, dropped = timed_steps(calls, args.steps, stream, barrier,
+                                             launches_per_call=launches_per_call)
     per_kernel = {}
     for name, ms in records:
         tot, n = per_kernel.get(name, (0.0, 0))
@@ -612,6 +624,8 @@ def main():
                            "share": tot / sum(v[0] for v in per_kernel.values())}
                        for k, (tot, n) in sorted(per_kernel.items())}
     roof["untimed_launches"] = dropped
+    roof["kernel_times_from"] = ("a second timed region of the same steps with the library's launch timer on "
+                                 f"({ms_timer / args.steps:.4f} ms per step with it)")
     roof["peak_source"] = peak_kind
     roof["kernel"] = dominant
     roof["algorithmic_bytes"] = bytes_alg
