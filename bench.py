@@ -333,6 +333,8 @@ def timed_steps(calls, steps, stream, barrier, launches_per_call=0, clocks=None)
     which adds a little time per launch: the headline number is taken with it
     off, the per-kernel device times in a second region with it on.
     Returns (ms for all steps, launch records, dropped launches)."""
+    import torch
+    from chunked_gated_delta_chunk_gb300 import binding as B
     if launches_per_call:
         B.gdn_launch_timer_start(steps * launches_per_call)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

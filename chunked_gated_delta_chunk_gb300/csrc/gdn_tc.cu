@@ -39,6 +39,8 @@
 // copies land and still frees its TMEM.
 #include <cuda.h>
 
+#include <utility>
+
 #include "gdn_common.cuh"
 #include "gdn_tc.cuh"
 #include "tc_ptx.cuh"
@@ -489,6 +491,8 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     Item cur;
     int64_t item = next_item(blockIdx.x, cur);
     if (item >= n_items) return;                            // no chunk for this CTA
+    griddep_wait();                                         // inputs and records of the grid before
+    griddep_launch_dependents();
     if (pt == 0) {
         for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
@@ -874,6 +878,8 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_wait();                                     // records, maps, states of the grid before
+    griddep_launch_dependents();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tZ = tmem + kColZ, tZb = tmem + kColZb, tX = tmem + kColX, tO = tmem + kColO,
                    tGW = tmem + kColGW, tU = tmem + kColU;
@@ -1650,6 +1656,8 @@ constexpr int kCombineSlab = kD * kCombineCols;
 constexpr uint32_t kCombineSmem = (2 * kCombineBuf + (1 + kCombineGroups) * kCombineSlab) * 4;
 
 __global__ void __launch_bounds__(kCombineThreads) seg_combine_kernel(const ChunkParams p) {
+    griddep_wait();                              // phase 1's maps
+    griddep_launch_dependents();
     const int h = blockIdx.x, n = blockIdx.y, slab = blockIdx.z;
     int64_t t_end_all = p.cu[p.B];
     if (t_end_all > p.t_cap) t_end_all = p.t_cap;
@@ -1777,6 +1785,25 @@ int tc_read_timeouts() {
 }
 
 
+// Launch as a programmatic dependent of the preceding grid in the stream: the
+// kernel's own griddep_wait() orders it after that grid, while its launch and
+// set-up overlap the end of it.
+template <typename... Kargs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Kargs...), dim3 grid, unsigned block, unsigned smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
     if (p.B == 0) return cudaSuccess;
     if (encode_fn() == nullptr) return cudaErrorNotSupported;
@@ -1796,8 +1823,8 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
     cudaError_t e = ensure_smem(state_kernel, int(kSmemBytes));
     if (e != cudaSuccess) return e;
     auto launch_state = [&](const ChunkParams& q, unsigned z) {
-        if (split) chunk_tc_kernel<true><<<dim3(q.Hv, q.B, z), kThreads, kSmemBytes, s>>>(q, maps);
-        else chunk_tc_kernel<false><<<dim3(q.Hv, q.B, z), kThreads, kSmemBytes, s>>>(q, maps);
+        return split ? launch_pdl(chunk_tc_kernel<true>, dim3(q.Hv, q.B, z), kThreads, kSmemBytes, s, q, maps)
+                     : launch_pdl(chunk_tc_kernel<false>, dim3(q.Hv, q.B, z), kThreads, kSmemBytes, s, q, maps);
     };
     if (split) {                                      // every chunk's S-independent part, in parallel
         if (p.prep_slots > INT32_MAX) return cudaErrorInvalidValue;
@@ -1809,38 +1836,38 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
         const int64_t items = p.prep_slots * int64_t(p.Hv);
         const int64_t grid = items < 2 * int64_t(sms) ? items : 2 * int64_t(sms);   // two CTAs per SM
         timer_begin(s, "chunk_prep_kernel");
-        chunk_prep_kernel<<<unsigned(grid), kPrepThreads, kPrepSmemBytes, s>>>(p, maps);
+        e = launch_pdl(chunk_prep_kernel, dim3(unsigned(grid)), kPrepThreads, kPrepSmemBytes, s, p, maps);
         timer_end(s);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (e != cudaSuccess) return e;
     }
     if (p.seg_chunks <= 0 || p.seg_max < 2) {
         ChunkParams q = p;
         q.seg_phase = 0;
         timer_begin(s, "chunk_tc_kernel");
-        launch_state(q, 1);
+        e = launch_state(q, 1);
         timer_end(s);
-        return cudaGetLastError();
+        return e;
     }
     ChunkParams q = p;
     q.seg_phase = 1;                                  // segment 0 in full; B_s and M_s
     timer_begin(s, "chunk_tc_kernel");
-    launch_state(q, unsigned(2 * p.seg_max - 1));
+    e = launch_state(q, unsigned(2 * p.seg_max - 1));
     timer_end(s);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess) return e;
     if (p.seg_max >= 3) {                             // S_{s+1} = M_s S_s + B_s
         if ((e = ensure_smem(reinterpret_cast<const void*>(seg_combine_kernel), int(kCombineSmem))) !=
             cudaSuccess)
             return e;
         timer_begin(s, "seg_combine_kernel");
-        seg_combine_kernel<<<dim3(p.Hv, p.B, kD / kCombineCols), kCombineThreads, kCombineSmem, s>>>(q);
+        e = launch_pdl(seg_combine_kernel, dim3(p.Hv, p.B, kD / kCombineCols), kCombineThreads, kCombineSmem, s, q);
         timer_end(s);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (e != cudaSuccess) return e;
     }
     q.seg_phase = 2;                                  // segments >= 1 in full
     timer_begin(s, "chunk_tc_kernel");
-    launch_state(q, unsigned(p.seg_max - 1));
+    e = launch_state(q, unsigned(p.seg_max - 1));
     timer_end(s);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace gdn
