@@ -492,7 +492,6 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     int64_t item = next_item(blockIdx.x, cur);
     if (item >= n_items) return;                            // no chunk for this CTA
     griddep_wait();                                         // inputs and records of the grid before
-    griddep_launch_dependents();
     if (pt == 0) {
         for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
@@ -879,7 +878,6 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     __syncthreads();
     tc_fence_after();
     griddep_wait();                                     // records, maps, states of the grid before
-    griddep_launch_dependents();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tZ = tmem + kColZ, tZb = tmem + kColZb, tX = tmem + kColX, tO = tmem + kColO,
                    tGW = tmem + kColGW, tU = tmem + kColU;
@@ -1657,7 +1655,6 @@ constexpr uint32_t kCombineSmem = (2 * kCombineBuf + (1 + kCombineGroups) * kCom
 
 __global__ void __launch_bounds__(kCombineThreads) seg_combine_kernel(const ChunkParams p) {
     griddep_wait();                              // phase 1's maps
-    griddep_launch_dependents();
     const int h = blockIdx.x, n = blockIdx.y, slab = blockIdx.z;
     int64_t t_end_all = p.cu[p.B];
     if (t_end_all > p.t_cap) t_end_all = p.t_cap;
@@ -1787,7 +1784,8 @@ int tc_read_timeouts() {
 
 // Launch as a programmatic dependent of the preceding grid in the stream: the
 // kernel's own griddep_wait() orders it after that grid, while its launch and
-// set-up overlap the end of it.
+// set-up overlap the end of it (its CTAs start on the SMs the preceding grid
+// has left).
 template <typename... Kargs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(Kargs...), dim3 grid, unsigned block, unsigned smem, cudaStream_t s,
                        Args&&... args) {

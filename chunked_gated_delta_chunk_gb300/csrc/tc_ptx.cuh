@@ -75,12 +75,11 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 // ---------------------------------------------------------------- grid dependencies
 // With a programmatic-dependent launch: wait until the preceding grid in the
-// stream has completed and its memory is visible (a no-op otherwise), and
-// let the next grid be scheduled while this one runs.
+// stream has completed and its memory is visible (a no-op otherwise).  The
+// kernels do not trigger their dependents early: a dependent CTA then starts
+// on an SM as soon as the CTAs there have exited, which overlaps the grids'
+// tails without parking waiting CTAs on SMs that are still busy.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
