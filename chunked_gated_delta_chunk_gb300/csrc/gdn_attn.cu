@@ -100,6 +100,7 @@ __device__ __forceinline__ int attn_find_seq(const int32_t* cu, int B, int64_t t
 // Prompt rows into the cache: row t of sequence n goes to position
 // cache_len[n] + (t - cu[n]) (rows past the capacity are dropped).
 __global__ void attn_append_kernel(const AttnParams p) {
+    griddep_wait();                                   // the grid before may still read the cache
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;   // (t, kv head, 16-byte word)
     const int words = kAD / 8;
     if (i >= p.T * p.Hkv * words) return;
@@ -118,6 +119,7 @@ __global__ void attn_append_kernel(const AttnParams p) {
 
 __global__ void __launch_bounds__(kAThreads, 1)
 attn_rows_kernel(const AttnParams p, const __grid_constant__ AttnMaps maps) {
+    griddep_wait();                                   // the cache rows attn_append_kernel wrote
     extern __shared__ uint8_t attn_smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(attn_smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kAOffBar);
@@ -426,9 +428,8 @@ cudaError_t launch_attn_rows(const AttnParams& p, cudaStream_t s) {
     if (p.T > 0) {
         const int64_t items = p.T * p.Hkv * (kAD / 8);
         timer_begin(s, "attn_append_kernel");
-        attn_append_kernel<<<unsigned((items + 255) / 256), 256, 0, s>>>(p);
+        cudaError_t e = launch_pdl(attn_append_kernel, dim3(unsigned((items + 255) / 256)), 256, 0, s, p);
         timer_end(s);
-        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (p.T == 0) return cudaSuccess;
@@ -443,9 +444,9 @@ cudaError_t launch_attn_rows(const AttnParams& p, cudaStream_t s) {
     const unsigned qtiles = unsigned((p.max_len + kAQ - 1) / kAQ);
     if (qtiles == 0) return cudaSuccess;
     timer_begin(s, "attn_rows_kernel");
-    attn_rows_kernel<<<dim3(qtiles, p.Hq, p.B), kAThreads, kASmem, s>>>(p, maps);
+    e = launch_pdl(attn_rows_kernel, dim3(qtiles, p.Hq, p.B), kAThreads, kASmem, s, p, maps);
     timer_end(s);
-    return cudaGetLastError();
+    return e;
 }
 
 int attn_read_timeouts() {

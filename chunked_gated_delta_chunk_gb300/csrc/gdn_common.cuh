@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "gdn.h"
 
 namespace gdn {
@@ -136,6 +138,26 @@ cudaError_t ensure_smem(const void* kernel, int bytes);
 // The part of gdn_workspace_bytes a prefill cannot run without (the short
 // convolution's output); the segment maps and chunk records are optional.
 size_t prefill_required_workspace(const gdn_prefill_desc* d);
+
+// Launch as a programmatic dependent of the preceding grid in the stream: the
+// kernel's own griddep_wait() orders it after that grid, while its launch and
+// set-up overlap the end of it (its CTAs start on the SMs the preceding grid
+// has left).
+template <typename... Kargs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Kargs...), dim3 grid, unsigned block, unsigned smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Launch timing: bracket a kernel launch with timer_begin / timer_end on the
 // launch stream (no-ops unless gdn_launch_timer_start turned recording on).

@@ -10,6 +10,7 @@
 // of 8 channels, so every 16-byte load and store of a warp is one contiguous
 // 512-byte segment of a token row.
 #include "gdn_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace gdn {
 namespace {
@@ -72,6 +73,7 @@ __device__ __forceinline__ void store8(float* p, const float* v) {
 // from that sequence's conv state.
 template <typename Tin, int K>
 __global__ void __launch_bounds__(kConvThreads) conv_kernel(const ConvParams p) {
+    ptx::griddep_wait();                      // the grid before may still read the workspace
     const int c0 = (blockIdx.y * kConvThreads + threadIdx.x) * 8;
     if (c0 >= p.C) return;
     const int64_t t0 = int64_t(blockIdx.x) * kConvRun;
@@ -155,6 +157,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_kernel(const ConvParams p) 
 // the same stream, so no reader of the old state is still in flight.
 template <typename Tin>
 __global__ void __launch_bounds__(kConvThreads) conv_state_kernel(const ConvParams p) {
+    ptx::griddep_wait();                      // the conv state is read and written in place
     const int64_t idx = int64_t(blockIdx.x) * kConvThreads + threadIdx.x;
     if (idx >= int64_t(p.B) * p.C) return;
     const int n = int(idx / p.C), c = int(idx % p.C);
@@ -180,15 +183,15 @@ __global__ void __launch_bounds__(kConvThreads) conv_state_kernel(const ConvPara
 }
 
 template <typename Tin>
-void launch_conv_k(const ConvParams& p, dim3 grid, cudaStream_t s) {
+cudaError_t launch_conv_k(const ConvParams& p, dim3 grid, cudaStream_t s) {
     switch (p.K) {
-        case 2: conv_kernel<Tin, 2><<<grid, kConvThreads, 0, s>>>(p); break;
-        case 3: conv_kernel<Tin, 3><<<grid, kConvThreads, 0, s>>>(p); break;
-        case 4: conv_kernel<Tin, 4><<<grid, kConvThreads, 0, s>>>(p); break;
-        case 5: conv_kernel<Tin, 5><<<grid, kConvThreads, 0, s>>>(p); break;
-        case 6: conv_kernel<Tin, 6><<<grid, kConvThreads, 0, s>>>(p); break;
-        case 7: conv_kernel<Tin, 7><<<grid, kConvThreads, 0, s>>>(p); break;
-        default: conv_kernel<Tin, 8><<<grid, kConvThreads, 0, s>>>(p); break;
+        case 2: return launch_pdl(conv_kernel<Tin, 2>, grid, kConvThreads, 0, s, p);
+        case 3: return launch_pdl(conv_kernel<Tin, 3>, grid, kConvThreads, 0, s, p);
+        case 4: return launch_pdl(conv_kernel<Tin, 4>, grid, kConvThreads, 0, s, p);
+        case 5: return launch_pdl(conv_kernel<Tin, 5>, grid, kConvThreads, 0, s, p);
+        case 6: return launch_pdl(conv_kernel<Tin, 6>, grid, kConvThreads, 0, s, p);
+        case 7: return launch_pdl(conv_kernel<Tin, 7>, grid, kConvThreads, 0, s, p);
+        default: return launch_pdl(conv_kernel<Tin, 8>, grid, kConvThreads, 0, s, p);
     }
 }
 
@@ -199,12 +202,9 @@ cudaError_t launch_conv(const ConvParams& p, int dtype, cudaStream_t s) {
     const dim3 grid(unsigned((p.T + kConvRun - 1) / kConvRun),
                     (p.C / 8 + kConvThreads - 1) / kConvThreads);
     timer_begin(s, "conv_kernel");
-    if (dtype == GDN_FP32)
-        launch_conv_k<float>(p, grid, s);
-    else
-        launch_conv_k<__nv_bfloat16>(p, grid, s);
+    const cudaError_t e = dtype == GDN_FP32 ? launch_conv_k<float>(p, grid, s) : launch_conv_k<__nv_bfloat16>(p, grid, s);
     timer_end(s);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_conv_state(const ConvParams& p, int dtype, cudaStream_t s) {
@@ -212,12 +212,11 @@ cudaError_t launch_conv_state(const ConvParams& p, int dtype, cudaStream_t s) {
     if (n == 0 || p.state_out == nullptr) return cudaSuccess;
     const unsigned blocks = unsigned((n + kConvThreads - 1) / kConvThreads);
     timer_begin(s, "conv_state_kernel");
-    if (dtype == GDN_FP32)
-        conv_state_kernel<float><<<blocks, kConvThreads, 0, s>>>(p);
-    else
-        conv_state_kernel<__nv_bfloat16><<<blocks, kConvThreads, 0, s>>>(p);
+    const cudaError_t e = dtype == GDN_FP32
+                              ? launch_pdl(conv_state_kernel<float>, dim3(blocks), kConvThreads, 0, s, p)
+                              : launch_pdl(conv_state_kernel<__nv_bfloat16>, dim3(blocks), kConvThreads, 0, s, p);
     timer_end(s);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace gdn

@@ -37,6 +37,7 @@ constexpr int kChainRows = kWarpRows / kChains;    // rows of one of a thread's 
 
 // Zero the ticket and the tile flags; end state of every empty sequence.
 __global__ void scan_init_kernel(const ScanParams p) {
+    ptx::griddep_wait();                              // the grid before may still use the flags
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i == 0) *p.ticket = 0;
     if (i < p.n_tiles) p.flags[i] = 0;
@@ -47,6 +48,7 @@ __global__ void scan_init_kernel(const ScanParams p) {
 }
 
 __global__ void __launch_bounds__(kThreads) scan_rows_kernel(const ScanParams p) {
+    griddep_wait();                                   // ticket and flags from scan_init_kernel
     extern __shared__ __align__(16) float sm_scan[];
     float* sa = sm_scan;                              // [kRows][kCols]
     float* sb = sm_scan + kRows * kCols;
@@ -222,9 +224,8 @@ cudaError_t launch_scan_rows(const ScanParams& p, cudaStream_t s) {
     const int64_t init_items = int64_t(p.B) * p.C > p.n_tiles ? int64_t(p.B) * p.C : p.n_tiles;
     if (init_items > 0) {
         timer_begin(s, "scan_init_kernel");
-        scan_init_kernel<<<unsigned((init_items + 255) / 256), 256, 0, s>>>(p);
+        cudaError_t e = launch_pdl(scan_init_kernel, dim3(unsigned((init_items + 255) / 256)), 256, 0, s, p);
         timer_end(s);
-        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (p.n_tiles == 0) return cudaSuccess;
@@ -232,9 +233,9 @@ cudaError_t launch_scan_rows(const ScanParams& p, cudaStream_t s) {
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(scan_rows_kernel), smem);
     if (e != cudaSuccess) return e;
     timer_begin(s, "scan_rows_kernel");
-    scan_rows_kernel<<<unsigned(p.n_tiles), rows::kThreads, smem, s>>>(p);
+    e = launch_pdl(scan_rows_kernel, dim3(unsigned(p.n_tiles)), rows::kThreads, unsigned(smem), s, p);
     timer_end(s);
-    return cudaGetLastError();
+    return e;
 }
 
 int scan_read_timeouts() {

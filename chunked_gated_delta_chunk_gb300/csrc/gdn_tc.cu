@@ -39,8 +39,6 @@
 // copies land and still frees its TMEM.
 #include <cuda.h>
 
-#include <utility>
-
 #include "gdn_common.cuh"
 #include "gdn_tc.cuh"
 #include "tc_ptx.cuh"
@@ -413,6 +411,7 @@ static_assert(2 * (kPrepSmemBytes + 1024) <= 233472, "two preparation CTAs per S
 // load latency is paid per chunk.
 __global__ void __launch_bounds__(kPrepThreads, 2)
 chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
+    griddep_wait();   // everything the grid before wrote (inputs, the records it may still read)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* kq = sm + kPOffKQ;
@@ -491,7 +490,6 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     Item cur;
     int64_t item = next_item(blockIdx.x, cur);
     if (item >= n_items) return;                            // no chunk for this CTA
-    griddep_wait();                                         // inputs and records of the grid before
     if (pt == 0) {
         for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
@@ -768,6 +766,7 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
+    griddep_wait();   // everything the grid before wrote (records, maps, states, even cu_seqlens)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* sA = reinterpret_cast<float*>(sm + kOffA);
@@ -877,7 +876,6 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    griddep_wait();                                     // records, maps, states of the grid before
     const uint32_t tmem = *tmem_slot;
     const uint32_t tZ = tmem + kColZ, tZb = tmem + kColZb, tX = tmem + kColX, tO = tmem + kColO,
                    tGW = tmem + kColGW, tU = tmem + kColU;
@@ -1781,26 +1779,6 @@ int tc_read_timeouts() {
     return v;
 }
 
-
-// Launch as a programmatic dependent of the preceding grid in the stream: the
-// kernel's own griddep_wait() orders it after that grid, while its launch and
-// set-up overlap the end of it (its CTAs start on the SMs the preceding grid
-// has left).
-template <typename... Kargs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(Kargs...), dim3 grid, unsigned block, unsigned smem, cudaStream_t s,
-                       Args&&... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
 
 cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
     if (p.B == 0) return cudaSuccess;

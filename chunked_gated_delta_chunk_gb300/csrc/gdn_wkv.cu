@@ -116,6 +116,7 @@ __device__ __forceinline__ St get(const float* v, size_t tiles, size_t slot) {
 }
 
 __global__ void wkv_init_kernel(const WkvParams p) {
+    griddep_wait();                                   // the grid before may still use the flags
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i == 0) *p.ticket = 0;
     if (i < p.n_tiles) p.flags[i] = 0;
@@ -126,6 +127,7 @@ __global__ void wkv_init_kernel(const WkvParams p) {
 }
 
 __global__ void __launch_bounds__(rows::kThreads) wkv_rows_kernel(const WkvParams p) {
+    griddep_wait();                                   // ticket and flags from wkv_init_kernel
     using namespace rows;
     constexpr int kRows = rows::kWkvRows;             // rows of a tile
     constexpr int kWarpRows = kRows / kWarps;         // rows of a warp
@@ -309,9 +311,8 @@ cudaError_t launch_wkv_rows(const WkvParams& p, cudaStream_t s) {
     const int64_t init_items = int64_t(p.B) * p.C > p.n_tiles ? int64_t(p.B) * p.C : p.n_tiles;
     if (init_items > 0) {
         timer_begin(s, "wkv_init_kernel");
-        wkv_init_kernel<<<unsigned((init_items + 255) / 256), 256, 0, s>>>(p);
+        cudaError_t e = launch_pdl(wkv_init_kernel, dim3(unsigned((init_items + 255) / 256)), 256, 0, s, p);
         timer_end(s);
-        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (p.n_tiles == 0) return cudaSuccess;
@@ -319,9 +320,9 @@ cudaError_t launch_wkv_rows(const WkvParams& p, cudaStream_t s) {
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(wkv_rows_kernel), smem);
     if (e != cudaSuccess) return e;
     timer_begin(s, "wkv_rows_kernel");
-    wkv_rows_kernel<<<unsigned(p.n_tiles), rows::kThreads, smem, s>>>(p);
+    e = launch_pdl(wkv_rows_kernel, dim3(unsigned(p.n_tiles)), rows::kThreads, unsigned(smem), s, p);
     timer_end(s);
-    return cudaGetLastError();
+    return e;
 }
 
 int wkv_read_timeouts() {
