@@ -130,10 +130,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-__device__ __forceinline__ float bf16_round(float x) {
-    return __bfloat162float(__float2bfloat16_rn(x));
-}
-
 __device__ __forceinline__ void store_chunk8(uint8_t* p, const float* v) {
     uint4 u;
     u.x = pack_bf16x2(v[0], v[1]);
@@ -143,16 +139,24 @@ __device__ __forceinline__ void store_chunk8(uint8_t* p, const float* v) {
     *reinterpret_cast<uint4*>(p) = u;
 }
 
+// A pair (a0, a1) as bf16 hi = (bf16(a0), bf16(a1)) and lo = bf16(a - hi),
+// each packed in one word: one paired conversion for hi, whose halves are
+// read back as floats by shifting.
+__device__ __forceinline__ void split_pair(float a0, float a1, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16x2(a0, a1);
+    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+    lo = pack_bf16x2(a0 - h0, a1 - h1);
+}
+
 // hi = bf16(v), lo = bf16(v - hi), 8 values each.
 __device__ __forceinline__ void store_split8(uint8_t* phi, uint8_t* plo, const float* v) {
-    float hi[8], lo[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        hi[q] = bf16_round(v[q]);
-        lo[q] = v[q] - hi[q];
-    }
-    store_chunk8(phi, hi);
-    store_chunk8(plo, lo);
+    uint4 h, l;
+    split_pair(v[0], v[1], h.x, l.x);
+    split_pair(v[2], v[3], h.y, l.y);
+    split_pair(v[4], v[5], h.z, l.z);
+    split_pair(v[6], v[7], h.w, l.w);
+    *reinterpret_cast<uint4*>(phi) = h;
+    *reinterpret_cast<uint4*>(plo) = l;
 }
 
 __device__ __forceinline__ void load_chunk8(const uint8_t* p, float* v) {
@@ -1483,13 +1487,8 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const float a0 = x[2 * i], a1 = x[2 * i + 1];
-                    const float h0 = bf16_round(a0), h1 = bf16_round(a1);
-                    uh[i] = pack_bf16x2(h0, h1);
-                    ul[i] = pack_bf16x2(a0 - h0, a1 - h1);
-                    const float s0 = a0 * e[2 * i], s1 = a1 * e[2 * i + 1];
-                    const float g0 = bf16_round(s0), g1 = bf16_round(s1);
-                    sh[i] = pack_bf16x2(g0, g1);
-                    sl[i] = pack_bf16x2(s0 - g0, s1 - g1);
+                    split_pair(a0, a1, uh[i], ul[i]);
+                    split_pair(a0 * e[2 * i], a1 * e[2 * i + 1], sh[i], sl[i]);
                 }
                 GDN_TMEM_ST_X16(tU + lane_addr + 0 + hf * 16, uh);
                 GDN_TMEM_ST_X16(tU + lane_addr + 32 + hf * 16, ul);
