@@ -52,6 +52,34 @@ __device__ __forceinline__ void load8(const float* p, float* v) {
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
+// Raw 16-byte words of 8 channels, kept packed while a group of rows is in
+// flight (bf16: one word, fp32: two), unpacked to floats when used.
+template <typename Tin> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+    uint4 w;
+    __device__ __forceinline__ void load(const __nv_bfloat16* p) { w = *reinterpret_cast<const uint4*>(p); }
+    __device__ __forceinline__ void unpack(float* v) const {
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(b[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+};
+template <> struct Raw8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const float* p) {
+        a = *reinterpret_cast<const float4*>(p);
+        b = *reinterpret_cast<const float4*>(p + 4);
+    }
+    __device__ __forceinline__ void unpack(float* v) const {
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+};
+
 __device__ __forceinline__ void store8(__nv_bfloat16* p, const float* v) {
     uint4 u;
     uint32_t* w = reinterpret_cast<uint32_t*>(&u);
@@ -138,11 +166,15 @@ __global__ void __launch_bounds__(kConvThreads) conv_kernel(const ConvParams p) 
         const int64_t end = t1 < stop ? t1 : stop;  // tokens of this sequence in the run
         // groups of kConvGroup rows: all loads of a group in flight together
         for (; t + kConvGroup <= end; t += kConvGroup) {
-            float cur[kConvGroup][8];
+            Raw8<Tin> raw[kConvGroup];
 #pragma unroll
-            for (int u = 0; u < kConvGroup; ++u) load8(x + (t + u) * p.C + c0, cur[u]);
+            for (int u = 0; u < kConvGroup; ++u) raw[u].load(x + (t + u) * p.C + c0);
 #pragma unroll
-            for (int u = 0; u < kConvGroup; ++u) emit(t + u, cur[u]);
+            for (int u = 0; u < kConvGroup; ++u) {
+                float cur[8];
+                raw[u].unpack(cur);
+                emit(t + u, cur);
+            }
         }
         for (; t < end; ++t) {
             float cur[8];
