@@ -16,7 +16,7 @@ namespace gdn {
 namespace {
 
 constexpr int kConvThreads = 128;
-constexpr int kConvRun = 32;            // tokens per thread
+constexpr int kConvRun = 128;           // tokens per thread (fewer halo re-reads)
 constexpr int kConvGroup = 8;           // token rows loaded together
 
 __device__ __forceinline__ float act_fn(float y, int act) {
