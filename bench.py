@@ -90,17 +90,18 @@ def kernel_source_hash(sources):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_name):
+def recorded_traffic(kernel_name, workload):
     """DRAM bytes (read + write) of the kernel's launches in one step, from
-    the committed ncu summary, if it was taken on the kernel's current source
-    files (the entry lists them); else None."""
+    the committed ncu summary, if it was taken on this workload (its short
+    name, before the colon) and on the kernel's current source files (the
+    entry lists them); else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     entry = d.get(kernel_name)
-    if not entry or not entry.get("sources"):
+    if not entry or not entry.get("sources") or entry.get("workload") != workload.split(":")[0]:
         return None
     try:
         if entry.get("source_hash") != kernel_source_hash(entry["sources"]):
@@ -433,7 +434,7 @@ def run_row(args, rank, world):
         achieved = spec.nbytes / (kern_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm}
     roof.update({
-            "traffic": recorded_traffic(dominant), "peak_source": peak_kind, "kernel": dominant,
+            "traffic": recorded_traffic(dominant, spec.workload), "peak_source": peak_kind, "kernel": dominant,
             "algorithmic_bytes": spec.nbytes, "kernel_ms_per_launch": kern_ms,
             "kernels": {k: {"launches_per_step": n / args.steps, "ms_per_launch": tot / n,
                             "share": tot / sum(v[0] for v in per_kernel.values())}
@@ -500,7 +501,7 @@ def run_row(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
@@ -619,7 +620,7 @@ def main():
         achieved = flops_alg / (kern_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
                 "frac": achieved / tflops}
-    roof["traffic"] = recorded_traffic(dominant)
+    roof["traffic"] = recorded_traffic(dominant, WORKLOADS[args.config])
     roof["kernel_ms_per_step"] = kern_ms
     roof["launches_per_step"] = per_kernel[dominant][1] / args.steps
     roof["kernels"] = {k: {"launches_per_step": n / args.steps, "ms_per_launch": tot / n,
