@@ -62,21 +62,41 @@ size_t conv_workspace(const gdn_prefill_desc* d) {
 
 constexpr int kSMs = 152;   // GB300: 2 dies x 76 SMs
 
+// Chunk groups per segment in seg_out_kernel: as many as let its CTAs (one
+// per group of every segment s >= 1, plus one for the final state, per
+// sequence and value head) fit one wave, at least one, at most one per chunk.
+// When even one group per segment leaves no room for the final state's CTA,
+// the last group's CTA of the last segment forms it (*final_cta = 0).
+int segment_groups(int64_t units, int64_t seg_max, int seg_chunks, int* final_cta) {
+    *final_cta = 1;
+    if (seg_max < 2) return 1;
+    const int64_t per_unit = kSMs / units;       // CTAs per (sequence, value head) in one wave
+    int64_t g = (per_unit - 1) / (seg_max - 1);
+    if (g < 1) {
+        *final_cta = 0;
+        g = per_unit / (seg_max - 1);
+    }
+    if (g < 1) g = 1;
+    if (g > seg_chunks) g = seg_chunks;
+    return int(g);
+}
+
 // Chunks per segment of the segment-parallel scan, or 0 for one pass.
 // Cost model in chunk periods of one CTA (one CTA per SM): with n segments of
 // L = ceil(chunks / n) chunks, phase 1 runs (2n - 1) CTAs per (sequence,
-// value head) and phase 2 runs n - 1, each phase taking L + kStartPeriods
-// periods per wave of kSMs CTAs (a CTA's first chunks run with cold
-// instruction caches and its incoming state still on the way); each of the
-// n - 2 sequential combine steps costs about one period.  One pass costs
-// chunks + kStartPeriods periods in ceil(units / kSMs) waves.  The cheapest n
-// wins; sequence lengths are taken as the batch average.
+// value head), each taking L + kStartPeriods periods per wave of kSMs CTAs
+// (a CTA's first chunks run with cold instruction caches and its incoming
+// state still on the way); seg_out_kernel then takes about one period per
+// state step (n - 1 of them) plus kOutPeriods per output chunk of a group,
+// per wave of its CTAs.  One pass costs chunks + kStartPeriods periods in
+// ceil(units / kSMs) waves.  The cheapest n wins; sequence lengths are taken
+// as the batch average.
 int segment_chunks(const gdn_prefill_desc* d) {
     if (d->dtype != GDN_BF16 || d->dk != 128 || d->dv != 128) return 0;   // tensor-core path only
     if (d->T_total <= 0 || d->B <= 0 || d->segment_chunks < 0) return 0;
     const int64_t chunks = (d->T_total + d->chunk - 1) / d->chunk;
     if (d->segment_chunks > 0) return d->segment_chunks < chunks ? d->segment_chunks : 0;
-    constexpr double kStartPeriods = 3.0, kCombinePeriods = 1.0;
+    constexpr double kStartPeriods = 3.0, kStepPeriods = 1.0, kOutPeriods = 0.25;
     const int64_t units = int64_t(d->Hv) * d->B;
     const int64_t per_seq = (chunks + d->B - 1) / d->B;
     auto waves = [&](int64_t ctas) { return (ctas + kSMs - 1) / kSMs; };
@@ -84,8 +104,11 @@ int segment_chunks(const gdn_prefill_desc* d) {
     int best_len = 0;
     for (int64_t n = 2; n <= 64 && n <= per_seq; ++n) {
         const int64_t len = (per_seq + n - 1) / n;
-        const double cost = double(waves(units * (2 * n - 1)) + waves(units * (n - 1))) * (double(len) + kStartPeriods) +
-                            double(n - 2) * kCombinePeriods;
+        int final_cta = 1;
+        const int64_t groups = segment_groups(units, n, int(len), &final_cta);
+        const double out = double(waves(units * ((n - 1) * groups + final_cta))) *
+                           (double(n - 1) * kStepPeriods + double((len + groups - 1) / groups) * kOutPeriods);
+        const double cost = double(waves(units * (2 * n - 1))) * (double(len) + kStartPeriods) + out;
         if (cost < best) {
             best = cost;
             best_len = int(len);
@@ -99,11 +122,18 @@ int64_t segment_slots(const gdn_prefill_desc* d, int seg_chunks) {
     return d->T_total / seg_tokens + d->B + 1;
 }
 
-size_t segment_workspace(const gdn_prefill_desc* d, int seg_chunks) {
-    if (seg_chunks <= 0) return 0;
+// The segment maps (B_s, M_s, S_s per value head and slot), then the output
+// map G (bf16, one row of Hv * dv per token).
+size_t segment_map_bytes(const gdn_prefill_desc* d, int seg_chunks) {
     const size_t bytes = size_t(d->Hv) * size_t(segment_slots(d, seg_chunks)) * 3 * size_t(d->dk) *
                          size_t(d->dv) * sizeof(float);
     return (bytes + 255) & ~size_t(255);
+}
+
+size_t segment_workspace(const gdn_prefill_desc* d, int seg_chunks) {
+    if (seg_chunks <= 0) return 0;
+    const size_t g_bytes = size_t(d->T_total) * size_t(d->Hv) * size_t(d->dv) * 2;
+    return segment_map_bytes(d, seg_chunks) + ((g_bytes + 255) & ~size_t(255));
 }
 
 // Chunk records of the split preparation: one per (value head, chunk slot),
@@ -204,6 +234,8 @@ int gdn_prefill_ex(const gdn_prefill_desc* d, gdn_stream_t stream) {
             p.seg_ws = reinterpret_cast<float*>(static_cast<char*>(d->workspace) + conv_bytes);
             p.seg_slots = segment_slots(d, sc);
             p.seg_max = int((d->T_total + seg_tokens - 1) / seg_tokens);
+            p.seg_groups = segment_groups(int64_t(d->Hv) * d->B, p.seg_max, sc, &p.seg_final_cta);
+            p.g_out = static_cast<char*>(d->workspace) + conv_bytes + segment_map_bytes(d, sc);
         }
         if (prep_bytes > 0 && d->workspace != nullptr &&
             d->workspace_bytes >= conv_bytes + seg_bytes + prep_bytes) {
@@ -352,8 +384,7 @@ int gdn_prefill_plan(const gdn_prefill_desc* d, const char** names, int max_name
         d->workspace_bytes >= conv_workspace(d) + segment_workspace(d, sc)) {
         const int64_t seg_tokens = int64_t(sc) * d->chunk;
         const int64_t seg_max = (d->T_total + seg_tokens - 1) / seg_tokens;
-        if (seg_max >= 3) plan[n++] = "seg_combine_kernel";
-        if (seg_max >= 2) plan[n++] = gdn::kTcKernelName;
+        if (seg_max >= 2) plan[n++] = "seg_out_kernel";
     }
     if (d->conv_x != nullptr && d->conv_state_out != nullptr) plan[n++] = "conv_state_kernel";
     for (int i = 0; i < n && i < max_names; ++i)

@@ -35,19 +35,25 @@ struct ChunkParams {
     float eps;
     float q_scale;
     // Segment-parallel scan (tensor-core path only).  seg_phase 0: one pass
-    // over every sequence.  Phase 1: segment 0 of each sequence in full,
-    // every later segment s twice, from a zero state (offset B_s) and from
-    // the identity with V = 0 (transition M_s).  Phase 2: every segment
-    // s >= 1 in full from its start state S_s.  seg_ws holds, per value head
-    // and segment slot, three 128 x 128 fp32 matrices: B_s and S_s row-major
-    // [dk][dv], M_s stored transposed (element (i, j) of M_s at j * dk + i,
-    // which the combine reads column by column); the slot of
-    // (sequence n, segment s) is cu[n] / (seg_chunks * chunk) + n + s.
+    // over every sequence.  Phase 1: segment 0 of each sequence in full, every
+    // later segment s twice: from a zero state (its end state is the offset
+    // B_s, its outputs O' go to `out`) and from the identity with V = 0 (its
+    // end state is the transition M_s, its outputs, the output map G, go to
+    // g_out).  seg_out_kernel then forms every segment's incoming state S_s
+    // (S_{s+1} = M_s S_s + B_s), the outputs O = O' + G S_s of segments
+    // s >= 1 and the final state.  seg_ws holds, per value head and segment
+    // slot, three 128 x 128 fp32 matrices: B_s and S_s row-major [dk][dv], M_s
+    // stored transposed (element (i, j) of M_s at j * dk + i); the slot of
+    // (sequence n, segment s) is cu[n] / (seg_chunks * chunk) + n + s.  g_out
+    // is bf16 laid out like `out`.
     int seg_chunks;
     int seg_phase;
     float* seg_ws;
     int64_t seg_slots;       // slots per value head
     int seg_max;             // most segments any sequence can have (grid size)
+    int seg_groups;          // chunk groups per segment in seg_out_kernel
+    int seg_final_cta;       // 1: a CTA of its own forms the final state; 0: the last group's
+    void* g_out;
     // Split preparation (tensor-core path only).  When prep_ws is set, a
     // separate pass solves every chunk's S-independent part (inverse, U0, W,
     // the intra-chunk output weights P, the scaled queries) in parallel over
@@ -205,7 +211,6 @@ struct StepParams {
 
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_chunk_simt(const ChunkParams& p, int dtype, cudaStream_t s);
-cudaError_t launch_seg_combine(const ChunkParams& p, cudaStream_t s);
 cudaError_t launch_conv(const ConvParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_conv_state(const ConvParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_step(const StepParams& p, int dtype, cudaStream_t s);

@@ -362,7 +362,8 @@ __device__ void block_inverse_64(const float* sA, float* sT, float* sTmp, int pt
 
 struct Maps {
     CUtensorMap q, k, v;
-    CUtensorMap o;            // the output (set with chunk records: tile stores)
+    CUtensorMap o;            // the output (chunk records or segments: tile stores)
+    CUtensorMap g;            // the output map G of the segment scan (bf16, laid out like o)
 };
 
 // ---- split preparation ------------------------------------------------------
@@ -821,8 +822,6 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     if (p.seg_phase == 1 && blockIdx.z > 0) {
         seg = int(blockIdx.z + 1) / 2;
         mode = (blockIdx.z & 1) ? kModeOffset : kModeTransition;
-    } else if (p.seg_phase == 2) {
-        seg = int(blockIdx.z) + 1;
     }
     // Segments of seg_chunks chunks; when they do not divide the sequence,
     // segment 0 is the short one: in phase 1 it is the only full pass, which
@@ -840,7 +839,11 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     const int64_t slot0 = t0 / p.chunk + n + c_begin;   // record slot of this CTA's first chunk
     t0 += int64_t(c_begin) * p.chunk;                   // first token of this CTA's part
     const bool last_seg = c_end >= seq_chunks;
-    const bool write_out = mode == kModeFull;
+    // Every pass writes its outputs: the full pass the final ones, the offset
+    // pass those from a zero incoming state (to the output, completed by
+    // seg_out_kernel), the transition pass the output map G.
+    const bool write_out = true;
+    const CUtensorMap* omap = mode == kModeTransition ? &maps.g : &maps.o;
     float* slot = nullptr;                              // B, M, S of this segment
     float* next_slot = nullptr;                         // of the next segment
     if (p.seg_phase) {
@@ -849,18 +852,24 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         slot = p.seg_ws + (size_t(h) * p.seg_slots + sl) * 3 * kD * kD;
         next_slot = slot + 3 * kD * kD;
     }
-    // incoming state: state_in (segment 0), S_s (later segments in full), zero
-    // (offset pass) or the identity (transition pass)
-    const float* init_src = seg == 0 ? (p.state_in ? p.state_in + sbase : nullptr)
-                                     : (mode == kModeFull ? slot + 2 * kD * kD : nullptr);
+    // incoming state: state_in (segment 0), zero (offset pass) or the identity
+    // (transition pass)
+    const float* init_src = seg == 0 && p.state_in ? p.state_in + sbase : nullptr;
     const bool init_identity = mode == kModeTransition;
     // final state: state_out (last segment), S_1 (segment 0 of phase 1), B_s / M_s
+    // (fp32, [dk][dv]) or, for S_1 and M_s, the bf16 hi / lo images that
+    // seg_out_kernel copies straight into shared memory: S_1^T K-major (row =
+    // value column) and M_s^T MN-major (row = key row of the input side), in
+    // both cases row = this thread's TMEM lane, 128-byte swizzled.
     float* final_dst = nullptr;
+    uint8_t* img_dst = nullptr;
     if (mode == kModeFull) {
         if (last_seg) final_dst = p.state_out ? p.state_out + sbase : nullptr;
-        else if (p.seg_phase == 1) final_dst = next_slot + 2 * kD * kD;
+        else if (p.seg_phase == 1) img_dst = reinterpret_cast<uint8_t*>(next_slot + 2 * kD * kD);
+    } else if (mode == kModeOffset) {
+        final_dst = slot;
     } else {
-        final_dst = slot + (mode == kModeOffset ? 0 : kD * kD);
+        img_dst = reinterpret_cast<uint8_t*>(slot + kD * kD);
     }
 
     if (tid == 0) {
@@ -1296,7 +1305,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         // follows through voting named barriers.
         const int ct = tid - 128;                        // == row
         const bool lead = ct == 0;
-        __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(p.out);
+        __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(mode == kModeTransition ? p.g_out : p.out);
         const uint32_t id_x = idesc_bf16(128, 64, 0, 1);    // B = -W^T, MN-major
         const uint32_t id_o = idesc_bf16(128, 64, 0, 0);    // B = Qs or P, K-major
         const uint32_t id_z = idesc_bf16(128, 128, 0, 1);   // B = raw K, MN-major [i][d]
@@ -1345,8 +1354,8 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             const uint8_t* st = o_stage + uint32_t(cc & 1) * 16384u;
             if (o_rows == kC || o_cs + o_rows >= p.t_cap) {
                 if (lead) {
-                    tma_store_2d(&maps.o, st, h * kD, int(o_cs));
-                    tma_store_2d(&maps.o, st + 8192, h * kD + 64, int(o_cs));
+                    tma_store_2d(omap, st, h * kD, int(o_cs));
+                    tma_store_2d(omap, st + 8192, h * kD + 64, int(o_cs));
                 }
             } else {
                 for (int idx = ct; idx < kC * 16; idx += int(kChainN)) {
@@ -1554,12 +1563,12 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     tmem_st16(tZ + lane_addr + hf * 64 + 16, z + 16);
                     tmem_st16(tZ + lane_addr + hf * 64 + 32, z + 32);
                     tmem_st16(tZ + lane_addr + hf * 64 + 48, z + 48);
-                } else if (final_dst && mode == kModeTransition) {
-                    // M_s transposed: this thread's column of M_s is one contiguous row
+                } else if (img_dst) {
+                    // this thread's lane is one row of either image
 #pragma unroll
-                    for (int i = 0; i < 64; i += 4)
-                        *reinterpret_cast<float4*>(final_dst + size_t(row) * kD + hf * 64 + i) =
-                            make_float4(z[i], z[i + 1], z[i + 2], z[i + 3]);
+                    for (int i = 0; i < 64; i += 8)
+                        store_split8(img_dst + toff(row, hf * 64 + i, 16384),
+                                     img_dst + 32768 + toff(row, hf * 64 + i, 16384), z + i);
                 } else if (final_dst) {
 #pragma unroll
                     for (int i = 0; i < 64; ++i) final_dst[size_t(hf * 64 + i) * kD + row] = z[i];
@@ -1633,107 +1642,355 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Phase 2 of the segment scan: S_{s+1} = M_s S_s + B_s for s = 1 .. nseg - 2,
-// per (value head, sequence), in fp32.  Columns of the state evolve
-// independently, so each CTA owns kCombineCols of them and keeps its slab of
-// S in shared memory from one segment to the next.  M_s (stored transposed,
-// 64 KB) and the CTA's columns of B_s are staged in shared memory by
-// cp.async, the next segment's copies in flight while the current ones are
-// used.  Four thread groups split the inner dimension k; in a group, thread
-// (rows 4i.., columns 4j..) reads four rows of M_s for one k as one 16-byte
-// word of M_s^T and four columns of S as one broadcast word.  The partial
-// sums meet in shared memory.
-constexpr int kCombineGroups = 4;
-constexpr int kCombineThreads = 128 * kCombineGroups;
-constexpr int kCombineCols = 16;
-constexpr int kCombineBuf = kD * kD + kD * kCombineCols;     // M_s^T, then B_s columns
-constexpr int kCombineSlab = kD * kCombineCols;
-constexpr uint32_t kCombineSmem = (2 * kCombineBuf + (1 + kCombineGroups) * kCombineSlab) * 4;
+// ---- segment outputs -----------------------------------------------------------
+// Phase 1 leaves, per (value head, sequence): S_1 (the end state of segment
+// 0, whose outputs are final), and for every later segment s its offset B_s
+// and transition M_s, the outputs O' of its chunks from a zero incoming state
+// (in `out`) and its output map G (the outputs from the identity with V = 0,
+// in the G buffer).  A chunk's outputs are linear in the segment's incoming
+// state, so with S_{s+1} = M_s S_s + B_s every output row is O = O' + G S_s.
+//
+// seg_out_kernel, grid (Hv, B, (seg_max - 1) * groups + final CTA), 256
+// threads: CTA z < (seg_max - 1) * groups takes chunk group z % groups of
+// segment 1 + z / groups, forms S_s from S_1 by s - 1 steps and then
+// O = O' + G S_s for its chunks.  The final state S_n of the sequence's n
+// segments (n - 1 steps) is formed by one more CTA when that fits the wave,
+// else by the last group's CTA of segment n - 1 after its outputs.  The CTA
+// keeps S^T as bf16 hi and lo images (the A operand: rows = value columns,
+// K = key rows); phase 1 leaves S_1 and every M_s^T as such images (M_s^T
+// MN-major), which arrive by bulk copy, M double-buffered.  A step is three
+// M = N = 128 tcgen05 products, D = S^T M^T from (hi, hi), (hi, lo), (lo, hi),
+// then S_{s+1}^T = D + B_s^T in fp32 (TMEM lane = value column) and back to
+// images.  An output chunk is one product O^T = bf16(S)^T G^T (the state
+// enters output products as a single bf16 in every pass of the scan; B = the
+// chunk's G tile, K-major as stored, in a ring of three); O' (a ring of two)
+// is added in fp32 in the epilogue, read from its tile in the same fragment
+// layout as the result is written back (ldmatrix / stmatrix, transposed), and
+// the tile is stored by TMA in place.
+constexpr uint32_t kSoThreads = 256;
+constexpr uint32_t kSoImg = 32768;                  // one 128 x 128 bf16 image, two 16 KB blocks
+constexpr uint32_t kSoOffS = 0;                     // S^T hi | lo, K-major
+constexpr uint32_t kSoOffM0 = 2 * kSoImg;           // M^T hi | lo, MN-major: buffer 0
+constexpr uint32_t kSoOffTile = 4 * kSoImg;         // M^T buffer 1 during the steps, then the tiles
+constexpr uint32_t kSoOffM1 = kSoOffTile;
+constexpr uint32_t kSoOffG = kSoOffTile;            // G tiles: three of 16 KB
+constexpr uint32_t kSoOffP = kSoOffTile + 3 * 16384;   // O' tiles: two of 16 KB
+constexpr uint32_t kSoOffBar = kSoOffTile + 5 * 16384;
+constexpr uint32_t kSoNumBars = 11;
+constexpr uint32_t kSoSmem = kSoOffBar + kSoNumBars * 8 + 16 + 1024;
+constexpr uint32_t kSoTmemCols = 256;               // step accumulator (128) | O^T, two buffers of 64
+static_assert(kSoOffM1 + 2 * kSoImg <= kSoOffBar, "M^T buffer 1 inside the tile region");
+static_assert(kSoSmem <= 232448, "dynamic shared memory above the 227 KB per-block limit");
+enum : int { SO_SI = 0, SO_MI0 = 1, SO_MI1 = 2, SO_STEP = 3, SO_G0 = 4, SO_P0 = 7, SO_O0 = 9 };
 
-__global__ void __launch_bounds__(kCombineThreads) seg_combine_kernel(const ChunkParams p) {
-    griddep_wait();                              // phase 1's maps
-    const int h = blockIdx.x, n = blockIdx.y, slab = blockIdx.z;
+// This thread's 64 entries of column r = tid % 128 of a row-major 128 x 128
+// fp32 matrix, rows (tid / 128) * 64 ... + 63: coalesced across a warp.
+__device__ __forceinline__ void so_load_col(const float* src, int tid, float* v) {
+    const int r = tid & 127, k0 = (tid >> 7) * 64;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = src[size_t(k0 + i) * kD + r];
+}
+
+// Row r = tid % 128, columns (tid / 128) * 64 ... + 63 of a hi / lo image pair.
+__device__ __forceinline__ void so_store_row(uint8_t* img, int tid, const float* v) {
+    const int r = tid & 127, k0 = (tid >> 7) * 64;
+#pragma unroll
+    for (int c = 0; c < 64; c += 8) store_split8(img + toff(r, k0 + c, 16384), img + kSoImg + toff(r, k0 + c, 16384), v + c);
+}
+
+__global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
+    griddep_wait();                                  // phase 1's outputs, maps and S_1
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSoOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kSoOffBar + kSoNumBars * 8);
+    const int h = blockIdx.x, n = blockIdx.y, z = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int Hv = p.Hv;
+
     int64_t t_end_all = p.cu[p.B];
     if (t_end_all > p.t_cap) t_end_all = p.t_cap;
     int64_t t0 = p.cu[n], t1 = p.cu[n + 1];
     t0 = t0 < 0 ? 0 : (t0 > t_end_all ? t_end_all : t0);
     t1 = t1 < t0 ? t0 : (t1 > t_end_all ? t_end_all : t1);
     const int seq_chunks = int((t1 - t0 + p.chunk - 1) / p.chunk);
-    const int nseg = (seq_chunks + p.seg_chunks - 1) / p.seg_chunks;
-    if (nseg < 3) return;
-    const int64_t seg_tokens = int64_t(p.seg_chunks) * p.chunk;
-    float* base = p.seg_ws + (size_t(h) * p.seg_slots + seg_slot(p.cu[n], n, 0, seg_tokens)) * 3 * kD * kD;
-    extern __shared__ __align__(16) float smc[];
-    float* sS = smc + 2 * kCombineBuf;           // [kD][kCombineCols]; M_s^T, B_s in buffer s & 1 before it
-    float* sPart = sS + kCombineSlab;            // partial sums of the groups, [group][kD][kCombineCols]
-    const int tid = threadIdx.x, grp = tid >> 7, lt = tid & 127;
-    const int r0 = (lt & 31) * 4, c0 = (lt >> 5) * 4, k0 = grp * (kD / kCombineGroups);
-    const int col0 = slab * kCombineCols;
-    auto stage = [&](int s) {                    // M_s^T and B_s columns -> buffer s & 1
-        const float* msrc = base + size_t(s) * 3 * kD * kD + kD * kD;
-        float* dst = smc + (s & 1) * kCombineBuf;
-        for (int i = tid; i < kD * kD / 4; i += kCombineThreads) cp_async16(dst + 4 * i, msrc + 4 * i);
-        const float* bsrc = base + size_t(s) * 3 * kD * kD + col0;
-        float* bdst = dst + kD * kD;
-        for (int i = tid; i < kCombineSlab / 4; i += kCombineThreads) {
-            const int row = i / (kCombineCols / 4), c4 = (i % (kCombineCols / 4)) * 4;
-            cp_async16(bdst + row * kCombineCols + c4, bsrc + size_t(row) * kD + c4);
-        }
-        cp_async_commit();
+    const int L = p.seg_chunks;
+    const int nseg = (seq_chunks + L - 1) / L;
+    const int short_by = nseg * L - seq_chunks;
+    const int groups = p.seg_groups;
+    const bool final_role = p.seg_final_cta && z == (p.seg_max - 1) * groups;
+    const int s = final_role ? nseg - 1 : 1 + z / groups;   // steps: s - 1, or nseg - 1 for the final state
+    if (nseg < 2 || s >= nseg) return;
+    if (final_role && p.state_out == nullptr) return;
+    int c_lo = 0, c_hi = 0;                          // this CTA's chunks (output role)
+    if (!final_role) {
+        const int cb = s * L - short_by, g = z % groups;
+        c_lo = cb + (g * L) / groups;
+        c_hi = cb + ((g + 1) * L) / groups;
+        if (c_lo >= c_hi) return;
+    }
+    const int nsteps = final_role ? nseg - 1 : s - 1;
+    // the final state after the outputs, by the last group of the last segment
+    const bool final_after = !final_role && !p.seg_final_cta && p.state_out != nullptr && s == nseg - 1 &&
+                             z % groups == groups - 1;
+    const int nout = c_hi - c_lo;
+    const bool tiles_early = nsteps < 2;             // M^T buffer 1 (the tile region) never used
+    const int64_t seg_tokens = int64_t(L) * p.chunk;
+    const float* slots = p.seg_ws + (size_t(h) * p.seg_slots + seg_slot(p.cu[n], n, 0, seg_tokens)) * 3 * kD * kD;
+    auto slot_of = [&](int j) { return slots + size_t(j) * 3 * kD * kD; };   // B_j, M_j^T image, S_j image
+
+    if (tid == 0) {
+        for (int i = 0; i < int(kSoNumBars); ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kSoTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tD = tmem, tOb = tmem + 128;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;             // TMEM lane: the value column
+    const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    auto wait = [&](int b, uint32_t parity) { return mbar_wait(&bars[b], parity, kWaitLimit, kSuspendNs); };
+    auto chunk_start = [&](int c) { return t0 + int64_t(c) * p.chunk; };
+    // Thread 0 issues every copy; these count them so that a failed CTA can
+    // let the ones in flight land before it exits.
+    int mi_loads[2] = {0, 0}, mi_waits[2] = {0, 0};
+    int g_issued = 0, p_issued = 0;
+    bool si_issued = false;
+    auto load_image = [&](uint8_t* dst, const void* src, uint64_t* bar) {   // 64 KB, two copies
+        mbar_arrive_expect_tx(bar, 2 * kSoImg);
+        bulk_load(dst, src, kSoImg, bar);
+        bulk_load(dst + kSoImg, static_cast<const uint8_t*>(src) + kSoImg, kSoImg, bar);
     };
-    stage(1);
-    for (int i = tid; i < kCombineSlab / 4; i += kCombineThreads) {
-        const int k = i / (kCombineCols / 4), c4 = (i % (kCombineCols / 4)) * 4;
-        *reinterpret_cast<float4*>(sS + k * kCombineCols + c4) =
-            *reinterpret_cast<const float4*>(base + size_t(1) * 3 * kD * kD + 2 * kD * kD + size_t(k) * kD + col0 + c4);
+    auto load_m = [&](int j, int mb) {               // M_j^T image into buffer mb
+        load_image(sm + (mb ? kSoOffM1 : kSoOffM0), slot_of(j) + kD * kD, &bars[SO_MI0 + mb]);
+        ++mi_loads[mb];
+    };
+    auto issue_g = [&](int i) {                      // G tile of output chunk i
+        uint64_t* bar = &bars[SO_G0 + i % 3];
+        uint8_t* dst = sm + kSoOffG + uint32_t(i % 3) * 16384u;
+        const int y = int(chunk_start(c_lo + i));
+        mbar_arrive_expect_tx(bar, 16384);
+        tma_load_2d(dst, &maps.g, bar, h * kD, y);
+        tma_load_2d(dst + 8192, &maps.g, bar, h * kD + 64, y);
+        g_issued = i + 1;
+    };
+    auto issue_p = [&](int i) {                      // O' tile of output chunk i
+        uint64_t* bar = &bars[SO_P0 + (i & 1)];
+        uint8_t* dst = sm + kSoOffP + uint32_t(i & 1) * 16384u;
+        const int y = int(chunk_start(c_lo + i));
+        mbar_arrive_expect_tx(bar, 16384);
+        tma_load_2d(dst, &maps.o, bar, h * kD, y);
+        tma_load_2d(dst + 8192, &maps.o, bar, h * kD + 64, y);
+        p_issued = i + 1;
+    };
+    auto issue_tiles = [&]() {
+        for (int i = 0; i < nout && i < 3; ++i) issue_g(i);
+        for (int i = 0; i < nout && i < 2; ++i) issue_p(i);
+    };
+    if (tid == 0) {
+        load_image(sm + kSoOffS, slot_of(1) + 2 * kD * kD, &bars[SO_SI]);   // S_1^T
+        si_issued = true;
+        if (nsteps > 0 || final_after) load_m(1, 0);
+        if (nsteps > 1) load_m(2, 1);
+        if (tiles_early) issue_tiles();
+    } else if (tid == 32) {                          // the offsets B_j toward L2
+        const int last = final_after ? s : nsteps;
+        for (int j = 1; j <= last; ++j)
+            for (int q = 0; q < 2; ++q) bulk_prefetch_l2(slot_of(j) + q * 8192, 32768);
+    } else if (tid == 64) {                          // and the tiles of later chunks
+        for (int i = tiles_early ? 3 : 0; i < nout && i < 6; ++i) {
+            const int y = int(chunk_start(c_lo + i));
+            tma_prefetch_2d(&maps.g, h * kD, y);
+            tma_prefetch_2d(&maps.g, h * kD + 64, y);
+            tma_prefetch_2d(&maps.o, h * kD, y);
+            tma_prefetch_2d(&maps.o, h * kD + 64, y);
+        }
     }
-    for (int s = 1; s + 1 < nseg; ++s) {
-        if (s + 2 < nseg) {
-            stage(s + 1);
-            cp_async_wait_group<1>();
+    __syncwarp();
+    bool fail = false;
+    const uint64_t dS = smem_desc(smem_u32(sm + kSoOffS), 16, 1024, kSwizzle128B);
+    const uint32_t id_step = idesc_bf16(128, 128, 0, 1);      // B = M^T image, MN-major
+    // Step j with M_j^T in buffer mb: S_{j+1}^T = S^T M_j^T + B_j^T into the S
+    // images, or into state_out; M_{j+2}^T follows into the freed buffer when
+    // next_load.  False when a wait ran out.
+    auto step = [&](int j, int mb, bool to_state, bool next_load) {
+        bool lf = false;
+        if (tid == 0) {
+            lf = !wait(SO_MI0 + mb, uint32_t(mi_waits[mb] & 1));
+            ++mi_waits[mb];
+        }
+        fence_proxy_async_smem();                             // S images written: visible to the tensor core
+        tc_fence_before();
+        if (__syncthreads_or(lf)) return false;
+        if (tid == 0) {
+            tc_fence_after();
+            const uint64_t dM = smem_desc(smem_u32(sm + (mb ? kSoOffM1 : kSoOffM0)), 16384, 1024, kSwizzle128B);
+            // D = S^T M^T from (S hi, M hi), (S hi, M lo), (S lo, M hi)
+#pragma unroll
+            for (int pass = 0; pass < 3; ++pass)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    umma_f16(tD, dS + (pass == 2 ? uint64_t(kSoImg >> 4) : 0) + uint64_t(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                             dM + (pass == 1 ? uint64_t(kSoImg >> 4) : 0) + uint64_t((k * 2048) >> 4), id_step,
+                             pass > 0 || k > 0);
+            umma_commit(&bars[SO_STEP]);
+        }
+        __syncwarp();
+        // while the products run: B_j^T for this thread's TMEM lane and column half
+        float b[64];
+        so_load_col(slot_of(j), tid, b);                      // B_j [dk][dv]
+        lf = tid == 0 && !wait(SO_STEP, uint32_t((j - 1) & 1));
+        if (tid == 0 && !lf && next_load) load_m(j + 2, mb);
+        if (__syncthreads_or(lf)) return false;
+        tc_fence_after();
+        float d[64];
+        tmem_ld64(tD + lane_addr + uint32_t(half * 64), d);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) d[i] += b[i];
+        if (to_state) {                                       // S_n: the sequence's final state
+            float* dst = p.state_out + (size_t(n) * Hv + h) * kD * kD;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) dst[size_t(half * 64 + i) * kD + row] = d[i];
         } else {
-            cp_async_wait_group<0>();
+            so_store_row(sm + kSoOffS, tid, d);
         }
-        __syncthreads();
-        const float* mt = smc + (s & 1) * kCombineBuf;
-        float acc[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 8
-        for (int k = k0; k < k0 + kD / kCombineGroups; ++k) {
-            const float4 m = *reinterpret_cast<const float4*>(mt + k * kD + r0);       // M[r0..r0+3][k]
-            const float4 v = *reinterpret_cast<const float4*>(sS + k * kCombineCols + c0);
-            const float mr[4] = {m.x, m.y, m.z, m.w}, sv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(mr[i], sv[j], acc[i][j]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<float4*>(sPart + grp * kCombineSlab + (r0 + i) * kCombineCols + c0) =
-                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        __syncthreads();                         // partials written; every read of sS done
-        {
-            // one 16-byte word of the slab per thread: B + the groups' partials
-            const int o = tid * 4, row = o / kCombineCols, col = o % kCombineCols;
-            float4 r = *reinterpret_cast<const float4*>(mt + kD * kD + o);
-#pragma unroll
-            for (int g = 0; g < kCombineGroups; ++g) {
-                const float4 q = *reinterpret_cast<const float4*>(sPart + g * kCombineSlab + o);
-                r.x += q.x;
-                r.y += q.y;
-                r.z += q.z;
-                r.w += q.w;
-            }
-            *reinterpret_cast<float4*>(sS + o) = r;
-            *reinterpret_cast<float4*>(base + size_t(s + 1) * 3 * kD * kD + 2 * kD * kD + size_t(row) * kD +
-                                       col0 + col) = r;
-        }
-        __syncthreads();                         // buffer s & 1 fully read: it may be restaged
+        return true;
+    };
+
+    // ---- S_s (or the final state) from S_1 -----------------------------------------
+    {
+        const bool lf = tid == 0 && !wait(SO_SI, 0);
+        if (__syncthreads_or(lf)) fail = true;
     }
+    for (int j = 1; j <= nsteps && !fail; ++j)
+        fail = !step(j, (j - 1) & 1, final_role && j == nsteps, j + 2 <= nsteps);
+
+    // ---- outputs O = O' + G S_s, chunk by chunk ---------------------------------------
+    if (!final_role && !fail) {
+        if (tid == 0 && !tiles_early) issue_tiles();          // the steps have left the tile region
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        const uint32_t id_o = idesc_bf16(128, 64, 0, 0);      // B = G tile, K-major [t][d]
+        auto issue_out = [&](int i) {                         // thread 0: O^T (buffer i & 1) = S^T G^T
+            if (!wait(SO_G0 + i % 3, uint32_t((i / 3) & 1))) return false;
+            tc_fence_after();
+            const uint64_t dG = smem_desc(smem_u32(sm + kSoOffG + uint32_t(i % 3) * 16384u), 16, 1024, kSwizzle128B);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                umma_f16(tOb + uint32_t(i & 1) * 64, dS + uint64_t(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                         dG + uint64_t(((k >> 2) * 8192 + (k & 3) * 32) >> 4), id_o, k > 0);
+            umma_commit(&bars[SO_O0 + (i & 1)]);
+            return true;
+        };
+        bool lf = tid == 0 && !issue_out(0);
+        const int m = lane >> 3, rr = lane & 7;
+        for (int i = 0; i < nout; ++i) {
+            const int bi = i & 1;
+            uint8_t* ot = sm + kSoOffP + uint32_t(bi) * 16384u;   // O' tile, then the result
+            if (tid == 0 && !lf) {
+                // the next chunk's products go to the other TMEM buffer, read
+                // out before the previous barrier
+                if (i + 1 < nout) lf = !issue_out(i + 1);
+                if (!lf) lf = !wait(SO_O0 + bi, uint32_t((i >> 1) & 1));
+                if (!lf && i + 3 < nout) issue_g(i + 3);      // this chunk's G tile is read
+                if (!lf) lf = !wait(SO_P0 + bi, uint32_t((i >> 1) & 1));
+            }
+            if (__syncthreads_or(lf)) {
+                fail = true;
+                break;
+            }
+            tc_fence_after();
+            // this warp's TMEM lanes (value columns) and token half as 16x256b
+            // fragments; O' in the same fragments from its tile; the sum back
+            uint32_t r[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                tmem_ld_16x256b_x2(tOb + uint32_t(bi * 64) + (uint32_t(quarter * 32 + 16 * (u >> 1)) << 16) +
+                                       uint32_t(half * 32 + 16 * (u & 1)),
+                                   r[u]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int t = half * 32 + 16 * (u & 1) + 8 * (m >> 1) + rr;
+                const int jj = quarter * 32 + 16 * (u >> 1) + 8 * (m & 1);
+                const uint32_t addr = smem_u32(ot + toff(t, jj, 8192));
+                uint32_t o[4], f[4];
+                ldmatrix_x4_trans(addr, o);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    f[e] = pack_bf16x2(__uint_as_float(r[u][2 * e]) + __uint_as_float(o[e] << 16),
+                                       __uint_as_float(r[u][2 * e + 1]) + __uint_as_float(o[e] & 0xffff0000u));
+                stmatrix_x4_trans(addr, f);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            const int64_t cs = chunk_start(c_lo + i);
+            const int rows = int(t1 - cs < p.chunk ? t1 - cs : p.chunk);
+            if (rows == kC || cs + rows >= p.t_cap) {         // every row of the box is ours or past the buffers
+                if (tid == 0) {
+                    tma_store_2d(&maps.o, ot, h * kD, int(cs));
+                    tma_store_2d(&maps.o, ot + 8192, h * kD + 64, int(cs));
+                    bulk_commit_group();
+                }
+            } else {                                          // the chunk ends inside the buffers
+                __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(p.out);
+                for (int idx = tid; idx < kC * 16; idx += int(kSoThreads)) {
+                    const int rw = idx >> 4, col = (idx & 15) * 8;
+                    if (rw < rows)
+                        *reinterpret_cast<uint4*>(gout + ((cs + rw) * Hv + h) * kD + col) =
+                            *reinterpret_cast<const uint4*>(ot + toff(rw, col, 8192));
+                }
+            }
+            if (i + 2 < nout) {                               // refill once the tile is read
+                __syncthreads();
+                if (tid == 0) {
+                    bulk_wait_group_read<0>();
+                    issue_p(i + 2);
+                    if (i + 6 < nout) {                       // and bring a later chunk's tiles toward L2
+                        const int y = int(chunk_start(c_lo + i + 6));
+                        tma_prefetch_2d(&maps.g, h * kD, y);
+                        tma_prefetch_2d(&maps.g, h * kD + 64, y);
+                        tma_prefetch_2d(&maps.o, h * kD, y);
+                        tma_prefetch_2d(&maps.o, h * kD + 64, y);
+                    }
+                }
+            }
+        }
+        if (tid == 0) bulk_wait_all();                        // tile stores done before the CTA exits
+    }
+    // the final state here when no CTA of its own forms it: one more step from S_{n-1}
+    if (final_after && !fail) {
+        if (tid == 0 && nsteps > 0) load_m(s, 0);             // M_1 is still in buffer 0 otherwise
+        fail = !step(s, 0, true, false);
+    }
+
+    // ---- teardown ----------------------------------------------------------------
+    tc_fence_before();
+    __syncthreads();
+    if (fail && tid == 0) {
+        atomicAdd(&g_tc_timeouts, 1);
+        // copies still in flight land before shared memory goes away
+        if (si_issued) mbar_wait(&bars[SO_SI], 0, kWaitLimit, kSuspendNs);
+        for (int b = 0; b < 2; ++b)
+            if (mi_loads[b] > mi_waits[b])
+                mbar_wait(&bars[SO_MI0 + b], uint32_t((mi_loads[b] - 1) & 1), kWaitLimit, kSuspendNs);
+        for (int i = g_issued - 3 < 0 ? 0 : g_issued - 3; i < g_issued; ++i)
+            mbar_wait(&bars[SO_G0 + i % 3], uint32_t((i / 3) & 1), kWaitLimit, kSuspendNs);
+        for (int i = p_issued - 2 < 0 ? 0 : p_issued - 2; i < p_issued; ++i)
+            mbar_wait(&bars[SO_P0 + (i & 1)], uint32_t((i >> 1) & 1), kWaitLimit, kSuspendNs);
+        bulk_wait_all();
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kSoTmemCols);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -1790,7 +2047,10 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
         !make_map(&maps.k, p.k, int64_t(p.Hk) * kD, rows, p.k_stride) ||
         !make_map(&maps.v, p.v, int64_t(p.Hv) * kD, rows, p.v_stride))
         return cudaErrorInvalidValue;
-    if (p.prep_ws != nullptr && !make_map(&maps.o, p.out, int64_t(p.Hv) * kD, rows, int64_t(p.Hv) * kD))
+    const bool segmented = p.seg_chunks > 0 && p.seg_max >= 2;
+    if ((p.prep_ws != nullptr || segmented) && !make_map(&maps.o, p.out, int64_t(p.Hv) * kD, rows, int64_t(p.Hv) * kD))
+        return cudaErrorInvalidValue;
+    if (segmented && !make_map(&maps.g, p.g_out, int64_t(p.Hv) * kD, rows, int64_t(p.Hv) * kD))
         return cudaErrorInvalidValue;
     const bool split = p.prep_ws != nullptr && p.prep_slots > 0;
     const void* state_kernel = split ? reinterpret_cast<const void*>(chunk_tc_kernel<true>)
@@ -1815,7 +2075,7 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
         timer_end(s);
         if (e != cudaSuccess) return e;
     }
-    if (p.seg_chunks <= 0 || p.seg_max < 2) {
+    if (!segmented) {
         ChunkParams q = p;
         q.seg_phase = 0;
         timer_begin(s, "chunk_tc_kernel");
@@ -1824,23 +2084,16 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
         return e;
     }
     ChunkParams q = p;
-    q.seg_phase = 1;                                  // segment 0 in full; B_s and M_s
+    q.seg_phase = 1;                                  // segment 0 in full; O', B_s and G, M_s of the others
     timer_begin(s, "chunk_tc_kernel");
     e = launch_state(q, unsigned(2 * p.seg_max - 1));
     timer_end(s);
     if (e != cudaSuccess) return e;
-    if (p.seg_max >= 3) {                             // S_{s+1} = M_s S_s + B_s
-        if ((e = ensure_smem(reinterpret_cast<const void*>(seg_combine_kernel), int(kCombineSmem))) !=
-            cudaSuccess)
-            return e;
-        timer_begin(s, "seg_combine_kernel");
-        e = launch_pdl(seg_combine_kernel, dim3(p.Hv, p.B, kD / kCombineCols), kCombineThreads, kCombineSmem, s, q);
-        timer_end(s);
-        if (e != cudaSuccess) return e;
-    }
-    q.seg_phase = 2;                                  // segments >= 1 in full
-    timer_begin(s, "chunk_tc_kernel");
-    e = launch_state(q, unsigned(p.seg_max - 1));
+    if ((e = ensure_smem(reinterpret_cast<const void*>(seg_out_kernel), int(kSoSmem))) != cudaSuccess) return e;
+    timer_begin(s, "seg_out_kernel");                 // S_s, O = O' + G S_s, the final state
+    e = launch_pdl(seg_out_kernel,
+                   dim3(p.Hv, p.B, unsigned((p.seg_max - 1) * p.seg_groups + (p.seg_final_cta ? 1 : 0))), kSoThreads,
+                   kSoSmem, s, q, maps);
     timer_end(s);
     return e;
 }

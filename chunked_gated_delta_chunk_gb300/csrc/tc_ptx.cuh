@@ -112,6 +112,16 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// Hints that bring data toward L2 ahead of use; nothing waits on them.
+// The untiled form wants a 16-byte aligned address and a multiple of 16 bytes.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Tiled TMA store of a box from shared memory (bulk-group completion); the
 // writing threads must have made their shared-memory stores visible to the
 // async proxy (fence_proxy_async_smem) before a barrier that precedes this.
@@ -297,6 +307,15 @@ __device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, uint32_t* r) 
 __device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, const uint32_t* f) {
     asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(f[0]),
                  "r"(f[1]), "r"(f[2]), "r"(f[3])
+                 : "memory");
+}
+
+// The inverse of stmatrix_x4_trans: given the same lane addresses, f
+// receives the fragments that stmatrix_x4_trans would have stored there.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t saddr, uint32_t* f) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
+                 : "r"(saddr)
                  : "memory");
 }
 

@@ -257,3 +257,27 @@ def test_attn_rows_argument_checks(lib):
     assert call(o=A + 2) == B.GDN_ERR_ALIGN
     assert call(cap=1 << 30) == B.GDN_ERR_TOO_LARGE
     assert call(B=0, T=0) == B.GDN_OK
+
+
+def test_segmented_plan_and_workspace(lib):
+    """A 4096-token prompt over 16 value heads takes the segment-parallel
+    scan: five segments of 13 chunks (phase 1 on 16 x 9 CTAs, one wave of the
+    152 SMs), then seg_out_kernel.  Its workspace holds the segment maps (three
+    128 x 128 fp32 matrices per head and slot), the output map G (bf16, one row
+    of Hv x dv per token) and the chunk records."""
+    d = B.make_desc(B=1, Hk=16, Hv=16, dk=128, dv=128, T_total=4096, q=A, k=A, v=A, g=A, beta=A,
+                    out=A, cu_seqlens=A)
+    slots = 4096 // (13 * 64) + 1 + 1
+    maps = ((16 * slots * 3 * 128 * 128 * 4 + 255) // 256) * 256
+    g_map = 4096 * 16 * 128 * 2
+    records = 16 * (4096 // 64 + 1 + 1) * 82432
+    assert B.gdn_workspace_bytes(d) == maps + g_map + records
+    d.workspace, d.workspace_bytes = A, B.gdn_workspace_bytes(d)
+    assert B.gdn_prefill_plan(d) == ["chunk_prep_kernel", "chunk_tc_kernel", "seg_out_kernel"]
+    d.workspace_bytes = maps + g_map                 # no room for the records: inline preparation
+    assert B.gdn_prefill_plan(d) == ["chunk_tc_kernel", "seg_out_kernel"]
+    d.workspace_bytes = maps + g_map - 1             # no room for G either: one pass
+    assert B.gdn_prefill_plan(d) == ["chunk_tc_kernel"]
+    d.segment_chunks = -1                            # one pass asked for
+    d.workspace_bytes = 1 << 40
+    assert B.gdn_prefill_plan(d) == ["chunk_prep_kernel", "chunk_tc_kernel"]

@@ -240,17 +240,36 @@ def test_prefill_then_decode_equals_token_loop():
     (1, [300], 64), (2, [640], 64), (3, [64 * 7 + 5], 64), (4, [1, 200, 0, 900], 64),
     (2, [333, 64 * 6], 32), (5, [4096], 64)])
 def test_segment_scan_matches_oracle(seg, lengths, chunk):
-    """The segment-parallel scan (maps of every segment from a zero state and
-    from the identity, fp32 combine, then every segment from its start
-    state) equals the token loop; segments end on full and partial chunks."""
+    """The segment-parallel scan (every later segment from a zero state and
+    from the identity with V = 0, outputs and maps of both, then the
+    segments' incoming states and O = O' + G S_s) equals the token loop;
+    segments end on full and partial chunks."""
     p = inputs.make_problem(40 + seg, lengths, 2, 4, 128, 128, chunk=chunk)
     call = runner.PrefillCall(p, segment_chunks=seg)
     from chunked_gated_delta_chunk_gb300 import binding as B
     plan = B.gdn_prefill_plan(call.desc)
-    assert plan.count("chunk_tc_kernel") == 2, plan
+    assert plan[-2:] == ["chunk_tc_kernel", "seg_out_kernel"] and plan.count("chunk_tc_kernel") == 1, plan
     call.run()
     torch.cuda.synchronize()
     compare({k: v.cpu() for k, v in call.results().items()}, run_oracle(p), TOL_BF16)
+
+
+def test_segment_scan_long_groups_and_no_state_out():
+    """32 value heads leave seg_out_kernel one chunk group per segment, so a
+    CTA walks ten chunks through both tile buffers and refills them; a null
+    state_out skips the final-state CTA without touching the outputs."""
+    p = inputs.make_problem(53, [64 * 40 + 17, 64 * 9], 16, 32, 128, 128)
+    ref = run_oracle(p)
+    call = runner.PrefillCall(p, segment_chunks=10)
+    call.run()
+    torch.cuda.synchronize()
+    compare({k: v.cpu() for k, v in call.results().items()}, ref, TOL_BF16)
+    p.state_in = None
+    ref = run_oracle(p)
+    nostate = runner.PrefillCall(p, segment_chunks=10, write_state=False)
+    nostate.run()
+    torch.cuda.synchronize()
+    compare({"out": nostate.out.cpu()}, {"out": ref["out"]}, TOL_BF16)
 
 
 def test_segment_scan_with_conv_and_gqa():
