@@ -1676,12 +1676,12 @@ constexpr uint32_t kSoOffM1 = kSoOffTile;
 constexpr uint32_t kSoOffG = kSoOffTile;            // G tiles: three of 16 KB
 constexpr uint32_t kSoOffP = kSoOffTile + 3 * 16384;   // O' tiles: two of 16 KB
 constexpr uint32_t kSoOffBar = kSoOffTile + 5 * 16384;
-constexpr uint32_t kSoNumBars = 11;
+constexpr uint32_t kSoNumBars = 8;
 constexpr uint32_t kSoSmem = kSoOffBar + kSoNumBars * 8 + 16 + 1024;
 constexpr uint32_t kSoTmemCols = 256;               // step accumulator (128) | O^T, two buffers of 64
 static_assert(kSoOffM1 + 2 * kSoImg <= kSoOffBar, "M^T buffer 1 inside the tile region");
 static_assert(kSoSmem <= 232448, "dynamic shared memory above the 227 KB per-block limit");
-enum : int { SO_SI = 0, SO_MI0 = 1, SO_MI1 = 2, SO_STEP = 3, SO_G0 = 4, SO_P0 = 7, SO_O0 = 9 };
+enum : int { SO_STEP = 0, SO_G0 = 1, SO_P0 = 4, SO_O0 = 6 };
 
 // This thread's 64 entries of column r = tid % 128 of a row-major 128 x 128
 // fp32 matrix, rows (tid / 128) * 64 ... + 63: coalesced across a warp.
@@ -1758,27 +1758,25 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
     auto wait = [&](int b, uint32_t parity) { return mbar_wait(&bars[b], parity, kWaitLimit, kSuspendNs); };
     auto chunk_start = [&](int c) { return t0 + int64_t(c) * p.chunk; };
-    // Thread 0 issues every copy; these count them so that a failed CTA can
-    // let the ones in flight land before it exits.
-    int mi_loads[2] = {0, 0}, mi_waits[2] = {0, 0};
+    // The images (64 KB) arrive by cp.async from every thread, one commit
+    // group each.  Thread 0 issues the tile copies and counts them, so that a
+    // failed CTA can let the ones in flight land before it exits.
     int g_issued = 0, p_issued = 0;
-    bool si_issued = false;
-    auto load_image = [&](uint8_t* dst, const void* src, uint64_t* bar) {   // 64 KB, two copies
-        mbar_arrive_expect_tx(bar, 2 * kSoImg);
-        bulk_load(dst, src, kSoImg, bar);
-        bulk_load(dst + kSoImg, static_cast<const uint8_t*>(src) + kSoImg, kSoImg, bar);
+    auto load_image = [&](uint8_t* dst, const void* src) {
+        const uint8_t* src8 = static_cast<const uint8_t*>(src);
+        for (int i = tid; i < int(2 * kSoImg / 16); i += int(kSoThreads)) cp_async16(dst + i * 16, src8 + i * 16);
+        cp_async_commit();
     };
     auto load_m = [&](int j, int mb) {               // M_j^T image into buffer mb
-        load_image(sm + (mb ? kSoOffM1 : kSoOffM0), slot_of(j) + kD * kD, &bars[SO_MI0 + mb]);
-        ++mi_loads[mb];
+        load_image(sm + (mb ? kSoOffM1 : kSoOffM0), slot_of(j) + kD * kD);
     };
     auto issue_g = [&](int i) {                      // G tile of output chunk i
         uint64_t* bar = &bars[SO_G0 + i % 3];
         uint8_t* dst = sm + kSoOffG + uint32_t(i % 3) * 16384u;
         const int y = int(chunk_start(c_lo + i));
         mbar_arrive_expect_tx(bar, 16384);
-        tma_load_2d(dst, &maps.g, bar, h * kD, y);
-        tma_load_2d(dst + 8192, &maps.g, bar, h * kD + 64, y);
+        tma_load_2d_hint(dst, &maps.g, bar, h * kD, y, l2_evict_first());
+        tma_load_2d_hint(dst + 8192, &maps.g, bar, h * kD + 64, y, l2_evict_first());
         g_issued = i + 1;
     };
     auto issue_p = [&](int i) {                      // O' tile of output chunk i
@@ -1786,49 +1784,46 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
         uint8_t* dst = sm + kSoOffP + uint32_t(i & 1) * 16384u;
         const int y = int(chunk_start(c_lo + i));
         mbar_arrive_expect_tx(bar, 16384);
-        tma_load_2d(dst, &maps.o, bar, h * kD, y);
-        tma_load_2d(dst + 8192, &maps.o, bar, h * kD + 64, y);
+        tma_load_2d_hint(dst, &maps.o, bar, h * kD, y, l2_evict_first());
+        tma_load_2d_hint(dst + 8192, &maps.o, bar, h * kD + 64, y, l2_evict_first());
         p_issued = i + 1;
     };
     auto issue_tiles = [&]() {
         for (int i = 0; i < nout && i < 3; ++i) issue_g(i);
         for (int i = 0; i < nout && i < 2; ++i) issue_p(i);
     };
-    if (tid == 0) {
-        load_image(sm + kSoOffS, slot_of(1) + 2 * kD * kD, &bars[SO_SI]);   // S_1^T
-        si_issued = true;
-        if (nsteps > 0 || final_after) load_m(1, 0);
-        if (nsteps > 1) load_m(2, 1);
-        if (tiles_early) issue_tiles();
-    } else if (tid == 32) {                          // the offsets B_j toward L2
-        const int last = final_after ? s : nsteps;
-        for (int j = 1; j <= last; ++j)
-            for (int q = 0; q < 2; ++q) bulk_prefetch_l2(slot_of(j) + q * 8192, 32768);
-    } else if (tid == 64) {                          // and the tiles of later chunks
-        for (int i = tiles_early ? 3 : 0; i < nout && i < 6; ++i) {
+    load_image(sm + kSoOffS, slot_of(1) + 2 * kD * kD);  // S_1^T
+    if (nsteps > 0 || final_after) load_m(1, 0);
+    if (nsteps > 1) load_m(2, 1);
+    if (tid == 0 && tiles_early) issue_tiles();
+    // the tiles of later chunks toward L2: after the images (a CTA with state
+    // steps asks during its last step)
+    auto prefetch_tiles = [&](int from, int to) {
+        for (int i = from; i < nout && i < to; ++i) {
             const int y = int(chunk_start(c_lo + i));
             tma_prefetch_2d(&maps.g, h * kD, y);
             tma_prefetch_2d(&maps.g, h * kD + 64, y);
             tma_prefetch_2d(&maps.o, h * kD, y);
             tma_prefetch_2d(&maps.o, h * kD + 64, y);
         }
-    }
+    };
+    if (tid == 64 && tiles_early) prefetch_tiles(3, 6);
     __syncwarp();
     bool fail = false;
     const uint64_t dS = smem_desc(smem_u32(sm + kSoOffS), 16, 1024, kSwizzle128B);
     const uint32_t id_step = idesc_bf16(128, 128, 0, 1);      // B = M^T image, MN-major
     // Step j with M_j^T in buffer mb: S_{j+1}^T = S^T M_j^T + B_j^T into the S
     // images, or into state_out; M_{j+2}^T follows into the freed buffer when
-    // next_load.  False when a wait ran out.
-    auto step = [&](int j, int mb, bool to_state, bool next_load) {
-        bool lf = false;
-        if (tid == 0) {
-            lf = !wait(SO_MI0 + mb, uint32_t(mi_waits[mb] & 1));
-            ++mi_waits[mb];
-        }
-        fence_proxy_async_smem();                             // S images written: visible to the tensor core
+    // next_load.  one_more: the copy of M_{j+1} may still be in flight.
+    // False when a wait ran out.
+    auto step = [&](int j, int mb, bool to_state, bool next_load, bool one_more) {
+        if (one_more)
+            cp_async_wait_group<1>();
+        else
+            cp_async_wait_group<0>();
+        fence_proxy_async_smem();                             // images written: visible to the tensor core
         tc_fence_before();
-        if (__syncthreads_or(lf)) return false;
+        __syncthreads();
         if (tid == 0) {
             tc_fence_after();
             const uint64_t dM = smem_desc(smem_u32(sm + (mb ? kSoOffM1 : kSoOffM0)), 16384, 1024, kSwizzle128B);
@@ -1841,14 +1836,15 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
                              dM + (pass == 1 ? uint64_t(kSoImg >> 4) : 0) + uint64_t((k * 2048) >> 4), id_step,
                              pass > 0 || k > 0);
             umma_commit(&bars[SO_STEP]);
+            if (j == nsteps && !to_state) prefetch_tiles(0, 6);
         }
         __syncwarp();
         // while the products run: B_j^T for this thread's TMEM lane and column half
         float b[64];
         so_load_col(slot_of(j), tid, b);                      // B_j [dk][dv]
-        lf = tid == 0 && !wait(SO_STEP, uint32_t((j - 1) & 1));
-        if (tid == 0 && !lf && next_load) load_m(j + 2, mb);
+        const bool lf = tid == 0 && !wait(SO_STEP, uint32_t((j - 1) & 1));
         if (__syncthreads_or(lf)) return false;
+        if (next_load) load_m(j + 2, mb);
         tc_fence_after();
         float d[64];
         tmem_ld64(tD + lane_addr + uint32_t(half * 64), d);
@@ -1865,12 +1861,9 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     };
 
     // ---- S_s (or the final state) from S_1 -----------------------------------------
-    {
-        const bool lf = tid == 0 && !wait(SO_SI, 0);
-        if (__syncthreads_or(lf)) fail = true;
-    }
     for (int j = 1; j <= nsteps && !fail; ++j)
-        fail = !step(j, (j - 1) & 1, final_role && j == nsteps, j + 2 <= nsteps);
+        fail = !step(j, (j - 1) & 1, final_role && j == nsteps, j + 2 <= nsteps, j + 1 <= nsteps);
+    if (nsteps == 0) cp_async_wait_all();                     // S_1 (and M_1 for a final step)
 
     // ---- outputs O = O' + G S_s, chunk by chunk ---------------------------------------
     if (!final_role && !fail) {
@@ -1955,13 +1948,7 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
                 if (tid == 0) {
                     bulk_wait_group_read<0>();
                     issue_p(i + 2);
-                    if (i + 6 < nout) {                       // and bring a later chunk's tiles toward L2
-                        const int y = int(chunk_start(c_lo + i + 6));
-                        tma_prefetch_2d(&maps.g, h * kD, y);
-                        tma_prefetch_2d(&maps.g, h * kD + 64, y);
-                        tma_prefetch_2d(&maps.o, h * kD, y);
-                        tma_prefetch_2d(&maps.o, h * kD + 64, y);
-                    }
+                    prefetch_tiles(i + 6, i + 7);             // and a later chunk's tiles toward L2
                 }
             }
         }
@@ -1969,20 +1956,17 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     }
     // the final state here when no CTA of its own forms it: one more step from S_{n-1}
     if (final_after && !fail) {
-        if (tid == 0 && nsteps > 0) load_m(s, 0);             // M_1 is still in buffer 0 otherwise
-        fail = !step(s, 0, true, false);
+        if (nsteps > 0) load_m(s, 0);                         // M_1 is still in buffer 0 otherwise
+        fail = !step(s, 0, true, false, false);
     }
 
     // ---- teardown ----------------------------------------------------------------
+    cp_async_wait_all();
     tc_fence_before();
     __syncthreads();
     if (fail && tid == 0) {
         atomicAdd(&g_tc_timeouts, 1);
-        // copies still in flight land before shared memory goes away
-        if (si_issued) mbar_wait(&bars[SO_SI], 0, kWaitLimit, kSuspendNs);
-        for (int b = 0; b < 2; ++b)
-            if (mi_loads[b] > mi_waits[b])
-                mbar_wait(&bars[SO_MI0 + b], uint32_t((mi_loads[b] - 1) & 1), kWaitLimit, kSuspendNs);
+        // tile copies still in flight land before shared memory goes away
         for (int i = g_issued - 3 < 0 ? 0 : g_issued - 3; i < g_issued; ++i)
             mbar_wait(&bars[SO_G0 + i % 3], uint32_t((i / 3) & 1), kWaitLimit, kSuspendNs);
         for (int i = p_issued - 2 < 0 ? 0 : p_issued - 2; i < p_issued; ++i)

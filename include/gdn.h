@@ -117,10 +117,14 @@ typedef struct gdn_prefill_desc {
 
     /* Segment-parallel chunk scan (bf16, dk = dv = 128, T_total known, and a
      * workspace): each sequence is cut into segments of this many chunks that
-     * run in parallel (every segment's affine map from a zero state and from
-     * the identity, a short fp32 combine of the maps, then every segment from
-     * its true start state).  0 = chosen from the shape (on only when it
-     * gives at least three segments per sequence on 152 SMs), < 0 = off. */
+     * run in parallel.  Every later segment runs from a zero state (its
+     * outputs O' and end state B_s) and from the identity with V = 0 (its
+     * output map G and transition M_s); one more pass forms each segment's
+     * incoming state S_s (S_{s+1} = M_s S_s + B_s) and its outputs
+     * O = O' + G S_s on the tensor cores.  The workspace then also holds the
+     * maps (3 x 64 KiB per value head and segment slot) and G (bf16, like
+     * out).  0 = chosen from the shape by a cost model of the passes on 152
+     * SMs (one pass when that is cheaper), < 0 = off. */
     int segment_chunks;
 
     /* Split preparation (bf16, dk = dv = 128, T_total known, and a
@@ -159,11 +163,12 @@ int gdn_prefill_ex(const gdn_prefill_desc* d, gdn_stream_t stream);
 
 /* Device workspace gdn_prefill_ex uses for *d, in bytes (0 if none), laid
  * out in this order: the output of the short convolution, the per-segment
- * maps of the segment-parallel scan when that is chosen, the chunk records of
+ * maps and the output map G of the segment-parallel scan when that is
+ * chosen, the chunk records of
  * the split preparation when that is on.  Reads only dtype, B, Hk, Hv, dk,
  * dv, chunk, T_total, segment_chunks, split_prep and whether conv_x is set;
  * returns (size_t)-1 when those are invalid.  Only the convolution's part is
- * required: a workspace too small for the segment maps runs the scan in one
+ * required: a workspace too small for the maps and G runs the scan in one
  * pass, one too small for the records solves each chunk inside the state
  * pass (same results either way). */
 size_t gdn_workspace_bytes(const gdn_prefill_desc* d);
