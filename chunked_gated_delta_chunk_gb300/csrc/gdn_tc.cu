@@ -824,8 +824,8 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         mode = (blockIdx.z & 1) ? kModeOffset : kModeTransition;
     }
     // Segments of seg_chunks chunks; when they do not divide the sequence,
-    // segment 0 is the short one: in phase 1 it is the only full pass, which
-    // costs more per chunk than the map passes beside it.
+    // segment 0 is the short one (the later segments' chunk ranges then
+    // depend only on the sequence's chunk count and L).
     int c_begin = 0, c_end = seq_chunks;
     if (p.seg_phase) {
         const int L = p.seg_chunks;
@@ -842,7 +842,6 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     // Every pass writes its outputs: the full pass the final ones, the offset
     // pass those from a zero incoming state (to the output, completed by
     // seg_out_kernel), the transition pass the output map G.
-    const bool write_out = true;
     const CUtensorMap* omap = mode == kModeTransition ? &maps.g : &maps.o;
     float* slot = nullptr;                              // B, M, S of this segment
     float* next_slot = nullptr;                         // of the next segment
@@ -992,12 +991,10 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 if (!lf) {
                     uint64_t* bar = &bars[B_RAW0 + b];
                     s_tma_last[b] = c;
-                    mbar_arrive_expect_tx(bar, 16384u + (write_out ? 32768u : 0u) + (tk ? 16384u : 0u));
+                    mbar_arrive_expect_tx(bar, 16384u + 32768u + (tk ? 16384u : 0u));
                     bulk_load(sm + (b ? kOffTb : kOffWt), rec + kRecWt, 16384, bar);
-                    if (write_out) {                 // P follows once its buffer is free (below)
-                        bulk_load(kq + 8192, rec + kRecQ, 8192, bar);
-                        bulk_load(kq + 24576, rec + kRecQ + 8192, 8192, bar);
-                    }
+                    bulk_load(kq + 8192, rec + kRecQ, 8192, bar);   // P follows once its buffer is free (below)
+                    bulk_load(kq + 24576, rec + kRecQ + 8192, 8192, bar);
                     if (tk) {
                         const int y = int(chunk_start(c));
                         tma_load_2d(kq + 0, &maps.k, bar, kh * kD, y);
@@ -1020,8 +1017,8 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             }
             if (pt < kC) cE[b * kC + pt] = reinterpret_cast<const float*>(rec + kRecVec)[pt];
             if (pt == kC) cGS[b] = reinterpret_cast<const float*>(rec + kRecVec)[kC];
-            if (write_out && c >= 1 && tid == 0) lf = !issue_oq(c - 1);
-            if (write_out && tid == 0 && !lf) {
+            if (c >= 1 && tid == 0) lf = !issue_oq(c - 1);
+            if (tid == 0 && !lf) {
                 // the chain frees P of chunk c - 2 once that chunk's outputs are complete
                 if (c >= 2) lf = !wait(B_PFREE0 + b, uint32_t(((c - 2) >> 1) & 1));
                 if (!lf) bulk_load(sm + kOffP + uint32_t(b * 2) * 8192u, rec + kRecP, 16384, &bars[B_RAW0 + b]);
@@ -1040,11 +1037,11 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             tc_fence_before();
             if (named_sync_or(kBarPrep, kLoadThreads, lf)) { fail = true; break; }
             if (tid == 0) mbar_arrive(&bars[B_READY0 + b]);
-            if (write_out && c >= 1 && tid == 0) lf = !issue_op(c - 1);
+            if (c >= 1 && tid == 0) lf = !issue_op(c - 1);
             __syncwarp();
             if (named_sync_or(kBarPrep, kLoadThreads, lf)) { fail = true; break; }
         }
-        if (!fail && write_out && nchunks > 0 && tid == 0)   // the last chunk's outputs
+        if (!fail && nchunks > 0 && tid == 0)   // the last chunk's outputs
             fail = !issue_oq(nchunks - 1) || !issue_op(nchunks - 1);
         __syncwarp();
         if (fail) *s_err = 1;
@@ -1155,14 +1152,12 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 const int isq = r >= kC, tr = r & 63;
                 const uint8_t* base = kq + (isq ? 8192 : 0);
                 float ss = 0.f;
-                if (write_out || !isq) {                   // q is not used by the map passes
 #pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        float v[8];
-                        load_chunk8(base + toff(tr, part * 64 + m * 8, 16384), v);
+                for (int m = 0; m < 8; ++m) {
+                    float v[8];
+                    load_chunk8(base + toff(tr, part * 64 + m * 8, 16384), v);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
-                    }
+                    for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
                 }
                 ss += __shfl_xor_sync(0xffffffffu, ss, 1);
                 if (part == 0) (isq ? vRq : vRk)[tr] = p.l2norm ? rsqrtf(ss + p.eps) : 1.f;
@@ -1202,7 +1197,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                         // each store phase hit disjoint banks
                         *reinterpret_cast<float4*>(sA + i * kLdA + phalf * 32 + q) = make_float4(a4[0], a4[1], a4[2], a4[3]);
                     }
-                } else if (write_out) {
+                } else {
                     const int t = row - kC;
                     const float rt = vRq[t], gt = vGam[t];
 #pragma unroll
@@ -1264,7 +1259,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 }
             }
             // ---- while U0/W run: scaled Q rows in place; chain scalars ----------
-            for (int idx = pt; write_out && idx < kC * 16; idx += kPrepThreads) {
+            for (int idx = pt; idx < kC * 16; idx += kPrepThreads) {
                 const int r = idx >> 4, cc = (idx & 15) * 8;
                 uint8_t* ptr = kq + 8192 + toff(r, cc, 16384);
                 const float f = r < rows ? vEg[r] * vRq[r] : 0.f;
@@ -1444,7 +1439,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                         umma_f16_tmemA(tX, tZb + s * 8, dWt + uint64_t(s * 2048 >> 4), id_x,
                                        mode != kModeTransition || s > 0);
                     umma_commit(&bars[B_X]);
-                    if (write_out && !split) {        // map passes: no outputs; split: the O issuer
+                    if (!split) {                     // with records the loader lead issues these
                         const uint64_t dQ = smem_desc(smem_u32(kq + 8192), 16, 1024, kSwizzle128B);
 #pragma unroll
                         for (int s = 0; s < 8; ++s) {
@@ -1459,7 +1454,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             // its O^T, once complete, is staged here and written after the
             // next barrier; its P buffer is free then)
             bool o_staged = false;
-            if (kSplit && c > 0 && write_out) {
+            if (kSplit && c > 0) {
                 if (lead && !lf) {
                     lf = !wait(B_O, uint32_t((c - 1) & 1));
                     if (!lf) mbar_arrive(&bars[B_PFREE0 + ((c - 1) & 1)]);
@@ -1520,7 +1515,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                         umma_f16_tmemA(tZ, tU + 64 + part * 32 + s * 8, dK + uint64_t(s * 2048 >> 4), id_z, 1);
                 umma_commit(&bars[B_Z]);
                 if (split) mbar_arrive(&bars[B_ZISS]);
-                if (write_out && !split) {
+                if (!split) {
                     // (U hi, P hi), (U hi, P lo), (U lo, P hi)
 #pragma unroll
                     for (int pr = 0; pr < 3; ++pr)
@@ -1537,7 +1532,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             if (lead) {
                 lf = !wait(B_Z, uint32_t(c & 1));
                 // the O issuer's Zb Qs^T must be done before Zb and the stage are reused
-                if (!lf && split && write_out) lf = !wait(B_OQ, uint32_t(c & 1));
+                if (!lf && split) lf = !wait(B_OQ, uint32_t(c & 1));
                 if (!lf) {
                     mbar_arrive(&bars[B_SFREE0 + b]);
                     if (!split && c + 2 < nchunks && tma_ok(c + 2)) issue_tma(c + 2);
@@ -1576,7 +1571,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             }
             tmem_st_wait();
             // ---- output rows to registers (stored during the next chunk) --------
-            if (write_out && !kSplit) {
+            if (!kSplit) {
                 if (lead) lf = !wait(B_O, uint32_t(c & 1));
                 __syncwarp();
                 if (named_sync_or(kBarChain, kChainN, lf)) { fail = true; break; }
@@ -1592,14 +1587,14 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 }
             }
             o_cs = cs;
-            o_rows = write_out ? rows : 0;
+            o_rows = rows;
             tc_fence_before();
             named_sync(kBarChain, kChainN);
             if (lead && !kSplit) mbar_arrive(&bars[B_PFREE0 + b]);   // with records: at the next chunk
             __syncwarp();
         }
         if (kSplit) {
-            if (!fail && write_out && nchunks > 0) {     // the last chunk's outputs
+            if (!fail && nchunks > 0) {                  // the last chunk's outputs
                 bool lf = lead && !wait(B_O, uint32_t((nchunks - 1) & 1));
                 if (lead) bulk_wait_group_read<1>();
                 __syncwarp();
