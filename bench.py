@@ -354,6 +354,51 @@ def timed_steps(calls, steps, stream, barrier, launches_per_call=0, clocks=None)
     return start.elapsed_time(stop), records, dropped
 
 
+def e2e_steps_ms(bufs, host_in, host_out, steps, barrier, dev):
+    """End to end through host buffers: every step copies its inputs from
+    pinned host memory into device set i % len(bufs) (an upload stream), runs
+    the library call on that set (a compute stream) and copies its outputs
+    back into pinned host memory (a download stream), so the upload of step
+    i + 1 and the download of step i - 1 overlap the kernels of step i.
+    Events order every reuse of a device set: its inputs are overwritten only
+    after the call that read them, its outputs only after their download.
+    Returns ms per step from the first timed upload to the last download."""
+    import torch
+    up, comp, down = (torch.cuda.Stream(dev) for _ in range(3))
+    nb = len(bufs)
+    comp_done, down_done = [None] * nb, [None] * nb
+    e0 = e1 = None
+    for it in range(steps + 2):                       # two untimed steps first
+        b = it % nb
+        if it == 2:
+            barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(up)
+        if comp_done[b] is not None:
+            up.wait_event(comp_done[b])
+        with torch.cuda.stream(up):
+            for n, t in host_in.items():
+                getattr(bufs[b], n).copy_(t, non_blocking=True)
+        landed = torch.cuda.Event()
+        landed.record(up)
+        comp.wait_event(landed)
+        if down_done[b] is not None:
+            comp.wait_event(down_done[b])
+        bufs[b].run(comp)
+        comp_done[b] = torch.cuda.Event()
+        comp_done[b].record(comp)
+        down.wait_event(comp_done[b])
+        with torch.cuda.stream(down):
+            for n, t in host_out.items():
+                t.copy_(getattr(bufs[b], n), non_blocking=True)
+        down_done[b] = torch.cuda.Event()
+        down_done[b].record(down)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e1.record(down)
+    barrier()
+    return e0.elapsed_time(e1) / steps
+
+
 def run_row(args, rank, world):
     """A row recurrence of the hot-path table's next rows (the selective-scan
     rows, the RWKV-4 WKV rows): one library call over its workload per step."""
@@ -447,20 +492,8 @@ def run_row(args, rank, world):
     host_out = {n: torch.empty_like(getattr(one, n), device="cpu").pin_memory() for n in spec.outputs}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-    e2e_steps = max(3, min(args.steps, 20))
-    for it in range(e2e_steps + 2):
-        if it == 2:
-            barrier()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        for n, t in host_in.items():
-            getattr(one, n).copy_(t, non_blocking=True)
-        one.run(stream)
-        for n, t in host_out.items():
-            t.copy_(getattr(one, n), non_blocking=True)
-    e1.record(stream)
-    barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_bufs = calls[:2] if len(calls) >= 2 else [one, spec.make_call(p, dev)]
+    e2e_ms = e2e_steps_ms(e2e_bufs, host_in, host_out, max(3, min(args.steps, 20)), barrier, dev)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -574,28 +607,16 @@ def main():
     tokens_per_s = world * p.T / (ms_step * 1e-3)
 
     # End to end through the C ABI with host buffers: pinned H2D of the step's
-    # inputs, the call, D2H of out and state_out, every step.
+    # inputs, the call, D2H of out and state_out, every step (pipelined over
+    # two device sets, see e2e_steps_ms).
     host_in = {name: getattr(one, name).cpu().pin_memory() for name in
                ("q", "k", "v", "x", "g", "beta", "state_in") if getattr(one, name) is not None}
     host_out = {name: torch.empty(getattr(one, name).shape, dtype=getattr(one, name).dtype).pin_memory()
                 for name in ("out", "state_out")}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-    e2e_steps = max(3, min(args.steps, 50))
-    for it in range(e2e_steps + 2):
-        if it == 2:
-            barrier()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        for name, t in host_in.items():
-            getattr(one, name).copy_(t, non_blocking=True)
-        one.run(stream)
-        for name, t in host_out.items():
-            t.copy_(getattr(one, name), non_blocking=True)
-    e1.record(stream)
-    barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_bufs = calls[:2] if len(calls) >= 2 else [one, runner.PrefillCall(p, dev)]
+    e2e_ms = e2e_steps_ms(e2e_bufs, host_in, host_out, max(3, min(args.steps, 50)), barrier, dev)
     if world > 1:
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
