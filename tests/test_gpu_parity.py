@@ -26,6 +26,17 @@ def _built():
     build_mod.build()
 
 
+@pytest.fixture(autouse=True)
+def _no_wait_ran_out():
+    """Every bounded wait of the tensor-core kernels (mbarriers, the segment
+    passes) must have been met: the device counter of waits that ran out
+    stays where it was."""
+    from chunked_gated_delta_chunk_gb300 import binding as B
+    before = B.gdn_wait_timeouts()
+    yield
+    assert B.gdn_wait_timeouts() == before
+
+
 def _gpu(p, **kw):
     return runner.prefill(p, **kw)
 
@@ -238,7 +249,7 @@ def test_prefill_then_decode_equals_token_loop():
 # ---------------------------------------------------------------- segment scan
 @pytest.mark.parametrize("seg,lengths,chunk", [
     (1, [300], 64), (2, [640], 64), (3, [64 * 7 + 5], 64), (4, [1, 200, 0, 900], 64),
-    (2, [333, 64 * 6], 32), (5, [4096], 64)])
+    (2, [333, 64 * 6], 32), (5, [4096], 64), (4, [64 * 7], 64)])
 def test_segment_scan_matches_oracle(seg, lengths, chunk):
     """The segment-parallel scan (every later segment from a zero state and
     from the identity with V = 0, outputs and maps of both, then the
@@ -270,6 +281,19 @@ def test_segment_scan_long_groups_and_no_state_out():
     nostate.run()
     torch.cuda.synchronize()
     compare({"out": nostate.out.cpu()}, {"out": ref["out"]}, TOL_BF16)
+
+
+def test_segment_scan_final_state_after_outputs_of_one_later_segment():
+    """96 (sequence, head) units leave no room for final-state CTAs of their
+    own, so the single output CTA of each two-segment sequence forms the final
+    state after its outputs, from the images it loaded at its start (no state
+    step before its outputs)."""
+    p = inputs.make_problem(54, [64 * 8, 64 * 7 + 3, 50], 16, 32, 128, 128)
+    ref = run_oracle(p)
+    call = runner.PrefillCall(p, segment_chunks=4)
+    call.run()
+    torch.cuda.synchronize()
+    compare({k: v.cpu() for k, v in call.results().items()}, ref, TOL_BF16)
 
 
 def test_segment_scan_with_conv_and_gqa():
