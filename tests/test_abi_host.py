@@ -281,3 +281,7 @@ def test_segmented_plan_and_workspace(lib):
     d.segment_chunks = -1                            # one pass asked for
     d.workspace_bytes = 1 << 40
     assert B.gdn_prefill_plan(d) == ["chunk_prep_kernel", "chunk_tc_kernel"]
+    d.split_prep = 1                                 # the look-ahead state pass
+    assert B.gdn_prefill_plan(d) == ["chunk_prep_kernel", "chunk_la_kernel"]
+    d.workspace_bytes = 0                            # no records: the inline pass
+    assert B.gdn_prefill_plan(d) == ["chunk_tc_kernel"]

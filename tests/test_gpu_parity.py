@@ -372,3 +372,22 @@ def test_launch_timer_records_every_planned_launch():
     assert all(ms > 0 for _, ms in records)
     torch.cuda.synchronize()
     compare({k: v.cpu() for k, v in call.results().items()}, run_oracle(p), TOL_BF16)
+
+
+# ---------------------------------------------------------------- look-ahead state pass
+@pytest.mark.parametrize("seg,lengths,chunk", [
+    (-1, [50], 64), (-1, [64 * 7 - 5], 64), (-1, [1, 200, 0, 700], 64), (3, [64 * 13 + 9, 300], 64),
+    (2, [333, 64 * 6], 32), (0, [4096], 64)])
+def test_lookahead_state_pass_matches_oracle(seg, lengths, chunk):
+    """The look-ahead state pass (split_prep = 1: the next chunk's X formed
+    from the current state and the correction R_c = K_c (-W_{c+1}^T), the
+    state update off the dependent chain) equals the token loop, in one pass,
+    with ragged and empty sequences, chunks below 64 rows and the segment
+    scan's three pass kinds."""
+    from chunked_gated_delta_chunk_gb300 import binding as B
+    p = inputs.make_problem(90 + len(lengths) + chunk, lengths, 2, 4, 128, 128, chunk=chunk)
+    call = runner.PrefillCall(p, segment_chunks=seg, split_prep=1)
+    assert "chunk_la_kernel" in B.gdn_prefill_plan(call.desc)
+    call.run()
+    torch.cuda.synchronize()
+    compare({k: v.cpu() for k, v in call.results().items()}, run_oracle(p), TOL_BF16)
