@@ -50,7 +50,7 @@ def _close(a, b, rtol=RTOL):
 
 
 # --------------------------------------------------------------------------
-# Brute force: the token loop against the spec matrix recurrence
+# Brute force: the token loop against the matrix recurrence as the pages state it
 #   S_t = exp(g_t)(I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T, o_t = S_t^T q_t
 # written as dense matrix products (a different formulation of the step).
 # Pins: decay placement, the sign and beta placement of the delta update, and
