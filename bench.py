@@ -211,8 +211,9 @@ def _prefix(p, S):
 def run_reference(args, rank, world):
     """The float64 oracle as it stands, on the host cores, on the same
     workload; each step is a prefix of the prompt sized so that all steps
-    together take about two minutes (tokens/s is then tokens of the prefix
-    over its time: the oracle's cost is linear in tokens)."""
+    together take about --reference-seconds (two minutes by default; tokens/s
+    is then tokens of the prefix over its time: the oracle's cost is linear in
+    tokens)."""
     if rank != 0:
         return
     import oracle
@@ -227,7 +228,7 @@ def run_reference(args, rank, world):
         t0 = time.perf_counter()
         run(_prefix(p, probe))
         per_token = (time.perf_counter() - t0) / probe
-        S = int(min(p.T, max(64, 120.0 / max(args.steps, 1) / max(per_token, 1e-9))))
+        S = int(min(p.T, max(64, args.reference_seconds / max(args.steps, 1) / max(per_token, 1e-9))))
         sample = _prefix(p, S)
         what = f"first {S} of {p.T} tokens, all heads, per step"
     else:
@@ -354,6 +355,18 @@ def timed_steps(calls, steps, stream, barrier, launches_per_call=0, clocks=None)
     return start.elapsed_time(stop), records, dropped
 
 
+def max_over_ranks(value, dev):
+    """The largest of every rank's value (the job's time is its slowest
+    rank's); the value itself outside a process group of more than one."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() < 2:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def e2e_steps_ms(bufs, host_in, host_out, steps, barrier, dev):
     """End to end through host buffers: every step copies its inputs from
     pinned host memory into device set i % len(bufs) (an upload stream), runs
@@ -463,10 +476,7 @@ def run_row(args, rank, world):
     for name, ms in records:
         tot, n = per_kernel.get(name, (0.0, 0))
         per_kernel[name] = (tot + ms, n + 1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
     dominant = max(per_kernel, key=lambda k: per_kernel[k][0])
     kern_ms = per_kernel[dominant][0] / per_kernel[dominant][1]
@@ -539,6 +549,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-seconds", type=float, default=120.0,
+                    help="host seconds the reference arm spends over all its steps (it sizes its sample to them)")
     ap.add_argument("--row", default="gdn", choices=["gdn", "scan", "wkv", "attn"],
                     help="gdn: the chunked gated delta rule prefill (the headline); "
                          "scan: the selective-scan rows; wkv: the RWKV-4 WKV rows; "
@@ -599,10 +611,7 @@ def main():
     for name, ms in records:
         tot, n = per_kernel.get(name, (0.0, 0))
         per_kernel[name] = (tot + ms, n + 1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
     tokens_per_s = world * p.T / (ms_step * 1e-3)
 
@@ -617,10 +626,7 @@ def main():
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     e2e_bufs = calls[:2] if len(calls) >= 2 else [one, runner.PrefillCall(p, dev)]
     e2e_ms = e2e_steps_ms(e2e_bufs, host_in, host_out, max(3, min(args.steps, 50)), barrier, dev)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     hbm, tflops, peak_kind = load_peaks()
     bytes_alg = algorithmic_bytes(p)
