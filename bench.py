@@ -27,6 +27,7 @@ import argparse
 import contextlib
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -36,7 +37,28 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-L2_BYTES = 129 * 1024 * 1024
+L2_FALLBACK_BYTES = 129 * 1024 * 1024   # GB300 L2, used only when the device cannot be queried
+L2_NOTE = "rotating independent buffer sets: each timed step touches buffers last used more than 2 x L2 bytes earlier"
+
+
+def l2_bytes(dev=None):
+    """The device's L2 size (cudaDevAttrL2CacheSize through torch)."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            n = int(torch.cuda.get_device_properties(dev if dev is not None else 0).L2_cache_size)
+            if n > 0:
+                return n
+    except (AttributeError, RuntimeError, AssertionError):
+        pass
+    return L2_FALLBACK_BYTES
+
+
+def config_dict(workload, p, world):
+    """The `config` object of both arms' JSON lines (identical for the same
+    workload and launch)."""
+    return {"workload": workload, "global_batch": p.B, "seq_len": p.T,
+            "parallelism": "replicas" if world > 1 else "single", "l2": L2_NOTE}
 WORKLOADS = {
     2: "prompt4k: B=1, Hk=Hv=16, dk=dv=128, T=4096, chunk 64, bf16 q/k/v/out, fp32 g/beta/state",
     4: "stress: B=2 x 1024 tokens, H=8, dk=dv=128, chunk 64, bf16, nearly parallel keys",
@@ -161,23 +183,37 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_oracle_tokens_per_s(p, budget_s=12.0):
-    """The float64 oracle, as it stands, on the host cores: whole workload
-    passes repeated until ``budget_s`` of wall time (at least one)."""
+def cpu_oracle_tokens_per_s(p, budget_s=12.0, nthreads=0):
+    """The float64 oracle, as it stands, on the host cores (``nthreads`` = 0:
+    all of them): whole-workload passes repeated until ``budget_s`` of wall
+    time, or, for a single prompt whose one pass would take longer than the
+    budget, a prefix of the prompt sized to it (the oracle's cost is linear in
+    tokens).  Returns (tokens/s, threads used, what was timed)."""
     import oracle
     oracle.build_oracle()
-    cores = oracle.max_threads()
-    done, tokens, t0 = 0, 0, time.perf_counter()
+    cores = oracle.max_threads() if nthreads <= 0 else nthreads
+    run = lambda q: oracle.oracle_prefill(q.q, q.k, q.v, q.g, q.beta, q.cu_seqlens, q.Hk, q.Hv, q.dk, q.dv,
+                                          state_in=q.state_in, conv=q.conv, use_l2norm=q.use_l2norm,
+                                          q_scale=q.q_scale, nthreads=nthreads)
+    sample, S = p, p.T
+    if p.B == 1:
+        probe = min(256, p.T)
+        t0 = time.perf_counter()
+        run(_prefix(p, probe))
+        per_token = (time.perf_counter() - t0) / probe
+        if per_token * p.T > budget_s:
+            S = int(max(64, budget_s / 2 / max(per_token, 1e-12)))
+            sample = _prefix(p, S)
+    done, t0 = 0, time.perf_counter()
     while True:
-        oracle.oracle_prefill(p.q, p.k, p.v, p.g, p.beta, p.cu_seqlens, p.Hk, p.Hv, p.dk, p.dv,
-                              state_in=p.state_in, conv=p.conv, use_l2norm=p.use_l2norm,
-                              q_scale=p.q_scale)
+        run(sample)
         done += 1
-        tokens += p.T
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return tokens / el, cores, f"{done} full passes of the workload ({p.T} tokens each) in {el:.1f} s"
+    what = (f"{done} full passes of the workload ({p.T} tokens each) in {el:.1f} s" if S == p.T else
+            f"{done} passes over the first {S} of {p.T} tokens, all heads, in {el:.1f} s")
+    return S * done / el, cores, what
 
 
 def make_workload(cfg):
@@ -244,8 +280,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": WORKLOADS[args.config], "global_batch": p.B, "seq_len": p.T,
-                       "parallelism": "replicas"},
+            "config": config_dict(WORKLOADS[args.config], p, world),
             "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": what},
             "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -355,6 +390,22 @@ def timed_steps(calls, steps, stream, barrier, launches_per_call=0, clocks=None)
     return start.elapsed_time(stop), records, dropped
 
 
+def timed_blocks(calls, steps, stream, barrier, dev, min_seconds, clocks):
+    """The K-step timed region of ``timed_steps``, repeated back to back until
+    about ``min_seconds`` have passed (the same repeat count on every rank:
+    the first block's time, max over ranks, sizes it), so that the clock
+    sampler sees the GPU under load.  Returns the per-block times in ms."""
+    first, _, _ = timed_steps(calls, steps, stream, barrier)
+    first = max_over_ranks(first, dev)
+    reps = max(1, min(200000, int(math.ceil(min_seconds * 1e3 / max(first, 1e-6)))))
+    blocks = []
+    with clocks:
+        for _ in range(reps):
+            ms, _, _ = timed_steps(calls, steps, stream, barrier)
+            blocks.append(ms)
+    return blocks
+
+
 def max_over_ranks(value, dev):
     """The largest of every rank's value (the job's time is its slowest
     rank's); the value itself outside a process group of more than one."""
@@ -438,8 +489,7 @@ def run_row(args, rank, world):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "impl": "reference",
-                "config": {"workload": spec.workload, "global_batch": p.B, "seq_len": p.T,
-                           "parallelism": "replicas"},
+                "config": config_dict(spec.workload, p, world),
                 "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": oracle.max_threads(),
                                  "kind": "oracle",
                                  "sample": (f"the first {cols} of {p.T} rows, all heads, per step"
@@ -457,7 +507,7 @@ def run_row(args, rank, world):
     build_mod.build()
     one = spec.make_call(p, dev)
     set_bytes = spec.nbytes
-    nsets = max(1, min(8, -(-2 * L2_BYTES // max(set_bytes, 1)) + 1))
+    nsets = max(1, min(8, -(-2 * l2_bytes(dev) // max(set_bytes, 1)) + 1))
     calls = [one] + [spec.make_call(p, dev) for _ in range(nsets - 1)]
     stream = torch.cuda.current_stream(dev)
     for i in range(args.warmup):
@@ -470,7 +520,8 @@ def run_row(args, rank, world):
         torch.cuda.synchronize(dev)
 
     clk = ClockSampler(local)
-    ms_total, _, _ = timed_steps(calls, args.steps, stream, barrier, clocks=clk)
+    blocks = timed_blocks(calls, args.steps, stream, barrier, dev, args.min_seconds, clk)
+    ms_total = statistics.median(blocks)
     ms_timer, records, dropped = timed_steps(calls, args.steps, stream, barrier, launches_per_call=2)
     per_kernel = {}
     for name, ms in records:
@@ -527,14 +578,14 @@ def run_row(args, rank, world):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if args.row == "attn" else "f32",
                 "data": "synthetic",
-                "config": {"workload": spec.workload, "global_batch": p.B, "seq_len": p.T,
-                           "parallelism": "replicas" if world > 1 else "single",
-                           "l2": (f"rotating {nsets} independent buffer sets "
-                                  f"({nsets * set_bytes / 2**20:.0f} MiB > 2 x L2)")},
+                "config": config_dict(spec.workload, p, world),
+                "l2_rotation": f"{nsets} independent buffer sets ({nsets * set_bytes / 2**20:.0f} MiB > 2 x L2)",
+                "timed_blocks": {"blocks": len(blocks), "steps_per_block": args.steps,
+                                 "seconds": sum(blocks) / 1e3, "statistic": "median block"},
                 "roofline": roof,
                 "e2e": {"value": world * p.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-                "gpu_launches": 2 * args.steps, "clocks": clk.summary(), "cpu_baseline": cpu}
+                "gpu_launches": 2 * args.steps * len(blocks), "clocks": clk.summary(), "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -549,6 +600,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-seconds", type=float, default=2.0,
+                    help="repeat the K-step timed block back to back for about this long (clocks sampled throughout)")
     ap.add_argument("--reference-seconds", type=float, default=120.0,
                     help="host seconds the reference arm spends over all its steps (it sizes its sample to them)")
     ap.add_argument("--row", default="gdn", choices=["gdn", "scan", "wkv", "attn"],
@@ -586,7 +639,7 @@ def main():
     set_bytes = sum(t.numel() * t.element_size() for t in
                     (one.q, one.k, one.v, one.x, one.g, one.beta, one.state_in, one.out,
                      one.state_out, one.workspace) if t is not None)
-    nsets = max(1, min(16, -(-2 * L2_BYTES // max(set_bytes, 1)) + 1))
+    nsets = max(1, min(16, -(-2 * l2_bytes(dev) // max(set_bytes, 1)) + 1))
     calls = [one] + [runner.PrefillCall(p, dev) for _ in range(nsets - 1)]
     stream = torch.cuda.current_stream(dev)
 
@@ -600,11 +653,14 @@ def main():
         torch.cuda.synchronize(dev)
 
     launches_per_call = len(B.gdn_prefill_plan(one.desc))
-    # value: K steps with nothing between the library's launches; then K more
-    # steps with the library bracketing each launch with CUDA events on the
-    # launch stream: the per-kernel device times
+    # value: blocks of K steps with nothing between the library's launches,
+    # repeated for about --min-seconds with the clocks sampled throughout (the
+    # median block is the figure); then K more steps with the library
+    # bracketing each launch with CUDA events on the launch stream: the
+    # per-kernel device times
     clk = ClockSampler(local)
-    ms_total, _, _ = timed_steps(calls, args.steps, stream, barrier, clocks=clk)
+    blocks = timed_blocks(calls, args.steps, stream, barrier, dev, args.min_seconds, clk)
+    ms_total = statistics.median(blocks)
     ms_timer, records, dropped = timed_steps(calls, args.steps, stream, barrier,
                                              launches_per_call=launches_per_call)
     per_kernel = {}
@@ -647,6 +703,15 @@ def main():
         achieved = flops_alg / (kern_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
                 "frac": achieved / tflops}
+    # the whole call against the path roofline (the slower of the algorithmic
+    # FLOPs at the bf16 peak and the algorithmic bytes at the HBM peak)
+    t_roof = max(t_bytes, t_flops)
+    roof["path_frac"] = t_roof / (ms_step * 1e-3)
+    roof["path_roofline_ms"] = t_roof * 1e3
+    roof["path_achieved"] = (bytes_alg / (ms_step * 1e-3) / 1e9 if bound == "hbm"
+                             else flops_alg / (ms_step * 1e-3) / 1e12)
+    roof["frac_of"] = ("frac: the dominant kernel's device time per step; path_frac: the whole call's "
+                       "time per step (ms_per_step)")
     roof["traffic"] = recorded_traffic(dominant, WORKLOADS[args.config])
     roof["kernel_ms_per_step"] = kern_ms
     roof["launches_per_step"] = per_kernel[dominant][1] / args.steps
@@ -661,10 +726,32 @@ def main():
     roof["algorithmic_bytes"] = bytes_alg
     roof["algorithmic_flops"] = flops_alg
 
+    # the spec entry point (gdn_prefill: no workspace, so no chunk
+    # records or segment maps) on the same inputs, where it applies (no conv)
+    plain = None
+    if p.conv is None:
+        B.gdn_prefill(one.q, one.k, one.v, one.g, one.beta, one.state_in, one.state_out, one.out, one.cu,
+                      p.B, p.Hk, p.Hv, p.dk, p.dv, 64)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, min(args.steps, 50))
+        barrier()
+        e0.record(stream)
+        for i in range(reps):
+            c = calls[i % nsets]
+            B.gdn_prefill(c.q, c.k, c.v, c.g, c.beta, c.state_in, c.state_out, c.out, c.cu,
+                          p.B, p.Hk, p.Hv, p.dk, p.dv, 64)
+        e1.record(stream)
+        barrier()
+        plain = {"ms_per_call": e0.elapsed_time(e1) / reps, "calls": reps,
+                 "note": "gdn_prefill has no workspace argument, so it runs the plan that needs none"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, cores, sample = cpu_oracle_tokens_per_s(p)
-        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+        tps1, _, sample1 = cpu_oracle_tokens_per_s(p, budget_s=10.0, nthreads=1)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+               "one_thread": {"value": tps1, "unit": "tokens/s", "cores": 1, "sample": sample1}}
 
     if rank == 0:
         line = {
@@ -672,16 +759,17 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOADS[args.config], "global_batch": p.B, "seq_len": p.T,
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": f"rotating {nsets} independent buffer sets "
-                             f"({nsets * set_bytes / 2**20:.0f} MiB > 2 x L2)"},
+            "config": config_dict(WORKLOADS[args.config], p, world),
+            "l2_rotation": f"{nsets} independent buffer sets ({nsets * set_bytes / 2**20:.0f} MiB > 2 x L2)",
+            "timed_blocks": {"blocks": len(blocks), "steps_per_block": args.steps,
+                             "seconds": sum(blocks) / 1e3, "statistic": "median block"},
             "roofline": roof,
             "e2e": {"value": world * p.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_call * args.steps,
+            "gpu_launches": launches_per_call * args.steps * len(blocks),
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
+            "gdn_prefill_entry": plain,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

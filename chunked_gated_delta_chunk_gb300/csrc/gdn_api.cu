@@ -1,6 +1,7 @@
 // C ABI of libgdn.so (declared in include/gdn.h): argument validation, launch
 // planning and status codes.  Every check runs before the first enqueue, so a
 // rejected call enqueues nothing; nothing here allocates or synchronises.
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -60,7 +61,27 @@ size_t conv_workspace(const gdn_prefill_desc* d) {
     return (bytes + 255) & ~size_t(255);
 }
 
-constexpr int kSMs = 152;   // GB300: 2 dies x 76 SMs
+// Streaming multiprocessors of the current device (cudaDevAttrMultiProcessorCount,
+// looked up once per device); 152, a GB300's count, where no device answers
+// (host-only planning, as in gdn_workspace_bytes on a machine without a GPU).
+int sm_count() {
+    constexpr int kFallback = 152;
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return kFallback;
+    }
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return kFallback;
+    }
+    cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
 
 // Chunk groups per segment in seg_out_kernel: as many as let its CTAs (one
 // per group of every segment s >= 1, plus one for the final state, per
@@ -70,7 +91,7 @@ constexpr int kSMs = 152;   // GB300: 2 dies x 76 SMs
 int segment_groups(int64_t units, int64_t seg_max, int seg_chunks, int* final_cta) {
     *final_cta = 1;
     if (seg_max < 2) return 1;
-    const int64_t per_unit = kSMs / units;       // CTAs per (sequence, value head) in one wave
+    const int64_t per_unit = sm_count() / units;   // CTAs per (sequence, value head) in one wave
     int64_t g = (per_unit - 1) / (seg_max - 1);
     if (g < 1) {
         *final_cta = 0;
@@ -84,12 +105,12 @@ int segment_groups(int64_t units, int64_t seg_max, int seg_chunks, int* final_ct
 // Chunks per segment of the segment-parallel scan, or 0 for one pass.
 // Cost model in chunk periods of one CTA (one CTA per SM): with n segments of
 // L = ceil(chunks / n) chunks, phase 1 runs (2n - 1) CTAs per (sequence,
-// value head), each taking L + kStartPeriods periods per wave of kSMs CTAs
+// value head), each taking L + kStartPeriods periods per wave of one CTA per SM
 // (a CTA's first chunks run with cold instruction caches and its incoming
 // state still on the way); seg_out_kernel then takes about one period per
 // state step (n - 1 of them) plus kOutPeriods per output chunk of a group,
 // per wave of its CTAs.  One pass costs chunks + kStartPeriods periods in
-// ceil(units / kSMs) waves.  The cheapest n wins; sequence lengths are taken
+// ceil(units / SMs) waves.  The cheapest n wins; sequence lengths are taken
 // as the batch average.
 int segment_chunks(const gdn_prefill_desc* d) {
     if (d->dtype != GDN_BF16 || d->dk != 128 || d->dv != 128) return 0;   // tensor-core path only
@@ -99,7 +120,8 @@ int segment_chunks(const gdn_prefill_desc* d) {
     constexpr double kStartPeriods = 3.0, kStepPeriods = 1.0, kOutPeriods = 0.25;
     const int64_t units = int64_t(d->Hv) * d->B;
     const int64_t per_seq = (chunks + d->B - 1) / d->B;
-    auto waves = [&](int64_t ctas) { return (ctas + kSMs - 1) / kSMs; };
+    const int64_t sms = sm_count();
+    auto waves = [&](int64_t ctas) { return (ctas + sms - 1) / sms; };
     double best = double(waves(units)) * (double(per_seq) + kStartPeriods);
     int best_len = 0;
     for (int64_t n = 2; n <= 64 && n <= per_seq; ++n) {

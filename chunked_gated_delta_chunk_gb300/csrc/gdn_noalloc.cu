@@ -7,16 +7,20 @@
 // device and break a latency budget.  This entry point uses a fixed scratch
 // array that is part of the library itself instead.
 //
-// The array is a file-scope __device__ variable, so every GPU that loads the
-// library keeps kNoAllocScratchBytes of device memory reserved until the
-// process exits.  Its device address is looked up once per device, on the
-// first call made with that device current (cudaGetSymbolAddress; this
-// allocates nothing).  That first call should therefore happen before any
-// stream capture.  All calls share the one array: calls whose work overlaps
+// The array is a file-scope __device__ variable of kNoAllocScratchBytes.  With
+// the CUDA runtime's default lazy module loading, its device memory is
+// reserved when this file's module is first loaded on a device, which the
+// first call on that device does (cudaGetSymbolAddress, made once per device
+// with that device current, loads the module and returns the address); it then
+// stays reserved until the process exits.  That first call should therefore
+// come at initialisation: before the caller's own pool takes the device's
+// memory (else the lookup fails for lack of memory and the call returns
+// GDN_ERR_CUDA) and before any stream capture.  Later calls on that device
+// allocate nothing.  All calls share the one array: calls whose work overlaps
 // on the GPU (different streams, or several host threads) race on it and
 // must be serialised by the caller.  Nothing in the array has to start at
-// zero: the convolution writes every element the chunk kernels read before
-// they read it.
+// zero: every kernel writes each scratch element it reads (the convolution's
+// output, the chunk records, the segment maps) before reading it.
 #include <mutex>
 
 #include "gdn_common.cuh"
@@ -56,10 +60,10 @@ size_t gdn_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 int gdn_prefill_noalloc(const gdn_prefill_desc* d, gdn_stream_t stream) {
     if (d == nullptr) return GDN_ERR_INVALID_ARG;
-    if (d->conv_x == nullptr) return gdn_prefill_ex(d, stream);   // no scratch needed
     if (gdn_workspace_bytes(d) == size_t(-1)) return gdn_prefill_ex(d, stream);   // let it report the error
-    // Only the convolution's output must fit; the segment maps and chunk
-    // records are used when they fit as well.
+    // Only the convolution's output must fit; the chunk records and the
+    // segment maps are used when they fit as well (gdn_prefill_ex takes the
+    // faster plans only when the workspace holds them).
     if (gdn::prefill_required_workspace(d) > kNoAllocScratchBytes) return GDN_ERR_TOO_LARGE;
     void* scratch = nullptr;
     const cudaError_t e = scratch_for_current_device(&scratch);

@@ -209,17 +209,22 @@ int gdn_prefill_plan(const gdn_prefill_desc* d, const char** names, int max_name
  * allocation can synchronise the device.  This entry point takes the same
  * description as gdn_prefill_ex (inputs and outputs still come from the
  * caller) but ignores d->workspace and uses a fixed scratch array inside the
- * library, gdn_noalloc_scratch_bytes() = 32 MiB, which every GPU that loads
- * the library keeps reserved until the process exits.  It allocates nothing.
- *   - A description whose workspace would exceed that size is rejected with
- *     GDN_ERR_TOO_LARGE (for the conv workspace: T_total * C * element size).
- *   - The first call on a device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress); make that first call
- *     before any stream capture.  GDN_ERR_CUDA if the lookup fails.
+ * library, gdn_noalloc_scratch_bytes() = 32 MiB, for the convolution's output
+ * and, when they fit beside it, the chunk records and segment maps that make
+ * a call faster (larger calls run the slower one-pass plan).  It allocates
+ * nothing itself.
+ *   - A description whose required workspace (the conv output: T_total * C *
+ *     element size) exceeds the array is rejected with GDN_ERR_TOO_LARGE.
+ *   - The array's device memory is reserved when the library's module that
+ *     holds it is loaded on a device: with the CUDA runtime's default lazy
+ *     module loading that is the first call on that device, which also looks
+ *     up the array's address (cudaGetSymbolAddress, device current).  Make
+ *     that first call at initialisation, before the caller's own pool takes
+ *     the device's memory (else GDN_ERR_CUDA) and before any stream capture;
+ *     later calls reserve nothing more.  The memory stays reserved until the
+ *     process exits.
  *   - Every call shares the one array: calls whose work overlaps on the GPU
  *     (other streams, other host threads) race on it; serialise them.
- *   - Without a convolution no scratch is needed and the call is exactly
- *     gdn_prefill_ex.
  */
 int gdn_prefill_noalloc(const gdn_prefill_desc* d, gdn_stream_t stream);
 

@@ -124,3 +124,49 @@ def compare(gpu: dict, ref: dict, tol: float, heads=None):
         # the new conv state is a copy of input columns: bit-exact
         errs["conv_state_out"] = assert_close(cs, ref["conv_state_out"], 0.0, "conv_state_out")
     return errs
+
+
+def assert_all_finite(gpu: dict):
+    """Every element of every returned tensor is finite (checked on the whole
+    tensors, before any head selection)."""
+    for name, t in gpu.items():
+        assert torch.isfinite(t.float()).all(), f"{name}: non-finite values"
+
+
+def compare_all_heads(gpu: dict, p, tol: float, batch: int = 8, **oracle_kw):
+    """Compare every value head of ``gpu`` with the oracle, running the oracle
+    over batches of ``batch`` heads to bound host memory.  The error of each
+    tensor is its largest deviation over all heads divided by its largest
+    oracle magnitude over all heads (the same per-tensor measure as
+    ``compare``, taken over the whole tensor); the conv state is compared bit
+    for bit on every channel."""
+    assert_all_finite(gpu)
+    err = {"out": 0.0, "state_out": 0.0}
+    scale = {"out": 0.0, "state_out": 0.0}
+    seen_channels = set()
+    for h0 in range(0, p.Hv, batch):
+        heads = list(range(h0, min(p.Hv, h0 + batch)))
+        ref = run_oracle(p, heads=heads, **oracle_kw)
+        pairs = [("out", gpu["out"][:, heads], ref["out"])]
+        if "state_out" in gpu:
+            pairs.append(("state_out", gpu["state_out"][:, heads], ref["state_out"]))
+        for name, g, r in pairs:
+            g, r = _np(g), _np(r)
+            assert g.shape == r.shape, (name, g.shape, r.shape)
+            if r.size:
+                err[name] = max(err[name], float(np.abs(g - r).max()))
+                scale[name] = max(scale[name], float(np.abs(r).max()))
+        if "conv_state_out" in gpu and "conv_state_out" in ref:
+            ch = ref["channels"]
+            assert_close(gpu["conv_state_out"][:, ch], ref["conv_state_out"], 0.0, "conv_state_out")
+            seen_channels.update(ch)
+    if "conv_state_out" in gpu and p.conv is not None:
+        assert len(seen_channels) == gpu["conv_state_out"].shape[1], "conv state: channels not all compared"
+    out = {}
+    for name in err:
+        if name == "state_out" and "state_out" not in gpu:
+            continue
+        e = err[name] / scale[name] if scale[name] > 0 else err[name]
+        assert e <= tol, f"{name}: max|gpu - oracle| / max|oracle| = {e:.3e} > {tol:.1e} (all heads)"
+        out[name] = e
+    return out
