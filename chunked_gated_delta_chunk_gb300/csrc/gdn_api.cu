@@ -263,7 +263,6 @@ int gdn_prefill_ex(const gdn_prefill_desc* d, gdn_stream_t stream) {
             d->workspace_bytes >= conv_bytes + seg_bytes + prep_bytes) {
             p.prep_ws = static_cast<uint8_t*>(d->workspace) + conv_bytes + seg_bytes;
             p.prep_slots = prep_slots(d);
-            p.lookahead = d->split_prep > 0;
         }
     }
 
@@ -402,7 +401,7 @@ int gdn_prefill_plan(const gdn_prefill_desc* d, const char** names, int max_name
     const bool records = prep_bytes > 0 && d->workspace != nullptr &&
                          d->workspace_bytes >= conv_workspace(d) + segment_workspace(d, sc) + prep_bytes;
     if (records) plan[n++] = "chunk_prep_kernel";
-    plan[n++] = !tc ? "chunk_simt_kernel" : (records && d->split_prep > 0 ? "chunk_la_kernel" : gdn::kTcKernelName);
+    plan[n++] = !tc ? "chunk_simt_kernel" : (records ? "chunk_state_kernel" : gdn::kTcKernelName);
     if (sc > 0 && d->workspace != nullptr &&
         d->workspace_bytes >= conv_workspace(d) + segment_workspace(d, sc)) {
         const int64_t seg_tokens = int64_t(sc) * d->chunk;

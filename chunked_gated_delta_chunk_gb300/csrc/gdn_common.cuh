@@ -63,7 +63,6 @@ struct ChunkParams {
     // first token.
     uint8_t* prep_ws;
     int64_t prep_slots;      // slots per value head
-    int lookahead;           // with records: the look-ahead state pass (chunk_la_kernel)
 };
 
 // Selective-scan rows (h_t = a_t h_{t-1} + b_t per channel).  a, b, h_rows

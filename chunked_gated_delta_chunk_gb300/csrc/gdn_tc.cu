@@ -372,17 +372,18 @@ struct Maps {
 // intra-chunk output weights P and the scaled queries) is solved by
 // chunk_prep_kernel for all chunks at once, one CTA per (chunk slot, value
 // head), two CTAs per SM.  It stores one record per chunk:
-//   -W^T   [128][64] bf16 image in the 128-byte-swizzled layout the chain MMA
-//          reads from shared memory,
+//   -W     the two 64-column blocks of -W [64 rows i][128 columns d], bf16,
+//          K-major in the 128-byte-swizzled layout the state MMA reads from
+//          shared memory,
 //   P      hi and lo images [64][64] bf16 (same layout),
 //   Qs     the two 64-column blocks of diag(Gamma r_q) Q, same layout,
 //   U0^T   the TMEM fragments of the 256 preparing threads, 32 fp32 each,
 //          stored in 16-byte groups interleaved across a warp's lanes, so that
-//          the thread with the same role reads them back coalesced,
+//          a thread of the state pass reads its lane's columns coalesced,
 //   vec    end weights e_i = exp(min(gamma_S - gamma_i, 0)) r_k,i and
 //          exp(gamma_S).
-// The state kernel then streams the records (bulk copies and one TMEM store
-// of U0^T per chunk) instead of solving them.
+// The state kernel (chunk_state_kernel) then streams the records instead of
+// solving them.
 constexpr uint32_t kRecWt = 0;
 constexpr uint32_t kRecP = 16384;
 constexpr uint32_t kRecQ = 32768;
@@ -731,12 +732,29 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             }
         }
         {
+            // -W, K-major ([64 rows i][128 columns d], two 64-column blocks):
+            // W^T (lane d, column i) read as MMA-ordered fragments and stored
+            // transposed
+            uint32_t r[4][8];
+            const int quarter = pw & 3;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                tmem_ld_16x256b_x2(tGW + (uint32_t(quarter * 32 + 16 * (u >> 1)) << 16) +
+                                       uint32_t(phalf * 32 + 16 * (u & 1)),
+                                   r[u]);
+            tmem_ld_wait();
+            const int m = lane >> 3, rr = lane & 7;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                uint32_t f[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    f[e] = pack_bf16x2(-__uint_as_float(r[u][2 * e]), -__uint_as_float(r[u][2 * e + 1]));
+                const int i = phalf * 32 + 16 * (u & 1) + 8 * (m >> 1) + rr;
+                const int d = quarter * 32 + 16 * (u >> 1) + 8 * (m & 1);
+                stmatrix_x4_trans(smem_u32(sm + kPOffT + toff(i, d, 8192)), f);
+            }
             float v[32];
-            tmem_ld32(tGW + lane_addr + phalf * 32, v);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = -v[q];
-#pragma unroll
-            for (int q = 0; q < 32; q += 8) store_chunk8(sm + kPOffT + toff(row, phalf * 32 + q, 16384), v + q);
             tmem_ld32(tX + lane_addr + phalf * 32, v);
             float4* u = reinterpret_cast<float4*>(sm + kPOffTb) + pw * 8 * 32 + lane;
 #pragma unroll
@@ -1637,85 +1655,54 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ---- look-ahead state pass (chunk records) -----------------------------------------
-// The chain of chunk_tc_kernel<true> runs X MMA -> U epilogue -> Z MMA -> Z
-// epilogue -> next X MMA, one after the other.  Since
-//   Z_{c+1} = e^{gamma_S,c} Z_c + Us_c^T K_c,
-// the next chunk's X_{c+1} = U0_{c+1}^T - Z_{c+1} W_{c+1}^T splits into
-//   X_{c+1} = U0_{c+1}^T + Zb_c (-e^{gamma_S,c} W_{c+1}^T) + Us_c^T R_c,
-//   R_c = K_c (-W_{c+1}^T)   (64 x 64, independent of the state),
-// whose first product needs only Z_c, known a chunk early, and whose second is
-// one K = 64 product on the chunk's own Us.  The Z update and its epilogue so
-// leave the dependent chain, which becomes U epilogue -> Us R product -> U
-// epilogue.  Roles (384 threads):
-//   warps 0-3  loader: records into rings (W image, R, vectors: three deep; K,
-//              Qs, P: two deep), U0^T into the X accumulator, R_c by warp
-//              MMAs from K_c and the unscaled W_{c+1} image, then the W image
-//              scaled by e^{gamma_S} of the chunk before;
-//   warps 4-7  U group: the U epilogue (one TMEM lane each, all 64 columns);
-//              its lead issues Us_c^T R_c into the next X accumulator;
-//   warps 8-11 Z group: the Z epilogue (Zb, the pre-scaled Z, the final
-//              state), the output tile; its lead issues every other MMA
-//              (Zb W^T, Z update, Zb Qs^T, U^T P^T).
-// TMEM: Z (128) | Zb (64) | X0, X1 (2 x 64) | U hi, U lo, Us hi, Us lo (4 x 32) | O (64).
-constexpr uint32_t kLaThreads = 384;
-constexpr uint32_t kLaColZ = 0, kLaColZb = 128, kLaColX = 192, kLaColU = 320, kLaColO = 448;
-constexpr uint32_t kLaKS = 49152;                        // K | Qs set: K b0, Qs b0, K b1, Qs b1 (8 KB each)
-constexpr uint32_t kLaOffW = 2 * kLaKS;                  // W^T images, ring of three (16 KB each)
-constexpr uint32_t kLaOffR = kLaOffW + 3 * 16384;        // R images, ring of three (8 KB each)
-constexpr uint32_t kLaOffP = kLaOffR + 3 * 8192;         // P hi | lo, two sets (16 KB each)
-constexpr uint32_t kLaOffO = kLaOffP + 2 * 16384;        // output staging (16 KB)
-constexpr uint32_t kLaOffVec = kLaOffO + 16384;          // vectors, ring of three 512-byte record copies
-constexpr uint32_t kLaOffBar = kLaOffVec + 2048;
-enum : int {
-    LA_XD0 = 0,        // X accumulator b complete (two arrivals: Zb W^T and Us R)
-    LA_XREAD0 = 2,     // (unused)
-    LA_U0S0 = 4,       // U0^T of the chunk stored into X accumulator b
-    LA_UDONE = 6,      // U epilogue of the chunk done
-    LA_ZOD = 7,        // Z update and outputs of the chunk done (and every earlier Z-lead MMA)
-    LA_KP0 = 8,        // Qs, P of set b landed
-    LA_W0 = 10,        // W image and vectors of ring slot r landed
-    LA_RR0 = 13,       // R of ring slot r ready
-    LA_WS0 = 16,       // W image of ring slot r scaled (and its vectors loaded)
-    LA_RFREE0 = 19,    // ring slot r free again (U epilogue and Z epilogue of its chunk done)
-    LA_FREE0 = 22,     // set b's Qs, P read by the chunk's MMAs
-    LA_KR0 = 24,       // K tile of K slot r landed
-    LA_KFREE0 = 27,    // K slot r read by its chunk's Z update
-    LA_NBARS = 30
-};
-constexpr uint32_t kLaSmemBytes = kLaOffBar + LA_NBARS * 8 + 64 + 1024;   // + TMEM slot, error flag, s_last[8]
-static_assert(kLaSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-block limit");
-constexpr uint32_t kBarL = 1, kBarU = 2, kBarZ = 3;      // named barriers of the three groups
+// ---- state pass over the chunk records --------------------------------------------
+// With the records of chunk_prep_kernel a CTA per (value head, sequence,
+// segment pass) carries the transposed state Z = S^T through its chunks.  Per
+// chunk c (rows i, value columns j):
+//   [X | O] = Zb [-W^T | Qs^T]          one N = 128 product, A = Zb from TMEM
+//   U^T = U0^T + X,  Us^T = U^T diag(e)  bf16 hi + lo into TMEM
+//   Z += Us^T K                          Z pre-scaled by exp(gamma_S)
+//   O += U^T P^T                         (U hi, P hi), (U hi, P lo), (U lo, P hi)
+//   Zb = bf16(Z), Z <- exp(gamma_S(c+1)) Z
+// Sixteen warps share every epilogue: four per TMEM lane quarter, each a
+// quarter of the columns, so no thread walks more than 32 columns.  The lead
+// thread issues every MMA and streams the records' MMA operands (the -W | Qs
+// tile, P, K) and U0^T into two slots, a chunk ahead; the end weights e and
+// exp(gamma_S) go from the record to the threads' registers.  The output
+// products of a chunk are issued right behind its state update, so they run
+// while the state epilogue works, and the output tile is stored during the
+// next chunk.
+constexpr uint32_t kStThreads = 512;
+constexpr uint32_t kStChainThreads = kStThreads;
+constexpr uint32_t kBarSt = 1;                           // named barrier of the chain warps
+// Shared memory: two slots of [-W | Qs tile (32 KB) | P hi, lo (16 KB) | K (16 KB) |
+// U0^T fragments (32 KB)], then two output staging tiles (16 KB each).
+constexpr uint32_t kStSlot = 98304;
+constexpr uint32_t kStOffP = 32768, kStOffK = 49152, kStOffU = 65536;
+constexpr uint32_t kStOffO = 2 * kStSlot;
+constexpr uint32_t kStOffBar = kStOffO + 2 * 16384;
+enum : int { ST_FULL0 = 0, ST_X = 2, ST_Z = 3, ST_O = 4, ST_DRAIN = 5, ST_NBARS = 6 };
+constexpr uint32_t kStSmemBytes = kStOffBar + ST_NBARS * 8 + 16 + 1024;
+static_assert(kStSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-block limit");
+// TMEM: Z (128) | Zb (64) | O odd (64) | X (64) | O even (64) | U hi, U lo, Us hi, Us lo (4 x 32).
+// [X | O even] and [O odd | X] are the two N = 128 accumulators of the merged product.
+constexpr uint32_t kStColZ = 0, kStColZb = 128, kStColOodd = 192, kStColX = 256, kStColOeven = 320,
+                   kStColU = 384;
 
-// d += a b for one m16n8k16 warp MMA, bf16 operands, fp32 accumulators.
-__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, const uint32_t* b) {
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-__device__ __forceinline__ void ldmatrix_x4(uint32_t saddr, uint32_t* f) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
-                 : "r"(saddr)
-                 : "memory");
-}
-
-__global__ void __launch_bounds__(kLaThreads, 1)
-chunk_la_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
-    griddep_wait();
+__global__ void __launch_bounds__(kStThreads, 1)
+chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
+    griddep_wait();   // the records, maps and states the grids before wrote
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* vec = reinterpret_cast<float*>(sm + kLaOffVec);         // [3][128]: e [64], exp(gamma_S) at [64]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kLaOffBar);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kLaOffBar + LA_NBARS * 8);
-    volatile int* s_err = reinterpret_cast<volatile int*>(sm + kLaOffBar + LA_NBARS * 8 + 4);
-    int* s_last = reinterpret_cast<int*>(sm + kLaOffBar + LA_NBARS * 8 + 8);   // W ring [3], Qs/P sets [2], K ring [3]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kStOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kStOffBar + ST_NBARS * 8);
+    volatile int* s_err = reinterpret_cast<volatile int*>(sm + kStOffBar + ST_NBARS * 8 + 4);
+    volatile int* s_issued = reinterpret_cast<volatile int*>(sm + kStOffBar + ST_NBARS * 8 + 8);
 
     const int h = blockIdx.x, n = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;                 // TMEM lane of this thread
+    const int quarter = warp & 3, sub = warp >> 2;
+    const int row = quarter * 32 + lane;                 // TMEM lane of this thread (value column j)
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
     const int kh = h / (p.Hv / p.Hk);
     const int Hv = p.Hv;
@@ -1732,6 +1719,8 @@ chunk_la_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         seg = int(blockIdx.z + 1) / 2;
         mode = (blockIdx.z & 1) ? kModeOffset : kModeTransition;
     }
+    // Segments of seg_chunks chunks; segment 0 is the short one when they do
+    // not divide the sequence.
     int c_begin = 0, c_end = seq_chunks;
     if (p.seg_phase) {
         const int L = p.seg_chunks;
@@ -1739,9 +1728,9 @@ chunk_la_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         c_begin = seg == 0 ? 0 : seg * L - short_by;
         c_end = min((seg + 1) * L - short_by, seq_chunks);
     }
-    if (c_begin >= c_end && !(seg == 0 && mode == kModeFull)) return;
+    if (c_begin >= c_end && !(seg == 0 && mode == kModeFull)) return;   // no such segment
     const int nchunks = c_end > c_begin ? c_end - c_begin : 0;
-    const int64_t slot0 = t0 / p.chunk + n + c_begin;
+    const int64_t slot0 = t0 / p.chunk + n + c_begin;   // record slot of this CTA's first chunk
     t0 += int64_t(c_begin) * p.chunk;
     const bool last_seg = c_end >= seq_chunks;
     const CUtensorMap* omap = mode == kModeTransition ? &maps.g : &maps.o;
@@ -1753,6 +1742,9 @@ chunk_la_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         slot = p.seg_ws + (size_t(h) * p.seg_slots + sl) * 3 * kD * kD;
         next_slot = slot + 3 * kD * kD;
     }
+    // incoming state: state_in (segment 0), zero (offset pass) or the identity
+    // (transition pass); final state: state_out (last segment), the S_1 image
+    // (segment 0 of phase 1), B_s (fp32) or the M_s^T image
     const float* init_src = seg == 0 && p.state_in ? p.state_in + sbase : nullptr;
     const bool init_identity = mode == kModeTransition;
     float* final_dst = nullptr;
@@ -1765,14 +1757,19 @@ chunk_la_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     } else {
         img_dst = reinterpret_cast<uint8_t*>(slot + kD * kD);
     }
+    auto record = [&](int c) {
+        return p.prep_ws + (size_t(h) * size_t(p.prep_slots) + size_t(slot0 + c)) * kPrepRecordBytes;
+    };
+    auto chunk_start = [&](int c) { return t0 + int64_t(c) * p.chunk; };
+    auto wait = [&](int b, uint32_t parity) { return mbar_wait(&bars[b], parity, kWaitLimit, kSuspendNs); };
 
     if (tid == 0) {
-        for (int i = 0; i < LA_NBARS; ++i)
-            mbar_init(&bars[i], (i == LA_XD0 || i == LA_XD0 + 1 || (i >= LA_RFREE0 && i < LA_RFREE0 + 3)) ? 2 : 1);
+        for (int i = 0; i < ST_NBARS; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         *s_err = 0;
-        for (int i = 0; i < 8; ++i) s_last[i] = -1;
+        *s_issued = 0;
         tma_prefetch_desc(&maps.k);
+        tma_prefetch_desc(omap);
     }
     __syncwarp();
     if (warp == 0) {
@@ -1783,466 +1780,341 @@ chunk_la_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tZ = tmem + kLaColZ, tZb = tmem + kLaColZb, tU = tmem + kLaColU, tO = tmem + kLaColO;
-    auto tX = [&](int c) { return tmem + kLaColX + uint32_t(c & 1) * 64u; };
-    auto ks = [&](int c) { return sm + uint32_t(c & 1) * kLaKS; };   // Qs of chunk c at +8192, +24576
-    // K ring: slots 0 and 1 in the K places of the two sets (64-column blocks
-    // 16 KB apart), slot 2 in their unused upper part (blocks 8 KB apart)
-    auto kbase = [&](int c) { return c % 3 == 2 ? sm + 32768u : sm + uint32_t(c % 3) * kLaKS; };
-    auto kstride = [&](int c) { return c % 3 == 2 ? 8192u : 16384u; };
-    auto cE = [&](int c) { return vec + (c % 3) * 128; };
-    auto cGS = [&](int c) { return vec[(c % 3) * 128 + kC]; };
-    auto wbuf = [&](int c) { return sm + kLaOffW + uint32_t(c % 3) * 16384u; };
-    auto rbuf = [&](int c) { return sm + kLaOffR + uint32_t(c % 3) * 8192u; };
-    auto pbuf = [&](int c) { return sm + kLaOffP + uint32_t(c & 1) * 16384u; };
-    auto chunk_start = [&](int c) { return t0 + int64_t(c) * p.chunk; };
-    auto tma_ok = [&](int c) { return chunk_start(c) + kC <= t_end_all; };
-    auto wait = [&](int b, uint32_t parity) { return mbar_wait(&bars[b], parity, kWaitLimit, kSuspendNs); };
-    auto record = [&](int c) {
-        return p.prep_ws + (size_t(h) * size_t(p.prep_slots) + size_t(slot0 + c)) * kPrepRecordBytes;
-    };
-    const uint32_t id_x = idesc_bf16(128, 64, 0, 1);      // B = -W^T or R, MN-major
-    const uint32_t id_o = idesc_bf16(128, 64, 0, 0);      // B = Qs or P, K-major
-    const uint32_t id_z = idesc_bf16(128, 128, 0, 1);     // B = raw K, MN-major [i][d]
-    bool fail = false;
 
-    if (warp < 4) {
-        // ================================================================ loader
-        // Thread 0 polls the mbarriers; the group learns the outcome through a
-        // voting named barrier.  Iteration c: R_{c-1} from K_{c-1} and the W
-        // image of record c (both fetched an iteration earlier), the W image
-        // scaled, then the W image and vectors of record c + 1 (ring slot, once
-        // chunk c - 2 has freed it), K_{c+1} (K ring, once chunk c - 2's Z
-        // update read its slot), and Qs_c, P_c (set c & 1, once chunk c - 2's
-        // output products read it).
-        const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
-        auto fetch_w = [&](int c) {                      // thread 0
+    {
+        // Thread 0 (the lead) polls the mbarriers, issues every MMA and every
+        // record copy; the group follows through voting named barriers.
+        const int ct = tid;
+        const bool lead = ct == 0;
+        __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(mode == kModeTransition ? p.g_out : p.out);
+        const uint32_t tZ = tmem + kStColZ, tZb = tmem + kStColZb, tX = tmem + kStColX, tU = tmem + kStColU;
+        auto tO = [&](int c) { return tmem + ((c & 1) ? kStColOodd : kStColOeven); };
+        auto tXO = [&](int c) { return tmem + ((c & 1) ? kStColOodd : kStColX); };
+        const uint32_t id_xo = idesc_bf16(128, 128, 0, 0);   // B = the merged tile, K-major
+        const uint32_t id_o = idesc_bf16(128, 64, 0, 0);     // B = P, K-major
+        const uint32_t id_z = idesc_bf16(128, 128, 0, 1);    // B = raw K, MN-major [i][d]
+        const bool has_u0 = mode != kModeTransition;
+        // This thread's part of a chunk's record vectors: the end weights e of
+        // columns 16 sub .. 16 sub + 15 and exp(gamma_S).
+        auto load_vec = [&](int c, float* e, float& gs) {
             const uint8_t* rec = record(c);
-            const int r3 = c % 3;
-            if (c >= 3 && !wait(LA_RFREE0 + r3, uint32_t(((c - 3) / 3) & 1))) return false;
-            s_last[r3] = c;
-            mbar_arrive_expect_tx(&bars[LA_W0 + r3], 16384u + 512u);
-            bulk_load(wbuf(c), rec + kRecWt, 16384, &bars[LA_W0 + r3]);
-            bulk_load(vec + r3 * 128, rec + kRecVec, 512, &bars[LA_W0 + r3]);
-            return true;
+            const float4* ev = reinterpret_cast<const float4*>(rec + kRecVec) + sub * 4;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 w = __ldg(ev + k);
+                e[4 * k] = w.x;
+                e[4 * k + 1] = w.y;
+                e[4 * k + 2] = w.z;
+                e[4 * k + 3] = w.w;
+            }
+            gs = __ldg(reinterpret_cast<const float*>(rec + kRecVec) + kC);
         };
-        // K_c into K slot c % 3: TMA, or plain loads where the box would pass the buffers
-        auto fetch_k = [&](int c) {
-            bool lf = false;
-            if (c >= 3 && tid == 0) lf = !wait(LA_KFREE0 + c % 3, uint32_t(((c - 3) / 3) & 1));
-            if (named_sync_or(kBarL, 128, lf)) return false;
-            const bool tk = tma_ok(c);
-            if (!tk) {
-                const int64_t cs = chunk_start(c);
-                for (int idx = tid; idx < kC * 16; idx += 128) {
-                    const int r = idx >> 4, cc = (idx & 15) * 8;
-                    const int64_t t = cs + r;
-                    uint4 zk = make_uint4(0, 0, 0, 0);
-                    if (t < t_end_all) zk = *reinterpret_cast<const uint4*>(gk + t * p.k_stride + kh * kD + cc);
-                    *reinterpret_cast<uint4*>(kbase(c) + toff(r, cc, kstride(c))) = zk;
-                }
-                fence_proxy_async_smem();
-                named_sync(kBarL, 128);
+        // U0^T of this thread's lane at columns 16 sub .. 16 sub + 15 from the
+        // slot's copy of the record's fragments (the preparing thread of that
+        // lane and column half wrote them as interleaved 16-byte groups).
+        const int u_pw = quarter + 4 * (sub >> 1);
+        auto load_u0 = [&](int b, float* u0) {
+            if (!has_u0) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) u0[k] = 0.f;
+                return;
             }
-            if (tid == 0) {
-                uint64_t* bar = &bars[LA_KR0 + c % 3];
-                s_last[5 + c % 3] = c;
-                mbar_arrive_expect_tx(bar, tk ? 16384u : 0u);
-                if (tk) {
-                    const int y = int(chunk_start(c));
-                    tma_load_2d(kbase(c), &maps.k, bar, kh * kD, y);
-                    tma_load_2d(kbase(c) + kstride(c), &maps.k, bar, kh * kD + 64, y);
-                }
+            const float4* us = reinterpret_cast<const float4*>(sm + uint32_t(b) * kStSlot + kStOffU) +
+                               (u_pw * 8 + 4 * (sub & 1)) * 32 + lane;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 w = us[k * 32];
+                u0[4 * k] = w.x;
+                u0[4 * k + 1] = w.y;
+                u0[4 * k + 2] = w.z;
+                u0[4 * k + 3] = w.w;
             }
-            return true;
         };
-        bool lf = false;
-        if (nchunks > 0) {
-            if (tid == 0) lf = !fetch_w(0);
-            if (named_sync_or(kBarL, 128, lf) || !fetch_k(0)) fail = true;
-        }
-        for (int c = 0; c < nchunks && !fail; ++c) {
-            const uint8_t* rec = record(c);
-            const int r3 = c % 3;
-            // ---- R_{c-1} = K_{c-1} (-W_c^T) by warp MMAs (warp w: rows 16w ..)
-            if (tid == 0) lf = !wait(LA_W0 + r3, uint32_t((c / 3) & 1));
-            if (c >= 1 && tid == 0 && !lf) lf = !wait(LA_KR0 + (c - 1) % 3, uint32_t(((c - 1) / 3) & 1));
-            if (named_sync_or(kBarL, 128, lf)) { fail = true; break; }
-            if (c >= 1) {
-                const uint8_t* kt = kbase(c - 1);        // [t][d] K-major
-                const uint32_t kst = kstride(c - 1);
-                const uint8_t* wt = wbuf(c);             // [d][t'] MN-major
-                const int m0 = warp * 16;
-                float acc[8][4];
+        // Output tiles: O^T of chunk cc read out of TMEM as MMA-ordered
+        // fragments (this warp: its 32 lanes, columns 16 sub .. 16 sub + 15)
+        // and stored transposed (stmatrix) into staging tile cc & 1
+        // ([64 rows][128 columns] bf16, 128-byte swizzle); after a barrier the
+        // lead writes it with TMA stores, or the group as 16-byte rows when
+        // the chunk ends inside the buffers (the box's other rows belong to
+        // the next sequence).
+        uint8_t* const o_stage = sm + kStOffO;
+        int64_t o_cs = 0;
+        int o_rows = 0;
+        auto stage_out = [&](int cc) {
+            uint8_t* st = o_stage + uint32_t(cc & 1) * 16384u;
+            uint32_t r[2][8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+            for (int u = 0; u < 2; ++u)
+                tmem_ld_16x256b_x2(tO(cc) + (uint32_t(quarter * 32 + 16 * u) << 16) + uint32_t(sub * 16), r[u]);
+            tmem_ld_wait();
+            const int m = lane >> 3, rr = lane & 7;
 #pragma unroll
-                for (int k0 = 0; k0 < kD; k0 += 16) {
-                    uint32_t a[4];
-                    ldmatrix_x4(smem_u32(kt + toff(m0 + (lane & 7) + 8 * ((lane >> 3) & 1), k0 + 8 * (lane >> 4), kst)), a);
+            for (int u = 0; u < 2; ++u) {
+                uint32_t f[4];
 #pragma unroll
-                    for (int nt = 0; nt < 8; nt += 2) {
-                        uint32_t b[4];
-                        ldmatrix_x4_trans(smem_u32(wt + toff(k0 + (lane & 7) + 8 * ((lane >> 3) & 1), nt * 8 + 8 * (lane >> 4), 16384)), b);
-                        mma_bf16_16816(acc[nt], a, b);
-                        mma_bf16_16816(acc[nt + 1], a, b + 2);
-                    }
-                }
-                uint8_t* rb = rbuf(c);                   // [t][t'] MN-major image, 64 rows
-                const int g = lane >> 2, tq = lane & 3;
-#pragma unroll
-                for (int nt = 0; nt < 8; ++nt) {
-                    const int col = nt * 8 + 2 * tq;
-                    *reinterpret_cast<uint32_t*>(rb + toff(m0 + g, col, 8192)) = pack_bf16x2(acc[nt][0], acc[nt][1]);
-                    *reinterpret_cast<uint32_t*>(rb + toff(m0 + g + 8, col, 8192)) = pack_bf16x2(acc[nt][2], acc[nt][3]);
-                }
-                fence_proxy_async_smem();
+                for (int e = 0; e < 4; ++e)
+                    f[e] = pack_bf16x2(__uint_as_float(r[u][2 * e]) * p.q_scale,
+                                       __uint_as_float(r[u][2 * e + 1]) * p.q_scale);
+                const int t = sub * 16 + 8 * (m >> 1) + rr;
+                const int j = quarter * 32 + 16 * u + 8 * (m & 1);
+                stmatrix_x4_trans(smem_u32(st + toff(t, j, 8192)), f);
             }
-            named_sync(kBarL, 128);
-            if (tid == 0) mbar_arrive(&bars[LA_RR0 + r3]);
-            // ---- the W image scaled by exp(gamma_S) of chunk c - 1 (R used it unscaled)
-            if (c >= 1) {
-                const float sc = cGS(c - 1);
-                uint4* w4 = reinterpret_cast<uint4*>(wbuf(c));
-                for (int i = tid; i < 1024; i += 128) {
-                    uint4 u = w4[i];
-                    uint32_t* pw = reinterpret_cast<uint32_t*>(&u);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        pw[q] = pack_bf16x2(__uint_as_float(pw[q] << 16) * sc, __uint_as_float(pw[q] & 0xffff0000u) * sc);
-                    w4[i] = u;
-                }
-                fence_proxy_async_smem();
-            }
-            named_sync(kBarL, 128);
-            if (tid == 0) mbar_arrive(&bars[LA_WS0 + r3]);
-            // ---- the next record's W image and vectors, and its K tile
-            if (c + 1 < nchunks) {
-                if (tid == 0) lf = !fetch_w(c + 1);
-                if (named_sync_or(kBarL, 128, lf) || !fetch_k(c + 1)) { fail = true; break; }
-            }
-            // ---- Qs_c, P_c into set c & 1
-            if (c >= 2 && tid == 0) lf = !wait(LA_FREE0 + (c & 1), uint32_t(((c - 2) >> 1) & 1));
-            if (named_sync_or(kBarL, 128, lf)) { fail = true; break; }
-            if (tid == 0) {
-                uint64_t* bar = &bars[LA_KP0 + (c & 1)];
-                s_last[3 + (c & 1)] = c;
-                mbar_arrive_expect_tx(bar, 32768u);
-                bulk_load(ks(c) + 8192, rec + kRecQ, 8192, bar);
-                bulk_load(ks(c) + 24576, rec + kRecQ + 8192, 8192, bar);
-                bulk_load(pbuf(c), rec + kRecP, 16384, bar);
-            }
-            __syncwarp();
-        }
-        if (fail) *s_err = 1;
-    } else if (warp < 8) {
-        // ================================================================ U group
-        // One TMEM lane per thread, all 64 columns of X.  Its lead issues the
-        // Us R term of the next chunk's X right after the epilogue; the group
-        // then stores U0^T (zero in the transition pass) of chunk c + 2 into
-        // the accumulator the epilogue has just read.
-        const bool lead = tid == 128;
-        bool lf = false;
-        auto store_u0 = [&](int c) {
-            float u[64];
-            if (mode != kModeTransition) {
-                const uint8_t* rec = record(c);
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const float4* src = reinterpret_cast<const float4*>(rec + kRecU) + (quarter + 4 * hf) * 8 * 32 + lane;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float4 w = __ldg(src + i * 32);
-                        u[hf * 32 + 4 * i] = w.x;
-                        u[hf * 32 + 4 * i + 1] = w.y;
-                        u[hf * 32 + 4 * i + 2] = w.z;
-                        u[hf * 32 + 4 * i + 3] = w.w;
-                    }
+            fence_proxy_async_smem();
+        };
+        auto write_out_tile = [&](int cc) {
+            const uint8_t* st = o_stage + uint32_t(cc & 1) * 16384u;
+            if (o_rows == kC || o_cs + o_rows >= p.t_cap) {
+                if (lead) {
+                    tma_store_2d(omap, st, h * kD, int(o_cs));
+                    tma_store_2d(omap, st + 8192, h * kD + 64, int(o_cs));
                 }
             } else {
-#pragma unroll
-                for (int q = 0; q < 64; ++q) u[q] = 0.f;
-            }
-#pragma unroll
-            for (int q = 0; q < 64; q += 16) tmem_st16(tX(c) + lane_addr + q, u + q);
-            tmem_st_wait();
-            tc_fence_before();
-            named_sync(kBarU, 128);
-            if (lead) mbar_arrive(&bars[LA_U0S0 + (c & 1)]);
-        };
-        if (nchunks > 0) {
-            if (lead) mbar_arrive(&bars[LA_XD0]);                 // X_0 has no Us R term
-            store_u0(0);
-            if (nchunks > 1) store_u0(1);
-        }
-        for (int c = 0; c < nchunks; ++c) {
-            if (lead && !lf) {
-                lf = !wait(LA_XD0 + (c & 1), uint32_t((c >> 1) & 1));
-                if (!lf) lf = !wait(LA_WS0 + c % 3, uint32_t((c / 3) & 1));   // the chunk's vectors
-                // U and Us of chunk c - 1 read by its Z update and outputs
-                if (!lf && c >= 1) lf = !wait(LA_ZOD, uint32_t((c - 1) & 1));
-            }
-            if (named_sync_or(kBarU, 128, lf)) { fail = true; break; }
-            tc_fence_after();
-            float x[64];
-            tmem_ld64(tX(c) + lane_addr, x);
-            const float* e = cE(c);
-            uint32_t uh[32], ul[32], sh[32], sl[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                split_pair(x[2 * i], x[2 * i + 1], uh[i], ul[i]);
-                split_pair(x[2 * i] * e[2 * i], x[2 * i + 1] * e[2 * i + 1], sh[i], sl[i]);
-            }
-            GDN_TMEM_ST_X16(tU + lane_addr + 0, uh);
-            GDN_TMEM_ST_X16(tU + lane_addr + 16, (uh + 16));
-            GDN_TMEM_ST_X16(tU + lane_addr + 32, ul);
-            GDN_TMEM_ST_X16(tU + lane_addr + 48, (ul + 16));
-            GDN_TMEM_ST_X16(tU + lane_addr + 64, sh);
-            GDN_TMEM_ST_X16(tU + lane_addr + 80, (sh + 16));
-            GDN_TMEM_ST_X16(tU + lane_addr + 96, sl);
-            GDN_TMEM_ST_X16(tU + lane_addr + 112, (sl + 16));
-            tmem_st_wait();
-            tc_fence_before();
-            named_sync(kBarU, 128);
-            if (lead) {
-                tc_fence_after();
-                mbar_arrive(&bars[LA_UDONE]);
-                mbar_arrive(&bars[LA_RFREE0 + c % 3]);
-                if (c + 1 < nchunks) {
-                    // X_{c+1} += Us_c^T R_c (Us hi, lo; R from record c + 1)
-                    lf = !wait(LA_RR0 + (c + 1) % 3, uint32_t(((c + 1) / 3) & 1));
-                    if (!lf) lf = !wait(LA_U0S0 + ((c + 1) & 1), uint32_t(((c + 1) >> 1) & 1));
-                    if (!lf) {
-                        tc_fence_after();
-                        const uint64_t dR = smem_desc(smem_u32(rbuf(c + 1)), 16384, 1024, kSwizzle128B);
-#pragma unroll
-                        for (int part = 0; part < 2; ++part)
-#pragma unroll
-                            for (int s = 0; s < 4; ++s)
-                                umma_f16_tmemA(tX(c + 1), tU + 64 + part * 32 + s * 8, dR + uint64_t(s * 2048 >> 4), id_x, 1);
-                        umma_commit(&bars[LA_XD0 + ((c + 1) & 1)]);
-                    }
+                for (int idx = ct; idx < kC * 16; idx += int(kStChainThreads)) {
+                    const int r = idx >> 4, col = (idx & 15) * 8;
+                    if (r < o_rows)
+                        *reinterpret_cast<uint4*>(gout + ((o_cs + r) * Hv + h) * kD + col) =
+                            *reinterpret_cast<const uint4*>(st + toff(r, col, 8192));
                 }
             }
-            __syncwarp();
-            if (c + 2 < nchunks) store_u0(c + 2);
-        }
-        if (lf) fail = true;
-        if (fail) *s_err = 1;
-    } else {
-        // ================================================================ Z group
-        // One TMEM lane per thread, all 128 columns of Z.  Its lead issues Zb
-        // W^T, the Z update and the output products; one commit after each
-        // chunk's last covers them all.
-        const int zt = tid - 256;
-        const bool lead = zt == 0;
-        __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(mode == kModeTransition ? p.g_out : p.out);
-        uint8_t* const o_stage = sm + kLaOffO;
-        bool lf = false;
-        // Zb (+)= for X accumulator c: Zb times the W image of record c
-        auto issue_t1 = [&](int c) {
-            if (!wait(LA_WS0 + c % 3, uint32_t((c / 3) & 1))) return false;
-            if (!wait(LA_U0S0 + (c & 1), uint32_t((c >> 1) & 1))) return false;
-            tc_fence_after();
-            const uint64_t dW = smem_desc(smem_u32(wbuf(c)), 16384, 1024, kSwizzle128B);
-#pragma unroll
-            for (int s = 0; s < 8; ++s) umma_f16_tmemA(tX(c), tZb + s * 8, dW + uint64_t(s * 2048 >> 4), id_x, 1);
-            umma_commit(&bars[LA_XD0 + (c & 1)]);
-            return true;
+            if (lead) bulk_commit_group();
         };
-        // The final state (or an image of it) from this thread's lane of Z.
-        auto write_final = [&](int hf, const float* z) {
-            if (img_dst) {
-#pragma unroll
-                for (int i = 0; i < 64; i += 8)
-                    store_split8(img_dst + toff(row, hf * 64 + i, 16384), img_dst + 32768 + toff(row, hf * 64 + i, 16384),
-                                 z + i);
-            } else if (final_dst) {
-#pragma unroll
-                for (int i = 0; i < 64; ++i) final_dst[size_t(hf * 64 + i) * kD + row] = z[i];
-            }
+        // Lead: the record operands of chunk c into slot c & 1: the merged B
+        // tile (K-major, 128 rows per 64-column block: -W then Qs for even
+        // chunks, Qs then -W for odd ones, matching the accumulator pairs
+        // [X | O even] and [O odd | X]), P hi | lo and the raw K tile (rows at
+        // or past the buffers' end read as zero; rows past the sequences' end
+        // are cleared after landing).
+        auto issue = [&](int c) {
+            const int b = c & 1;
+            uint8_t* sp = sm + uint32_t(b) * kStSlot;
+            const uint8_t* rec = record(c);
+            uint64_t* bar = &bars[ST_FULL0 + b];
+            mbar_arrive_expect_tx(bar, 65536u + (has_u0 ? 32768u : 0u));
+            const uint32_t w_at = b ? 8192u : 0u, q_at = b ? 0u : 8192u;
+            bulk_load(sp + w_at, rec + kRecWt, 8192, bar);
+            bulk_load(sp + 16384 + w_at, rec + kRecWt + 8192, 8192, bar);
+            bulk_load(sp + q_at, rec + kRecQ, 8192, bar);
+            bulk_load(sp + 16384 + q_at, rec + kRecQ + 8192, 8192, bar);
+            bulk_load(sp + kStOffP, rec + kRecP, 16384, bar);
+            tma_load_2d(sp + kStOffK, &maps.k, bar, kh * kD, int(chunk_start(c)));
+            tma_load_2d(sp + kStOffK + 8192, &maps.k, bar, kh * kD + 64, int(chunk_start(c)));
+            if (has_u0) bulk_load(sp + kStOffU, rec + kRecU, 32768, bar);
+            *s_issued = c + 1;
         };
+        bool fail = false;
         if (nchunks == 0) {
-            for (int hf = 0; hf < 2; ++hf) {
-                float z[64];
+            if (final_dst)
+                for (int d = sub * 32; d < sub * 32 + 32; ++d)
+                    final_dst[size_t(d) * kD + row] = init_src ? init_src[size_t(d) * kD + row] : 0.f;
+        } else {
+            if (lead) {
+                issue(0);
+                if (nchunks > 1) issue(1);
+            }
+            float ev[16], gs;
+            load_vec(0, ev, gs);
+            {
+                // ---- incoming state (this thread: key rows 32 sub .. 32 sub + 31):
+                // Zb = bf16(S_0^T), Z = exp(gamma_S(0)) S_0^T
+                float z[32];
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const int d = hf * 64 + i;
+                for (int i = 0; i < 32; ++i) {
+                    const int d = sub * 32 + i;
                     z[i] = init_src ? init_src[size_t(d) * kD + row] : (init_identity && d == row ? 1.f : 0.f);
                 }
-                write_final(hf, z);
-            }
-        } else {
-            // ---- incoming state: Zb = bf16(S_0^T), Z = exp(gamma_S,0) S_0^T
-            if (lead) lf = !wait(LA_WS0, 0);
-            if (!named_sync_or(kBarZ, 128, lf)) {
-                const float gs0 = cGS(0);
-                for (int hf = 0; hf < 2; ++hf) {
-                    float z[64];
+                uint32_t zb[16];
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        const int d = hf * 64 + i;
-                        z[i] = init_src ? init_src[size_t(d) * kD + row] : (init_identity && d == row ? 1.f : 0.f);
-                    }
-                    uint32_t zb[32];
+                for (int i = 0; i < 16; ++i) zb[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
+                GDN_TMEM_ST_X16(tZb + lane_addr + sub * 16, zb);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) zb[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
-                    GDN_TMEM_ST_X16(tZb + lane_addr + hf * 32, zb);
-                    GDN_TMEM_ST_X16(tZb + lane_addr + hf * 32 + 16, (zb + 16));
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) z[i] *= gs0;
-#pragma unroll
-                    for (int q = 0; q < 64; q += 16) tmem_st16(tZ + lane_addr + hf * 64 + q, z + q);
-                }
+                for (int i = 0; i < 32; ++i) z[i] *= gs;
+                tmem_st16(tZ + lane_addr + sub * 32, z);
+                tmem_st16(tZ + lane_addr + sub * 32 + 16, z + 16);
                 tmem_st_wait();
-                tc_fence_before();
-                named_sync(kBarZ, 128);
-                if (lead) {
-                    tc_fence_after();
-                    mbar_arrive(&bars[LA_RFREE0]);      // slot 0's vectors read
-                    lf = !issue_t1(0);                   // record 0's W image is not scaled
-                    if (!lf && nchunks > 1) lf = !issue_t1(1);
-                }
-            } else {
-                fail = true;
             }
-            const int m = lane >> 3, rr = lane & 7;
-            for (int c = 0; c < nchunks && !fail; ++c) {
-                // ---- outputs and Z update of chunk c
-                if (lead && !lf) {
-                    lf = !wait(LA_KP0 + (c & 1), uint32_t((c >> 1) & 1));
+            tc_fence_before();
+            named_sync(kBarSt, kStChainThreads);
+            for (int c = 0; c < nchunks; ++c) {
+                const int b = c & 1;
+                const int64_t cs = chunk_start(c);
+                const int rows = int(t1 - cs < p.chunk ? t1 - cs : p.chunk);
+                const bool has_next = c + 1 < nchunks;
+                // ---- [X | O] = Zb [-W^T | Qs^T] ------------------------------------
+                bool lf = false;
+                if (lead) {
+                    lf = !wait(ST_FULL0 + b, uint32_t((c >> 1) & 1));
                     if (!lf) {
                         tc_fence_after();
-                        const uint64_t dQ = smem_desc(smem_u32(ks(c) + 8192), 16, 1024, kSwizzle128B);
+                        const uint64_t dB = smem_desc(smem_u32(sm + uint32_t(b) * kStSlot), 16, 1024, kSwizzle128B);
 #pragma unroll
                         for (int s = 0; s < 8; ++s) {
                             const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
-                            umma_f16_tmemA(tO, tZb + s * 8, dQ + (off >> 4), id_o, s > 0);
+                            umma_f16_tmemA(tXO(c), tZb + s * 8, dB + (off >> 4), id_xo, s > 0);
                         }
-                        lf = !wait(LA_UDONE, uint32_t(c & 1));
-                        if (!lf) lf = !wait(LA_KR0 + c % 3, uint32_t((c / 3) & 1));
+                        umma_commit(&bars[ST_X]);
                     }
-                    if (!lf) {
-                        tc_fence_after();
-                        const uint64_t dK = smem_desc(smem_u32(kbase(c)), kstride(c), 1024, kSwizzle128B);
-#pragma unroll
-                        for (int part = 0; part < 2; ++part)
-#pragma unroll
-                            for (int s = 0; s < 4; ++s)
-                                umma_f16_tmemA(tZ, tU + 64 + part * 32 + s * 8, dK + uint64_t(s * 2048 >> 4), id_z, 1);
-                        const uint64_t dP = smem_desc(smem_u32(pbuf(c)), 16, 1024, kSwizzle128B);
-                        // (U hi, P hi), (U hi, P lo), (U lo, P hi)
-#pragma unroll
-                        for (int pr = 0; pr < 3; ++pr)
-#pragma unroll
-                            for (int s = 0; s < 4; ++s)
-                                umma_f16_tmemA(tO, tU + (pr == 2 ? 32 : 0) + s * 8,
-                                               dP + uint64_t(((pr == 1 ? 8192 : 0) + s * 32) >> 4), id_o, 1);
-                        umma_commit(&bars[LA_ZOD]);
-                        umma_commit(&bars[LA_FREE0 + (c & 1)]);
-                        umma_commit(&bars[LA_KFREE0 + c % 3]);
-                        lf = !wait(LA_ZOD, uint32_t(c & 1));
-                    }
-                    // the next chunk's vectors, for the Z epilogue
-                    if (!lf && c + 1 < nchunks) lf = !wait(LA_WS0 + (c + 1) % 3, uint32_t(((c + 1) / 3) & 1));
                 }
-                if (named_sync_or(kBarZ, 128, lf)) { fail = true; break; }
-                tc_fence_after();
-                // ---- Z epilogue: Z_{c+1} -> final state, or Zb and the pre-scaled Z
-                {
-                    const bool last = c + 1 == nchunks;
-                    const float gsn = last ? 1.f : cGS(c + 1);
-                    for (int hf = 0; hf < 2; ++hf) {
-                        float z[64];
-                        tmem_ld64(tZ + lane_addr + hf * 64, z);
-                        if (last) {
-                            write_final(hf, z);
-                        } else {
-                            uint32_t zb[32];
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) zb[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
-                            GDN_TMEM_ST_X16(tZb + lane_addr + hf * 32, zb);
-                            GDN_TMEM_ST_X16(tZb + lane_addr + hf * 32 + 16, (zb + 16));
-#pragma unroll
-                            for (int i = 0; i < 64; ++i) z[i] *= gsn;
-#pragma unroll
-                            for (int q = 0; q < 64; q += 16) tmem_st16(tZ + lane_addr + hf * 64 + q, z + q);
-                        }
+                // ---- the previous chunk's output tile ------------------------------
+                if (c > 0) {
+                    if (lead && !lf) {
+                        lf = !wait(ST_O, uint32_t((c - 1) & 1));
+                        // every product of chunk c - 1 is done: its slot takes chunk c + 1
+                        if (!lf && has_next) issue(c + 1);
+                        bulk_wait_group_read<1>();        // staging tile (c - 1) & 1 read by its last store
                     }
+                    __syncwarp();
+                    if (named_sync_or(kBarSt, kStChainThreads, lf)) {
+                        fail = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    stage_out(c - 1);
+                }
+                if (lead && !lf) lf = !wait(ST_X, uint32_t(c & 1));
+                __syncwarp();
+                if (named_sync_or(kBarSt, kStChainThreads, lf)) {
+                    fail = true;
+                    break;
+                }
+                tc_fence_after();
+                if (c > 0) write_out_tile(c - 1);
+                if (cs + kC > t_end_all) {
+                    // K rows past the sequences' end (another caller's rows, or
+                    // unset) must not meet the zero rows of Us: clear them
+                    uint8_t* kt = sm + uint32_t(b) * kStSlot + kStOffK;
+                    const int valid = int(t_end_all - cs);
+                    for (int idx = ct; idx < kC * 16; idx += int(kStChainThreads)) {
+                        const int r = idx >> 4, cc = (idx & 15) * 8;
+                        if (r >= valid) *reinterpret_cast<uint4*>(kt + toff(r, cc, 8192)) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                // ---- U^T = U0^T + X; U and Us = U diag(e) as bf16 hi + lo -----------
+                {
+                    uint32_t xr[16];
+                    float u0[16];
+                    __syncwarp();
+                    GDN_TMEM_LD_X16(tX + lane_addr + sub * 16, xr);
+                    load_u0(b, u0);
+                    tmem_ld_wait();
+                    uint32_t uh[8], ul[8], sh[8], sl[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float a0 = u0[2 * i] + __uint_as_float(xr[2 * i]);
+                        const float a1 = u0[2 * i + 1] + __uint_as_float(xr[2 * i + 1]);
+                        split_pair(a0, a1, uh[i], ul[i]);
+                        split_pair(a0 * ev[2 * i], a1 * ev[2 * i + 1], sh[i], sl[i]);
+                    }
+                    GDN_TMEM_ST_X8(tU + lane_addr + 0 + sub * 8, uh);
+                    GDN_TMEM_ST_X8(tU + lane_addr + 32 + sub * 8, ul);
+                    GDN_TMEM_ST_X8(tU + lane_addr + 64 + sub * 8, sh);
+                    GDN_TMEM_ST_X8(tU + lane_addr + 96 + sub * 8, sl);
                     tmem_st_wait();
                 }
                 tc_fence_before();
-                named_sync(kBarZ, 128);
+                named_sync(kBarSt, kStChainThreads);
+                // the next chunk's record values travel while the state update runs
+                float evn[16], gsn = 1.f;
+                if (has_next) load_vec(c + 1, evn, gsn);
+                // ---- Z += Us^T K; then O += U^T P^T behind it ------------------------
                 if (lead) {
                     tc_fence_after();
-                    if (c + 1 < nchunks) mbar_arrive(&bars[LA_RFREE0 + (c + 1) % 3]);
-                    if (c + 2 < nchunks) lf = !issue_t1(c + 2);
-                    bulk_wait_group_read<0>();           // the staging tile's last store has read it
+                    const uint8_t* sp = sm + uint32_t(b) * kStSlot;
+                    const uint64_t dK = smem_desc(smem_u32(sp + kStOffK), 8192, 1024, kSwizzle128B);
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int s = 0; s < 4; ++s)
+                            umma_f16_tmemA(tZ, tU + 64 + part * 32 + s * 8, dK + uint64_t(s * 2048 >> 4), id_z, 1);
+                    umma_commit(&bars[ST_Z]);
+                    const uint64_t dP = smem_desc(smem_u32(sp + kStOffP), 16, 1024, kSwizzle128B);
+#pragma unroll
+                    for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+                        for (int s = 0; s < 4; ++s)
+                            umma_f16_tmemA(tO(c), tU + (pr == 2 ? 32 : 0) + s * 8,
+                                           dP + uint64_t(((pr == 1 ? 8192 : 0) + s * 32) >> 4), id_o, 1);
+                    umma_commit(&bars[ST_O]);
+                    lf = !wait(ST_Z, uint32_t(c & 1));
                 }
-                if (named_sync_or(kBarZ, 128, lf)) { fail = true; break; }
-                // ---- output tile of chunk c: O^T as 16x256b fragments, stored
-                // transposed (stmatrix) into the 128-byte-swizzled staging tile
-#pragma unroll
-                for (int hc = 0; hc < 2; ++hc) {
-                    uint32_t r[4][8];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        tmem_ld_16x256b_x2(tO + (uint32_t(quarter * 32 + 16 * (u >> 1)) << 16) + uint32_t(hc * 32 + 16 * (u & 1)),
-                                           r[u]);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint32_t f[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            f[e] = pack_bf16x2(__uint_as_float(r[u][2 * e]) * p.q_scale,
-                                               __uint_as_float(r[u][2 * e + 1]) * p.q_scale);
-                        const int t = hc * 32 + 16 * (u & 1) + 8 * (m >> 1) + rr;
-                        const int j = quarter * 32 + 16 * (u >> 1) + 8 * (m & 1);
-                        stmatrix_x4_trans(smem_u32(o_stage + toff(t, j, 8192)), f);
-                    }
+                __syncwarp();
+                if (named_sync_or(kBarSt, kStChainThreads, lf)) {
+                    fail = true;
+                    break;
                 }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                named_sync(kBarZ, 128);
+                tc_fence_after();
+                // ---- new state: Zb = bf16(Z); Z <- exp(gamma_S(c+1)) Z --------------
                 {
-                    const int64_t cs = chunk_start(c);
-                    const int rows = int(t1 - cs < p.chunk ? t1 - cs : p.chunk);
-                    if (rows == kC || cs + rows >= p.t_cap) {
-                        if (lead) {
-                            tma_store_2d(omap, o_stage, h * kD, int(cs));
-                            tma_store_2d(omap, o_stage + 8192, h * kD + 64, int(cs));
-                        }
-                    } else {
-                        for (int idx = zt; idx < kC * 16; idx += 128) {
-                            const int r = idx >> 4, col = (idx & 15) * 8;
-                            if (r < rows)
-                                *reinterpret_cast<uint4*>(gout + ((cs + r) * Hv + h) * kD + col) =
-                                    *reinterpret_cast<const uint4*>(o_stage + toff(r, col, 8192));
-                        }
-                        named_sync(kBarZ, 128);              // the rows are read before the tile is reused
+                    float z[32];
+                    tmem_ld32(tZ + lane_addr + sub * 32, z);
+                    uint32_t zb[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) zb[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
+                    GDN_TMEM_ST_X16(tZb + lane_addr + sub * 16, zb);
+                    if (has_next) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) z[i] *= gsn;
+                        tmem_st16(tZ + lane_addr + sub * 32, z);
+                        tmem_st16(tZ + lane_addr + sub * 32 + 16, z + 16);
+                    } else if (img_dst) {
+                        // this thread's lane is one row of either image
+#pragma unroll
+                        for (int i = 0; i < 32; i += 8)
+                            store_split8(img_dst + toff(row, sub * 32 + i, 16384),
+                                         img_dst + 32768 + toff(row, sub * 32 + i, 16384), z + i);
+                    } else if (final_dst) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) final_dst[size_t(sub * 32 + i) * kD + row] = z[i];
                     }
-                    if (lead) bulk_commit_group();
+                    tmem_st_wait();
+                }
+                o_cs = cs;
+                o_rows = rows;
+                if (has_next) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) ev[k] = evn[k];
+                }
+                tc_fence_before();
+                named_sync(kBarSt, kStChainThreads);
+            }
+            if (!fail) {                                 // the last chunk's output tile
+                bool lf = false;
+                if (lead) {
+                    lf = !wait(ST_O, uint32_t((nchunks - 1) & 1));
+                    bulk_wait_group_read<1>();
+                }
+                __syncwarp();
+                if (!named_sync_or(kBarSt, kStChainThreads, lf)) {
+                    tc_fence_after();
+                    stage_out(nchunks - 1);
+                    named_sync(kBarSt, kStChainThreads);
+                    write_out_tile(nchunks - 1);
+                } else {
+                    fail = true;
                 }
             }
-            if (lead) bulk_wait_all();
+            if (lead) bulk_wait_all();                   // tile stores done before the CTA exits
         }
-        if (lf) fail = true;
         if (fail) *s_err = 1;
     }
 
-    // ---- teardown -----------------------------------------------------------------
+    // ---- teardown ------------------------------------------------------------------
     tc_fence_before();
     __syncthreads();
-    if (*s_err && tid == 0) {
-        atomicAdd(&g_tc_timeouts, 1);
-        // copies still in flight land before shared memory goes away
-        for (int r = 0; r < 3; ++r)
-            if (s_last[r] >= 0) mbar_wait(&bars[LA_W0 + r], uint32_t((s_last[r] / 3) & 1), kWaitLimit, kSuspendNs);
-        for (int b = 0; b < 2; ++b)
-            if (s_last[3 + b] >= 0) mbar_wait(&bars[LA_KP0 + b], uint32_t((s_last[3 + b] >> 1) & 1), kWaitLimit, kSuspendNs);
-        for (int r = 0; r < 3; ++r)
-            if (s_last[5 + r] >= 0) mbar_wait(&bars[LA_KR0 + r], uint32_t((s_last[5 + r] / 3) & 1), kWaitLimit, kSuspendNs);
+    if (tid == 0) {
+        tc_fence_after();
+        // every product this thread issued has completed before TMEM and
+        // shared memory go away (a no-op wait on a clean finish)
+        umma_commit(&bars[ST_DRAIN]);
+        if (!mbar_wait(&bars[ST_DRAIN], 0, kWaitLimit, kSuspendNs)) *s_err = 1;
+        if (*s_err) {
+            atomicAdd(&g_tc_timeouts, 1);
+            // record copies still in flight land before shared memory goes away
+            const int issued = *s_issued;
+            for (int c = issued - 2 < 0 ? 0 : issued - 2; c < issued; ++c)
+                mbar_wait(&bars[ST_FULL0 + (c & 1)], uint32_t((c >> 1) & 1), kWaitLimit, kSuspendNs);
+            bulk_wait_all();
+        }
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
@@ -2643,16 +2515,13 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
     if (segmented && !make_map(&maps.g, p.g_out, int64_t(p.Hv) * kD, rows, int64_t(p.Hv) * kD))
         return cudaErrorInvalidValue;
     const bool split = p.prep_ws != nullptr && p.prep_slots > 0;
-    const void* state_kernel = split ? reinterpret_cast<const void*>(chunk_tc_kernel<true>)
+    const void* state_kernel = split ? reinterpret_cast<const void*>(chunk_state_kernel)
                                      : reinterpret_cast<const void*>(chunk_tc_kernel<false>);
-    cudaError_t e = ensure_smem(state_kernel, int(kSmemBytes));
+    cudaError_t e = ensure_smem(state_kernel, int(split ? kStSmemBytes : kSmemBytes));
     if (e != cudaSuccess) return e;
-    const bool lookahead = split && p.lookahead;
-    if (lookahead && (e = ensure_smem(reinterpret_cast<const void*>(chunk_la_kernel), int(kLaSmemBytes))) != cudaSuccess)
-        return e;
+    const char* state_name = split ? "chunk_state_kernel" : kTcKernelName;
     auto launch_state = [&](const ChunkParams& q, unsigned z) {
-        if (lookahead) return launch_pdl(chunk_la_kernel, dim3(q.Hv, q.B, z), kLaThreads, kLaSmemBytes, s, q, maps);
-        return split ? launch_pdl(chunk_tc_kernel<true>, dim3(q.Hv, q.B, z), kThreads, kSmemBytes, s, q, maps)
+        return split ? launch_pdl(chunk_state_kernel, dim3(q.Hv, q.B, z), kStThreads, kStSmemBytes, s, q, maps)
                      : launch_pdl(chunk_tc_kernel<false>, dim3(q.Hv, q.B, z), kThreads, kSmemBytes, s, q, maps);
     };
     if (split) {                                      // every chunk's S-independent part, in parallel
@@ -2672,14 +2541,14 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
     if (!segmented) {
         ChunkParams q = p;
         q.seg_phase = 0;
-        timer_begin(s, lookahead ? "chunk_la_kernel" : "chunk_tc_kernel");
+        timer_begin(s, state_name);
         e = launch_state(q, 1);
         timer_end(s);
         return e;
     }
     ChunkParams q = p;
     q.seg_phase = 1;                                  // segment 0 in full; O', B_s and G, M_s of the others
-    timer_begin(s, lookahead ? "chunk_la_kernel" : "chunk_tc_kernel");
+    timer_begin(s, state_name);
     e = launch_state(q, unsigned(2 * p.seg_max - 1));
     timer_end(s);
     if (e != cudaSuccess) return e;

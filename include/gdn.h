@@ -135,11 +135,9 @@ typedef struct gdn_prefill_desc {
      * scaled queries) is solved first for all chunks in parallel and stored
      * as one 82432-byte record per (value head, chunk slot), Hv *
      * (T_total / chunk + B + 1) records; the state pass then streams the
-     * records.  The results are the same as without it.  0 = on when the
-     * workspace holds the records, < 0 = off, 1 = on with the look-ahead state
-     * pass chunk_la_kernel (the next chunk's X formed from the current state
-     * and a 64 x 64 state-independent correction, so the state update leaves
-     * the dependent chain; same results within rounding, not faster yet). */
+     * records (chunk_state_kernel).  The results agree with those without
+     * it within rounding.  >= 0 = on when the workspace holds the records,
+     * < 0 = off. */
     int split_prep;
 } gdn_prefill_desc;
 

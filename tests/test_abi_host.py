@@ -167,7 +167,7 @@ def test_launch_plan_names(lib):
     assert B.gdn_prefill_plan(d64) == ["chunk_simt_kernel"]
     dc = _desc(conv_state_out=A)
     dc.workspace, dc.workspace_bytes = A, 1 << 40
-    assert B.gdn_prefill_plan(dc) == ["conv_kernel", "chunk_prep_kernel", "chunk_tc_kernel",
+    assert B.gdn_prefill_plan(dc) == ["conv_kernel", "chunk_prep_kernel", "chunk_state_kernel",
                                       "conv_state_kernel"]
     dc.split_prep = -1
     assert B.gdn_prefill_plan(dc) == ["conv_kernel", "chunk_tc_kernel", "conv_state_kernel"]
@@ -273,15 +273,15 @@ def test_segmented_plan_and_workspace(lib):
     records = 16 * (4096 // 64 + 1 + 1) * 82432
     assert B.gdn_workspace_bytes(d) == maps + g_map + records
     d.workspace, d.workspace_bytes = A, B.gdn_workspace_bytes(d)
-    assert B.gdn_prefill_plan(d) == ["chunk_prep_kernel", "chunk_tc_kernel", "seg_out_kernel"]
+    assert B.gdn_prefill_plan(d) == ["chunk_prep_kernel", "chunk_state_kernel", "seg_out_kernel"]
     d.workspace_bytes = maps + g_map                 # no room for the records: inline preparation
     assert B.gdn_prefill_plan(d) == ["chunk_tc_kernel", "seg_out_kernel"]
     d.workspace_bytes = maps + g_map - 1             # no room for G either: one pass
     assert B.gdn_prefill_plan(d) == ["chunk_tc_kernel"]
     d.segment_chunks = -1                            # one pass asked for
     d.workspace_bytes = 1 << 40
-    assert B.gdn_prefill_plan(d) == ["chunk_prep_kernel", "chunk_tc_kernel"]
-    d.split_prep = 1                                 # the look-ahead state pass
-    assert B.gdn_prefill_plan(d) == ["chunk_prep_kernel", "chunk_la_kernel"]
+    assert B.gdn_prefill_plan(d) == ["chunk_prep_kernel", "chunk_state_kernel"]
+    d.split_prep = 1                                 # any value >= 0: on when the records fit
+    assert B.gdn_prefill_plan(d) == ["chunk_prep_kernel", "chunk_state_kernel"]
     d.workspace_bytes = 0                            # no records: the inline pass
     assert B.gdn_prefill_plan(d) == ["chunk_tc_kernel"]

@@ -166,11 +166,13 @@ def test_no_l2norm_and_q_scale():
 
 
 def test_plain_entry_point_matches_ex():
-    """gdn_prefill (bf16, L2 norm on, no conv) gives the same bits as
-    gdn_prefill_ex with the same description."""
+    """gdn_prefill (bf16, L2 norm on, no conv, no workspace) gives the same
+    bits as gdn_prefill_ex with the same description and no workspace, and
+    matches the oracle."""
     from chunked_gated_delta_chunk_gb300 import binding as B
     p = inputs.make_problem(14, [300, 64], 4, 8, 128, 128)
-    call = runner.PrefillCall(p)
+    call = runner.PrefillCall(p, segment_chunks=-1, split_prep=-1)
+    assert call.workspace is None
     call.run()
     out2 = torch.empty_like(call.out)
     st2 = torch.empty_like(call.state_out)
@@ -178,6 +180,7 @@ def test_plain_entry_point_matches_ex():
                   p.B, p.Hk, p.Hv, p.dk, p.dv, 64)
     torch.cuda.synchronize()
     assert torch.equal(out2, call.out) and torch.equal(st2, call.state_out)
+    compare({"out": out2.cpu(), "state_out": st2.cpu()}, run_oracle(p), TOL_BF16)
 
 
 def test_two_calls_resume_with_conv():
@@ -257,7 +260,7 @@ def test_segment_scan_matches_oracle(seg, lengths, chunk):
     call = runner.PrefillCall(p, segment_chunks=seg)
     from chunked_gated_delta_chunk_gb300 import binding as B
     plan = B.gdn_prefill_plan(call.desc)
-    assert plan[-2:] == ["chunk_tc_kernel", "seg_out_kernel"] and plan.count("chunk_tc_kernel") == 1, plan
+    assert plan[-2:] == ["chunk_state_kernel", "seg_out_kernel"] and plan.count("chunk_state_kernel") == 1, plan
     call.run()
     torch.cuda.synchronize()
     compare({k: v.cpu() for k, v in call.results().items()}, run_oracle(p), TOL_BF16)
@@ -318,24 +321,27 @@ def test_segment_scan_off_equals_on_bits_of_segment_zero():
 @pytest.mark.parametrize("seg,lengths,chunk", [
     (-1, [300], 64), (-1, [1, 64, 0, 129, 7], 64), (3, [64 * 7 + 5], 64),
     (4, [1, 200, 0, 900], 64), (2, [333, 64 * 6], 32), (-1, [250, 3], 17)])
-def test_split_preparation_matches_inline_bits_and_oracle(seg, lengths, chunk):
-    """Chunk records solved ahead of the state pass (all chunks in parallel)
-    give the same bits as the preparation inside the state pass: the same
-    arithmetic in the same order, only stored and streamed back.  Both match
-    the token loop.  Ragged ends, empty sequences, chunks below 64 rows and
-    the segment scan's map passes all read records."""
+def test_split_preparation_matches_inline_and_oracle(seg, lengths, chunk):
+    """Chunk records solved ahead of the state pass (all chunks in parallel,
+    then chunk_state_kernel) and the preparation inside the one-kernel pass
+    agree with each other and with the token loop.  Ragged ends, empty
+    sequences, chunks below 64 rows and the segment scan's map passes all read
+    records."""
     from chunked_gated_delta_chunk_gb300 import binding as B
     p = inputs.make_problem(60 + seg + len(lengths), lengths, 2, 4, 128, 128, chunk=chunk)
     inline = runner.PrefillCall(p, segment_chunks=seg, split_prep=-1)
     split = runner.PrefillCall(p, segment_chunks=seg)
     assert "chunk_prep_kernel" not in B.gdn_prefill_plan(inline.desc)
-    assert B.gdn_prefill_plan(split.desc)[0] == "chunk_prep_kernel"
+    plan = B.gdn_prefill_plan(split.desc)
+    assert plan[0] == "chunk_prep_kernel" and plan[1] == "chunk_state_kernel", plan
     inline.run()
     split.run()
     torch.cuda.synchronize()
-    assert torch.equal(inline.out, split.out)
-    assert torch.equal(inline.state_out, split.state_out)
-    compare({k: v.cpu() for k, v in split.results().items()}, run_oracle(p), TOL_BF16)
+    ref = run_oracle(p)
+    compare({k: v.cpu() for k, v in split.results().items()}, ref, TOL_BF16)
+    compare({k: v.cpu() for k, v in inline.results().items()}, ref, TOL_BF16)
+    compare({"out": split.out.cpu(), "state_out": split.state_out.cpu()},
+            {"out": inline.out.cpu(), "state_out": inline.state_out.cpu()}, TOL_BF16)
 
 
 def test_split_preparation_with_conv_gqa_and_aliased_state():
@@ -368,24 +374,5 @@ def test_launch_timer_records_every_planned_launch():
     assert [n for n, _ in records] == (plan + plan)[:len(plan) + 1]
     assert dropped == len(plan) - 1
     assert all(ms > 0 for _, ms in records)
-    torch.cuda.synchronize()
-    compare({k: v.cpu() for k, v in call.results().items()}, run_oracle(p), TOL_BF16)
-
-
-# ---------------------------------------------------------------- look-ahead state pass
-@pytest.mark.parametrize("seg,lengths,chunk", [
-    (-1, [50], 64), (-1, [64 * 7 - 5], 64), (-1, [1, 200, 0, 700], 64), (3, [64 * 13 + 9, 300], 64),
-    (2, [333, 64 * 6], 32), (0, [4096], 64)])
-def test_lookahead_state_pass_matches_oracle(seg, lengths, chunk):
-    """The look-ahead state pass (split_prep = 1: the next chunk's X formed
-    from the current state and the correction R_c = K_c (-W_{c+1}^T), the
-    state update off the dependent chain) equals the token loop, in one pass,
-    with ragged and empty sequences, chunks below 64 rows and the segment
-    scan's three pass kinds."""
-    from chunked_gated_delta_chunk_gb300 import binding as B
-    p = inputs.make_problem(90 + len(lengths) + chunk, lengths, 2, 4, 128, 128, chunk=chunk)
-    call = runner.PrefillCall(p, segment_chunks=seg, split_prep=1)
-    assert "chunk_la_kernel" in B.gdn_prefill_plan(call.desc)
-    call.run()
     torch.cuda.synchronize()
     compare({k: v.cpu() for k, v in call.results().items()}, run_oracle(p), TOL_BF16)
