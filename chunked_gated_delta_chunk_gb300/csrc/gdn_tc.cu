@@ -80,10 +80,9 @@ constexpr uint32_t kOffTmp = kOffT + kC * kLdA * 4;      // inverse scratch, 153
 constexpr uint32_t kOffVec = kOffTmp + 1536 * 4;         // vectors
 constexpr uint32_t kVecFloats = 8 * kC + 2 * 2 * kC + 2 * kC + 2;   // prep, staging, chain
 constexpr uint32_t kOffBar = kOffVec + ((kVecFloats * 4 + 127) / 128) * 128;
-constexpr uint32_t kNumBars = 18;
+constexpr uint32_t kNumBars = 15;
 constexpr uint32_t kSmemBytes = kOffBar + kNumBars * 8 + 32 + 1024;
 static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-block limit");
-static_assert(kOffA % 1024 == 0 && kOffA + 2 * 16384 <= kOffVec, "two output staging tiles where A, T, scratch live");
 
 // Barrier slots.
 enum : int {
@@ -94,10 +93,7 @@ enum : int {
     B_XREAD = 9,                   // chain has read U^T out of D_X
     B_WTFREE = 10,                 // chain MMA no longer reads -W^T
     B_PFREE0 = 11, B_PFREE1 = 12,  // chain MMA no longer reads P of a buffer
-    B_SFREE0 = 13, B_SFREE1 = 14,  // chain no longer reads a raw stage
-    B_WTFREE1 = 15,                // split preparation: second -W^T buffer free
-    B_OQ = 16,                     // split preparation: O^T = Zb Qs^T done
-    B_ZISS = 17                    // split preparation: Z MMAs of the chunk issued
+    B_SFREE0 = 13, B_SFREE1 = 14   // chain no longer reads a raw stage
 };
 
 // TMEM columns.
@@ -372,11 +368,12 @@ struct Maps {
 // intra-chunk output weights P and the scaled queries) is solved by
 // chunk_prep_kernel for all chunks at once, one CTA per (chunk slot, value
 // head), two CTAs per SM.  It stores one record per chunk:
-//   -W     the two 64-column blocks of -W [64 rows i][128 columns d], bf16,
-//          K-major in the 128-byte-swizzled layout the state MMA reads from
-//          shared memory,
+//   WQ     the B operand of the state pass's first product as it lies in
+//          shared memory: for each 64-column block of d, 128 rows of bf16,
+//          K-major with the 128-byte swizzle, -W [64 rows i] and
+//          Qs = diag(Gamma r_q) Q [64 rows t]; -W first when the chunk is an
+//          even chunk of the pass that reads it, Qs first for an odd one,
 //   P      hi and lo images [64][64] bf16 (same layout),
-//   Qs     the two 64-column blocks of diag(Gamma r_q) Q, same layout,
 //   U0^T   the TMEM fragments of the 256 preparing threads, 32 fp32 each,
 //          stored in 16-byte groups interleaved across a warp's lanes, so that
 //          a thread of the state pass reads its lane's columns coalesced,
@@ -384,9 +381,8 @@ struct Maps {
 //          exp(gamma_S).
 // The state kernel (chunk_state_kernel) then streams the records instead of
 // solving them.
-constexpr uint32_t kRecWt = 0;
-constexpr uint32_t kRecP = 16384;
-constexpr uint32_t kRecQ = 32768;
+constexpr uint32_t kRecWQ = 0;
+constexpr uint32_t kRecP = 32768;
 constexpr uint32_t kRecU = 49152;
 constexpr uint32_t kRecVec = 81920;
 static_assert(kRecVec + 512 == kPrepRecordBytes, "record layout");
@@ -452,11 +448,15 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     // The chunk of item = h * prep_slots + slot: the last sequence n with
     // t0_n / chunk + n <= slot, chunk c = slot - (t0_n / chunk + n); false
     // when the slot holds no chunk.
+    // odd: the chunk is an odd chunk of the state pass that reads it (its
+    // segment's passes with the segment scan, else the whole sequence), which
+    // fixes the order of the record's WQ tile.
     struct Item {
         int h, slot, rows;
         int64_t cs;
-        bool tma;
+        bool tma, odd;
     };
+    const bool segmented = p.seg_chunks > 0 && p.seg_max >= 2;
     auto resolve = [&](int64_t item, Item& it) {
         it.h = int(item / p.prep_slots);
         it.slot = int(item % p.prep_slots);
@@ -474,6 +474,15 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         it.cs = t0 + c * p.chunk;
         it.rows = int(t1 - it.cs < p.chunk ? t1 - it.cs : p.chunk);
         it.tma = it.cs + kC <= t_end_all;
+        int64_t local = c;
+        if (segmented) {
+            const int64_t L = p.seg_chunks;
+            const int64_t seq_chunks = (t1 - t0 + p.chunk - 1) / p.chunk;
+            const int64_t short_by = ((seq_chunks + L - 1) / L) * L - seq_chunks;
+            const int64_t seg = (c + short_by) / L;
+            local = c - (seg == 0 ? 0 : seg * L - short_by);
+        }
+        it.odd = (local & 1) != 0;
         return true;
     };
     auto next_item = [&](int64_t from, Item& it) {
@@ -713,7 +722,7 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             load_chunk8(kq + 8192 + toff(r, cc, 16384), v);
 #pragma unroll
             for (int q = 0; q < 8; ++q) v[q] *= f;
-            store_chunk8(rec + kRecQ + toff(r, cc, 8192), v);
+            store_chunk8(rec + kRecWQ + (cur.odd ? 0u : 8192u) + toff(r, cc, 16384), v);
         }
         if (pt == 0) lf = !mbar_wait(&bars[2], mma_phase & 1, kWaitLimit, kSuspendNs);
         if (__syncthreads_or(lf)) { fail = true; break; }
@@ -764,7 +773,9 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         tc_fence_before();
         __syncthreads();                                   // TMEM read, vectors free for the next item
         if (pt == 0) {
-            bulk_store(rec + kRecWt, sm + kPOffT, 16384);
+            const uint32_t w_at = cur.odd ? 8192u : 0u;     // -W's rows in each 128-row block
+            bulk_store(rec + kRecWQ + w_at, sm + kPOffT, 8192);
+            bulk_store(rec + kRecWQ + 16384 + w_at, sm + kPOffT + 8192, 8192);
             bulk_store(rec + kRecU, sm + kPOffTb, 32768);
             bulk_commit_group();
         }
@@ -784,12 +795,11 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     if (pw == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
-// kSplit: the preparation comes from chunk records (chunk_prep_kernel) and
-// warps 0-3 stream them; otherwise warps 0-3 and 8-11 solve it inline.
-template <bool kSplit>
+// The one-kernel pass (no chunk records): warps 0-3 and 8-11 solve each
+// chunk's preparation inline, one chunk ahead of the chain warps 4-7.
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
-    griddep_wait();   // everything the grid before wrote (records, maps, states, even cu_seqlens)
+    griddep_wait();   // everything the grid before wrote (maps, states, even cu_seqlens)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* sA = reinterpret_cast<float*>(sm + kOffA);
@@ -817,13 +827,11 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;                 // TMEM lane of this thread
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
-    // The chain: warps 4-7 (all columns of their TMEM lanes); with split
-    // preparation also warps 8-11, each chain thread then owning one column
-    // half (hc) of its lane.
-    const bool is_chain = kSplit ? warp >= 4 : (warp >= 4 && warp < 8);
-    const int hc = (kSplit && warp >= 8) ? 1 : 0;
-    constexpr int kHalves = kSplit ? 1 : 2;
-    constexpr uint32_t kChainN = kSplit ? 2 * kChainThreads : kChainThreads;
+    // The chain: warps 4-7 (all columns of their TMEM lanes).
+    const bool is_chain = warp >= 4 && warp < 8;
+    constexpr int hc = 0;
+    constexpr int kHalves = 2;
+    constexpr uint32_t kChainN = kChainThreads;
     const int kh = h / (p.Hv / p.Hk);
     const int Hv = p.Hv;
 
@@ -853,14 +861,11 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     }
     if (c_begin >= c_end && !(seg == 0 && mode == kModeFull)) return;   // no such segment
     const int nchunks = c_end > c_begin ? c_end - c_begin : 0;
-    constexpr bool split = kSplit;
-    const int64_t slot0 = t0 / p.chunk + n + c_begin;   // record slot of this CTA's first chunk
     t0 += int64_t(c_begin) * p.chunk;                   // first token of this CTA's part
     const bool last_seg = c_end >= seq_chunks;
     // Every pass writes its outputs: the full pass the final ones, the offset
     // pass those from a zero incoming state (to the output, completed by
     // seg_out_kernel), the transition pass the output map G.
-    const CUtensorMap* omap = mode == kModeTransition ? &maps.g : &maps.o;
     float* slot = nullptr;                              // B, M, S of this segment
     float* next_slot = nullptr;                         // of the next segment
     if (p.seg_phase) {
@@ -931,139 +936,13 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     // barriers (named_sync_or) and leaves its loop together.
     auto wait = [&](int slot, uint32_t parity) { return mbar_wait(&bars[slot], parity, kWaitLimit, kSuspendNs); };
 
-    if (tid == 0 && !split) {
+    if (tid == 0) {
         if (nchunks > 0 && tma_ok(0)) issue_tma(0);
         if (nchunks > 1 && tma_ok(1)) issue_tma(1);
     }
     __syncwarp();
 
-    if (!is_chain && split && warp < 4) {
-        // ============================================================== loader
-        // Warps 0-3 stream the chunk records of the split preparation: -W^T, P
-        // and Qs by bulk copy, K by TMA (plain loads at the ragged end of the
-        // buffers), U0^T from global memory into D_X (both column halves of
-        // the thread's TMEM lane), the chain's vectors into shared memory.
-        // Thread 0 also issues the output MMAs of the chain's previous chunk
-        // (the chain's lead thread, whose MMA issue blocks at the tensor
-        // pipe's pace, then only issues the state-critical ones): O^T =
-        // Zb Qs^T once that chunk's X MMAs have completed and U^T P^T once its
-        // Z MMAs were issued, so neither delays the state chain in the pipe.
-        constexpr uint32_t kLoadThreads = 128;
-        const int pt = tid;
-        const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
-        const uint32_t id_o = idesc_bf16(128, 64, 0, 0);    // B = Qs or P, K-major
-        auto issue_oq = [&](int c) {                        // thread 0: O^T = Zb Qs^T of chunk c
-            if (!wait(B_X, uint32_t(c & 1))) return false;
-            tc_fence_after();
-            const uint64_t dQ = smem_desc(smem_u32(stage_ptr(c) + 8192), 16, 1024, kSwizzle128B);
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
-                umma_f16_tmemA((c & 1) ? tGW : tO, tZb + s * 8, dQ + (off >> 4), id_o, s > 0);
-            }
-            umma_commit(&bars[B_OQ]);
-            return true;
-        };
-        auto issue_op = [&](int c) {                        // thread 0: O^T += U^T P^T of chunk c
-            if (!wait(B_ZISS, uint32_t(c & 1))) return false;
-            tc_fence_after();
-            const uint64_t dP = smem_desc(smem_u32(sm + kOffP + uint32_t((c & 1) * 2) * 8192u), 16, 1024,
-                                          kSwizzle128B);
-            // (U hi, P hi), (U hi, P lo), (U lo, P hi)
-#pragma unroll
-            for (int pr = 0; pr < 3; ++pr)
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    umma_f16_tmemA((c & 1) ? tGW : tO, tU + (pr == 2 ? 32 : 0) + s * 8,
-                                   dP + uint64_t(((pr == 1 ? 8192 : 0) + s * 32) >> 4), id_o, 1);
-            umma_commit(&bars[B_O]);
-            return true;
-        };
-        bool fail = false;
-        for (int c = 0; c < nchunks; ++c) {
-            const int b = c & 1;
-            uint8_t* kq = stage_ptr(c);
-            const uint8_t* rec = p.prep_ws + (size_t(h) * size_t(p.prep_slots) + size_t(slot0 + c)) * kPrepRecordBytes;
-            const bool tk = tma_ok(c);
-            // U0^T of this thread's TMEM lane (the fragments of preparing
-            // warps w and w + 4), loaded early and consumed after XREAD
-            float u[64];
-            if (mode != kModeTransition) {
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const float4* src = reinterpret_cast<const float4*>(rec + kRecU) + (warp + 4 * hf) * 8 * 32 + lane;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float4 w = __ldg(src + i * 32);
-                        u[hf * 32 + 4 * i] = w.x;
-                        u[hf * 32 + 4 * i + 1] = w.y;
-                        u[hf * 32 + 4 * i + 2] = w.z;
-                        u[hf * 32 + 4 * i + 3] = w.w;
-                    }
-                }
-            }
-            bool lf = false;
-            if (tid == 0) {
-                if (c >= 2) lf = !wait(B_SFREE0 + b, uint32_t(((c - 2) >> 1) & 1));
-                if (c >= 2 && !lf) lf = !wait(b ? B_WTFREE1 : B_WTFREE, uint32_t(((c - 2) >> 1) & 1));
-                if (!lf) {
-                    uint64_t* bar = &bars[B_RAW0 + b];
-                    s_tma_last[b] = c;
-                    mbar_arrive_expect_tx(bar, 16384u + 32768u + (tk ? 16384u : 0u));
-                    bulk_load(sm + (b ? kOffTb : kOffWt), rec + kRecWt, 16384, bar);
-                    bulk_load(kq + 8192, rec + kRecQ, 8192, bar);   // P follows once its buffer is free (below)
-                    bulk_load(kq + 24576, rec + kRecQ + 8192, 8192, bar);
-                    if (tk) {
-                        const int y = int(chunk_start(c));
-                        tma_load_2d(kq + 0, &maps.k, bar, kh * kD, y);
-                        tma_load_2d(kq + 16384, &maps.k, bar, kh * kD + 64, y);
-                    }
-                }
-            }
-            __syncwarp();
-            if (named_sync_or(kBarPrep, kLoadThreads, lf)) { fail = true; break; }
-            if (!tk) {
-                const int64_t cs = chunk_start(c);
-                for (int idx = pt; idx < kC * 16; idx += kLoadThreads) {
-                    const int r = idx >> 4, cc = (idx & 15) * 8;
-                    const int64_t t = cs + r;
-                    uint4 zk = make_uint4(0, 0, 0, 0);
-                    if (t < t_end_all) zk = *reinterpret_cast<const uint4*>(gk + t * p.k_stride + kh * kD + cc);
-                    *reinterpret_cast<uint4*>(kq + toff(r, cc, 16384)) = zk;
-                }
-                fence_proxy_async_smem();
-            }
-            if (pt < kC) cE[b * kC + pt] = reinterpret_cast<const float*>(rec + kRecVec)[pt];
-            if (pt == kC) cGS[b] = reinterpret_cast<const float*>(rec + kRecVec)[kC];
-            if (c >= 1 && tid == 0) lf = !issue_oq(c - 1);
-            if (tid == 0 && !lf) {
-                // the chain frees P of chunk c - 2 once that chunk's outputs are complete
-                if (c >= 2) lf = !wait(B_PFREE0 + b, uint32_t(((c - 2) >> 1) & 1));
-                if (!lf) bulk_load(sm + kOffP + uint32_t(b * 2) * 8192u, rec + kRecP, 16384, &bars[B_RAW0 + b]);
-            }
-            if (mode != kModeTransition) {
-                if (tid == 0 && c >= 1 && !lf) lf = !wait(B_XREAD, uint32_t((c - 1) & 1));
-                __syncwarp();
-                if (named_sync_or(kBarPrep, kLoadThreads, lf)) { fail = true; break; }
-                tc_fence_after();
-#pragma unroll
-                for (int q = 0; q < 64; q += 16) tmem_st16(tX + lane_addr + q, u + q);
-                tmem_st_wait();
-            }
-            if (tid == 0 && !lf) lf = !wait(B_RAW0 + b, uint32_t((c >> 1) & 1));
-            __syncwarp();
-            tc_fence_before();
-            if (named_sync_or(kBarPrep, kLoadThreads, lf)) { fail = true; break; }
-            if (tid == 0) mbar_arrive(&bars[B_READY0 + b]);
-            if (c >= 1 && tid == 0) lf = !issue_op(c - 1);
-            __syncwarp();
-            if (named_sync_or(kBarPrep, kLoadThreads, lf)) { fail = true; break; }
-        }
-        if (!fail && nchunks > 0 && tid == 0)   // the last chunk's outputs
-            fail = !issue_oq(nchunks - 1) || !issue_op(nchunks - 1);
-        __syncwarp();
-        if (fail) *s_err = 1;
-    } else if (!is_chain) {
+    if (!is_chain) {
         // ================================================================ prep
         // Thread 0 alone polls mbarriers; the group learns the outcome through
         // a voting named barrier (many pollers would starve the other warps).
@@ -1328,87 +1207,10 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         uint32_t opk[32];
         int64_t o_cs = 0;
         int o_rows = 0;
-        // With records a chunk's output tile is staged in shared memory
-        // ([64 rows][128 columns] bf16, 128-byte swizzle, two buffers where the
-        // inline preparation keeps A, T and its scratch): read out of TMEM as
-        // MMA-ordered fragments and stored transposed (stmatrix), then written
-        // by one TMA store, or as 16-byte rows where the chunk ends inside the
-        // buffers (its other rows belong to the next sequence).
-        uint8_t* const o_stage = sm + kOffA;
-        // O^T of chunk cc (TMEM buffer cc & 1) into staging buffer cc & 1:
-        // this warp's lanes (j) and column half (t) as 16x256b fragments.
-        auto stage_out = [&](int cc) {
-            uint8_t* st = o_stage + uint32_t(cc & 1) * 16384u;
-            const uint32_t tOc = (cc & 1) ? tGW : tO;
-            uint32_t r[4][8];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                tmem_ld_16x256b_x2(tOc + (uint32_t(quarter * 32 + 16 * (u >> 1)) << 16) + uint32_t(hc * 32 + 16 * (u & 1)),
-                                   r[u]);
-            tmem_ld_wait();
-            const int m = lane >> 3, rr = lane & 7;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                uint32_t f[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    f[e] = pack_bf16x2(__uint_as_float(r[u][2 * e]) * p.q_scale,
-                                       __uint_as_float(r[u][2 * e + 1]) * p.q_scale);
-                const int t = hc * 32 + 16 * (u & 1) + 8 * (m >> 1) + rr;
-                const int j = quarter * 32 + 16 * (u >> 1) + 8 * (m & 1);
-                stmatrix_x4_trans(smem_u32(st + toff(t, j, 8192)), f);
-            }
-            fence_proxy_async_smem();
-        };
-        // After a barrier: the staged tile of chunk cc to the output, by one
-        // TMA store when every row of the box is this sequence's or lies past
-        // the buffers, else as 16-byte rows.
-        auto write_out_tile = [&](int cc) {
-            const uint8_t* st = o_stage + uint32_t(cc & 1) * 16384u;
-            if (o_rows == kC || o_cs + o_rows >= p.t_cap) {
-                if (lead) {
-                    tma_store_2d(omap, st, h * kD, int(o_cs));
-                    tma_store_2d(omap, st + 8192, h * kD + 64, int(o_cs));
-                }
-            } else {
-                for (int idx = ct; idx < kC * 16; idx += int(kChainN)) {
-                    const int r = idx >> 4, col = (idx & 15) * 8;
-                    if (r < o_rows)
-                        *reinterpret_cast<uint4*>(gout + ((o_cs + r) * Hv + h) * kD + col) =
-                            *reinterpret_cast<const uint4*>(st + toff(r, col, 8192));
-                }
-            }
-            if (lead) bulk_commit_group();
-        };
         if (nchunks == 0) {
             if (final_dst)
                 for (int d = hc * 64; d < (hc + kHalves) * 64; ++d)
                     final_dst[size_t(d) * kD + row] = init_src ? init_src[size_t(d) * kD + row] : 0.f;
-        } else if (split) {
-            // ---- incoming state (this thread's column half), loaded while the
-            // loader fetches the first record: Zb = bf16(S_0^T), Z = exp(gamma_S(0)) S_0^T
-            float z[64];
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const int d = hc * 64 + i;
-                z[i] = init_src ? init_src[size_t(d) * kD + row] : (init_identity && d == row ? 1.f : 0.f);
-            }
-            bool lf = lead && !wait(B_READY0, 0);
-            __syncwarp();
-            fail = named_sync_or(kBarChain, kChainN, lf);
-            const float gs0 = cGS[0];
-            uint32_t zb[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) zb[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
-            GDN_TMEM_ST_X16(tZb + lane_addr + hc * 32, zb);
-            GDN_TMEM_ST_X16(tZb + lane_addr + hc * 32 + 16, (zb + 16));
-#pragma unroll
-            for (int i = 0; i < 64; ++i) z[i] *= gs0;
-#pragma unroll
-            for (int q = 0; q < 64; q += 16) tmem_st16(tZ + lane_addr + hc * 64 + q, z + q);
-            tmem_st_wait();
-            tc_fence_before();
-            named_sync(kBarChain, kChainN);
         } else {
             // ---- incoming state: Zb = bf16(Z), Z <- exp(gamma_S(0)) Z -----------
             bool lf = lead && !wait(B_READY0, 0);
@@ -1449,15 +1251,14 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 lf = !wait(B_READY0 + b, uint32_t((c >> 1) & 1));
                 if (!lf) {
                     tc_fence_after();
-                    // -W^T: one buffer inline; two (even, odd chunks) with split preparation
-                    const uint64_t dWt = smem_desc(smem_u32(sm + (split && b ? kOffTb : kOffWt)), 16384, 1024,
+                    const uint64_t dWt = smem_desc(smem_u32(sm + kOffWt), 16384, 1024,
                                                    kSwizzle128B);
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
                         umma_f16_tmemA(tX, tZb + s * 8, dWt + uint64_t(s * 2048 >> 4), id_x,
                                        mode != kModeTransition || s > 0);
                     umma_commit(&bars[B_X]);
-                    if (!split) {                     // with records the loader lead issues these
+                    {
                         const uint64_t dQ = smem_desc(smem_u32(kq + 8192), 16, 1024, kSwizzle128B);
 #pragma unroll
                         for (int s = 0; s < 8; ++s) {
@@ -1471,19 +1272,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             // previous chunk's output rows, while the MMAs run (with records:
             // its O^T, once complete, is staged here and written after the
             // next barrier; its P buffer is free then)
-            bool o_staged = false;
-            if (kSplit && c > 0) {
-                if (lead && !lf) {
-                    lf = !wait(B_O, uint32_t((c - 1) & 1));
-                    if (!lf) mbar_arrive(&bars[B_PFREE0 + ((c - 1) & 1)]);
-                    bulk_wait_group_read<1>();           // staging buffer (c - 1) & 1 read by its last store
-                }
-                __syncwarp();
-                if (named_sync_or(kBarChain, kChainN, lf)) { fail = true; break; }
-                tc_fence_after();
-                stage_out(c - 1);
-                o_staged = true;
-            } else if (!kSplit && c > 0) {
+            if (c > 0) {
                 __nv_bfloat16* dst = gout + (o_cs * Hv + h) * kD + row;
 #pragma unroll
                 for (int k = 0; k < kHalves * 16; ++k) {
@@ -1497,9 +1286,8 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             __syncwarp();
             if (named_sync_or(kBarChain, kChainN, lf)) { fail = true; break; }
             tc_fence_after();
-            if (lead) mbar_arrive(&bars[split && b ? B_WTFREE1 : B_WTFREE]);
+            if (lead) mbar_arrive(&bars[B_WTFREE]);
             __syncwarp();
-            if (o_staged) write_out_tile(c - 1);
             // ---- U (hi, lo) and Us = U diag(e) (hi, lo) into TMEM --------------
             for (int hf = hc; hf < hc + kHalves; ++hf) {
                 float x[32];
@@ -1532,8 +1320,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     for (int s = 0; s < 4; ++s)
                         umma_f16_tmemA(tZ, tU + 64 + part * 32 + s * 8, dK + uint64_t(s * 2048 >> 4), id_z, 1);
                 umma_commit(&bars[B_Z]);
-                if (split) mbar_arrive(&bars[B_ZISS]);
-                if (!split) {
+                {
                     // (U hi, P hi), (U hi, P lo), (U lo, P hi)
 #pragma unroll
                     for (int pr = 0; pr < 3; ++pr)
@@ -1550,10 +1337,9 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             if (lead) {
                 lf = !wait(B_Z, uint32_t(c & 1));
                 // the O issuer's Zb Qs^T must be done before Zb and the stage are reused
-                if (!lf && split) lf = !wait(B_OQ, uint32_t(c & 1));
                 if (!lf) {
                     mbar_arrive(&bars[B_SFREE0 + b]);
-                    if (!split && c + 2 < nchunks && tma_ok(c + 2)) issue_tma(c + 2);
+                    if (c + 2 < nchunks && tma_ok(c + 2)) issue_tma(c + 2);
                     if (has_next) lf = !wait(B_READY0 + (b ^ 1), uint32_t(((c + 1) >> 1) & 1));
                 }
             }
@@ -1589,7 +1375,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             }
             tmem_st_wait();
             // ---- output rows to registers (stored during the next chunk) --------
-            if (!kSplit) {
+            {
                 if (lead) lf = !wait(B_O, uint32_t(c & 1));
                 __syncwarp();
                 if (named_sync_or(kBarChain, kChainN, lf)) { fail = true; break; }
@@ -1608,25 +1394,10 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             o_rows = rows;
             tc_fence_before();
             named_sync(kBarChain, kChainN);
-            if (lead && !kSplit) mbar_arrive(&bars[B_PFREE0 + b]);   // with records: at the next chunk
+            if (lead) mbar_arrive(&bars[B_PFREE0 + b]);
             __syncwarp();
         }
-        if (kSplit) {
-            if (!fail && nchunks > 0) {                  // the last chunk's outputs
-                bool lf = lead && !wait(B_O, uint32_t((nchunks - 1) & 1));
-                if (lead) bulk_wait_group_read<1>();
-                __syncwarp();
-                if (!named_sync_or(kBarChain, kChainN, lf)) {
-                    tc_fence_after();
-                    stage_out(nchunks - 1);
-                    named_sync(kBarChain, kChainN);
-                    write_out_tile(nchunks - 1);
-                } else {
-                    fail = true;
-                }
-            }
-            if (lead) bulk_wait_all();                   // tile stores done before the CTA exits
-        } else if (!fail && nchunks > 0) {
+        if (!fail && nchunks > 0) {
             __nv_bfloat16* dst = gout + (o_cs * Hv + h) * kD + row;
 #pragma unroll
             for (int k = 0; k < kHalves * 16; ++k) {
@@ -1660,31 +1431,53 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 // segment pass) carries the transposed state Z = S^T through its chunks.  Per
 // chunk c (rows i, value columns j):
 //   [X | O] = Zb [-W^T | Qs^T]          one N = 128 product, A = Zb from TMEM
-//   U^T = U0^T + X,  Us^T = U^T diag(e)  bf16 hi + lo into TMEM
+//   U^T = U0^T + X,  Us^T = U^T diag(e)  Us as bf16 hi + lo, U as bf16
 //   Z += Us^T K                          Z pre-scaled by exp(gamma_S)
-//   O += U^T P^T                         (U hi, P hi), (U hi, P lo), (U lo, P hi)
+//   O += U^T P^T                         (U, P hi), (U, P lo)
 //   Zb = bf16(Z), Z <- exp(gamma_S(c+1)) Z
-// Sixteen warps share every epilogue: four per TMEM lane quarter, each a
-// quarter of the columns, so no thread walks more than 32 columns.  The lead
-// thread issues every MMA and streams the records' MMA operands (the -W | Qs
-// tile, P, K) and U0^T into two slots, a chunk ahead; the end weights e and
-// exp(gamma_S) go from the record to the threads' registers.  The output
-// products of a chunk are issued right behind its state update, so they run
-// while the state epilogue works, and the output tile is stored during the
-// next chunk.
-constexpr uint32_t kStThreads = 512;
-constexpr uint32_t kStChainThreads = kStThreads;
-constexpr uint32_t kBarSt = 1;                           // named barrier of the chain warps
-// Shared memory: two slots of [-W | Qs tile (32 KB) | P hi, lo (16 KB) | K (16 KB) |
-// U0^T fragments (32 KB)], then two output staging tiles (16 KB each).
+// Roles.  An MMA issue blocks the issuing thread at the tensor pipe's pace
+// (about 70 cycles per instruction), so one thread of a warp of its own (the
+// MMA issuer) issues every product, and one thread of another (the copier)
+// every record copy (the WQ tile, P and U0^T, K and the vectors of a chunk
+// into one of two slots, a chunk ahead) and the output tile stores.  Sixteen
+// epilogue warps share every epilogue: four per
+// TMEM lane quarter, each a quarter of the columns.  The hand-offs are
+// mbarriers: the issuer's commits (X, Z, O done) and one arrival per epilogue
+// warp (Us written, U written, output tile staged, Zb written).  The
+// dependent chain of a chunk is [X | O] product -> Us epilogue -> Z product ->
+// Zb epilogue; U, the state's pre-scaling, the output products and the
+// previous chunk's output tile all fill the gaps.  The output products of
+// chunk c - 1 are issued right behind chunk c's [X | O] product (U is double
+// buffered for them), so they run while the Us epilogue works.
+constexpr uint32_t kStEpiWarps = 16;
+constexpr uint32_t kStEpiThreads = kStEpiWarps * 32;
+constexpr uint32_t kStThreads = kStEpiThreads + 64;       // + the MMA issuer's and the copier's warps
+// Shared memory: two slots of [WQ tile (32 KB) | P hi, lo (16 KB) | U0^T fragments
+// (32 KB) | K (16 KB)] (P and U0^T as one copy: they follow each other in the
+// record), two output staging tiles (16 KB each), the two slots' record
+// vectors (512 B each).
 constexpr uint32_t kStSlot = 98304;
-constexpr uint32_t kStOffP = 32768, kStOffK = 49152, kStOffU = 65536;
+constexpr uint32_t kStOffP = 32768, kStOffU = 49152, kStOffK = 81920;
+static_assert(kStOffP - 0 == kRecP - kRecWQ && kStOffU - kStOffP == kRecU - kRecP, "slot mirrors the record");
 constexpr uint32_t kStOffO = 2 * kStSlot;
-constexpr uint32_t kStOffBar = kStOffO + 2 * 16384;
-enum : int { ST_FULL0 = 0, ST_X = 2, ST_Z = 3, ST_O = 4, ST_DRAIN = 5, ST_NBARS = 6 };
+constexpr uint32_t kStOffVec = kStOffO + 2 * 16384;
+constexpr uint32_t kStOffBar = kStOffVec + 2 * 512;
+enum : int {
+    ST_FULL0 = 0,        // slot b's record copies landed (issuer's expect_tx)
+    ST_X = 2,            // [X | O] product of the chunk done
+    ST_Z = 3,            // state update done
+    ST_O0 = 4,           // output products of a chunk into O buffer b done (and every earlier product)
+    ST_UREADY = 6,       // Us in TMEM (one arrival per epilogue warp)
+    ST_ZBREADY = 7,      // Zb in TMEM
+    ST_OSTAGED = 8,      // output tile staged
+    ST_SFREE0 = 9,       // staging tile b read by its store
+    ST_UHREADY = 11,     // U in TMEM
+    ST_DRAIN = 12,
+    ST_NBARS = 13
+};
 constexpr uint32_t kStSmemBytes = kStOffBar + ST_NBARS * 8 + 16 + 1024;
 static_assert(kStSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-block limit");
-// TMEM: Z (128) | Zb (64) | O odd (64) | X (64) | O even (64) | U hi, U lo, Us hi, Us lo (4 x 32).
+// TMEM: Z (128) | Zb (64) | O odd (64) | X (64) | O even (64) | U even, U odd, Us hi, Us lo (4 x 32).
 // [X | O even] and [O odd | X] are the two N = 128 accumulators of the merged product.
 constexpr uint32_t kStColZ = 0, kStColZb = 128, kStColOodd = 192, kStColX = 256, kStColOeven = 320,
                    kStColU = 384;
@@ -1701,7 +1494,9 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 
     const int h = blockIdx.x, n = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, sub = warp >> 2;
+    const bool is_issuer = warp == int(kStEpiWarps);
+    const bool is_copier = warp == int(kStEpiWarps) + 1;
+    const int quarter = warp & 3, sub = (warp >> 2) & 3;
     const int row = quarter * 32 + lane;                 // TMEM lane of this thread (value column j)
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
     const int kh = h / (p.Hv / p.Hk);
@@ -1747,6 +1542,7 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     // (segment 0 of phase 1), B_s (fp32) or the M_s^T image
     const float* init_src = seg == 0 && p.state_in ? p.state_in + sbase : nullptr;
     const bool init_identity = mode == kModeTransition;
+    const bool has_u0 = mode != kModeTransition;
     float* final_dst = nullptr;
     uint8_t* img_dst = nullptr;
     if (mode == kModeFull) {
@@ -1761,15 +1557,23 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         return p.prep_ws + (size_t(h) * size_t(p.prep_slots) + size_t(slot0 + c)) * kPrepRecordBytes;
     };
     auto chunk_start = [&](int c) { return t0 + int64_t(c) * p.chunk; };
+    auto chunk_rows = [&](int c) {
+        const int64_t cs = chunk_start(c);
+        return int(t1 - cs < p.chunk ? t1 - cs : p.chunk);
+    };
+    // A chunk's output tile goes out by TMA when every row of the box is this
+    // sequence's or lies past the buffers; else as 16-byte rows (the box's
+    // other rows belong to the next sequence).
+    auto tile_by_tma = [&](int c) { return chunk_rows(c) == kC || chunk_start(c) + chunk_rows(c) >= p.t_cap; };
     auto wait = [&](int b, uint32_t parity) { return mbar_wait(&bars[b], parity, kWaitLimit, kSuspendNs); };
 
     if (tid == 0) {
-        for (int i = 0; i < ST_NBARS; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < ST_NBARS; ++i)
+            mbar_init(&bars[i], (i == ST_UREADY || i == ST_UHREADY || i == ST_ZBREADY || i == ST_OSTAGED)
+                                    ? kStEpiWarps : 1);
         fence_mbar_init();
         *s_err = 0;
         *s_issued = 0;
-        tma_prefetch_desc(&maps.k);
-        tma_prefetch_desc(omap);
     }
     __syncwarp();
     if (warp == 0) {
@@ -1780,69 +1584,156 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t tZ = tmem + kStColZ, tZb = tmem + kStColZb, tX = tmem + kStColX, tU = tmem + kStColU;
+    auto tO = [&](int c) { return tmem + ((c & 1) ? kStColOodd : kStColOeven); };
+    auto tXO = [&](int c) { return tmem + ((c & 1) ? kStColOodd : kStColX); };
+    uint8_t* const o_stage = sm + kStOffO;
 
-    {
-        // Thread 0 (the lead) polls the mbarriers, issues every MMA and every
-        // record copy; the group follows through voting named barriers.
-        const int ct = tid;
-        const bool lead = ct == 0;
+    if (is_copier) {
+        // ============================================================ copier
+        if (lane == 0 && nchunks > 0) {
+            tma_prefetch_desc(&maps.k);
+            tma_prefetch_desc(omap);
+            // The record operands of chunk c into slot c & 1: the merged B
+            // tile (the record's WQ tile, whose order matches the accumulator
+            // pair [X | O even] or [O odd | X] of the chunk's parity), P hi | lo
+            // with U0^T, the raw K tile (rows at or past the buffers' end read
+            // as zero; rows past the sequences' end are cleared by the
+            // epilogue warps) and the vectors.
+            auto issue_copies = [&](int c) {
+                const int b = c & 1;
+                uint8_t* sp = sm + uint32_t(b) * kStSlot;
+                const uint8_t* rec = record(c);
+                uint64_t* bar = &bars[ST_FULL0 + b];
+                mbar_arrive_expect_tx(bar, 32768u + 16384u + 16384u + 512u + (has_u0 ? 32768u : 0u));
+                bulk_load(sp, rec + kRecWQ, 32768, bar);
+                bulk_load(sp + kStOffP, rec + kRecP, has_u0 ? 49152u : 16384u, bar);
+                tma_load_2d(sp + kStOffK, &maps.k, bar, kh * kD, int(chunk_start(c)));
+                tma_load_2d(sp + kStOffK + 8192, &maps.k, bar, kh * kD + 64, int(chunk_start(c)));
+                bulk_load(sm + kStOffVec + uint32_t(b) * 512u, rec + kRecVec, 512, bar);
+                *s_issued = c + 1;
+            };
+            // the staged output tile of chunk cc to the output (TMA; one bulk
+            // group per chunk, empty when the epilogue warps stored the rows);
+            // chunk cc - 1's staging tile is free once its store has read it
+            auto store_tile = [&](int cc) {
+                if (!wait(ST_OSTAGED, uint32_t(cc & 1))) return false;
+                const uint8_t* st = o_stage + uint32_t(cc & 1) * 16384u;
+                if (tile_by_tma(cc)) {
+                    tma_store_2d(omap, st, h * kD, int(chunk_start(cc)));
+                    tma_store_2d(omap, st + 8192, h * kD + 64, int(chunk_start(cc)));
+                }
+                bulk_commit_group();
+                bulk_wait_group_read<1>();
+                if (cc >= 1) mbar_arrive(&bars[ST_SFREE0 + ((cc - 1) & 1)]);
+                return true;
+            };
+            issue_copies(0);
+            if (nchunks > 1) issue_copies(1);
+            bool fail = false;
+            for (int c = 1; c < nchunks && !fail; ++c) {
+                // slot (c + 1) & 1 held chunk c - 1, whose products are done once
+                // its output products are: it takes chunk c + 1
+                if (!wait(ST_O0 + ((c - 1) & 1), uint32_t(((c - 1) >> 1) & 1))) {
+                    fail = true;
+                    break;
+                }
+                if (c + 1 < nchunks) issue_copies(c + 1);
+                if (!store_tile(c - 1)) fail = true;
+            }
+            if (!fail && !store_tile(nchunks - 1)) fail = true;
+            bulk_wait_all();                              // tile stores done before the CTA exits
+            if (fail) *s_err = 1;
+        }
+    } else if (is_issuer) {
+        // ========================================================= MMA issuer
+        if (lane == 0 && nchunks > 0) {
+            const uint32_t id_xo = idesc_bf16(128, 128, 0, 0);   // B = the merged tile, K-major
+            const uint32_t id_o = idesc_bf16(128, 64, 0, 0);     // B = P, K-major
+            const uint32_t id_z = idesc_bf16(128, 128, 0, 1);    // B = raw K, MN-major [i][d]
+            // O += U^T P^T of chunk cc: (U, P hi), (U, P lo); U of chunk cc in
+            // TMEM buffer cc & 1 (written once ST_UHREADY's phase cc completed)
+            auto issue_op = [&](int cc) {
+                tc_fence_after();
+                const uint8_t* sp = sm + uint32_t(cc & 1) * kStSlot;
+                const uint64_t dP = smem_desc(smem_u32(sp + kStOffP), 16, 1024, kSwizzle128B);
+#pragma unroll
+                for (int pr = 0; pr < 2; ++pr)
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        umma_f16_tmemA(tO(cc), tU + uint32_t(cc & 1) * 32 + s * 8,
+                                       dP + uint64_t((pr * 8192 + s * 32) >> 4), id_o, 1);
+                umma_commit(&bars[ST_O0 + (cc & 1)]);
+            };
+            bool fail = false;
+            for (int c = 0; c < nchunks && !fail; ++c) {
+                const int b = c & 1;
+                // ---- [X | O] = Zb [-W^T | Qs^T] ------------------------------------
+                // (U of chunk c - 1 is known before this product is issued, so
+                // that phase of ST_UHREADY cannot be overtaken)
+                if (!wait(ST_FULL0 + b, uint32_t((c >> 1) & 1)) || !wait(ST_ZBREADY, uint32_t(c & 1)) ||
+                    (c >= 1 && !wait(ST_UHREADY, uint32_t((c - 1) & 1)))) {
+                    fail = true;
+                    break;
+                }
+                tc_fence_after();
+                {
+                    const uint64_t dB = smem_desc(smem_u32(sm + uint32_t(b) * kStSlot), 16, 1024, kSwizzle128B);
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
+                        umma_f16_tmemA(tXO(c), tZb + s * 8, dB + (off >> 4), id_xo, s > 0);
+                    }
+                    umma_commit(&bars[ST_X]);
+                }
+                // ---- O += U^T P^T of the previous chunk, behind it -------------------
+                if (c >= 1) issue_op(c - 1);
+                // ---- Z += Us^T K -------------------------------------------------------
+                if (!wait(ST_UREADY, uint32_t(c & 1))) { fail = true; break; }
+                tc_fence_after();
+                {
+                    const uint8_t* sp = sm + uint32_t(b) * kStSlot;
+                    const uint64_t dK = smem_desc(smem_u32(sp + kStOffK), 8192, 1024, kSwizzle128B);
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int s = 0; s < 4; ++s)
+                            umma_f16_tmemA(tZ, tU + 64 + part * 32 + s * 8, dK + uint64_t(s * 2048 >> 4), id_z, 1);
+                    umma_commit(&bars[ST_Z]);
+                }
+            }
+            if (!fail) {
+                if (wait(ST_UHREADY, uint32_t((nchunks - 1) & 1))) issue_op(nchunks - 1);
+                else fail = true;
+            }
+            if (fail) *s_err = 1;
+        }
+    } else {
+        // =========================================================== epilogue
+        // Lane 0 of each warp polls the mbarriers; the warp follows.
         __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(mode == kModeTransition ? p.g_out : p.out);
-        const uint32_t tZ = tmem + kStColZ, tZb = tmem + kStColZb, tX = tmem + kStColX, tU = tmem + kStColU;
-        auto tO = [&](int c) { return tmem + ((c & 1) ? kStColOodd : kStColOeven); };
-        auto tXO = [&](int c) { return tmem + ((c & 1) ? kStColOodd : kStColX); };
-        const uint32_t id_xo = idesc_bf16(128, 128, 0, 0);   // B = the merged tile, K-major
-        const uint32_t id_o = idesc_bf16(128, 64, 0, 0);     // B = P, K-major
-        const uint32_t id_z = idesc_bf16(128, 128, 0, 1);    // B = raw K, MN-major [i][d]
-        const bool has_u0 = mode != kModeTransition;
-        // This thread's part of a chunk's record vectors: the end weights e of
-        // columns 16 sub .. 16 sub + 15 and exp(gamma_S).
-        auto load_vec = [&](int c, float* e, float& gs) {
-            const uint8_t* rec = record(c);
-            const float4* ev = reinterpret_cast<const float4*>(rec + kRecVec) + sub * 4;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float4 w = __ldg(ev + k);
-                e[4 * k] = w.x;
-                e[4 * k + 1] = w.y;
-                e[4 * k + 2] = w.z;
-                e[4 * k + 3] = w.w;
-            }
-            gs = __ldg(reinterpret_cast<const float*>(rec + kRecVec) + kC);
+        auto warp_wait = [&](int b, uint32_t parity) {
+            bool ok = true;
+            if (lane == 0) ok = wait(b, parity);
+            return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         };
-        // U0^T of this thread's lane at columns 16 sub .. 16 sub + 15 from the
-        // slot's copy of the record's fragments (the preparing thread of that
-        // lane and column half wrote them as interleaved 16-byte groups).
-        const int u_pw = quarter + 4 * (sub >> 1);
-        auto load_u0 = [&](int b, float* u0) {
-            if (!has_u0) {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) u0[k] = 0.f;
-                return;
-            }
-            const float4* us = reinterpret_cast<const float4*>(sm + uint32_t(b) * kStSlot + kStOffU) +
-                               (u_pw * 8 + 4 * (sub & 1)) * 32 + lane;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float4 w = us[k * 32];
-                u0[4 * k] = w.x;
-                u0[4 * k + 1] = w.y;
-                u0[4 * k + 2] = w.z;
-                u0[4 * k + 3] = w.w;
-            }
+        auto warp_arrive = [&](int b) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[b]);
         };
-        // Output tiles: O^T of chunk cc read out of TMEM as MMA-ordered
+        // Output tile of chunk cc: O^T read out of TMEM as MMA-ordered
         // fragments (this warp: its 32 lanes, columns 16 sub .. 16 sub + 15)
-        // and stored transposed (stmatrix) into staging tile cc & 1
-        // ([64 rows][128 columns] bf16, 128-byte swizzle); after a barrier the
-        // lead writes it with TMA stores, or the group as 16-byte rows when
-        // the chunk ends inside the buffers (the box's other rows belong to
-        // the next sequence).
-        uint8_t* const o_stage = sm + kStOffO;
-        int64_t o_cs = 0;
-        int o_rows = 0;
+        // and stored transposed (stmatrix) into staging tile cc & 1 ([64 rows]
+        // [128 columns] bf16, 128-byte swizzle); where the tile cannot go out
+        // by TMA the warps store its rows.
         auto stage_out = [&](int cc) {
+            // staging tile cc & 1 was last read by chunk cc - 2's store
+            if (cc >= 2 && !warp_wait(ST_SFREE0 + (cc & 1), uint32_t(((cc - 2) >> 1) & 1))) return false;
+            if (!warp_wait(ST_O0 + (cc & 1), uint32_t((cc >> 1) & 1))) return false;
+            tc_fence_after();
             uint8_t* st = o_stage + uint32_t(cc & 1) * 16384u;
             uint32_t r[2][8];
+            __syncwarp();
 #pragma unroll
             for (int u = 0; u < 2; ++u)
                 tmem_ld_16x256b_x2(tO(cc) + (uint32_t(quarter * 32 + 16 * u) << 16) + uint32_t(sub * 16), r[u]);
@@ -1860,46 +1751,23 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 stmatrix_x4_trans(smem_u32(st + toff(t, j, 8192)), f);
             }
             fence_proxy_async_smem();
-        };
-        auto write_out_tile = [&](int cc) {
-            const uint8_t* st = o_stage + uint32_t(cc & 1) * 16384u;
-            if (o_rows == kC || o_cs + o_rows >= p.t_cap) {
-                if (lead) {
-                    tma_store_2d(omap, st, h * kD, int(o_cs));
-                    tma_store_2d(omap, st + 8192, h * kD + 64, int(o_cs));
-                }
-            } else {
-                for (int idx = ct; idx < kC * 16; idx += int(kStChainThreads)) {
-                    const int r = idx >> 4, col = (idx & 15) * 8;
-                    if (r < o_rows)
-                        *reinterpret_cast<uint4*>(gout + ((o_cs + r) * Hv + h) * kD + col) =
-                            *reinterpret_cast<const uint4*>(st + toff(r, col, 8192));
+            if (!tile_by_tma(cc)) {
+                // this warp's part of the tile (rows 16 sub .., columns 32 quarter ..)
+                __syncwarp();
+                const int64_t o_cs = chunk_start(cc);
+                const int o_rows = chunk_rows(cc);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int idx = lane + 32 * k;
+                    const int r2 = sub * 16 + (idx >> 2), col = quarter * 32 + (idx & 3) * 8;
+                    if (r2 < o_rows)
+                        *reinterpret_cast<uint4*>(gout + ((o_cs + r2) * Hv + h) * kD + col) =
+                            *reinterpret_cast<const uint4*>(st + toff(r2, col, 8192));
                 }
             }
-            if (lead) bulk_commit_group();
-        };
-        // Lead: the record operands of chunk c into slot c & 1: the merged B
-        // tile (K-major, 128 rows per 64-column block: -W then Qs for even
-        // chunks, Qs then -W for odd ones, matching the accumulator pairs
-        // [X | O even] and [O odd | X]), P hi | lo and the raw K tile (rows at
-        // or past the buffers' end read as zero; rows past the sequences' end
-        // are cleared after landing).
-        auto issue = [&](int c) {
-            const int b = c & 1;
-            uint8_t* sp = sm + uint32_t(b) * kStSlot;
-            const uint8_t* rec = record(c);
-            uint64_t* bar = &bars[ST_FULL0 + b];
-            mbar_arrive_expect_tx(bar, 65536u + (has_u0 ? 32768u : 0u));
-            const uint32_t w_at = b ? 8192u : 0u, q_at = b ? 0u : 8192u;
-            bulk_load(sp + w_at, rec + kRecWt, 8192, bar);
-            bulk_load(sp + 16384 + w_at, rec + kRecWt + 8192, 8192, bar);
-            bulk_load(sp + q_at, rec + kRecQ, 8192, bar);
-            bulk_load(sp + 16384 + q_at, rec + kRecQ + 8192, 8192, bar);
-            bulk_load(sp + kStOffP, rec + kRecP, 16384, bar);
-            tma_load_2d(sp + kStOffK, &maps.k, bar, kh * kD, int(chunk_start(c)));
-            tma_load_2d(sp + kStOffK + 8192, &maps.k, bar, kh * kD + 64, int(chunk_start(c)));
-            if (has_u0) bulk_load(sp + kStOffU, rec + kRecU, 32768, bar);
-            *s_issued = c + 1;
+            tc_fence_before();
+            warp_arrive(ST_OSTAGED);
+            return true;
         };
         bool fail = false;
         if (nchunks == 0) {
@@ -1907,15 +1775,10 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 for (int d = sub * 32; d < sub * 32 + 32; ++d)
                     final_dst[size_t(d) * kD + row] = init_src ? init_src[size_t(d) * kD + row] : 0.f;
         } else {
-            if (lead) {
-                issue(0);
-                if (nchunks > 1) issue(1);
-            }
-            float ev[16], gs;
-            load_vec(0, ev, gs);
             {
                 // ---- incoming state (this thread: key rows 32 sub .. 32 sub + 31):
                 // Zb = bf16(S_0^T), Z = exp(gamma_S(0)) S_0^T
+                const float gs = __ldg(reinterpret_cast<const float*>(record(0) + kRecVec) + kC);
                 float z[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -1931,119 +1794,85 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 tmem_st16(tZ + lane_addr + sub * 32, z);
                 tmem_st16(tZ + lane_addr + sub * 32 + 16, z + 16);
                 tmem_st_wait();
+                tc_fence_before();
+                warp_arrive(ST_ZBREADY);
             }
-            tc_fence_before();
-            named_sync(kBarSt, kStChainThreads);
             for (int c = 0; c < nchunks; ++c) {
                 const int b = c & 1;
                 const int64_t cs = chunk_start(c);
-                const int rows = int(t1 - cs < p.chunk ? t1 - cs : p.chunk);
                 const bool has_next = c + 1 < nchunks;
-                // ---- [X | O] = Zb [-W^T | Qs^T] ------------------------------------
-                bool lf = false;
-                if (lead) {
-                    lf = !wait(ST_FULL0 + b, uint32_t((c >> 1) & 1));
-                    if (!lf) {
-                        tc_fence_after();
-                        const uint64_t dB = smem_desc(smem_u32(sm + uint32_t(b) * kStSlot), 16, 1024, kSwizzle128B);
-#pragma unroll
-                        for (int s = 0; s < 8; ++s) {
-                            const uint32_t off = uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u;
-                            umma_f16_tmemA(tXO(c), tZb + s * 8, dB + (off >> 4), id_xo, s > 0);
-                        }
-                        umma_commit(&bars[ST_X]);
-                    }
-                }
-                // ---- the previous chunk's output tile ------------------------------
-                if (c > 0) {
-                    if (lead && !lf) {
-                        lf = !wait(ST_O, uint32_t((c - 1) & 1));
-                        // every product of chunk c - 1 is done: its slot takes chunk c + 1
-                        if (!lf && has_next) issue(c + 1);
-                        bulk_wait_group_read<1>();        // staging tile (c - 1) & 1 read by its last store
-                    }
-                    __syncwarp();
-                    if (named_sync_or(kBarSt, kStChainThreads, lf)) {
-                        fail = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    stage_out(c - 1);
-                }
-                if (lead && !lf) lf = !wait(ST_X, uint32_t(c & 1));
-                __syncwarp();
-                if (named_sync_or(kBarSt, kStChainThreads, lf)) {
+                // exp(gamma_S) of the next chunk, for the state's pre-scaling
+                const float gsn = has_next ? __ldg(reinterpret_cast<const float*>(record(c + 1) + kRecVec) + kC) : 1.f;
+                if (!warp_wait(ST_FULL0 + b, uint32_t((c >> 1) & 1)) || !warp_wait(ST_X, uint32_t(c & 1))) {
                     fail = true;
                     break;
                 }
                 tc_fence_after();
-                if (c > 0) write_out_tile(c - 1);
                 if (cs + kC > t_end_all) {
                     // K rows past the sequences' end (another caller's rows, or
                     // unset) must not meet the zero rows of Us: clear them
                     uint8_t* kt = sm + uint32_t(b) * kStSlot + kStOffK;
                     const int valid = int(t_end_all - cs);
-                    for (int idx = ct; idx < kC * 16; idx += int(kStChainThreads)) {
-                        const int r = idx >> 4, cc = (idx & 15) * 8;
-                        if (r >= valid) *reinterpret_cast<uint4*>(kt + toff(r, cc, 8192)) = make_uint4(0, 0, 0, 0);
+                    for (int idx = tid; idx < kC * 16; idx += int(kStEpiThreads)) {
+                        const int r2 = idx >> 4, cc = (idx & 15) * 8;
+                        if (r2 >= valid) *reinterpret_cast<uint4*>(kt + toff(r2, cc, 8192)) = make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();
                 }
-                // ---- U^T = U0^T + X; U and Us = U diag(e) as bf16 hi + lo -----------
+                // ---- U^T = U0^T + X; Us = U diag(e) as bf16 hi + lo, then U as bf16 ----
+                // (this thread: columns 16 sub .. 16 sub + 15 of its lane; U0^T
+                // from the slot's copy of the record's fragments, which the
+                // preparing thread of that lane and column half wrote as
+                // interleaved 16-byte groups)
                 {
                     uint32_t xr[16];
-                    float u0[16];
                     __syncwarp();
                     GDN_TMEM_LD_X16(tX + lane_addr + sub * 16, xr);
-                    load_u0(b, u0);
+                    const float* ev = reinterpret_cast<const float*>(sm + kStOffVec + uint32_t(b) * 512u) + sub * 16;
+                    const float4* us = reinterpret_cast<const float4*>(sm + uint32_t(b) * kStSlot + kStOffU) +
+                                       ((quarter + 4 * (sub >> 1)) * 8 + 4 * (sub & 1)) * 32 + lane;
+                    float u[16];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 w = has_u0 ? us[k * 32] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        u[4 * k] = w.x;
+                        u[4 * k + 1] = w.y;
+                        u[4 * k + 2] = w.z;
+                        u[4 * k + 3] = w.w;
+                    }
                     tmem_ld_wait();
-                    uint32_t uh[8], ul[8], sh[8], sl[8];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) u[i] += __uint_as_float(xr[i]);
+                    uint32_t sh[8], sl[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float a0 = u0[2 * i] + __uint_as_float(xr[2 * i]);
-                        const float a1 = u0[2 * i + 1] + __uint_as_float(xr[2 * i + 1]);
-                        split_pair(a0, a1, uh[i], ul[i]);
-                        split_pair(a0 * ev[2 * i], a1 * ev[2 * i + 1], sh[i], sl[i]);
+                        const float2 e2 = *reinterpret_cast<const float2*>(ev + 2 * i);
+                        split_pair(u[2 * i] * e2.x, u[2 * i + 1] * e2.y, sh[i], sl[i]);
                     }
-                    GDN_TMEM_ST_X8(tU + lane_addr + 0 + sub * 8, uh);
-                    GDN_TMEM_ST_X8(tU + lane_addr + 32 + sub * 8, ul);
                     GDN_TMEM_ST_X8(tU + lane_addr + 64 + sub * 8, sh);
                     GDN_TMEM_ST_X8(tU + lane_addr + 96 + sub * 8, sl);
                     tmem_st_wait();
+                    tc_fence_before();
+                    warp_arrive(ST_UREADY);
+                    uint32_t uh[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) uh[i] = pack_bf16x2(u[2 * i], u[2 * i + 1]);
+                    GDN_TMEM_ST_X8(tU + lane_addr + uint32_t(b) * 32 + sub * 8, uh);
+                    tmem_st_wait();
                 }
                 tc_fence_before();
-                named_sync(kBarSt, kStChainThreads);
-                // the next chunk's record values travel while the state update runs
-                float evn[16], gsn = 1.f;
-                if (has_next) load_vec(c + 1, evn, gsn);
-                // ---- Z += Us^T K; then O += U^T P^T behind it ------------------------
-                if (lead) {
-                    tc_fence_after();
-                    const uint8_t* sp = sm + uint32_t(b) * kStSlot;
-                    const uint64_t dK = smem_desc(smem_u32(sp + kStOffK), 8192, 1024, kSwizzle128B);
-#pragma unroll
-                    for (int part = 0; part < 2; ++part)
-#pragma unroll
-                        for (int s = 0; s < 4; ++s)
-                            umma_f16_tmemA(tZ, tU + 64 + part * 32 + s * 8, dK + uint64_t(s * 2048 >> 4), id_z, 1);
-                    umma_commit(&bars[ST_Z]);
-                    const uint64_t dP = smem_desc(smem_u32(sp + kStOffP), 16, 1024, kSwizzle128B);
-#pragma unroll
-                    for (int pr = 0; pr < 3; ++pr)
-#pragma unroll
-                        for (int s = 0; s < 4; ++s)
-                            umma_f16_tmemA(tO(c), tU + (pr == 2 ? 32 : 0) + s * 8,
-                                           dP + uint64_t(((pr == 1 ? 8192 : 0) + s * 32) >> 4), id_o, 1);
-                    umma_commit(&bars[ST_O]);
-                    lf = !wait(ST_Z, uint32_t(c & 1));
+                warp_arrive(ST_UHREADY);
+                // ---- the previous chunk's output tile, while the state update runs --
+                if (c >= 1 && !stage_out(c - 1)) {
+                    fail = true;
+                    break;
                 }
-                __syncwarp();
-                if (named_sync_or(kBarSt, kStChainThreads, lf)) {
+                // ---- new state: Zb = bf16(Z); Z <- exp(gamma_S(c+1)) Z --------------
+                if (!warp_wait(ST_Z, uint32_t(c & 1))) {
                     fail = true;
                     break;
                 }
                 tc_fence_after();
-                // ---- new state: Zb = bf16(Z); Z <- exp(gamma_S(c+1)) Z --------------
                 {
                     float z[32];
                     tmem_ld32(tZ + lane_addr + sub * 32, z);
@@ -2051,6 +1880,11 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) zb[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
                     GDN_TMEM_ST_X16(tZb + lane_addr + sub * 16, zb);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    warp_arrive(ST_ZBREADY);
+                    // the pre-scaling for the next chunk's update (or the final
+                    // state) while the next [X | O] product runs
                     if (has_next) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) z[i] *= gsn;
@@ -2068,32 +1902,8 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     }
                     tmem_st_wait();
                 }
-                o_cs = cs;
-                o_rows = rows;
-                if (has_next) {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) ev[k] = evn[k];
-                }
-                tc_fence_before();
-                named_sync(kBarSt, kStChainThreads);
             }
-            if (!fail) {                                 // the last chunk's output tile
-                bool lf = false;
-                if (lead) {
-                    lf = !wait(ST_O, uint32_t((nchunks - 1) & 1));
-                    bulk_wait_group_read<1>();
-                }
-                __syncwarp();
-                if (!named_sync_or(kBarSt, kStChainThreads, lf)) {
-                    tc_fence_after();
-                    stage_out(nchunks - 1);
-                    named_sync(kBarSt, kStChainThreads);
-                    write_out_tile(nchunks - 1);
-                } else {
-                    fail = true;
-                }
-            }
-            if (lead) bulk_wait_all();                   // tile stores done before the CTA exits
+            if (!fail && !stage_out(nchunks - 1)) fail = true;   // the last chunk's output tile
         }
         if (fail) *s_err = 1;
     }
@@ -2101,9 +1911,9 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     // ---- teardown ------------------------------------------------------------------
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
+    if (tid == int(kStEpiThreads)) {
         tc_fence_after();
-        // every product this thread issued has completed before TMEM and
+        // every product the issuer started has completed before TMEM and
         // shared memory go away (a no-op wait on a clean finish)
         umma_commit(&bars[ST_DRAIN]);
         if (!mbar_wait(&bars[ST_DRAIN], 0, kWaitLimit, kSuspendNs)) *s_err = 1;
@@ -2516,13 +2326,13 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const bool split = p.prep_ws != nullptr && p.prep_slots > 0;
     const void* state_kernel = split ? reinterpret_cast<const void*>(chunk_state_kernel)
-                                     : reinterpret_cast<const void*>(chunk_tc_kernel<false>);
+                                                     : reinterpret_cast<const void*>(chunk_tc_kernel);
     cudaError_t e = ensure_smem(state_kernel, int(split ? kStSmemBytes : kSmemBytes));
     if (e != cudaSuccess) return e;
     const char* state_name = split ? "chunk_state_kernel" : kTcKernelName;
     auto launch_state = [&](const ChunkParams& q, unsigned z) {
         return split ? launch_pdl(chunk_state_kernel, dim3(q.Hv, q.B, z), kStThreads, kStSmemBytes, s, q, maps)
-                     : launch_pdl(chunk_tc_kernel<false>, dim3(q.Hv, q.B, z), kThreads, kSmemBytes, s, q, maps);
+                     : launch_pdl(chunk_tc_kernel, dim3(q.Hv, q.B, z), kThreads, kSmemBytes, s, q, maps);
     };
     if (split) {                                      // every chunk's S-independent part, in parallel
         if (p.prep_slots > INT32_MAX) return cudaErrorInvalidValue;

@@ -49,10 +49,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
     return done != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // Wait for the phase with the given parity; false after `limit` attempts
 // (each attempt sleeps at most ~suspend_ns, so the wait is bounded in time).
+// A phase that has already completed is seen by one non-blocking test.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit,
                                           uint32_t suspend_ns = 2000) {
+    if (mbar_test(bar, parity)) return true;
     for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity, suspend_ns)) return true;
     return false;
