@@ -402,7 +402,7 @@ constexpr uint32_t kPOffTmp = kPOffT + kC * kLdA * 4;
 constexpr uint32_t kPOffVec = kPOffTmp + 1536 * 4;
 constexpr uint32_t kPOffBar = kPOffVec + 8 * kC * 4;
 constexpr uint32_t kPrepSmemBytes = kPOffBar + 3 * 8 + 8 + 1024;
-constexpr uint32_t kPrepTmemCols = 128;                  // Gram, then W^T (64); U0^T (64)
+constexpr uint32_t kPrepTmemCols = 256;                  // Gram [K; Q][K; Q]^T (128), then W^T (64); U0^T (64)
 static_assert(kC * kLdA * 4 <= 4 * 8192 && kPOffT >= kPOffTb + 4 * 8192, "A and the P staging beside Tb");
 static_assert(kC * kLdA * 4 >= 16384, "-W^T staging fits in T's place");
 static_assert(2 * (kPrepSmemBytes + 1024) <= 233472, "two preparation CTAs per SM");
@@ -529,7 +529,7 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tGW = tmem, tX = tmem + 64;
+    const uint32_t tGW = tmem, tX = tmem + 128;
     uint32_t raw_phase = 0, mma_phase = 0;                 // completed phases of bars[0], of bars[1] / bars[2]
     bool raw_pending = cur.tma, fail = false;
     while (item < n_items) {
@@ -569,10 +569,11 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             ++raw_phase;
             raw_pending = false;
         }
-        // ---- Gram MMA [K; Q] K^T; cumsum (log2 domain); row norms -------------
+        // ---- Gram MMA [K; Q] [K; Q]^T (its diagonal gives the row norms); ------
+        // ---- cumsum of g (log2 domain) while it runs ----------------------------
         tc_fence_after();
         if (pt == 32) {
-            const uint32_t id_gram = idesc_bf16(128, 64, 0, 0);
+            const uint32_t id_gram = idesc_bf16(128, 128, 0, 0);
             const uint64_t d0 = smem_desc(smem_u32(kq), 16, 1024, kSwizzle128B);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
@@ -595,21 +596,25 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             vGam[2 * lane] = a * kLog2e;
             vGam[2 * lane + 1] = s * kLog2e;
         }
-        {
-            // 128 rows (K 0..63, Q 0..63); two threads per row, 64 columns each
-            const int r = pt >> 1, part = pt & 1;
-            const int isq = r >= kC, tr = r & 63;
-            const uint8_t* base = kq + (isq ? 8192 : 0);
+        if (pt == 0) {
+            lf = !mbar_wait(&bars[1], mma_phase & 1, kWaitLimit, kSuspendNs);
+            bulk_wait_group_read<0>();                    // the last item's staged images are read
+        }
+        if (__syncthreads_or(lf)) { fail = true; break; }
+        tc_fence_after();
+        if (phalf == 0) {
+            // row norms: |k_i|^2 and |q_t|^2 on the diagonal (TMEM lane r, column r)
+            uint32_t d[32];
+            __syncwarp();
+            GDN_TMEM_LD_X16(tGW + lane_addr + (pw & 3) * 32, d);
+            GDN_TMEM_LD_X16(tGW + lane_addr + (pw & 3) * 32 + 16, (d + 16));
+            tmem_ld_wait();
             float ss = 0.f;
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                float v[8];
-                load_chunk8(base + toff(tr, part * 64 + m * 8, 16384), v);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
-            }
-            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-            if (part == 0) (isq ? vRq : vRk)[tr] = p.l2norm ? rsqrtf(ss + p.eps) : 1.f;
+            for (int k = 0; k < 32; ++k) ss = k == lane ? __uint_as_float(d[k]) : ss;
+            const float r = p.l2norm ? rsqrtf(ss + p.eps) : 1.f;
+            if (row < kC) vRk[row] = r;
+            else vRq[row - kC] = r;
         }
         __syncthreads();
         if (pt < kC) {
@@ -624,12 +629,7 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             if (pt == rows - 1) reinterpret_cast<float*>(rec + kRecVec)[kC] = eg;
         }
         // ---- masks and decays on the Gram matrices: A to shared, P to the record
-        if (pt == 0) {
-            lf = !mbar_wait(&bars[1], mma_phase & 1, kWaitLimit, kSuspendNs);
-            bulk_wait_group_read<0>();                    // the last item's staged images are read
-        }
-        if (__syncthreads_or(lf)) { fail = true; break; }
-        tc_fence_after();
+        __syncthreads();
         if (mma_phase > 0)                                // T's place held the last -W^T image: T = 0 again
             for (int idx = pt; idx < kC * kLdA / 4; idx += kPrepThreads)
                 reinterpret_cast<float4*>(sT)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -763,9 +763,11 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 const int d = quarter * 32 + 16 * (u >> 1) + 8 * (m & 1);
                 stmatrix_x4_trans(smem_u32(sm + kPOffT + toff(i, d, 8192)), f);
             }
+            // U0^T straight to the record: this thread's 32 columns as eight
+            // 16-byte groups interleaved across the warp's lanes
             float v[32];
             tmem_ld32(tX + lane_addr + phalf * 32, v);
-            float4* u = reinterpret_cast<float4*>(sm + kPOffTb) + pw * 8 * 32 + lane;
+            float4* u = reinterpret_cast<float4*>(rec + kRecU) + pw * 8 * 32 + lane;
 #pragma unroll
             for (int i = 0; i < 8; ++i) u[i * 32] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
@@ -776,7 +778,6 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             const uint32_t w_at = cur.odd ? 8192u : 0u;     // -W's rows in each 128-row block
             bulk_store(rec + kRecWQ + w_at, sm + kPOffT, 8192);
             bulk_store(rec + kRecWQ + 16384 + w_at, sm + kPOffT + 8192, 8192);
-            bulk_store(rec + kRecU, sm + kPOffTb, 32768);
             bulk_commit_group();
         }
         item = next;
