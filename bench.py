@@ -600,6 +600,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefix-tokens", type=int, default=0,
+                    help="time only the first N tokens of a single-prompt workload (0: all)")
     ap.add_argument("--min-seconds", type=float, default=2.0,
                     help="repeat the K-step timed block back to back for about this long (clocks sampled throughout)")
     ap.add_argument("--reference-seconds", type=float, default=120.0,
@@ -635,6 +637,12 @@ def main():
     build_mod.build()
 
     p = make_workload(args.config)
+    if args.prefix_tokens:
+        # the first N tokens of a single-prompt workload (for captures whose
+        # device footprint must stay small)
+        assert p.B == 1 and 0 < args.prefix_tokens <= p.T, "--prefix-tokens needs one prompt and 0 < N <= T"
+        p = _prefix(p, args.prefix_tokens)
+    workload = WORKLOADS[args.config] + (f"; its first {args.prefix_tokens} tokens" if args.prefix_tokens else "")
     one = runner.PrefillCall(p, dev)
     set_bytes = sum(t.numel() * t.element_size() for t in
                     (one.q, one.k, one.v, one.x, one.g, one.beta, one.state_in, one.out,
@@ -712,7 +720,7 @@ def main():
                              else flops_alg / (ms_step * 1e-3) / 1e12)
     roof["frac_of"] = ("frac: the dominant kernel's device time per step; path_frac: the whole call's "
                        "time per step (ms_per_step)")
-    roof["traffic"] = recorded_traffic(dominant, WORKLOADS[args.config])
+    roof["traffic"] = recorded_traffic(dominant, WORKLOADS[args.config]) if not args.prefix_tokens else None
     roof["kernel_ms_per_step"] = kern_ms
     roof["launches_per_step"] = per_kernel[dominant][1] / args.steps
     roof["kernels"] = {k: {"launches_per_step": n / args.steps, "ms_per_launch": tot / n,
@@ -759,7 +767,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": config_dict(WORKLOADS[args.config], p, world),
+            "config": config_dict(workload, p, world),
             "l2_rotation": f"{nsets} independent buffer sets ({nsets * set_bytes / 2**20:.0f} MiB > 2 x L2)",
             "timed_blocks": {"blocks": len(blocks), "steps_per_block": args.steps,
                              "seconds": sum(blocks) / 1e3, "statistic": "median block"},

@@ -148,7 +148,13 @@ void gdn_prefill_desc_init(gdn_prefill_desc* d);
  * gdn_prefill — chunked prefill, bf16 q/k/v/out, fp32 g/beta/state, q/k L2
  * normalisation on (eps 1e-6), q_scale 1, no convolution.  Grids are sized
  * from (B, Hv); cu_seqlens is read on the device, so the total length is not
- * needed.  Needs no workspace.
+ * needed.  Needs no workspace, and so runs neither the segment-parallel scan
+ * nor the split preparation: one CTA per (sequence, value head) walks all of
+ * its chunks in one kernel (chunk_tc_kernel for bf16, dk = dv = 128).  That
+ * is several times slower than gdn_prefill_ex with a workspace on a long or
+ * few-sequence batch (4096 tokens x 16 heads on a GB300: about 0.46 ms
+ * against 0.11 ms); callers that can spare the workspace should use
+ * gdn_prefill_ex.
  *   q, k      bf16 [T, Hk, dk]      v, out   bf16 [T, Hv, dv]
  *   g, beta   fp32 [T, Hv]          state_in / state_out  fp32 [B, Hv, dk, dv]
  *   cu_seqlens int32 [B+1] (device)  chunk in 1..64
