@@ -734,8 +734,8 @@ def main():
     roof["algorithmic_bytes"] = bytes_alg
     roof["algorithmic_flops"] = flops_alg
 
-    # the spec entry point (gdn_prefill: no workspace, so no chunk
-    # records or segment maps) on the same inputs, where it applies (no conv)
+    # the plain entry point (gdn_prefill: bf16, no conv, no workspace, so no
+    # chunk records or segment maps) on the same inputs, where it applies
     plain = None
     if p.conv is None:
         B.gdn_prefill(one.q, one.k, one.v, one.g, one.beta, one.state_in, one.state_out, one.out, one.cu,
