@@ -541,6 +541,26 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             vGam[pt] = g_in;
             vBeta[pt] = b_in;
         }
+        // the next item now: its tiles toward L2 and its g, beta into
+        // registers, so that neither latency lands on this item's path
+        Item nxt;
+        const int64_t next = next_item(item + gridDim.x, nxt);
+        float g_nx = 0.f, b_nx = 0.f;
+        if (next < n_items) {
+            if (pt == 0 && nxt.tma) {
+                const int nkh = nxt.h / (Hv / p.Hk), y = int(nxt.cs);
+                tma_prefetch_2d(&maps.k, nkh * kD, y);
+                tma_prefetch_2d(&maps.k, nkh * kD + 64, y);
+                tma_prefetch_2d(&maps.q, nkh * kD, y);
+                tma_prefetch_2d(&maps.q, nkh * kD + 64, y);
+                tma_prefetch_2d(&maps.v, nxt.h * kD, y);
+                tma_prefetch_2d(&maps.v, nxt.h * kD + 64, y);
+            }
+            if (pt < nxt.rows) {
+                g_nx = p.g[(nxt.cs + pt) * Hv + nxt.h];
+                b_nx = p.beta[(nxt.cs + pt) * Hv + nxt.h];
+            }
+        }
         // ---- raw tiles: TMA when the whole 64-row box lies inside the buffers,
         // else plain loads (rows past the buffers are zero)
         if (!cur.tma) {
@@ -729,16 +749,11 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         ++mma_phase;
         tc_fence_after();
         // ---- raw tiles are free: fetch the next item's while this one is stored
-        Item nxt;
-        const int64_t next = next_item(item + gridDim.x, nxt);
         if (next < n_items) {
             if (pt == 0 && nxt.tma) issue_raw(nxt);
             raw_pending = nxt.tma;
-            g_in = b_in = 0.f;
-            if (pt < nxt.rows) {
-                g_in = p.g[(nxt.cs + pt) * Hv + nxt.h];
-                b_in = p.beta[(nxt.cs + pt) * Hv + nxt.h];
-            }
+            g_in = g_nx;
+            b_in = b_nx;
         }
         {
             // -W, K-major ([64 rows i][128 columns d], two 64-column blocks):
@@ -1939,7 +1954,7 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 // in the G buffer).  A chunk's outputs are linear in the segment's incoming
 // state, so with S_{s+1} = M_s S_s + B_s every output row is O = O' + G S_s.
 //
-// seg_out_kernel, grid (Hv, B, (seg_max - 1) * groups + final CTA), 256
+// seg_out_kernel, grid (Hv, B, (seg_max - 1) * groups + final CTA), 288
 // threads: CTA z < (seg_max - 1) * groups takes chunk group z % groups of
 // segment 1 + z / groups, forms S_s from S_1 by s - 1 steps and then
 // O = O' + G S_s for its chunks.  The final state S_n of the sequence's n
@@ -1952,25 +1967,40 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 // then S_{s+1}^T = D + B_s^T in fp32 (TMEM lane = value column) and back to
 // images.  An output chunk is one product O^T = bf16(S)^T G^T (the state
 // enters output products as a single bf16 in every pass of the scan; B = the
-// chunk's G tile, K-major as stored, in a ring of three); O' (a ring of two)
+// chunk's G tile, K-major as stored, in a ring of three); O' (a ring of three)
 // is added in fp32 in the epilogue, read from its tile in the same fragment
 // layout as the result is written back (ldmatrix / stmatrix, transposed), and
-// the tile is stored by TMA in place.
-constexpr uint32_t kSoThreads = 256;
+// the tile is stored by TMA in place.  During the outputs one thread of a
+// control warp issues the products (into two TMEM buffers), the tile loads
+// and the tile stores, and eight epilogue warps hand over through mbarriers
+// (product done, TMEM buffer read, tile written), so that the product of
+// chunk i + 1 and the store of chunk i - 1 run while chunk i's epilogue does.
+constexpr uint32_t kSoEpiWarps = 8;
+constexpr uint32_t kSoEpiThreads = kSoEpiWarps * 32;
+constexpr uint32_t kSoThreads = kSoEpiThreads + 32;  // + the control warp
+constexpr int kSoCtl = int(kSoEpiThreads);           // the control thread
 constexpr uint32_t kSoImg = 32768;                  // one 128 x 128 bf16 image, two 16 KB blocks
 constexpr uint32_t kSoOffS = 0;                     // S^T hi | lo, K-major
 constexpr uint32_t kSoOffM0 = 2 * kSoImg;           // M^T hi | lo, MN-major: buffer 0
 constexpr uint32_t kSoOffTile = 4 * kSoImg;         // M^T buffer 1 during the steps, then the tiles
 constexpr uint32_t kSoOffM1 = kSoOffTile;
 constexpr uint32_t kSoOffG = kSoOffTile;            // G tiles: three of 16 KB
-constexpr uint32_t kSoOffP = kSoOffTile + 3 * 16384;   // O' tiles: two of 16 KB
-constexpr uint32_t kSoOffBar = kSoOffTile + 5 * 16384;
-constexpr uint32_t kSoNumBars = 8;
+constexpr uint32_t kSoOffP = kSoOffTile + 3 * 16384;   // O' tiles: three of 16 KB
+constexpr uint32_t kSoOffBar = kSoOffTile + 6 * 16384;
+constexpr uint32_t kSoNumBars = 14;
 constexpr uint32_t kSoSmem = kSoOffBar + kSoNumBars * 8 + 16 + 1024;
 constexpr uint32_t kSoTmemCols = 256;               // step accumulator (128) | O^T, two buffers of 64
 static_assert(kSoOffM1 + 2 * kSoImg <= kSoOffBar, "M^T buffer 1 inside the tile region");
 static_assert(kSoSmem <= 232448, "dynamic shared memory above the 227 KB per-block limit");
-enum : int { SO_STEP = 0, SO_G0 = 1, SO_P0 = 4, SO_O0 = 6 };
+enum : int {
+    SO_STEP = 0,         // the step's products done
+    SO_G0 = 1,           // G tile b landed (three)
+    SO_P0 = 4,           // O' tile b landed (three)
+    SO_O0 = 7,           // output product into TMEM buffer b done (two)
+    SO_OFREE0 = 9,       // TMEM buffer b read by the epilogue warps (two; one arrival per warp)
+    SO_STAGED0 = 11,     // the result of a chunk written into its tile (two; one arrival per warp)
+    SO_DRAIN = 13        // the control thread's products done (teardown after a failure)
+};
 
 // This thread's 64 entries of column r = tid % 128 of a row-major 128 x 128
 // fp32 matrix, rows (tid / 128) * 64 ... + 63: coalesced across a warp.
@@ -1993,8 +2023,10 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSoOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kSoOffBar + kSoNumBars * 8);
+    volatile int* s_err = reinterpret_cast<volatile int*>(sm + kSoOffBar + kSoNumBars * 8 + 4);
     const int h = blockIdx.x, n = blockIdx.y, z = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool epi = warp < int(kSoEpiWarps);
     const int Hv = p.Hv;
 
     int64_t t_end_all = p.cu[p.B];
@@ -2029,8 +2061,10 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     auto slot_of = [&](int j) { return slots + size_t(j) * 3 * kD * kD; };   // B_j, M_j^T image, S_j image
 
     if (tid == 0) {
-        for (int i = 0; i < int(kSoNumBars); ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < int(kSoNumBars); ++i)
+            mbar_init(&bars[i], (i >= SO_OFREE0 && i < SO_DRAIN) ? kSoEpiWarps : 1);
         fence_mbar_init();
+        *s_err = 0;
     }
     __syncwarp();
     if (warp == 0) {
@@ -2042,14 +2076,21 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tD = tmem, tOb = tmem + 128;
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int row = quarter * 32 + lane;             // TMEM lane: the value column
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
     auto wait = [&](int b, uint32_t parity) { return mbar_wait(&bars[b], parity, kWaitLimit, kSuspendNs); };
     auto chunk_start = [&](int c) { return t0 + int64_t(c) * p.chunk; };
+    // Output chunk i's tile goes out by TMA when every row of the box is this
+    // sequence's or lies past the buffers; else as 16-byte rows.
+    auto out_rows = [&](int i) {
+        const int64_t cs = chunk_start(c_lo + i);
+        return int(t1 - cs < p.chunk ? t1 - cs : p.chunk);
+    };
+    auto tile_by_tma = [&](int i) { return out_rows(i) == kC || chunk_start(c_lo + i) + out_rows(i) >= p.t_cap; };
     // The images (64 KB) arrive by cp.async from every thread, one commit
-    // group each.  Thread 0 issues the tile copies and counts them, so that a
-    // failed CTA can let the ones in flight land before it exits.
+    // group each.  The control thread issues the tile copies and counts them,
+    // so that a failed CTA can let the ones in flight land before it exits.
     int g_issued = 0, p_issued = 0;
     auto load_image = [&](uint8_t* dst, const void* src) {
         const uint8_t* src8 = static_cast<const uint8_t*>(src);
@@ -2069,8 +2110,8 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
         g_issued = i + 1;
     };
     auto issue_p = [&](int i) {                      // O' tile of output chunk i
-        uint64_t* bar = &bars[SO_P0 + (i & 1)];
-        uint8_t* dst = sm + kSoOffP + uint32_t(i & 1) * 16384u;
+        uint64_t* bar = &bars[SO_P0 + i % 3];
+        uint8_t* dst = sm + kSoOffP + uint32_t(i % 3) * 16384u;
         const int y = int(chunk_start(c_lo + i));
         mbar_arrive_expect_tx(bar, 16384);
         tma_load_2d_hint(dst, &maps.o, bar, h * kD, y, l2_evict_first());
@@ -2079,12 +2120,12 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     };
     auto issue_tiles = [&]() {
         for (int i = 0; i < nout && i < 3; ++i) issue_g(i);
-        for (int i = 0; i < nout && i < 2; ++i) issue_p(i);
+        for (int i = 0; i < nout && i < 3; ++i) issue_p(i);
     };
     load_image(sm + kSoOffS, slot_of(1) + 2 * kD * kD);  // S_1^T
     if (nsteps > 0 || final_after) load_m(1, 0);
     if (nsteps > 1) load_m(2, 1);
-    if (tid == 0 && tiles_early) issue_tiles();
+    if (tid == kSoCtl && tiles_early) issue_tiles();
     // the tiles of later chunks toward L2: after the images (a CTA with state
     // steps asks during its last step)
     auto prefetch_tiles = [&](int from, int to) {
@@ -2104,7 +2145,8 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     // Step j with M_j^T in buffer mb: S_{j+1}^T = S^T M_j^T + B_j^T into the S
     // images, or into state_out; M_{j+2}^T follows into the freed buffer when
     // next_load.  one_more: the copy of M_{j+1} may still be in flight.
-    // False when a wait ran out.
+    // False when a wait ran out.  (The control warp takes part in the copies
+    // and the block barriers only.)
     auto step = [&](int j, int mb, bool to_state, bool next_load, bool one_more) {
         if (one_more)
             cp_async_wait_group<1>();
@@ -2130,7 +2172,7 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
         __syncwarp();
         // while the products run: B_j^T for this thread's TMEM lane and column half
         float b[64];
-        so_load_col(slot_of(j), tid, b);                      // B_j [dk][dv]
+        so_load_col(slot_of(j), tid & int(kSoEpiThreads - 1), b);   // B_j [dk][dv] (the control warp: unused)
         const bool lf = tid == 0 && !wait(SO_STEP, uint32_t((j - 1) & 1));
         if (__syncthreads_or(lf)) return false;
         if (next_load) load_m(j + 2, mb);
@@ -2139,7 +2181,8 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
         tmem_ld64(tD + lane_addr + uint32_t(half * 64), d);
 #pragma unroll
         for (int i = 0; i < 64; ++i) d[i] += b[i];
-        if (to_state) {                                       // S_n: the sequence's final state
+        if (!epi) {
+        } else if (to_state) {                                // S_n: the sequence's final state
             float* dst = p.state_out + (size_t(n) * Hv + h) * kD * kD;
 #pragma unroll
             for (int i = 0; i < 64; ++i) dst[size_t(half * 64 + i) * kD + row] = d[i];
@@ -2156,92 +2199,117 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
 
     // ---- outputs O = O' + G S_s, chunk by chunk ---------------------------------------
     if (!final_role && !fail) {
-        if (tid == 0 && !tiles_early) issue_tiles();          // the steps have left the tile region
+        if (tid == kSoCtl && !tiles_early) issue_tiles();     // the steps have left the tile region
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        const uint32_t id_o = idesc_bf16(128, 64, 0, 0);      // B = G tile, K-major [t][d]
-        auto issue_out = [&](int i) {                         // thread 0: O^T (buffer i & 1) = S^T G^T
-            if (!wait(SO_G0 + i % 3, uint32_t((i / 3) & 1))) return false;
-            tc_fence_after();
-            const uint64_t dG = smem_desc(smem_u32(sm + kSoOffG + uint32_t(i % 3) * 16384u), 16, 1024, kSwizzle128B);
+        if (!epi) {
+            // ---- control: products into TMEM buffer i & 1, tile loads, tile stores
+            if (lane == 0) {
+                const uint32_t id_o = idesc_bf16(128, 64, 0, 0);   // B = G tile, K-major [t][d]
+                auto issue_out = [&](int i) {                 // O^T (buffer i & 1) = S^T G^T
+                    if (!wait(SO_G0 + i % 3, uint32_t((i / 3) & 1))) return false;
+                    // the epilogue has read chunk i - 2 out of this buffer
+                    if (i >= 2 && !wait(SO_OFREE0 + (i & 1), uint32_t(((i - 2) >> 1) & 1))) return false;
+                    tc_fence_after();
+                    const uint64_t dG = smem_desc(smem_u32(sm + kSoOffG + uint32_t(i % 3) * 16384u), 16, 1024, kSwizzle128B);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                umma_f16(tOb + uint32_t(i & 1) * 64, dS + uint64_t(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
-                         dG + uint64_t(((k >> 2) * 8192 + (k & 3) * 32) >> 4), id_o, k > 0);
-            umma_commit(&bars[SO_O0 + (i & 1)]);
-            return true;
-        };
-        bool lf = tid == 0 && !issue_out(0);
-        const int m = lane >> 3, rr = lane & 7;
-        for (int i = 0; i < nout; ++i) {
-            const int bi = i & 1;
-            uint8_t* ot = sm + kSoOffP + uint32_t(bi) * 16384u;   // O' tile, then the result
-            if (tid == 0 && !lf) {
-                // the next chunk's products go to the other TMEM buffer, read
-                // out before the previous barrier
-                if (i + 1 < nout) lf = !issue_out(i + 1);
-                if (!lf) lf = !wait(SO_O0 + bi, uint32_t((i >> 1) & 1));
-                if (!lf && i + 3 < nout) issue_g(i + 3);      // this chunk's G tile is read
-                if (!lf) lf = !wait(SO_P0 + bi, uint32_t((i >> 1) & 1));
-            }
-            if (__syncthreads_or(lf)) {
-                fail = true;
-                break;
-            }
-            tc_fence_after();
-            // this warp's TMEM lanes (value columns) and token half as 16x256b
-            // fragments; O' in the same fragments from its tile; the sum back
-            uint32_t r[4][8];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                tmem_ld_16x256b_x2(tOb + uint32_t(bi * 64) + (uint32_t(quarter * 32 + 16 * (u >> 1)) << 16) +
-                                       uint32_t(half * 32 + 16 * (u & 1)),
-                                   r[u]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int t = half * 32 + 16 * (u & 1) + 8 * (m >> 1) + rr;
-                const int jj = quarter * 32 + 16 * (u >> 1) + 8 * (m & 1);
-                const uint32_t addr = smem_u32(ot + toff(t, jj, 8192));
-                uint32_t o[4], f[4];
-                ldmatrix_x4_trans(addr, o);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    f[e] = pack_bf16x2(__uint_as_float(r[u][2 * e]) + __uint_as_float(o[e] << 16),
-                                       __uint_as_float(r[u][2 * e + 1]) + __uint_as_float(o[e] & 0xffff0000u));
-                stmatrix_x4_trans(addr, f);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            const int64_t cs = chunk_start(c_lo + i);
-            const int rows = int(t1 - cs < p.chunk ? t1 - cs : p.chunk);
-            if (rows == kC || cs + rows >= p.t_cap) {         // every row of the box is ours or past the buffers
-                if (tid == 0) {
-                    tma_store_2d(&maps.o, ot, h * kD, int(cs));
-                    tma_store_2d(&maps.o, ot + 8192, h * kD + 64, int(cs));
+                    for (int k = 0; k < 8; ++k)
+                        umma_f16(tOb + uint32_t(i & 1) * 64, dS + uint64_t(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                                 dG + uint64_t(((k >> 2) * 8192 + (k & 3) * 32) >> 4), id_o, k > 0);
+                    umma_commit(&bars[SO_O0 + (i & 1)]);
+                    return true;
+                };
+                bool ok = issue_out(0);
+                for (int i = 0; i < nout && ok; ++i) {
+                    if (i + 1 < nout) ok = issue_out(i + 1);
+                    // chunk i's product has read its G tile: the tile takes chunk i + 3
+                    if (ok) ok = wait(SO_O0 + (i & 1), uint32_t((i >> 1) & 1));
+                    if (ok && i + 3 < nout) issue_g(i + 3);
+                    if (ok) ok = wait(SO_STAGED0 + (i & 1), uint32_t((i >> 1) & 1));
+                    if (!ok) break;
+                    if (tile_by_tma(i)) {
+                        const uint8_t* ot = sm + kSoOffP + uint32_t(i % 3) * 16384u;
+                        const int cs = int(chunk_start(c_lo + i));
+                        tma_store_2d(&maps.o, ot, h * kD, cs);
+                        tma_store_2d(&maps.o, ot + 8192, h * kD + 64, cs);
+                    }
                     bulk_commit_group();
-                }
-            } else {                                          // the chunk ends inside the buffers
-                __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(p.out);
-                for (int idx = tid; idx < kC * 16; idx += int(kSoThreads)) {
-                    const int rw = idx >> 4, col = (idx & 15) * 8;
-                    if (rw < rows)
-                        *reinterpret_cast<uint4*>(gout + ((cs + rw) * Hv + h) * kD + col) =
-                            *reinterpret_cast<const uint4*>(ot + toff(rw, col, 8192));
-                }
-            }
-            if (i + 2 < nout) {                               // refill once the tile is read
-                __syncthreads();
-                if (tid == 0) {
-                    bulk_wait_group_read<0>();
-                    issue_p(i + 2);
+                    // chunk i - 1's store has read its tile: the tile takes chunk i + 2
+                    bulk_wait_group_read<1>();
+                    if (i >= 1 && i + 2 < nout) issue_p(i + 2);
                     prefetch_tiles(i + 6, i + 7);             // and a later chunk's tiles toward L2
                 }
+                bulk_wait_all();                              // tile stores done before the CTA exits
+                if (!ok) *s_err = 1;
+            }
+        } else {
+            // ---- epilogue warps: O = O' + (this warp's lanes, token half) ------------
+            __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(p.out);
+            auto warp_wait = [&](int b, uint32_t parity) {
+                bool okw = true;
+                if (lane == 0) okw = wait(b, parity);
+                return __shfl_sync(0xffffffffu, okw ? 1 : 0, 0) != 0;
+            };
+            auto warp_arrive = [&](int b) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[b]);
+            };
+            const int m = lane >> 3, rr = lane & 7;
+            for (int i = 0; i < nout; ++i) {
+                const int bi = i & 1;
+                if (!warp_wait(SO_O0 + bi, uint32_t((i >> 1) & 1)) || !warp_wait(SO_P0 + i % 3, uint32_t((i / 3) & 1))) {
+                    *s_err = 1;
+                    break;
+                }
+                tc_fence_after();
+                uint8_t* ot = sm + kSoOffP + uint32_t(i % 3) * 16384u;   // O' tile, then the result
+                // this warp's TMEM lanes (value columns) and token half as 16x256b
+                // fragments; O' in the same fragments from its tile; the sum back
+                uint32_t r[4][8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    tmem_ld_16x256b_x2(tOb + uint32_t(bi * 64) + (uint32_t(quarter * 32 + 16 * (u >> 1)) << 16) +
+                                           uint32_t(half * 32 + 16 * (u & 1)),
+                                       r[u]);
+                tmem_ld_wait();
+                tc_fence_before();
+                warp_arrive(SO_OFREE0 + bi);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int t = half * 32 + 16 * (u & 1) + 8 * (m >> 1) + rr;
+                    const int jj = quarter * 32 + 16 * (u >> 1) + 8 * (m & 1);
+                    const uint32_t addr = smem_u32(ot + toff(t, jj, 8192));
+                    uint32_t o[4], f[4];
+                    ldmatrix_x4_trans(addr, o);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        f[e] = pack_bf16x2(__uint_as_float(r[u][2 * e]) + __uint_as_float(o[e] << 16),
+                                           __uint_as_float(r[u][2 * e + 1]) + __uint_as_float(o[e] & 0xffff0000u));
+                    stmatrix_x4_trans(addr, f);
+                }
+                fence_proxy_async_smem();
+                if (!tile_by_tma(i)) {
+                    // the chunk ends inside the buffers: this warp's part of the
+                    // tile (rows 32 half .., columns 32 quarter ..) as 16-byte rows
+                    __syncwarp();
+                    const int64_t cs = chunk_start(c_lo + i);
+                    const int rows = out_rows(i);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int idx = lane + 32 * k;
+                        const int rw = half * 32 + (idx >> 2), col = quarter * 32 + (idx & 3) * 8;
+                        if (rw < rows)
+                            *reinterpret_cast<uint4*>(gout + ((cs + rw) * Hv + h) * kD + col) =
+                                *reinterpret_cast<const uint4*>(ot + toff(rw, col, 8192));
+                    }
+                }
+                warp_arrive(SO_STAGED0 + bi);
             }
         }
-        if (tid == 0) bulk_wait_all();                        // tile stores done before the CTA exits
+        tc_fence_before();
+        __syncthreads();
+        if (*s_err) fail = true;
     }
     // the final state here when no CTA of its own forms it: one more step from S_{n-1}
     if (final_after && !fail) {
@@ -2253,13 +2321,17 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     cp_async_wait_all();
     tc_fence_before();
     __syncthreads();
-    if (fail && tid == 0) {
+    if (tid == kSoCtl && (fail || *s_err)) {
         atomicAdd(&g_tc_timeouts, 1);
-        // tile copies still in flight land before shared memory goes away
+        // every product issued has completed and the tile copies still in
+        // flight land before TMEM and shared memory go away
+        tc_fence_after();
+        umma_commit(&bars[SO_DRAIN]);
+        mbar_wait(&bars[SO_DRAIN], 0, kWaitLimit, kSuspendNs);
         for (int i = g_issued - 3 < 0 ? 0 : g_issued - 3; i < g_issued; ++i)
             mbar_wait(&bars[SO_G0 + i % 3], uint32_t((i / 3) & 1), kWaitLimit, kSuspendNs);
-        for (int i = p_issued - 2 < 0 ? 0 : p_issued - 2; i < p_issued; ++i)
-            mbar_wait(&bars[SO_P0 + (i & 1)], uint32_t((i >> 1) & 1), kWaitLimit, kSuspendNs);
+        for (int i = p_issued - 3 < 0 ? 0 : p_issued - 3; i < p_issued; ++i)
+            mbar_wait(&bars[SO_P0 + i % 3], uint32_t((i / 3) & 1), kWaitLimit, kSuspendNs);
         bulk_wait_all();
     }
     __syncthreads();
