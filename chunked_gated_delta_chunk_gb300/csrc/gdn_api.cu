@@ -83,23 +83,69 @@ int sm_count() {
     return n;
 }
 
-// Chunk groups per segment in seg_out_kernel: as many as let its CTAs (one
-// per group of every segment s >= 1, plus one for the final state, per
-// sequence and value head) fit one wave, at least one, at most one per chunk.
-// When even one group per segment leaves no room for the final state's CTA,
-// the last group's CTA of the last segment forms it (*final_cta = 0).
-int segment_groups(int64_t units, int64_t seg_max, int seg_chunks, int* final_cta) {
+// seg_out_kernel's work per (sequence, value head), in chunk periods of the
+// state pass: a CTA of segment s takes s - 1 state steps (kSoStep each) and
+// then its chunk group's outputs (kSoOut each).
+constexpr double kSoStep = 1.0, kSoOut = 0.35;
+
+// seg_out_kernel's CTAs per (sequence, value head): one per chunk group of
+// every segment s >= 1, plus one for the final state, as many as fit one
+// wave.  Each segment starts with one group; the remaining CTAs go one by one
+// to the segment whose CTAs finish last (the later a segment, the more state
+// steps precede its outputs), at most one group per chunk.  When even one
+// group per segment leaves no room for the final state's CTA, the last
+// group's CTA of the last segment forms it after its outputs
+// (*final_cta = 0).  gstart (seg_max entries, may be null) receives the
+// first CTA of every segment s >= 1 (gstart[s - 1]) and their total
+// (gstart[seg_max - 1]); *groups the uniform group count used beyond the
+// table.  Returns the cost of the slowest CTA.
+double seg_out_plan(int64_t units, int64_t seg_max, int seg_chunks, int* final_cta, int* groups,
+                    int16_t* gstart) {
     *final_cta = 1;
-    if (seg_max < 2) return 1;
+    *groups = 1;
+    if (seg_max < 2) return 0.0;
     const int64_t per_unit = sm_count() / units;   // CTAs per (sequence, value head) in one wave
-    int64_t g = (per_unit - 1) / (seg_max - 1);
-    if (g < 1) {
+    const int64_t nout = seg_max - 1;               // output segments
+    int64_t budget;
+    if (per_unit >= nout + 1) {
+        budget = per_unit - 1;
+    } else {
         *final_cta = 0;
-        g = per_unit / (seg_max - 1);
+        budget = per_unit > nout ? per_unit : nout;
     }
+    int64_t g = budget / nout;
     if (g < 1) g = 1;
     if (g > seg_chunks) g = seg_chunks;
-    return int(g);
+    *groups = int(g);
+    auto cost = [&](int64_t s, int64_t gs) {
+        double c = double(s - 1) * kSoStep + double((seg_chunks + gs - 1) / gs) * kSoOut;
+        if (!*final_cta && s == nout) c += kSoStep;   // the final state after the outputs
+        return c;
+    };
+    const double final_cost = *final_cta ? double(nout) * kSoStep : 0.0;
+    if (nout > gdn::kSegTable) {
+        const double worst = cost(nout, g);
+        return worst > final_cost ? worst : final_cost;
+    }
+    int64_t gs[gdn::kSegTable + 1];
+    for (int64_t s = 1; s <= nout; ++s) gs[s] = 1;
+    for (int64_t left = budget - nout; left > 0; --left) {
+        int64_t worst = 1;
+        for (int64_t s = 2; s <= nout; ++s)
+            if (cost(s, gs[s]) >= cost(worst, gs[worst])) worst = s;
+        if (gs[worst] >= seg_chunks) break;       // its chunks cannot be split further
+        ++gs[worst];
+    }
+    double worst = final_cost;
+    int64_t z = 0;
+    for (int64_t s = 1; s <= nout; ++s) {
+        if (gstart) gstart[s - 1] = int16_t(z);
+        z += gs[s];
+        const double c = cost(s, gs[s]);
+        if (c > worst) worst = c;
+    }
+    if (gstart) gstart[nout] = int16_t(z);
+    return worst;
 }
 
 // Chunks per segment of the segment-parallel scan, or 0 for one pass.
@@ -107,17 +153,16 @@ int segment_groups(int64_t units, int64_t seg_max, int seg_chunks, int* final_ct
 // L = ceil(chunks / n) chunks, phase 1 runs (2n - 1) CTAs per (sequence,
 // value head), each taking L + kStartPeriods periods per wave of one CTA per SM
 // (a CTA's first chunks run with cold instruction caches and its incoming
-// state still on the way); seg_out_kernel then takes about one period per
-// state step (n - 1 of them) plus kOutPeriods per output chunk of a group,
-// per wave of its CTAs.  One pass costs chunks + kStartPeriods periods in
-// ceil(units / SMs) waves.  The cheapest n wins; sequence lengths are taken
-// as the batch average.
+// state still on the way); seg_out_kernel then takes its slowest CTA's state
+// steps and output chunks (seg_out_plan) per wave of its CTAs.  One pass
+// costs chunks + kStartPeriods periods in ceil(units / SMs) waves.  The
+// cheapest n wins; sequence lengths are taken as the batch average.
 int segment_chunks(const gdn_prefill_desc* d) {
     if (d->dtype != GDN_BF16 || d->dk != 128 || d->dv != 128) return 0;   // tensor-core path only
     if (d->T_total <= 0 || d->B <= 0 || d->segment_chunks < 0) return 0;
     const int64_t chunks = (d->T_total + d->chunk - 1) / d->chunk;
     if (d->segment_chunks > 0) return d->segment_chunks < chunks ? d->segment_chunks : 0;
-    constexpr double kStartPeriods = 3.0, kStepPeriods = 1.0, kOutPeriods = 0.25;
+    constexpr double kStartPeriods = 3.0;
     const int64_t units = int64_t(d->Hv) * d->B;
     const int64_t per_seq = (chunks + d->B - 1) / d->B;
     const int64_t sms = sm_count();
@@ -126,10 +171,11 @@ int segment_chunks(const gdn_prefill_desc* d) {
     int best_len = 0;
     for (int64_t n = 2; n <= 64 && n <= per_seq; ++n) {
         const int64_t len = (per_seq + n - 1) / n;
-        int final_cta = 1;
-        const int64_t groups = segment_groups(units, n, int(len), &final_cta);
-        const double out = double(waves(units * ((n - 1) * groups + final_cta))) *
-                           (double(n - 1) * kStepPeriods + double((len + groups - 1) / groups) * kOutPeriods);
+        int final_cta = 1, groups = 1;
+        int16_t gstart[gdn::kSegTable + 1];
+        const double worst = seg_out_plan(units, n, int(len), &final_cta, &groups, gstart);
+        const int64_t so_ctas = n - 1 <= gdn::kSegTable ? gstart[n - 1] : (n - 1) * groups;
+        const double out = double(waves(units * (so_ctas + final_cta))) * worst;
         const double cost = double(waves(units * (2 * n - 1))) * (double(len) + kStartPeriods) + out;
         if (cost < best) {
             best = cost;
@@ -256,7 +302,8 @@ int gdn_prefill_ex(const gdn_prefill_desc* d, gdn_stream_t stream) {
             p.seg_ws = reinterpret_cast<float*>(static_cast<char*>(d->workspace) + conv_bytes);
             p.seg_slots = segment_slots(d, sc);
             p.seg_max = int((d->T_total + seg_tokens - 1) / seg_tokens);
-            p.seg_groups = segment_groups(int64_t(d->Hv) * d->B, p.seg_max, sc, &p.seg_final_cta);
+            seg_out_plan(int64_t(d->Hv) * d->B, p.seg_max, sc, &p.seg_final_cta, &p.seg_groups,
+                         p.seg_max - 1 <= gdn::kSegTable ? p.seg_gstart : nullptr);
             p.g_out = static_cast<char*>(d->workspace) + conv_bytes + segment_map_bytes(d, sc);
         }
         if (prep_bytes > 0 && d->workspace != nullptr &&

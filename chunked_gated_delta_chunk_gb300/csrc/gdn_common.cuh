@@ -18,6 +18,10 @@ constexpr int kNeumann = 8;       // diagonal block size of the Neumann stage
 // Everything a chunk kernel needs.  Token strides are in elements so that q,
 // k, v can be read from separate [T, H, d] tensors or from the [T, C]
 // output of the short convolution.
+// Segments of the segment-parallel scan that seg_out_kernel's group table
+// covers (more use uniform groups).
+constexpr int kSegTable = 64;
+
 struct ChunkParams {
     const void* q;
     const void* k;
@@ -51,8 +55,14 @@ struct ChunkParams {
     float* seg_ws;
     int64_t seg_slots;       // slots per value head
     int seg_max;             // most segments any sequence can have (grid size)
-    int seg_groups;          // chunk groups per segment in seg_out_kernel
+    int seg_groups;          // chunk groups per segment in seg_out_kernel, beyond the table
     int seg_final_cta;       // 1: a CTA of its own forms the final state; 0: the last group's
+    // seg_out_kernel's CTAs per (sequence, value head) when seg_max - 1 <=
+    // kSegTable: segment s >= 1 takes CTAs z with seg_gstart[s - 1] <= z <
+    // seg_gstart[s] (seg_gstart[0] = 0), one chunk group each; the final
+    // state's CTA, if any, is z = seg_gstart[seg_max - 1].  Later segments
+    // (more state steps before their outputs) get more groups.
+    int16_t seg_gstart[kSegTable + 1];
     void* g_out;
     // Split preparation (tensor-core path only).  When prep_ws is set, a
     // separate pass solves every chunk's S-independent part (inverse, U0, W,

@@ -59,7 +59,8 @@ constexpr uint32_t kChainThreads = 128;
 constexpr uint32_t kBarPrep = 1, kBarChain = 2;
 // mbarrier waits: attempts of at most kSuspendNs each (a short hint: a
 // waiter suspended for longer can oversleep the phase change), bounded in
-// total to about two seconds.
+// total to about two seconds; the polled waits (mbar_spin) of the chunk
+// chain make at most kWaitLimit polls, under a second.
 constexpr uint32_t kSuspendNs = 32;
 constexpr uint32_t kWaitLimit = 1u << 26;
 constexpr int kLdA = kC + 4;         // fp32 row stride of A and T: 16-byte aligned rows
@@ -1582,6 +1583,8 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     // other rows belong to the next sequence).
     auto tile_by_tma = [&](int c) { return chunk_rows(c) == kC || chunk_start(c) + chunk_rows(c) >= p.t_cap; };
     auto wait = [&](int b, uint32_t parity) { return mbar_wait(&bars[b], parity, kWaitLimit, kSuspendNs); };
+    // the hand-offs of the chunk chain: polled (see mbar_spin)
+    auto spin = [&](int b, uint32_t parity) { return mbar_spin(&bars[b], parity, kWaitLimit); };
 
     if (tid == 0) {
         for (int i = 0; i < ST_NBARS; ++i)
@@ -1687,8 +1690,8 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 // ---- [X | O] = Zb [-W^T | Qs^T] ------------------------------------
                 // (U of chunk c - 1 is known before this product is issued, so
                 // that phase of ST_UHREADY cannot be overtaken)
-                if (!wait(ST_FULL0 + b, uint32_t((c >> 1) & 1)) || !wait(ST_ZBREADY, uint32_t(c & 1)) ||
-                    (c >= 1 && !wait(ST_UHREADY, uint32_t((c - 1) & 1)))) {
+                if (!spin(ST_FULL0 + b, uint32_t((c >> 1) & 1)) || !spin(ST_ZBREADY, uint32_t(c & 1)) ||
+                    (c >= 1 && !spin(ST_UHREADY, uint32_t((c - 1) & 1)))) {
                     fail = true;
                     break;
                 }
@@ -1705,7 +1708,7 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 // ---- O += U^T P^T of the previous chunk, behind it -------------------
                 if (c >= 1) issue_op(c - 1);
                 // ---- Z += Us^T K -------------------------------------------------------
-                if (!wait(ST_UREADY, uint32_t(c & 1))) { fail = true; break; }
+                if (!spin(ST_UREADY, uint32_t(c & 1))) { fail = true; break; }
                 tc_fence_after();
                 {
                     const uint8_t* sp = sm + uint32_t(b) * kStSlot;
@@ -1730,7 +1733,7 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(mode == kModeTransition ? p.g_out : p.out);
         auto warp_wait = [&](int b, uint32_t parity) {
             bool ok = true;
-            if (lane == 0) ok = wait(b, parity);
+            if (lane == 0) ok = spin(b, parity);
             return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         };
         auto warp_arrive = [&](int b) {
@@ -1954,9 +1957,10 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 // in the G buffer).  A chunk's outputs are linear in the segment's incoming
 // state, so with S_{s+1} = M_s S_s + B_s every output row is O = O' + G S_s.
 //
-// seg_out_kernel, grid (Hv, B, (seg_max - 1) * groups + final CTA), 288
-// threads: CTA z < (seg_max - 1) * groups takes chunk group z % groups of
-// segment 1 + z / groups, forms S_s from S_1 by s - 1 steps and then
+// seg_out_kernel, grid (Hv, B, output CTAs + final CTA), 320 threads: an
+// output CTA takes one chunk group of one segment s >= 1 (ChunkParams::
+// seg_gstart; later segments have more groups, as their CTAs first take
+// more state steps), forms S_s from S_1 by s - 1 steps and then
 // O = O' + G S_s for its chunks.  The final state S_n of the sequence's n
 // segments (n - 1 steps) is formed by one more CTA when that fits the wave,
 // else by the last group's CTA of segment n - 1 after its outputs.  The CTA
@@ -1970,15 +1974,17 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 // chunk's G tile, K-major as stored, in a ring of three); O' (a ring of three)
 // is added in fp32 in the epilogue, read from its tile in the same fragment
 // layout as the result is written back (ldmatrix / stmatrix, transposed), and
-// the tile is stored by TMA in place.  During the outputs one thread of a
-// control warp issues the products (into two TMEM buffers), the tile loads
-// and the tile stores, and eight epilogue warps hand over through mbarriers
-// (product done, TMEM buffer read, tile written), so that the product of
-// chunk i + 1 and the store of chunk i - 1 run while chunk i's epilogue does.
+// the tile is stored by TMA in place.  During the outputs one thread of an
+// issuer warp issues the products (into two TMEM buffers) and the G tile
+// loads, one thread of a tile warp the tile stores and the O' tile loads,
+// and eight epilogue warps hand over through mbarriers (product done, TMEM
+// buffer read, tile written), so that the product of chunk i + 1 and the
+// store of chunk i - 1 run while chunk i's epilogue does.
 constexpr uint32_t kSoEpiWarps = 8;
 constexpr uint32_t kSoEpiThreads = kSoEpiWarps * 32;
-constexpr uint32_t kSoThreads = kSoEpiThreads + 32;  // + the control warp
-constexpr int kSoCtl = int(kSoEpiThreads);           // the control thread
+constexpr uint32_t kSoThreads = kSoEpiThreads + 64;  // + the issuer's and the tile warp
+constexpr int kSoMma = int(kSoEpiThreads);           // the issuer thread
+constexpr int kSoCtl = int(kSoEpiThreads) + 32;      // the tile thread
 constexpr uint32_t kSoImg = 32768;                  // one 128 x 128 bf16 image, two 16 KB blocks
 constexpr uint32_t kSoOffS = 0;                     // S^T hi | lo, K-major
 constexpr uint32_t kSoOffM0 = 2 * kSoImg;           // M^T hi | lo, MN-major: buffer 0
@@ -2024,6 +2030,8 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSoOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kSoOffBar + kSoNumBars * 8);
     volatile int* s_err = reinterpret_cast<volatile int*>(sm + kSoOffBar + kSoNumBars * 8 + 4);
+    volatile int* s_g_issued = reinterpret_cast<volatile int*>(sm + kSoOffBar + kSoNumBars * 8 + 8);
+    volatile int* s_p_issued = reinterpret_cast<volatile int*>(sm + kSoOffBar + kSoNumBars * 8 + 12);
     const int h = blockIdx.x, n = blockIdx.y, z = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool epi = warp < int(kSoEpiWarps);
@@ -2038,14 +2046,27 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     const int L = p.seg_chunks;
     const int nseg = (seq_chunks + L - 1) / L;
     const int short_by = nseg * L - seq_chunks;
-    const int groups = p.seg_groups;
-    const bool final_role = p.seg_final_cta && z == (p.seg_max - 1) * groups;
-    const int s = final_role ? nseg - 1 : 1 + z / groups;   // steps: s - 1, or nseg - 1 for the final state
+    // this CTA's segment s and chunk group g of its segment's groups
+    const bool table = p.seg_max - 1 <= kSegTable;
+    const int so_ctas = table ? int(p.seg_gstart[p.seg_max - 1]) : (p.seg_max - 1) * p.seg_groups;
+    const bool final_role = p.seg_final_cta && z == so_ctas;
+    int s = 1, g = 0, groups = 1;                    // steps: s - 1, or nseg - 1 for the final state
+    if (final_role) {
+        s = nseg - 1;
+    } else if (table) {
+        while (s < p.seg_max - 1 && z >= int(p.seg_gstart[s])) ++s;
+        g = z - int(p.seg_gstart[s - 1]);
+        groups = int(p.seg_gstart[s]) - int(p.seg_gstart[s - 1]);
+    } else {
+        groups = p.seg_groups;
+        s = 1 + z / groups;
+        g = z % groups;
+    }
     if (nseg < 2 || s >= nseg) return;
     if (final_role && p.state_out == nullptr) return;
     int c_lo = 0, c_hi = 0;                          // this CTA's chunks (output role)
     if (!final_role) {
-        const int cb = s * L - short_by, g = z % groups;
+        const int cb = s * L - short_by;
         c_lo = cb + (g * L) / groups;
         c_hi = cb + ((g + 1) * L) / groups;
         if (c_lo >= c_hi) return;
@@ -2053,7 +2074,7 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     const int nsteps = final_role ? nseg - 1 : s - 1;
     // the final state after the outputs, by the last group of the last segment
     const bool final_after = !final_role && !p.seg_final_cta && p.state_out != nullptr && s == nseg - 1 &&
-                             z % groups == groups - 1;
+                             g == groups - 1;
     const int nout = c_hi - c_lo;
     const bool tiles_early = nsteps < 2;             // M^T buffer 1 (the tile region) never used
     const int64_t seg_tokens = int64_t(L) * p.chunk;
@@ -2065,6 +2086,8 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
             mbar_init(&bars[i], (i >= SO_OFREE0 && i < SO_DRAIN) ? kSoEpiWarps : 1);
         fence_mbar_init();
         *s_err = 0;
+        *s_g_issued = 0;
+        *s_p_issued = 0;
     }
     __syncwarp();
     if (warp == 0) {
@@ -2089,9 +2112,8 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     };
     auto tile_by_tma = [&](int i) { return out_rows(i) == kC || chunk_start(c_lo + i) + out_rows(i) >= p.t_cap; };
     // The images (64 KB) arrive by cp.async from every thread, one commit
-    // group each.  The control thread issues the tile copies and counts them,
-    // so that a failed CTA can let the ones in flight land before it exits.
-    int g_issued = 0, p_issued = 0;
+    // group each.  The tile copies are counted, so that a failed CTA can let
+    // the ones in flight land before it exits.
     auto load_image = [&](uint8_t* dst, const void* src) {
         const uint8_t* src8 = static_cast<const uint8_t*>(src);
         for (int i = tid; i < int(2 * kSoImg / 16); i += int(kSoThreads)) cp_async16(dst + i * 16, src8 + i * 16);
@@ -2107,7 +2129,7 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
         mbar_arrive_expect_tx(bar, 16384);
         tma_load_2d_hint(dst, &maps.g, bar, h * kD, y, l2_evict_first());
         tma_load_2d_hint(dst + 8192, &maps.g, bar, h * kD + 64, y, l2_evict_first());
-        g_issued = i + 1;
+        *s_g_issued = i + 1;
     };
     auto issue_p = [&](int i) {                      // O' tile of output chunk i
         uint64_t* bar = &bars[SO_P0 + i % 3];
@@ -2116,11 +2138,14 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
         mbar_arrive_expect_tx(bar, 16384);
         tma_load_2d_hint(dst, &maps.o, bar, h * kD, y, l2_evict_first());
         tma_load_2d_hint(dst + 8192, &maps.o, bar, h * kD + 64, y, l2_evict_first());
-        p_issued = i + 1;
+        *s_p_issued = i + 1;
     };
+    // the first G tiles and O' tiles (O' tile i + 2 follows once chunk i is
+    // staged, so that the phases of SO_STAGED cannot run two ahead of the
+    // tile thread)
     auto issue_tiles = [&]() {
         for (int i = 0; i < nout && i < 3; ++i) issue_g(i);
-        for (int i = 0; i < nout && i < 3; ++i) issue_p(i);
+        for (int i = 0; i < nout && i < 2; ++i) issue_p(i);
     };
     load_image(sm + kSoOffS, slot_of(1) + 2 * kD * kD);  // S_1^T
     if (nsteps > 0 || final_after) load_m(1, 0);
@@ -2203,9 +2228,9 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (!epi) {
-            // ---- control: products into TMEM buffer i & 1, tile loads, tile stores
-            if (lane == 0) {
+        if (tid == kSoMma) {
+            // ---- issuer: products into TMEM buffer i & 1, G tile loads -------------
+            {
                 const uint32_t id_o = idesc_bf16(128, 64, 0, 0);   // B = G tile, K-major [t][d]
                 auto issue_out = [&](int i) {                 // O^T (buffer i & 1) = S^T G^T
                     if (!wait(SO_G0 + i % 3, uint32_t((i / 3) & 1))) return false;
@@ -2226,8 +2251,18 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
                     // chunk i's product has read its G tile: the tile takes chunk i + 3
                     if (ok) ok = wait(SO_O0 + (i & 1), uint32_t((i >> 1) & 1));
                     if (ok && i + 3 < nout) issue_g(i + 3);
-                    if (ok) ok = wait(SO_STAGED0 + (i & 1), uint32_t((i >> 1) & 1));
-                    if (!ok) break;
+                }
+                if (!ok) *s_err = 1;
+            }
+        } else if (tid == kSoCtl) {
+            // ---- tile thread: stores of the results, O' tile loads ------------------
+            {
+                bool ok = true;
+                for (int i = 0; i < nout; ++i) {
+                    if (!wait(SO_STAGED0 + (i & 1), uint32_t((i >> 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
                     if (tile_by_tma(i)) {
                         const uint8_t* ot = sm + kSoOffP + uint32_t(i % 3) * 16384u;
                         const int cs = int(chunk_start(c_lo + i));
@@ -2237,13 +2272,13 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
                     bulk_commit_group();
                     // chunk i - 1's store has read its tile: the tile takes chunk i + 2
                     bulk_wait_group_read<1>();
-                    if (i >= 1 && i + 2 < nout) issue_p(i + 2);
+                    if (i + 2 < nout) issue_p(i + 2);
                     prefetch_tiles(i + 6, i + 7);             // and a later chunk's tiles toward L2
                 }
                 bulk_wait_all();                              // tile stores done before the CTA exits
                 if (!ok) *s_err = 1;
             }
-        } else {
+        } else if (epi) {
             // ---- epilogue warps: O = O' + (this warp's lanes, token half) ------------
             __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(p.out);
             auto warp_wait = [&](int b, uint32_t parity) {
@@ -2321,13 +2356,16 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     cp_async_wait_all();
     tc_fence_before();
     __syncthreads();
-    if (tid == kSoCtl && (fail || *s_err)) {
-        atomicAdd(&g_tc_timeouts, 1);
-        // every product issued has completed and the tile copies still in
-        // flight land before TMEM and shared memory go away
+    if (tid == kSoMma && (fail || *s_err)) {
+        // every output product issued has completed before TMEM goes away
         tc_fence_after();
         umma_commit(&bars[SO_DRAIN]);
         mbar_wait(&bars[SO_DRAIN], 0, kWaitLimit, kSuspendNs);
+    }
+    if (tid == kSoCtl && (fail || *s_err)) {
+        atomicAdd(&g_tc_timeouts, 1);
+        // the tile copies still in flight land before shared memory goes away
+        const int g_issued = *s_g_issued, p_issued = *s_p_issued;
         for (int i = g_issued - 3 < 0 ? 0 : g_issued - 3; i < g_issued; ++i)
             mbar_wait(&bars[SO_G0 + i % 3], uint32_t((i / 3) & 1), kWaitLimit, kSuspendNs);
         for (int i = p_issued - 3 < 0 ? 0 : p_issued - 3; i < p_issued; ++i)
@@ -2437,8 +2475,8 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if ((e = ensure_smem(reinterpret_cast<const void*>(seg_out_kernel), int(kSoSmem))) != cudaSuccess) return e;
     timer_begin(s, "seg_out_kernel");                 // S_s, O = O' + G S_s, the final state
-    e = launch_pdl(seg_out_kernel,
-                   dim3(p.Hv, p.B, unsigned((p.seg_max - 1) * p.seg_groups + (p.seg_final_cta ? 1 : 0))), kSoThreads,
+    const int so_ctas = p.seg_max - 1 <= kSegTable ? int(p.seg_gstart[p.seg_max - 1]) : (p.seg_max - 1) * p.seg_groups;
+    e = launch_pdl(seg_out_kernel, dim3(p.Hv, p.B, unsigned(so_ctas + (p.seg_final_cta ? 1 : 0))), kSoThreads,
                    kSoSmem, s, q, maps);
     timer_end(s);
     return e;

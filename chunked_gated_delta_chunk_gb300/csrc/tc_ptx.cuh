@@ -62,6 +62,16 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
+// Wait for the phase with the given parity by polling without suspending
+// (the lowest wake-up latency, for hand-offs on a dependent chain; the
+// polling warp takes issue slots from the others on its scheduler); false
+// after `limit` polls.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_test(bar, parity)) return true;
+    return false;
+}
+
 // Wait for the phase with the given parity; false after `limit` attempts
 // (each attempt sleeps at most ~suspend_ns, so the wait is bounded in time).
 // A phase that has already completed is seen by one non-blocking test.
