@@ -1490,7 +1490,8 @@ enum : int {
     ST_SFREE0 = 9,       // staging tile b read by its store
     ST_UHREADY = 11,     // U in TMEM
     ST_DRAIN = 12,
-    ST_NBARS = 13
+    ST_IMG = 13,         // the final state's image staged (one arrival per epilogue warp)
+    ST_NBARS = 14
 };
 constexpr uint32_t kStSmemBytes = kStOffBar + ST_NBARS * 8 + 16 + 1024;
 static_assert(kStSmemBytes <= 232448, "dynamic shared memory above the 227 KB per-block limit");
@@ -1586,13 +1587,40 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     // the hand-offs of the chunk chain: polled (see mbar_spin)
     auto spin = [&](int b, uint32_t parity) { return mbar_spin(&bars[b], parity, kWaitLimit); };
 
-    if (tid == 0) {
+    // The record operands of chunk c into slot c & 1: the merged B
+    // tile (the record's WQ tile, whose order matches the accumulator
+    // pair [X | O even] or [O odd | X] of the chunk's parity), P hi | lo
+    // with U0^T, the raw K tile (rows at or past the buffers' end read
+    // as zero; rows past the sequences' end are cleared by the
+    // epilogue warps) and the vectors.
+    auto issue_copies = [&](int c) {
+        const int b = c & 1;
+        uint8_t* sp = sm + uint32_t(b) * kStSlot;
+        const uint8_t* rec = record(c);
+        uint64_t* bar = &bars[ST_FULL0 + b];
+        mbar_arrive_expect_tx(bar, 32768u + 16384u + 16384u + 512u + (has_u0 ? 32768u : 0u));
+        bulk_load(sp, rec + kRecWQ, 32768, bar);
+        bulk_load(sp + kStOffP, rec + kRecP, has_u0 ? 49152u : 16384u, bar);
+        tma_load_2d(sp + kStOffK, &maps.k, bar, kh * kD, int(chunk_start(c)));
+        tma_load_2d(sp + kStOffK + 8192, &maps.k, bar, kh * kD + 64, int(chunk_start(c)));
+        bulk_load(sm + kStOffVec + uint32_t(b) * 512u, rec + kRecVec, 512, bar);
+        *s_issued = c + 1;
+    };
+    // The copier thread sets up the barriers and starts the first record's
+    // copies before the block's first barrier.
+    if (is_copier && lane == 0) {
         for (int i = 0; i < ST_NBARS; ++i)
-            mbar_init(&bars[i], (i == ST_UREADY || i == ST_UHREADY || i == ST_ZBREADY || i == ST_OSTAGED)
+            mbar_init(&bars[i], (i == ST_UREADY || i == ST_UHREADY || i == ST_ZBREADY || i == ST_OSTAGED ||
+                                 i == ST_IMG)
                                     ? kStEpiWarps : 1);
         fence_mbar_init();
         *s_err = 0;
         *s_issued = 0;
+        if (nchunks > 0) {
+            tma_prefetch_desc(&maps.k);
+            tma_prefetch_desc(omap);
+            issue_copies(0);
+        }
     }
     __syncwarp();
     if (warp == 0) {
@@ -1611,27 +1639,6 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     if (is_copier) {
         // ============================================================ copier
         if (lane == 0 && nchunks > 0) {
-            tma_prefetch_desc(&maps.k);
-            tma_prefetch_desc(omap);
-            // The record operands of chunk c into slot c & 1: the merged B
-            // tile (the record's WQ tile, whose order matches the accumulator
-            // pair [X | O even] or [O odd | X] of the chunk's parity), P hi | lo
-            // with U0^T, the raw K tile (rows at or past the buffers' end read
-            // as zero; rows past the sequences' end are cleared by the
-            // epilogue warps) and the vectors.
-            auto issue_copies = [&](int c) {
-                const int b = c & 1;
-                uint8_t* sp = sm + uint32_t(b) * kStSlot;
-                const uint8_t* rec = record(c);
-                uint64_t* bar = &bars[ST_FULL0 + b];
-                mbar_arrive_expect_tx(bar, 32768u + 16384u + 16384u + 512u + (has_u0 ? 32768u : 0u));
-                bulk_load(sp, rec + kRecWQ, 32768, bar);
-                bulk_load(sp + kStOffP, rec + kRecP, has_u0 ? 49152u : 16384u, bar);
-                tma_load_2d(sp + kStOffK, &maps.k, bar, kh * kD, int(chunk_start(c)));
-                tma_load_2d(sp + kStOffK + 8192, &maps.k, bar, kh * kD + 64, int(chunk_start(c)));
-                bulk_load(sm + kStOffVec + uint32_t(b) * 512u, rec + kRecVec, 512, bar);
-                *s_issued = c + 1;
-            };
             // the staged output tile of chunk cc to the output (TMA; one bulk
             // group per chunk, empty when the epilogue warps stored the rows);
             // chunk cc - 1's staging tile is free once its store has read it
@@ -1647,7 +1654,6 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 if (cc >= 1) mbar_arrive(&bars[ST_SFREE0 + ((cc - 1) & 1)]);
                 return true;
             };
-            issue_copies(0);
             if (nchunks > 1) issue_copies(1);
             bool fail = false;
             for (int c = 1; c < nchunks && !fail; ++c) {
@@ -1910,11 +1916,24 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                         tmem_st16(tZ + lane_addr + sub * 32, z);
                         tmem_st16(tZ + lane_addr + sub * 32 + 16, z + 16);
                     } else if (img_dst) {
-                        // this thread's lane is one row of either image
+                        // this thread's lane is one row of either image, staged
+                        // in the slot of the (absent) next chunk, whose last
+                        // chunk's products are done; then every warp copies a
+                        // sixteenth of the staged images out in whole lines
+                        uint8_t* st = sm + uint32_t(nchunks & 1) * kStSlot;
 #pragma unroll
                         for (int i = 0; i < 32; i += 8)
-                            store_split8(img_dst + toff(row, sub * 32 + i, 16384),
-                                         img_dst + 32768 + toff(row, sub * 32 + i, 16384), z + i);
+                            store_split8(st + toff(row, sub * 32 + i, 16384), st + 32768 + toff(row, sub * 32 + i, 16384),
+                                         z + i);
+                        warp_arrive(ST_IMG);
+                        if (!warp_wait(ST_IMG, 0)) {
+                            fail = true;
+                            break;
+                        }
+                        const uint4* src = reinterpret_cast<const uint4*>(st) + warp * 256;
+                        uint4* dst = reinterpret_cast<uint4*>(img_dst) + warp * 256;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) dst[k * 32 + lane] = src[k * 32 + lane];
                     } else if (final_dst) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) final_dst[size_t(sub * 32 + i) * kD + row] = z[i];
