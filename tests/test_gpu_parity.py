@@ -250,12 +250,13 @@ def test_prefill_then_decode_equals_token_loop():
 # ---------------------------------------------------------------- segment scan
 @pytest.mark.parametrize("seg,lengths,chunk", [
     (1, [300], 64), (2, [640], 64), (3, [64 * 7 + 5], 64), (4, [1, 200, 0, 900], 64),
-    (2, [333, 64 * 6], 32), (5, [4096], 64), (4, [64 * 7], 64)])
+    (2, [333, 64 * 6], 32), (5, [4096], 64), (4, [64 * 7], 64), (1, [64 * 70 + 3], 64)])
 def test_segment_scan_matches_oracle(seg, lengths, chunk):
     """The segment-parallel scan (every later segment from a zero state and
     from the identity with V = 0, outputs and maps of both, then the
     segments' incoming states and O = O' + G S_s) equals the token loop;
-    segments end on full and partial chunks."""
+    segments end on full and partial chunks.  71 segments of one chunk pass
+    the 64 segments seg_out_kernel's group table covers (uniform groups)."""
     p = inputs.make_problem(40 + seg, lengths, 2, 4, 128, 128, chunk=chunk)
     call = runner.PrefillCall(p, segment_chunks=seg)
     from chunked_gated_delta_chunk_gb300 import binding as B
