@@ -1,7 +1,7 @@
-// Tensor-core chunk kernel (bf16, dk = dv = 128) for sm_103a: tcgen05 MMAs
+// Tensor-core chunk kernels (bf16, dk = dv = 128) for sm_103a: tcgen05 MMAs
 // with TMEM accumulators and TMEM-resident A operands, B operands in
 // 128-byte-swizzled shared memory fed by TMA, the fp32 state carried in TMEM
-// through all chunks of a sequence.
+// through the chunks of a sequence (or of a segment of one).
 //
 // Method: the chunked delta rule of "perf(qwen3_5): prefill text prompts in
 // multi-token chunks" (Implementation section).  Per chunk of n <= 64 rows
@@ -12,31 +12,37 @@
 //   O = diag(Gamma) Q S_0 + (exp(gamma_t - gamma_i) q_t.k_i)_{i<=t} U
 //   S_S = exp(gamma_S) S_0 + (K * exp(min(gamma_S - gamma, 0)))^T U
 // T is the 64-row padded blocked inverse (8x8 Neumann blocks, then 2x2 block
-// inversion level by level) in fp32 on the CUDA cores.
+// inversion level by level) in fp32 on the CUDA cores and the warp MMA.
 //
 // GB300 mapping.  The state is kept transposed, Z = S^T [dv, dk], as an fp32
 // TMEM accumulator (lane = value column j, column = key row d), so that every
 // contraction is an M = 128 tcgen05.mma:
-//   Gram   D_G  = [K; Q] K^T                         raw bf16 q, k (smem, K-major)
-//   U0^T   D_X  = V^T (T diag beta)^T                T split into bf16 hi + lo
-//   W^T    D_W  = K^T (T diag(beta Gamma r_k))^T     T split into bf16 hi + lo
-//   chain  D_X += Zb (-W^T)          -> U^T          Zb = bf16(Z) in TMEM
-//          D_O  = Zb Qs^T                            Qs = diag(Gamma r_q) Q
-//          Z   += Us^T K   (Z pre-scaled by exp(gamma_S))
-//                                                    Us = U diag(exp(min(gamma_S-gamma,0)) r_k),
-//                                                    bf16 hi + lo, in TMEM
-//          D_O += U^T P^T                            U, P each split into bf16 hi + lo
+//   Gram   [K; Q] [K; Q]^T (split preparation) or [K; Q] K^T (one pass)
+//   U0^T   V^T (T diag beta)^T                T split into bf16 hi + lo
+//   W^T    K^T (T diag(beta Gamma r_k))^T     T split into bf16 hi + lo
+//   chain  X = Zb (-W^T), U^T = U0^T + X      Zb = bf16(Z) in TMEM
+//          O = Zb Qs^T                        Qs = diag(Gamma r_q) Q
+//          Z += Us^T K  (Z pre-scaled by exp(gamma_S))
+//                                             Us = U diag(exp(min(gamma_S-gamma,0)) r_k),
+//                                             bf16 hi + lo, in TMEM
+//          O += U^T P^T                       P split into bf16 hi + lo
 // L2 normalisation of q and k is folded into row scalings (r = 1/|x|); every
 // exponent is clamped at zero and only evaluated where its mask keeps it.
-// The hi/lo splits keep every intermediate to ~16 bits before it meets a bf16
-// operand, so in O mainly the bf16 output rounding remains visible.
+// The hi/lo splits keep the inverse's products and the state update to
+// ~16 bits before they meet a bf16 operand.
 //
-// Warp specialisation (384 threads): warps 0-3 and 8-11 prepare chunk c + 1
-// (norms, cumsum, masks, inverse, U0 and W) while warps 4-7 run the
-// S-dependent chain of chunk c.  mbarriers hand over each stage; TMA brings
-// the raw tiles of chunk c + 2 while chunk c finishes.  Every wait is
-// bounded; a CTA that runs out records it in a device counter, lets its TMA
-// copies land and still frees its TMEM.
+// The kernels of this file:
+//   chunk_prep_kernel   the state-independent part of every chunk, all chunks
+//                       in parallel, into one record per (value head, chunk);
+//   chunk_state_kernel  the chain over the records (one CTA per value head,
+//                       sequence and segment pass);
+//   seg_out_kernel      the segment scan's combine: each segment's incoming
+//                       state and its outputs O = O' + G S_s;
+//   chunk_tc_kernel     the one-kernel pass without records or a workspace
+//                       (384 threads: warps 0-3 and 8-11 prepare chunk c + 1
+//                       while warps 4-7 run the chain of chunk c).
+// Every wait is bounded; a CTA that runs out records it in a device counter,
+// lets its TMA copies land and still frees its TMEM.
 #include <cuda.h>
 
 #include "gdn_common.cuh"
