@@ -101,14 +101,39 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def _code_only(text):
+    """C/C++ source without its comments and whitespace (so that a comment
+    edit leaves a kernel's hash, and its recorded counters, valid)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"' or c == "'":                       # string or character literal
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join("".join(out).split())
+
+
 def kernel_source_hash(sources):
-    """Hash of the kernel's source files (names under the package's csrc/)."""
+    """Hash of the code of the kernel's source files (names under the
+    package's csrc/), comments and whitespace left out."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunked_gated_delta_chunk_gb300", "csrc")
     for name in sorted(sources):
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

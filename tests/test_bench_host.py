@@ -64,3 +64,15 @@ def test_reference_arm_under_torchrun_prints_one_line():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_kernel_hash_ignores_comments_not_code():
+    """The recorded DRAM counters stay valid across comment edits of a
+    kernel's sources and lapse on any code change."""
+    bench = _load_bench()
+    base = 'int a = 1; // one\n/* block\n comment */ const char* s = "x // y";\n'
+    assert bench._code_only(base) == bench._code_only(base.replace("// one", "// changed"))
+    assert bench._code_only(base) == bench._code_only(base.replace("/* block\n comment */", ""))
+    assert bench._code_only(base) != bench._code_only(base.replace("a = 1", "a = 2"))
+    assert bench._code_only(base) != bench._code_only(base.replace('"x // y"', '"x // z"'))
+
