@@ -112,6 +112,37 @@ constexpr uint32_t kColO = 256;    // O^T (64)
 constexpr uint32_t kColGW = 320;   // Gram, then W^T (64)
 constexpr uint32_t kColU = 384;    // U hi, U lo, Us hi, Us lo (4 x 32)
 
+// The sequence whose chains the CTAs of grid row y run: the sequences in
+// order of decreasing length (ties by index).  The block scheduler hands out
+// CTAs in index order, so when the (sequence, head) units fill more than one
+// wave the longest chains start in the first.  Every CTA derives the same
+// permutation from cu_seqlens (one warp: each lane ranks one or two
+// sequences); up to 64 sequences, else the identity.  Called by whole warps.
+constexpr int kLongestFirstMax = 64;
+__device__ __forceinline__ int seq_of_row(const int32_t* cu, int B, int y) {
+    if (B <= 1 || B > kLongestFirstMax) return y;
+    const int lane = threadIdx.x & 31;
+    auto len = [&](int i) {
+        const int a = cu[i], b = cu[i + 1];
+        return b > a ? b - a : 0;
+    };
+    for (int base = 0; base < B; base += 32) {
+        const int i = base + lane;
+        int rank = -1;
+        if (i < B) {
+            const int li = len(i);
+            rank = 0;
+            for (int j = 0; j < B; ++j) {
+                const int lj = len(j);
+                rank += (lj > li || (lj == li && j < i)) ? 1 : 0;
+            }
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, rank == y);
+        if (m) return base + __ffs(int(m)) - 1;
+    }
+    return y;
+}
+
 // Offset of (row, col) in a swizzled tile of 64-column blocks (128-byte rows).
 __device__ __forceinline__ uint32_t toff(int row, int col, uint32_t block_stride) {
     const int blk = col >> 6, c = col & 63;
@@ -845,7 +876,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     volatile int* s_err = reinterpret_cast<volatile int*>(sm + kOffBar + kNumBars * 8 + 4);
     int* s_tma_last = reinterpret_cast<int*>(sm + kOffBar + kNumBars * 8 + 8);   // [2]
 
-    const int h = blockIdx.x, n = blockIdx.y;
+    const int h = blockIdx.x, n = seq_of_row(p.cu, p.B, blockIdx.y);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;                 // TMEM lane of this thread
@@ -1516,7 +1547,7 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     volatile int* s_err = reinterpret_cast<volatile int*>(sm + kStOffBar + ST_NBARS * 8 + 4);
     volatile int* s_issued = reinterpret_cast<volatile int*>(sm + kStOffBar + ST_NBARS * 8 + 8);
 
-    const int h = blockIdx.x, n = blockIdx.y;
+    const int h = blockIdx.x, n = seq_of_row(p.cu, p.B, blockIdx.y);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool is_issuer = warp == int(kStEpiWarps);
     const bool is_copier = warp == int(kStEpiWarps) + 1;
@@ -2057,7 +2088,7 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     volatile int* s_err = reinterpret_cast<volatile int*>(sm + kSoOffBar + kSoNumBars * 8 + 4);
     volatile int* s_g_issued = reinterpret_cast<volatile int*>(sm + kSoOffBar + kSoNumBars * 8 + 8);
     volatile int* s_p_issued = reinterpret_cast<volatile int*>(sm + kSoOffBar + kSoNumBars * 8 + 12);
-    const int h = blockIdx.x, n = blockIdx.y, z = blockIdx.z;
+    const int h = blockIdx.x, n = seq_of_row(p.cu, p.B, blockIdx.y), z = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool epi = warp < int(kSoEpiWarps);
     const int Hv = p.Hv;
