@@ -123,8 +123,11 @@ typedef struct gdn_prefill_desc {
      * incoming state S_s (S_{s+1} = M_s S_s + B_s) and its outputs
      * O = O' + G S_s on the tensor cores.  The workspace then also holds the
      * maps (3 x 64 KiB per value head and segment slot) and G (bf16, like
-     * out).  0 = chosen from the shape by a cost model of the passes on 152
-     * SMs (one pass when that is cheaper), < 0 = off. */
+     * out).  0 = chosen from the shape by a cost model of the passes on the
+     * current device's SMs (one pass when that is cheaper), < 0 = off.  The
+     * chain kernels take the sequences longest first, so that with more
+     * (sequence, head) units than one wave holds the longest chains start
+     * first. */
     int segment_chunks;
 
     /* Split preparation (bf16, dk = dv = 128, T_total known, and a
