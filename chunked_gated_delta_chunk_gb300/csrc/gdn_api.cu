@@ -219,7 +219,22 @@ size_t workspace_needed(const gdn_prefill_desc* d) {
 }
 
 int check_prefill(const gdn_prefill_desc* d) {
-    int st = check_common(d);
+    if (d == nullptr) return GDN_ERR_INVALID_ARG;
+    int st;
+    if (d->T_total == 0) {
+        // no token rows: the token tensors may have no storage (null pointers)
+        alignas(16) static const float kNoRows[4] = {};
+        gdn_prefill_desc e = *d;
+        e.q = e.k = e.v = kNoRows;
+        e.out = const_cast<float*>(kNoRows);            // only validated, never written
+        e.g = e.beta = kNoRows;
+        e.conv_x = nullptr;
+        st = check_common(&e);
+        if (st == GDN_OK && d->conv_state_out != nullptr && (d->conv_kernel < 2 || d->conv_kernel > 8))
+            st = GDN_ERR_UNSUPPORTED;
+    } else {
+        st = check_common(d);
+    }
     if (st != GDN_OK) return st;
     if (d->chunk < 1 || d->chunk > gdn::kMaxChunk) return GDN_ERR_CHUNK;
     if (d->cu_seqlens == nullptr) return GDN_ERR_INVALID_ARG;
@@ -232,6 +247,25 @@ int check_prefill(const gdn_prefill_desc* d) {
         }
     }
     return GDN_OK;
+}
+
+// A batch without a token (T_total == 0): every sequence keeps its states
+// (an empty sequence returns its incoming state), by stream-ordered device
+// copies or, without an incoming state, zero fills.  No kernel runs.
+int empty_prefill(const gdn_prefill_desc* d, cudaStream_t s) {
+    const size_t state_bytes = size_t(d->B) * size_t(d->Hv) * size_t(d->dk) * size_t(d->dv) * sizeof(float);
+    cudaError_t e = cudaSuccess;
+    if (d->state_out != nullptr && d->state_out != d->state_in)
+        e = d->state_in != nullptr
+                ? cudaMemcpyAsync(d->state_out, d->state_in, state_bytes, cudaMemcpyDeviceToDevice, s)
+                : cudaMemsetAsync(d->state_out, 0, state_bytes, s);
+    if (e == cudaSuccess && d->conv_state_out != nullptr && d->conv_state_out != d->conv_state_in) {
+        const size_t conv_bytes = size_t(d->B) * size_t(conv_channels(d)) * size_t(d->conv_kernel - 1) * sizeof(float);
+        e = d->conv_state_in != nullptr
+                ? cudaMemcpyAsync(d->conv_state_out, d->conv_state_in, conv_bytes, cudaMemcpyDeviceToDevice, s)
+                : cudaMemsetAsync(d->conv_state_out, 0, conv_bytes, s);
+    }
+    return cuda_status(e);
 }
 
 }  // namespace
@@ -271,6 +305,7 @@ int gdn_prefill_ex(const gdn_prefill_desc* d, gdn_stream_t stream) {
     if (st != GDN_OK) return st;
     if (d->B == 0) return GDN_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (d->T_total == 0) return empty_prefill(d, s);
 
     gdn::ChunkParams p{};
     p.g = d->g;
@@ -432,7 +467,7 @@ int gdn_step(const void* q, const void* k, const void* v, const float* g, const 
 int gdn_prefill_plan(const gdn_prefill_desc* d, const char** names, int max_names) {
     const int st = check_prefill(d);
     if (st != GDN_OK) return -st;
-    if (d->B == 0) return 0;
+    if (d->B == 0 || d->T_total == 0) return 0;      // nothing, or stream-ordered copies only
     const char* plan[6];
     int n = 0;
     gdn::ChunkParams p{};

@@ -83,7 +83,12 @@ typedef struct gdn_prefill_desc {
     int Hk, Hv;              /* key and value heads, Hv % Hk == 0 */
     int dk, dv;              /* head dims, each in {16, 32, 64, 128} */
     int chunk;               /* rows per chunk, 1..64 (results do not depend on it) */
-    int64_t T_total;         /* cu_seqlens[B]; required with conv_x, else may be -1 */
+    int64_t T_total;         /* cu_seqlens[B]; required with conv_x, else may be -1.
+                              * 0: no token in the batch; the token tensors may then
+                              * be NULL and the call only returns every sequence's
+                              * states (state_out <- state_in, conv_state_out <-
+                              * conv_state_in, zeros without them) by stream-ordered
+                              * device copies, launching no kernel */
 
     const void* q;           /* [T, Hk, dk] dtype; ignored when conv_x != NULL */
     const void* k;           /* [T, Hk, dk] dtype; ignored when conv_x != NULL */

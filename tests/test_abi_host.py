@@ -285,3 +285,17 @@ def test_segmented_plan_and_workspace(lib):
     assert B.gdn_prefill_plan(d) == ["chunk_prep_kernel", "chunk_state_kernel"]
     d.workspace_bytes = 0                            # no records: the inline pass
     assert B.gdn_prefill_plan(d) == ["chunk_tc_kernel"]
+
+
+def test_batch_without_tokens_needs_no_token_tensors(lib):
+    """T_total == 0 (every sequence empty): the token tensors may be NULL; the
+    plan launches no kernel, and with no state to return nothing is enqueued."""
+    d = B.make_desc(B=3, Hk=2, Hv=4, dk=128, dv=128, T_total=0, cu_seqlens=A)
+    assert B.gdn_prefill_plan(d) == []
+    assert lib.gdn_prefill_ex(ctypes.byref(d), None) == B.GDN_OK
+    # the rest is still validated
+    assert lib.gdn_prefill_ex(ctypes.byref(B.make_desc(B=3, Hk=2, Hv=4, dk=128, dv=128, T_total=0)),
+                              None) == B.GDN_ERR_INVALID_ARG                 # no cu_seqlens
+    d_conv = B.make_desc(B=3, Hk=2, Hv=4, dk=128, dv=128, T_total=0, cu_seqlens=A, conv_state_out=A,
+                         conv_kernel=1)
+    assert lib.gdn_prefill_ex(ctypes.byref(d_conv), None) == B.GDN_ERR_UNSUPPORTED

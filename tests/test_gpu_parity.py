@@ -377,3 +377,22 @@ def test_launch_timer_records_every_planned_launch():
     assert all(ms > 0 for _, ms in records)
     torch.cuda.synchronize()
     compare({k: v.cpu() for k, v in call.results().items()}, run_oracle(p), TOL_BF16)
+
+
+@pytest.mark.parametrize("conv_kernel,s0_sd,alias", [(4, 0.05, False), (0, None, False), (4, 0.05, True)])
+def test_batch_without_tokens_returns_states(conv_kernel, s0_sd, alias):
+    """Every sequence empty (T_total == 0) on the tensor-core shape: the token
+    tensors have no storage, no kernel runs, and every sequence's states come
+    back unchanged (zeros without an incoming state; in place when aliased)."""
+    p = inputs.make_problem(61, [0, 0, 0], 2, 4, 128, 128, conv_kernel=conv_kernel, s0_sd=s0_sd)
+    call = runner.PrefillCall(p, alias_state=alias, alias_conv_state=alias and conv_kernel > 0)
+    from chunked_gated_delta_chunk_gb300 import binding as B
+    assert B.gdn_prefill_plan(call.desc) == []
+    call.run()
+    torch.cuda.synchronize()
+    res = {k: v.cpu() for k, v in call.results().items()}
+    assert res["out"].numel() == 0
+    want = p.state_in if p.state_in is not None else torch.zeros(3, 4, 128, 128)
+    assert torch.equal(res["state_out"], want)
+    if conv_kernel:
+        assert torch.equal(res["conv_state_out"], p.conv["state_in"])
