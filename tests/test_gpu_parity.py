@@ -396,3 +396,20 @@ def test_batch_without_tokens_returns_states(conv_kernel, s0_sd, alias):
     assert torch.equal(res["state_out"], want)
     if conv_kernel:
         assert torch.equal(res["conv_state_out"], p.conv["state_in"])
+
+
+@pytest.mark.parametrize("lengths", [
+    [130, 130, 64, 130, 0, 1, 64],                                       # equal lengths: ties by index
+    [int(x) for x in torch.randint(0, 100, (80,), generator=torch.Generator().manual_seed(62))],  # > 64 sequences
+])
+def test_many_sequences_longest_first_and_ties(lengths):
+    """The chain kernels take sequences longest first (ties by index, the
+    identity past 64 sequences); every sequence's rows and state still match
+    the oracle, with the records and without them."""
+    p = inputs.make_problem(63, lengths, 2, 4, 128, 128)
+    ref = run_oracle(p)
+    for split in (0, -1):
+        call = runner.PrefillCall(p, split_prep=split, segment_chunks=-1)
+        call.run()
+        torch.cuda.synchronize()
+        compare({k: v.cpu() for k, v in call.results().items()}, ref, TOL_BF16)
