@@ -341,7 +341,8 @@ int gdn_prefill_ex(const gdn_prefill_desc* d, gdn_stream_t stream) {
                          p.seg_max - 1 <= gdn::kSegTable ? p.seg_gstart : nullptr);
             p.g_out = static_cast<char*>(d->workspace) + conv_bytes + segment_map_bytes(d, sc);
         }
-        if (prep_bytes > 0 && d->workspace != nullptr &&
+        // the preparation counts its items (Hv x slots) in 32 bits
+        if (prep_bytes > 0 && d->workspace != nullptr && int64_t(d->Hv) * prep_slots(d) < (int64_t(1) << 31) &&
             d->workspace_bytes >= conv_bytes + seg_bytes + prep_bytes) {
             p.prep_ws = static_cast<uint8_t*>(d->workspace) + conv_bytes + seg_bytes;
             p.prep_slots = prep_slots(d);

@@ -439,7 +439,12 @@ constexpr uint32_t kPOffT = kPOffPst + 16384;
 constexpr uint32_t kPOffTmp = kPOffT + kC * kLdA * 4;
 constexpr uint32_t kPOffVec = kPOffTmp + 1536 * 4;
 constexpr uint32_t kPOffBar = kPOffVec + 8 * kC * 4;
-constexpr uint32_t kPrepSmemBytes = kPOffBar + 3 * 8 + 8 + 1024;
+constexpr int kPrepRing = 32;                            // items one lookup finds (one per lane)
+constexpr uint32_t kPOffRing = kPOffBar + 3 * 8 + 8;     // the CTA's next items: kPrepRing x 32 B
+constexpr uint32_t kPOffRingIdx = kPOffRing + kPrepRing * 32;   // their item numbers, then count, next candidate
+constexpr int kPrepSeqs = 64;                            // sequences whose bounds sit in shared memory
+constexpr uint32_t kPOffSeq = kPOffRingIdx + kPrepRing * 8 + 16;   // first token, first slot: 2 x (kPrepSeqs + 1)
+constexpr uint32_t kPrepSmemBytes = kPOffSeq + 2 * (kPrepSeqs + 1) * 4 + 8 + 1024;
 constexpr uint32_t kPrepTmemCols = 256;                  // Gram [K; Q][K; Q]^T (128), then W^T (64); U0^T (64)
 static_assert(kC * kLdA * 4 <= 4 * 8192 && kPOffT >= kPOffTb + 4 * 8192, "A and the P staging beside Tb");
 static_assert(kC * kLdA * 4 >= 16384, "-W^T staging fits in T's place");
@@ -495,38 +500,86 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         bool tma, odd;
     };
     const bool segmented = p.seg_chunks > 0 && p.seg_max >= 2;
+    // Each sequence's first token and first chunk slot (t0_n / chunk + n),
+    // from shared memory for up to kPrepSeqs sequences, else from cu_seqlens.
+    // Items, slots and token indices fit in 32 bits (the host runs this
+    // kernel only when Hv * prep_slots < 2^31; cu_seqlens is int32).
+    int32_t* s_first = reinterpret_cast<int32_t*>(sm + kPOffSeq);
+    int32_t* s_slot0 = s_first + kPrepSeqs + 1;
+    const bool seq_table = p.B <= kPrepSeqs;
+    if (seq_table && pt <= p.B) {
+        const int32_t t = int32_t(seq_first(pt));
+        s_first[pt] = t;
+        s_slot0[pt] = int32_t(uint32_t(t) / uint32_t(p.chunk)) + pt;
+    }
+    __syncthreads();
+    auto first_of = [&](int m) { return seq_table ? int64_t(s_first[m]) : seq_first(m); };
+    auto slot0_of = [&](int m) {
+        return seq_table ? int64_t(s_slot0[m]) : int64_t(uint32_t(seq_first(m)) / uint32_t(p.chunk)) + m;
+    };
     auto resolve = [&](int64_t item, Item& it) {
-        it.h = int(item / p.prep_slots);
-        it.slot = int(item % p.prep_slots);
+        const uint32_t slots = uint32_t(p.prep_slots), chunk = uint32_t(p.chunk);
+        it.h = int(uint32_t(item) / slots);
+        it.slot = int(uint32_t(item) - uint32_t(it.h) * slots);
         int lo = 0, hi = p.B - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (seq_first(mid) / p.chunk + mid <= it.slot) lo = mid;
+            if (slot0_of(mid) <= it.slot) lo = mid;
             else hi = mid - 1;
         }
-        const int64_t t0 = seq_first(lo);
-        int64_t t1 = p.cu[lo + 1];
-        t1 = t1 < t0 ? t0 : (t1 > t_end_all ? t_end_all : t1);
-        const int64_t c = int64_t(it.slot) - (t0 / p.chunk + lo);
-        if (c < 0 || c * p.chunk >= t1 - t0) return false;
-        it.cs = t0 + c * p.chunk;
-        it.rows = int(t1 - it.cs < p.chunk ? t1 - it.cs : p.chunk);
+        const int64_t t0 = first_of(lo);
+        int64_t t1 = first_of(lo + 1);                    // cu_seqlens[lo + 1] clamped to [t0, T]
+        t1 = t1 < t0 ? t0 : t1;
+        const int64_t c = int64_t(it.slot) - slot0_of(lo);
+        if (c < 0 || c * chunk >= t1 - t0) return false;
+        it.cs = t0 + c * chunk;
+        it.rows = int(t1 - it.cs < int64_t(chunk) ? t1 - it.cs : int64_t(chunk));
         it.tma = it.cs + kC <= t_end_all;
-        int64_t local = c;
+        uint32_t local = uint32_t(c);
         if (segmented) {
-            const int64_t L = p.seg_chunks;
-            const int64_t seq_chunks = (t1 - t0 + p.chunk - 1) / p.chunk;
-            const int64_t short_by = ((seq_chunks + L - 1) / L) * L - seq_chunks;
-            const int64_t seg = (c + short_by) / L;
-            local = c - (seg == 0 ? 0 : seg * L - short_by);
+            const uint32_t L = uint32_t(p.seg_chunks);
+            const uint32_t seq_chunks = (uint32_t(t1 - t0) + chunk - 1) / chunk;
+            const uint32_t short_by = ((seq_chunks + L - 1) / L) * L - seq_chunks;
+            const uint32_t seg = (local + short_by) / L;
+            local -= seg == 0 ? 0u : seg * L - short_by;
         }
         it.odd = (local & 1) != 0;
         return true;
     };
-    auto next_item = [&](int64_t from, Item& it) {
-        for (int64_t i = from; i < n_items; i += gridDim.x)
-            if (resolve(i, it)) return i;
-        return n_items;
+    // The CTA's items are blockIdx.x + k * gridDim.x that hold a chunk.  The
+    // last warp looks up the next kPrepRing candidates at once, one per lane,
+    // and packs those that hold a chunk into a ring in shared memory; the
+    // items are then read from the ring (a lookup costs a thread about 1K
+    // cycles, too much to make once per item).
+    static_assert(sizeof(Item) <= 32, "an item's place in the ring");
+    Item* ring = reinterpret_cast<Item*>(sm + kPOffRing);
+    int64_t* ring_idx = reinterpret_cast<int64_t*>(sm + kPOffRingIdx);
+    int* ring_n = reinterpret_cast<int*>(ring_idx + kPrepRing);
+    int64_t* ring_cand = ring_idx + kPrepRing + 1;
+    auto fill_ring = [&](int64_t cand) {          // the last warp, all lanes
+        int n = 0;
+        while (n == 0 && cand < n_items) {
+            const int64_t idx = cand + int64_t(lane) * gridDim.x;
+            Item it;
+            const bool ok = idx < n_items && resolve(idx, it);
+            const uint32_t m = __ballot_sync(0xffffffffu, ok);
+            if (ok) {
+                const int pos = __popc(m & ((1u << lane) - 1u));
+                ring[pos] = it;
+                ring_idx[pos] = idx;
+            }
+            n = __popc(m);
+            cand += int64_t(kPrepRing) * gridDim.x;
+        }
+        if (lane == 0) {
+            *ring_n = n;
+            *ring_cand = cand;
+        }
+    };
+    auto prefetch_box = [&](const Item& it, int b) {   // box b of K (0, 1), Q (2, 3), V (4, 5) toward L2
+        const CUtensorMap* map = b < 2 ? &maps.k : (b < 4 ? &maps.q : &maps.v);
+        const int head = b < 4 ? it.h / (Hv / p.Hk) : it.h;
+        tma_prefetch_2d(map, head * kD + (b & 1) * 64, int(it.cs));
     };
     auto issue_raw = [&](const Item& it) {      // thread 0: the 64-row boxes of K, Q, V
         const int kh = it.h / (Hv / p.Hk);
@@ -540,9 +593,12 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         tma_load_2d(vv + 8192, &maps.v, &bars[0], it.h * kD + 64, y);
     };
 
-    Item cur;
-    int64_t item = next_item(blockIdx.x, cur);
-    if (item >= n_items) return;                            // no chunk for this CTA
+    if (pw == kPrepThreads / 32 - 1) fill_ring(blockIdx.x);
+    __syncthreads();
+    int rn = *ring_n, rp = 0;                               // items in the ring, the current one's place
+    if (rn == 0) return;                                    // no chunk for this CTA
+    Item cur = ring[0];
+    int64_t item = ring_idx[0];
     if (pt == 0) {
         for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
@@ -578,26 +634,6 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         if (pt < kC) {
             vGam[pt] = g_in;
             vBeta[pt] = b_in;
-        }
-        // the next item now: its tiles toward L2 and its g, beta into
-        // registers, so that neither latency lands on this item's path
-        Item nxt;
-        const int64_t next = next_item(item + gridDim.x, nxt);
-        float g_nx = 0.f, b_nx = 0.f;
-        if (next < n_items) {
-            if (pt == 0 && nxt.tma) {
-                const int nkh = nxt.h / (Hv / p.Hk), y = int(nxt.cs);
-                tma_prefetch_2d(&maps.k, nkh * kD, y);
-                tma_prefetch_2d(&maps.k, nkh * kD + 64, y);
-                tma_prefetch_2d(&maps.q, nkh * kD, y);
-                tma_prefetch_2d(&maps.q, nkh * kD + 64, y);
-                tma_prefetch_2d(&maps.v, nxt.h * kD, y);
-                tma_prefetch_2d(&maps.v, nxt.h * kD + 64, y);
-            }
-            if (pt < nxt.rows) {
-                g_nx = p.g[(nxt.cs + pt) * Hv + nxt.h];
-                b_nx = p.beta[(nxt.cs + pt) * Hv + nxt.h];
-            }
         }
         // ---- raw tiles: TMA when the whole 64-row box lies inside the buffers,
         // else plain loads (rows past the buffers are zero)
@@ -654,11 +690,39 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             vGam[2 * lane] = a * kLog2e;
             vGam[2 * lane + 1] = s * kLog2e;
         }
+        // the next item comes from the ring, which the last warp refills when
+        // this item is its last.  While the Gram product runs, warps 2-7 (idle
+        // here) send the next item's six tile boxes toward L2, one each: a
+        // prefetch holds its thread a few hundred cycles
+        const bool refill = rp + 1 >= rn;
+        if (refill) {
+            if (pw == kPrepThreads / 32 - 1) {
+                fill_ring(*ring_cand);
+                __syncwarp();
+                if (lane < 6 && *ring_n > 0 && ring[0].tma) prefetch_box(ring[0], lane);
+            }
+        } else if (pw >= 2 && lane == 0 && ring[rp + 1].tma) {
+            prefetch_box(ring[rp + 1], pw - 2);
+        }
         if (pt == 0) {
             lf = !mbar_wait(&bars[1], mma_phase & 1, kWaitLimit, kSuspendNs);
             bulk_wait_group_read<0>();                    // the last item's staged images are read
         }
         if (__syncthreads_or(lf)) { fail = true; break; }
+        // the next item, and its g, beta into registers: needed once this
+        // item's products have read the tiles
+        if (refill) {
+            rn = *ring_n;
+            rp = -1;
+        }
+        const int np = rp + 1;
+        const Item nxt = np < rn ? ring[np] : cur;
+        const int64_t next = np < rn ? ring_idx[np] : n_items;
+        float g_nx = 0.f, b_nx = 0.f;
+        if (next < n_items && pt < nxt.rows) {
+            g_nx = p.g[(nxt.cs + pt) * Hv + nxt.h];
+            b_nx = p.beta[(nxt.cs + pt) * Hv + nxt.h];
+        }
         tc_fence_after();
         if (phalf == 0) {
             // row norms: |k_i|^2 and |q_t|^2 on the diagonal (TMEM lane r, column r)
@@ -835,6 +899,7 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         }
         item = next;
         cur = nxt;
+        rp = np;
     }
 
     // ---- teardown: a CTA whose bounded wait ran out lets its copies land ------
