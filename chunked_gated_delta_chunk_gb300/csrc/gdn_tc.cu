@@ -85,7 +85,7 @@ constexpr uint32_t kOffA = kOffTb + 4 * 8192;            // A fp32 [64][68]
 constexpr uint32_t kOffT = kOffA + kC * kLdA * 4;        // T fp32 [64][68]
 constexpr uint32_t kOffTmp = kOffT + kC * kLdA * 4;      // inverse scratch, 1536 floats
 constexpr uint32_t kOffVec = kOffTmp + 1536 * 4;         // vectors
-constexpr uint32_t kVecFloats = 8 * kC + 2 * 2 * kC + 2 * kC + 2;   // prep, staging, chain
+constexpr uint32_t kVecFloats = 11 * kC + 2 * 2 * kC + 2 * kC + 2;   // prep, staging, chain
 constexpr uint32_t kOffBar = kOffVec + ((kVecFloats * 4 + 127) / 128) * 128;
 constexpr uint32_t kNumBars = 15;
 constexpr uint32_t kSmemBytes = kOffBar + kNumBars * 8 + 32 + 1024;
@@ -156,8 +156,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // 2^x with the hardware approximation (relative error about 2^-22; results
-// below the smallest normal flush to zero).  Every exponent here is <= 0, so
-// the values lie in (0, 1].
+// below the smallest normal flush to zero).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -438,7 +437,7 @@ constexpr uint32_t kPOffPst = kPOffTb + kC * kLdA * 4;   // P hi | lo staging, a
 constexpr uint32_t kPOffT = kPOffPst + 16384;
 constexpr uint32_t kPOffTmp = kPOffT + kC * kLdA * 4;
 constexpr uint32_t kPOffVec = kPOffTmp + 1536 * 4;
-constexpr uint32_t kPOffBar = kPOffVec + 8 * kC * 4;
+constexpr uint32_t kPOffBar = kPOffVec + 11 * kC * 4;
 constexpr int kPrepRing = 32;                            // items one lookup finds (one per lane)
 constexpr uint32_t kPOffRing = kPOffBar + 3 * 8 + 8;     // the CTA's next items: kPrepRing x 32 B
 constexpr uint32_t kPOffRingIdx = kPOffRing + kPrepRing * 32;   // their item numbers, then count, next candidate
@@ -472,6 +471,9 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     float* vEnd = vRq + kC;                                 // e_i
     float* vFb = vEnd + kC;                                 // beta_i
     float* vFbg = vFb + kC;                                 // beta_i Gamma_i r_k,i
+    float* vCol = vFbg + kC;                                // gamma_j - log2 r_k,j (log2 domain)
+    float* vRowA = vCol + kC;                               // gamma_i + log2 r_k,i
+    float* vRowP = vRowA + kC;                              // gamma_t + log2 r_q,t
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPOffBar);   // raw tiles, Gram, U0 / W
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kPOffBar + 24);
 
@@ -747,6 +749,12 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             vEnd[pt] = e;
             vFb[pt] = vBeta[pt];
             vFbg[pt] = vBeta[pt] * eg * vRk[pt];
+            // the masks' decays and row norms as one power of two per entry:
+            // exp(gamma_i - gamma_j) r_i r_j = 2^(row_i - col_j)
+            const float lk = log2f(vRk[pt]);
+            vCol[pt] = gm - lk;
+            vRowA[pt] = gm + lk;
+            vRowP[pt] = gm + log2f(vRq[pt]);
             reinterpret_cast<float*>(rec + kRecVec)[pt] = e;
             if (pt == rows - 1) reinterpret_cast<float*>(rec + kRecVec)[kC] = eg;
         }
@@ -758,26 +766,36 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         {
             float v[32];
             tmem_ld32(tGW + lane_addr + phalf * 32, v);
+            // A_ij = beta_i exp(gamma_i - gamma_j) r_i r_j k_i.k_j (j < i) and
+            // P_tj = exp(gamma_t - gamma_j) r_t r_j q_t.k_j (j <= t); the
+            // exponents need no clamp, as g <= 0 makes gamma non-increasing
             if (row < kC) {
                 const int i = row;
-                const float bi = vBeta[i] * vRk[i], gi = vGam[i];
+                const float bi = vBeta[i], ai = vRowA[i];
 #pragma unroll
                 for (int q = 0; q < 32; q += 4) {
+                    const float4 c4 = *reinterpret_cast<const float4*>(vCol + phalf * 32 + q);
+                    const float cj[4] = {c4.x, c4.y, c4.z, c4.w};
                     float a4[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int j = phalf * 32 + q + u;
-                        a4[u] = (i < rows && j < i) ? bi * fast_exp2(fminf(gi - vGam[j], 0.f)) * vRk[j] * v[q + u] : 0.f;
+                        a4[u] = (i < rows && j < i) ? bi * (v[q + u] * fast_exp2(ai - cj[u])) : 0.f;
                     }
                     *reinterpret_cast<float4*>(sA + i * kLdA + phalf * 32 + q) = make_float4(a4[0], a4[1], a4[2], a4[3]);
                 }
             } else {
                 const int t = row - kC;
-                const float rt = vRq[t], gt = vGam[t];
+                const float at = vRowP[t];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int j = phalf * 32 + q;
-                    v[q] = (t < rows && j <= t) ? rt * fast_exp2(fminf(gt - vGam[j], 0.f)) * vRk[j] * v[q] : 0.f;
+                for (int q = 0; q < 32; q += 4) {
+                    const float4 c4 = *reinterpret_cast<const float4*>(vCol + phalf * 32 + q);
+                    const float cj[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int j = phalf * 32 + q + u;
+                        v[q + u] = (t < rows && j <= t) ? v[q + u] * fast_exp2(at - cj[u]) : 0.f;
+                    }
                 }
 #pragma unroll
                 for (int q = 0; q < 32; q += 8) {
@@ -932,7 +950,10 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     float* vEnd = vRq + kC;                                 // prep: exp(min(gamma_S - gamma_i, 0)) r_k,i
     float* vFb = vEnd + kC;                                 // prep: beta_i (column factor)
     float* vFbg = vFb + kC;                                 // prep: beta_i Gamma_i r_k,i
-    float* sG = vFbg + kC;                                  // prep: [2][64] g staging (cp.async)
+    float* vCol = vFbg + kC;                                // prep: gamma_j - log2 r_k,j (log2 domain)
+    float* vRowA = vCol + kC;                               // prep: gamma_i + log2 r_k,i
+    float* vRowP = vRowA + kC;                              // prep: gamma_t + log2 r_q,t
+    float* sG = vRowP + kC;                                 // prep: [2][64] g staging (cp.async)
     float* sB = sG + 2 * kC;                                // prep: [2][64] beta staging
     float* cE = sB + 2 * kC;                                // chain: [2][64] end weights
     float* cGS = cE + 2 * kC;                               // chain: [2] exp(gamma_S)
@@ -1186,6 +1207,10 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 vEnd[pt] = pt < rows ? exp2f(fminf(vGam[rows - 1] - gm, 0.f)) * vRk[pt] : 0.f;
                 vFb[pt] = vBeta[pt];
                 vFbg[pt] = vBeta[pt] * eg * vRk[pt];
+                const float lk = log2f(vRk[pt]);           // the masks' 2^(row_i - col_j)
+                vCol[pt] = gm - lk;
+                vRowA[pt] = gm + lk;
+                vRowP[pt] = gm + log2f(vRq[pt]);
             }
             // ---- masks and decays on the Gram matrices --------------------------
             if (tid == 0) {
@@ -1198,16 +1223,21 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             {
                 float v[32];
                 tmem_ld32(tGW + lane_addr + phalf * 32, v);
+                // A_ij = beta_i 2^(row_i - col_j) k_i.k_j (j < i), P_tj =
+                // 2^(row_t - col_j) q_t.k_j (j <= t): decays and row norms in
+                // one power of two (g <= 0: the exponents need no clamp)
                 if (row < kC) {
                     const int i = row;
-                    const float bi = vBeta[i] * vRk[i], gi = vGam[i];
+                    const float bi = vBeta[i], ai = vRowA[i];
 #pragma unroll
                     for (int q = 0; q < 32; q += 4) {
+                        const float4 c4 = *reinterpret_cast<const float4*>(vCol + phalf * 32 + q);
+                        const float cj[4] = {c4.x, c4.y, c4.z, c4.w};
                         float a4[4];
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const int j = phalf * 32 + q + u;
-                            a4[u] = (i < rows && j < i) ? bi * fast_exp2(fminf(gi - vGam[j], 0.f)) * vRk[j] * v[q + u] : 0.f;
+                            a4[u] = (i < rows && j < i) ? bi * (v[q + u] * fast_exp2(ai - cj[u])) : 0.f;
                         }
                         // 16-byte stores: with the 68-float row stride the 8 lanes of
                         // each store phase hit disjoint banks
@@ -1215,11 +1245,16 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     }
                 } else {
                     const int t = row - kC;
-                    const float rt = vRq[t], gt = vGam[t];
+                    const float at = vRowP[t];
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const int j = phalf * 32 + q;
-                        v[q] = (t < rows && j <= t) ? rt * fast_exp2(fminf(gt - vGam[j], 0.f)) * vRk[j] * v[q] : 0.f;
+                    for (int q = 0; q < 32; q += 4) {
+                        const float4 c4 = *reinterpret_cast<const float4*>(vCol + phalf * 32 + q);
+                        const float cj[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int j = phalf * 32 + q + u;
+                            v[q + u] = (t < rows && j <= t) ? v[q + u] * fast_exp2(at - cj[u]) : 0.f;
+                        }
                     }
                     uint8_t* phi = sm + kOffP + uint32_t(b * 2) * 8192u;
 #pragma unroll
