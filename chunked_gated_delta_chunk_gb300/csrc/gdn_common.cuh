@@ -183,11 +183,6 @@ void timer_end(cudaStream_t s);
 // Bytes of one chunk record of the split preparation.
 constexpr size_t kPrepRecordBytes = 82432;
 
-// Segment slot of (sequence n, segment s).
-__host__ __device__ inline int64_t seg_slot(int64_t seq_start, int n, int s, int64_t seg_tokens) {
-    return seq_start / seg_tokens + n + s;
-}
-
 struct ConvParams {
     const void* x;           // [T, C]
     const float* w;          // [C, K]

@@ -143,6 +143,15 @@ __device__ __forceinline__ int seq_of_row(const int32_t* cu, int B, int y) {
     return y;
 }
 
+// Index arithmetic of the chain kernels in 32 bits: token indices fit
+// (cu_seqlens is int32), and every thread of a CTA computes them, where the
+// 64-bit divisions cost a few thousand cycles of issue.
+__device__ __forceinline__ int ceil_div32(int64_t a, int b) { return int((uint32_t(a) + uint32_t(b) - 1u) / uint32_t(b)); }
+// Segment slot of (sequence n starting at token t0, segment s).
+__device__ __forceinline__ int64_t seg_slot32(int64_t t0, int n, int s, int64_t seg_tokens) {
+    return int64_t(uint32_t(t0) / uint32_t(seg_tokens)) + n + s;
+}
+
 // Offset of (row, col) in a swizzled tile of 64-column blocks (128-byte rows).
 __device__ __forceinline__ uint32_t toff(int row, int col, uint32_t block_stride) {
     const int blk = col >> 6, c = col & 63;
@@ -980,7 +989,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     int64_t t0 = p.cu[n], t1 = p.cu[n + 1];
     t0 = t0 < 0 ? 0 : (t0 > t_end_all ? t_end_all : t0);
     t1 = t1 < t0 ? t0 : (t1 > t_end_all ? t_end_all : t1);
-    const int seq_chunks = int((t1 - t0 + p.chunk - 1) / p.chunk);
+    const int seq_chunks = ceil_div32(t1 - t0, p.chunk);
     const size_t sbase = (size_t(n) * Hv + h) * kD * kD;
 
     // ---- which part of the sequence this CTA runs, and in which mode ------------
@@ -1001,6 +1010,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     }
     if (c_begin >= c_end && !(seg == 0 && mode == kModeFull)) return;   // no such segment
     const int nchunks = c_end > c_begin ? c_end - c_begin : 0;
+    const int64_t seq_t0 = t0;
     t0 += int64_t(c_begin) * p.chunk;                   // first token of this CTA's part
     const bool last_seg = c_end >= seq_chunks;
     // Every pass writes its outputs: the full pass the final ones, the offset
@@ -1010,7 +1020,7 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     float* next_slot = nullptr;                         // of the next segment
     if (p.seg_phase) {
         const int64_t seg_tokens = int64_t(p.seg_chunks) * p.chunk;
-        const int64_t sl = seg_slot(p.cu[n], n, seg, seg_tokens);
+        const int64_t sl = seg_slot32(seq_t0, n, seg, seg_tokens);
         slot = p.seg_ws + (size_t(h) * p.seg_slots + sl) * 3 * kD * kD;
         next_slot = slot + 3 * kD * kD;
     }
@@ -1639,7 +1649,10 @@ constexpr uint32_t kStColZ = 0, kStColZb = 128, kStColOodd = 192, kStColX = 256,
 
 __global__ void __launch_bounds__(kStThreads, 1)
 chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
-    griddep_wait();   // the records, maps and states the grids before wrote
+    // Up to the wait below this reads cu_seqlens only: an input of the call,
+    // which no kernel writes and which the preparation (always the grid
+    // before, itself behind a full wait) has read; so the index arithmetic
+    // runs while the preparation's last CTAs finish.
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kStOffBar);
@@ -1662,7 +1675,7 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     int64_t t0 = p.cu[n], t1 = p.cu[n + 1];
     t0 = t0 < 0 ? 0 : (t0 > t_end_all ? t_end_all : t0);
     t1 = t1 < t0 ? t0 : (t1 > t_end_all ? t_end_all : t1);
-    const int seq_chunks = int((t1 - t0 + p.chunk - 1) / p.chunk);
+    const int seq_chunks = ceil_div32(t1 - t0, p.chunk);
     const size_t sbase = (size_t(n) * Hv + h) * kD * kD;
     int seg = 0, mode = kModeFull;
     if (p.seg_phase == 1 && blockIdx.z > 0) {
@@ -1680,7 +1693,8 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     }
     if (c_begin >= c_end && !(seg == 0 && mode == kModeFull)) return;   // no such segment
     const int nchunks = c_end > c_begin ? c_end - c_begin : 0;
-    const int64_t slot0 = t0 / p.chunk + n + c_begin;   // record slot of this CTA's first chunk
+    const int64_t slot0 = int64_t(uint32_t(t0) / uint32_t(p.chunk)) + n + c_begin;   // record slot of this CTA's first chunk
+    const int64_t seq_t0 = t0;
     t0 += int64_t(c_begin) * p.chunk;
     const bool last_seg = c_end >= seq_chunks;
     const CUtensorMap* omap = mode == kModeTransition ? &maps.g : &maps.o;
@@ -1688,7 +1702,7 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
     float* next_slot = nullptr;
     if (p.seg_phase) {
         const int64_t seg_tokens = int64_t(p.seg_chunks) * p.chunk;
-        const int64_t sl = seg_slot(p.cu[n], n, seg, seg_tokens);
+        const int64_t sl = seg_slot32(seq_t0, n, seg, seg_tokens);
         slot = p.seg_ws + (size_t(h) * p.seg_slots + sl) * 3 * kD * kD;
         next_slot = slot + 3 * kD * kD;
     }
@@ -1743,6 +1757,7 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         bulk_load(sm + kStOffVec + uint32_t(b) * 512u, rec + kRecVec, 512, bar);
         *s_issued = c + 1;
     };
+    griddep_wait();   // the records, maps and states the grids before wrote
     // The copier thread sets up the barriers and starts the first record's
     // copies before the block's first barrier.
     if (is_copier && lane == 0) {
@@ -1940,6 +1955,9 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             {
                 // ---- incoming state (this thread: key rows 32 sub .. 32 sub + 31):
                 // Zb = bf16(S_0^T), Z = exp(gamma_S(0)) S_0^T
+                // (Zb is handed over first: the first product reads it, while Z
+                // is read only by the state update, which waits for this warp's
+                // Us and with it for these stores)
                 const float gs = __ldg(reinterpret_cast<const float*>(record(0) + kRecVec) + kC);
                 float z[32];
 #pragma unroll
@@ -1951,13 +1969,13 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) zb[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
                 GDN_TMEM_ST_X16(tZb + lane_addr + sub * 16, zb);
+                tmem_st_wait();
+                tc_fence_before();
+                warp_arrive(ST_ZBREADY);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) z[i] *= gs;
                 tmem_st16(tZ + lane_addr + sub * 32, z);
                 tmem_st16(tZ + lane_addr + sub * 32 + 16, z + 16);
-                tmem_st_wait();
-                tc_fence_before();
-                warp_arrive(ST_ZBREADY);
             }
             for (int c = 0; c < nchunks; ++c) {
                 const int b = c & 1;
@@ -2180,7 +2198,9 @@ __device__ __forceinline__ void so_store_row(uint8_t* img, int tid, const float*
 }
 
 __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
-    griddep_wait();                                  // phase 1's outputs, maps and S_1
+    // Up to the wait below this reads cu_seqlens only (an input of the call,
+    // which no kernel writes and which the grids before have read behind
+    // their own waits), so the index arithmetic overlaps phase 1's end.
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSoOffBar);
@@ -2198,7 +2218,7 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     int64_t t0 = p.cu[n], t1 = p.cu[n + 1];
     t0 = t0 < 0 ? 0 : (t0 > t_end_all ? t_end_all : t0);
     t1 = t1 < t0 ? t0 : (t1 > t_end_all ? t_end_all : t1);
-    const int seq_chunks = int((t1 - t0 + p.chunk - 1) / p.chunk);
+    const int seq_chunks = ceil_div32(t1 - t0, p.chunk);
     const int L = p.seg_chunks;
     const int nseg = (seq_chunks + L - 1) / L;
     const int short_by = nseg * L - seq_chunks;
@@ -2234,9 +2254,10 @@ __global__ void __launch_bounds__(kSoThreads, 1) seg_out_kernel(const ChunkParam
     const int nout = c_hi - c_lo;
     const bool tiles_early = nsteps < 2;             // M^T buffer 1 (the tile region) never used
     const int64_t seg_tokens = int64_t(L) * p.chunk;
-    const float* slots = p.seg_ws + (size_t(h) * p.seg_slots + seg_slot(p.cu[n], n, 0, seg_tokens)) * 3 * kD * kD;
+    const float* slots = p.seg_ws + (size_t(h) * p.seg_slots + seg_slot32(t0, n, 0, seg_tokens)) * 3 * kD * kD;
     auto slot_of = [&](int j) { return slots + size_t(j) * 3 * kD * kD; };   // B_j, M_j^T image, S_j image
 
+    griddep_wait();                                  // phase 1's outputs, maps and S_1
     if (tid == 0) {
         for (int i = 0; i < int(kSoNumBars); ++i)
             mbar_init(&bars[i], (i >= SO_OFREE0 && i < SO_DRAIN) ? kSoEpiWarps : 1);
