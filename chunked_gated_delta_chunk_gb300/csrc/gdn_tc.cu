@@ -772,7 +772,24 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         if (mma_phase > 0)                                // T's place held the last -W^T image: T = 0 again
             for (int idx = pt; idx < kC * kLdA / 4; idx += kPrepThreads)
                 reinterpret_cast<float4*>(sT)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
-        {
+        if (phalf == 1 && (pw & 1) == 0) {
+            // warps 4 and 6: rows 0-31 of A and of P against columns 32-63,
+            // every entry masked (j > i, j > t)
+            const int r0 = row & (kC - 1);
+            if (row < kC) {
+#pragma unroll
+                for (int q = 0; q < 32; q += 4)
+                    *reinterpret_cast<float4*>(sA + r0 * kLdA + 32 + q) = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int q = 0; q < 32; q += 8) {
+                    const uint32_t o = toff(r0, 32 + q, 8192);
+                    *reinterpret_cast<uint4*>(sm + kPOffPst + o) = z;
+                    *reinterpret_cast<uint4*>(sm + kPOffPst + 8192 + o) = z;
+                }
+            }
+        } else {
             float v[32];
             tmem_ld32(tGW + lane_addr + phalf * 32, v);
             // A_ij = beta_i exp(gamma_i - gamma_j) r_i r_j k_i.k_j (j < i) and
@@ -823,8 +840,20 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         block_inverse_64(sA, sT, sTmp, pt);
         if (pt == 0) bulk_wait_group_read<0>();             // the P staging, which Tb overlaps
         __syncthreads();
+        // A warp takes 32 rows of one 8-column group: the groups above the
+        // diagonal (T is lower triangular) are zeros, written without the
+        // arithmetic
         for (int idx = pt; idx < kC * 8; idx += kPrepThreads) {
-            const int t = idx >> 3, i0 = (idx & 7) * 8;
+            const int t = idx & (kC - 1), i0 = (idx >> 6) * 8;
+            const uint32_t o = toff(t, i0, 8192);
+            if (i0 > (t | 31)) {                           // the warp's every row lies above the group
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sm + kPOffTb + o) = z;
+                *reinterpret_cast<uint4*>(sm + kPOffTb + 8192 + o) = z;
+                *reinterpret_cast<uint4*>(sm + kPOffTb + 16384 + o) = z;
+                *reinterpret_cast<uint4*>(sm + kPOffTb + 24576 + o) = z;
+                continue;
+            }
             float a[8], bg[8], fb[8], fbg[8], tr[8];
             *reinterpret_cast<float4*>(fb) = *reinterpret_cast<const float4*>(vFb + i0);
             *reinterpret_cast<float4*>(fb + 4) = *reinterpret_cast<const float4*>(vFb + i0 + 4);
@@ -837,7 +866,6 @@ chunk_prep_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                 a[q] = tr[q] * fb[q];
                 bg[q] = tr[q] * fbg[q];
             }
-            const uint32_t o = toff(t, i0, 8192);
             store_split8(sm + kPOffTb + o, sm + kPOffTb + 8192 + o, a);
             store_split8(sm + kPOffTb + 16384 + o, sm + kPOffTb + 24576 + o, bg);
         }
@@ -1230,7 +1258,25 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             __syncwarp();
             if (named_sync_or(kBarPrep, kPrepThreads, lf)) { fail = true; break; }
             tc_fence_after();
-            {
+            if (phalf == 1 && (pw & 1) == 0) {
+                // prep warps 4 and 6: rows 0-31 of A and of P against columns
+                // 32-63, every entry masked (j > i, j > t)
+                const int r0 = row & (kC - 1);
+                if (row < kC) {
+#pragma unroll
+                    for (int q = 0; q < 32; q += 4)
+                        *reinterpret_cast<float4*>(sA + r0 * kLdA + 32 + q) = make_float4(0.f, 0.f, 0.f, 0.f);
+                } else {
+                    uint8_t* phi = sm + kOffP + uint32_t(b * 2) * 8192u;
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int q = 0; q < 32; q += 8) {
+                        const uint32_t o = toff(r0, 32 + q, 8192);
+                        *reinterpret_cast<uint4*>(phi + o) = z;
+                        *reinterpret_cast<uint4*>(phi + 8192 + o) = z;
+                    }
+                }
+            } else {
                 float v[32];
                 tmem_ld32(tGW + lane_addr + phalf * 32, v);
                 // A_ij = beta_i 2^(row_i - col_j) k_i.k_j (j < i), P_tj =
@@ -1277,8 +1323,19 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
             named_sync(kBarPrep, kPrepThreads);
             // ---- blocked inverse; T diag(beta), T diag(beta Gamma r_k) as hi + lo -
             block_inverse_64(sA, sT, sTmp, pt);
+            // a prep warp takes 32 rows of one 8-column group; the groups above
+            // the diagonal are zeros, written without the arithmetic
             for (int idx = pt; idx < kC * 8; idx += kPrepThreads) {
-                const int t = idx >> 3, i0 = (idx & 7) * 8;
+                const int t = idx & (kC - 1), i0 = (idx >> 6) * 8;
+                const uint32_t o = toff(t, i0, 8192);
+                if (i0 > (t | 31)) {
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(sm + kOffTb + o) = z;
+                    *reinterpret_cast<uint4*>(sm + kOffTb + 8192 + o) = z;
+                    *reinterpret_cast<uint4*>(sm + kOffTb + 16384 + o) = z;
+                    *reinterpret_cast<uint4*>(sm + kOffTb + 24576 + o) = z;
+                    continue;
+                }
                 float a[8], bg[8], fb[8], fbg[8];
                 *reinterpret_cast<float4*>(fb) = *reinterpret_cast<const float4*>(vFb + i0);
                 *reinterpret_cast<float4*>(fb + 4) = *reinterpret_cast<const float4*>(vFb + i0 + 4);
@@ -1292,7 +1349,6 @@ chunk_tc_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
                     a[q] = tr[q] * fb[q];
                     bg[q] = tr[q] * fbg[q];
                 }
-                const uint32_t o = toff(t, i0, 8192);
                 store_split8(sm + kOffTb + o, sm + kOffTb + 8192 + o, a);
                 store_split8(sm + kOffTb + 16384 + o, sm + kOffTb + 24576 + o, bg);
             }
