@@ -160,8 +160,8 @@ void gdn_prefill_desc_init(gdn_prefill_desc* d);
  * nor the split preparation: one CTA per (sequence, value head) walks all of
  * its chunks in one kernel (chunk_tc_kernel for bf16, dk = dv = 128).  That
  * is several times slower than gdn_prefill_ex with a workspace on a long or
- * few-sequence batch (4096 tokens x 16 heads on a GB300: about 0.46 ms
- * against 0.10 ms); callers that can spare the workspace should use
+ * few-sequence batch (4096 tokens x 16 heads on a GB300: about 0.45 ms
+ * against 0.095 ms); callers that can spare the workspace should use
  * gdn_prefill_ex.
  *   q, k      bf16 [T, Hk, dk]      v, out   bf16 [T, Hv, dv]
  *   g, beta   fp32 [T, Hv]          state_in / state_out  fp32 [B, Hv, dk, dv]
