@@ -1943,12 +1943,14 @@ chunk_state_kernel(const ChunkParams p, const __grid_constant__ Maps maps) {
         }
     } else {
         // =========================================================== epilogue
-        // Lane 0 of each warp polls the mbarriers; the warp follows.
+        // Thread 0 polls the mbarriers and the sixteen warps follow through a
+        // named barrier (every wait below is reached by all of them), so that
+        // one thread polls instead of sixteen beside the issuer's polls.
         __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(mode == kModeTransition ? p.g_out : p.out);
         auto warp_wait = [&](int b, uint32_t parity) {
-            bool ok = true;
-            if (lane == 0) ok = spin(b, parity);
-            return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            bool bad = false;
+            if (tid == 0) bad = !spin(b, parity);
+            return !named_sync_or(kBarPrep, kStEpiThreads, bad);
         };
         auto warp_arrive = [&](int b) {
             __syncwarp();
