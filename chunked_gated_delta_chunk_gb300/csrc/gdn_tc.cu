@@ -26,8 +26,11 @@
 //                                             Us = U diag(exp(min(gamma_S-gamma,0)) r_k),
 //                                             bf16 hi + lo, in TMEM
 //          O += U^T P^T                       P split into bf16 hi + lo
-// L2 normalisation of q and k is folded into row scalings (r = 1/|x|); every
-// exponent is clamped at zero and only evaluated where its mask keeps it.
+// L2 normalisation of q and k is folded into row scalings (r = 1/|x|).  The
+// masks of A and P take the decay and both norms as one power of two per
+// entry, evaluated only where the mask keeps it (with g <= 0, gamma never
+// increases, so these exponents need no clamp); the state update's weights
+// keep the clamp at zero of exp(min(gamma_S - gamma, 0)).
 // The hi/lo splits keep the inverse's products and the state update to
 // ~16 bits before they meet a bf16 operand.
 //
