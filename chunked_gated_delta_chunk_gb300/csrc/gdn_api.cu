@@ -211,6 +211,8 @@ int64_t prep_slots(const gdn_prefill_desc* d) { return d->T_total / d->chunk + d
 size_t prep_workspace(const gdn_prefill_desc* d) {
     if (d->dtype != GDN_BF16 || d->dk != 128 || d->dv != 128) return 0;   // tensor-core path only
     if (d->T_total <= 0 || d->B <= 0 || d->split_prep < 0) return 0;
+    // the preparation counts its items (Hv x slots) in 32 bits
+    if (int64_t(d->Hv) * prep_slots(d) >= (int64_t(1) << 31)) return 0;
     return size_t(d->Hv) * size_t(prep_slots(d)) * gdn::kPrepRecordBytes;
 }
 
@@ -341,8 +343,7 @@ int gdn_prefill_ex(const gdn_prefill_desc* d, gdn_stream_t stream) {
                          p.seg_max - 1 <= gdn::kSegTable ? p.seg_gstart : nullptr);
             p.g_out = static_cast<char*>(d->workspace) + conv_bytes + segment_map_bytes(d, sc);
         }
-        // the preparation counts its items (Hv x slots) in 32 bits
-        if (prep_bytes > 0 && d->workspace != nullptr && int64_t(d->Hv) * prep_slots(d) < (int64_t(1) << 31) &&
+        if (prep_bytes > 0 && d->workspace != nullptr &&
             d->workspace_bytes >= conv_bytes + seg_bytes + prep_bytes) {
             p.prep_ws = static_cast<uint8_t*>(d->workspace) + conv_bytes + seg_bytes;
             p.prep_slots = prep_slots(d);

@@ -144,8 +144,9 @@ typedef struct gdn_prefill_desc {
      * as one 82432-byte record per (value head, chunk slot), Hv *
      * (T_total / chunk + B + 1) records; the state pass then streams the
      * records (chunk_state_kernel).  The results agree with those without
-     * it within rounding.  >= 0 = on when the workspace holds the records,
-     * < 0 = off. */
+     * it within rounding.  >= 0 = on when the workspace holds the records
+     * and there are fewer than 2^31 of them (else, as with < 0, off and
+     * not asked for by gdn_workspace_bytes). */
     int split_prep;
 } gdn_prefill_desc;
 

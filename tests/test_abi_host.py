@@ -299,3 +299,19 @@ def test_batch_without_tokens_needs_no_token_tensors(lib):
     d_conv = B.make_desc(B=3, Hk=2, Hv=4, dk=128, dv=128, T_total=0, cu_seqlens=A, conv_state_out=A,
                          conv_kernel=1)
     assert lib.gdn_prefill_ex(ctypes.byref(d_conv), None) == B.GDN_ERR_UNSUPPORTED
+
+
+def test_preparation_counts_items_in_32_bits(lib):
+    """The split preparation numbers its items (Hv x chunk slots) in 32 bits:
+    a description with 2^31 or more of them asks for no chunk records and
+    runs the chain with the inline preparation, one with fewer uses them."""
+    T = 1 << 30
+    slots = T // 64 + 1 + 1
+    for hv, records in ((127, True), (128, False)):
+        assert (hv * slots < (1 << 31)) == records
+        d = B.make_desc(B=1, Hk=hv, Hv=hv, dk=128, dv=128, T_total=T, segment_chunks=-1,
+                        q=A, k=A, v=A, g=A, beta=A, out=A, cu_seqlens=A)
+        assert B.gdn_workspace_bytes(d) == (hv * slots * 82432 if records else 0)
+        d.workspace, d.workspace_bytes = A, 1 << 62
+        assert B.gdn_prefill_plan(d) == (["chunk_prep_kernel", "chunk_state_kernel"] if records
+                                         else ["chunk_tc_kernel"])
