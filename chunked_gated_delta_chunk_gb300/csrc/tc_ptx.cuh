@@ -366,15 +366,5 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Byte offset of element (row, col) in a K-major tile stored with the
-// 128-byte swizzle: rows of 64 bf16 (128 B), 16-byte chunks XOR-ed with the
-// row index modulo 8.  `rows` rows per 64-column block; blocks of 64 columns
-// follow each other.  The tile base must be 1024-byte aligned.
-__host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int rows) {
-    const int blk = col >> 6, c = col & 63;
-    const int chunk = (c >> 3) ^ (row & 7);
-    return uint32_t(blk * rows * 128 + row * 128 + chunk * 16 + (c & 7) * 2);
-}
-
 }  // namespace ptx
 }  // namespace gdn
