@@ -76,3 +76,17 @@ def test_kernel_hash_ignores_comments_not_code():
     assert bench._code_only(base) != bench._code_only(base.replace("a = 1", "a = 2"))
     assert bench._code_only(base) != bench._code_only(base.replace('"x // y"', '"x // z"'))
 
+
+
+def test_roofline_numerators_of_prompt4k():
+    """The path roofline's numerators for the 4096-token prompt (B=1, 16 heads,
+    dk=dv=128, bf16): q, k, v, out in bf16, g and beta in fp32, the fp32 state
+    in and out, cu_seqlens; and the FLOPs of full 64-row tiles."""
+    bench = _load_bench()
+    from chunked_gated_delta_chunk_gb300 import inputs
+    p = inputs.make_config(2)
+    T, H, d = 4096, 16, 128
+    want_bytes = T * 4 * H * d * 2 + T * H * 8 + 2 * H * d * d * 4 + 2 * 4
+    assert bench.algorithmic_bytes(p) == want_bytes == 69730312
+    want_flops = T * (H * 4 * 64 * d + H * (6 * d * d + 4 * 64 * d))
+    assert bench.algorithmic_flops(p) == want_flops == 10737418240
